@@ -1,0 +1,378 @@
+"""Benchmark: block-sparse attention fwd+bwd at seq 8192 on GB300.
+
+One step = bsr_attn_fwd + bsr_attn_bwd over one batch of synthetic inputs
+(default workload: batch 1, heads 16, seq 8192, head_dim 128, bf16, block
+mask = band |m-n| <= 2 plus block row 0 and block column 0, 436 stored
+blocks).  Throughput is counted over stored blocks only: 4*128^2*D FLOP
+forward and 10*128^2*D backward per stored block and head.
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
+
+Prints ONE JSON line on rank 0.  Multi-GPU runs (torchrun) are independent
+replicas with the whole workload per rank (weak scaling); timing is the max
+over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from block_sparse_attention_bsr_gb300 import inputs  # noqa: E402
+
+BLOCK = 128
+METRIC = "fwd+bwd ms & TFLOP/s over stored blocks at seq 8192; % of GB300 bf16 TC peak"
+# contraction FLOP per stored block and head, as each kernel executes them
+FLOP_PER_BLOCK = {"fwd": 4, "dq": 6, "dkdv": 8}  # x 128^2 * D
+
+
+def alg_flops(wl, nnzb, part="total"):
+    per = {"fwd": 4, "bwd": 10, "total": 14}[part]
+    return per * BLOCK * BLOCK * wl.head_dim * nnzb * wl.batch * wl.heads
+
+
+def kernel_flops(name, wl, nnzb):
+    for key, mult in FLOP_PER_BLOCK.items():
+        if name.startswith(key):
+            return mult * BLOCK * BLOCK * wl.head_dim * nnzb * wl.batch * wl.heads
+    return None
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(bf16=d.get("bf16_tflops"), bf16_sustained=d.get("bf16_tflops_sustained"),
+                    hbm=d.get("hbm_gbs"), source="measured")
+    return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def flush_l2(buf):
+    buf.add_(1)  # writes the whole buffer (larger than the 129 MB L2)
+
+
+def run_ours(args, rank, world, dev):
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    wl = inputs.WORKLOADS[args.workload]
+    bm = wl.block_mask()
+    rp, ci = inputs.bsr_from_block_mask(bm)
+    st = bsr.Structure(rp, ci, wl.nb, dev)
+    nnzb = st.nnzb
+    hQ, hK, hV, hdO = wl.inputs(seed=0)
+    Q, K, V, dO = (t.to(dev) for t in (hQ, hK, hV, hdO))
+    O = torch.empty_like(Q)
+    rm = torch.empty(Q.shape[:3], device=dev, dtype=torch.float32)
+    rd = torch.empty_like(rm)
+    dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q, k, v, do, o, m, d, gq, gk, gv):
+        bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale, o, m, d, stream)
+        bsr.bsr_attn_bwd(q, k, v, o, do, m, d, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, wl.scale,
+                         gq, gk, gv, stream)
+
+    args_dev = (Q, K, V, dO, O, rm, rd, dQ, dK, dV)
+    l2 = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        flush_l2(l2)
+        step(*args_dev)
+    bsr.bsr_attn_check()
+
+    # device-resident timed region: per-step CUDA events, L2 flushed before each step
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    bsr.profile_collect()
+    bsr.profile_enable(True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for i in range(args.steps):
+            flush_l2(l2)
+            evs[i][0].record(stream)
+            step(*args_dev)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    bsr.profile_enable(False)
+    prof = bsr.profile_collect()
+    bsr.bsr_attn_check()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+
+    # forward alone and backward alone (same protocol, untimed for the headline)
+    def time_part(fn, reps):
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i in range(reps):
+            flush_l2(l2)
+            e[i][0].record(stream)
+            fn()
+            e[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in e)
+
+    ms_fwd = time_part(lambda: bsr.bsr_attn_fwd(Q, K, V, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale,
+                                                 O, rm, rd, stream), max(args.steps, 5))
+    ms_bwd = time_part(lambda: bsr.bsr_attn_bwd(Q, K, V, O, dO, rm, rd, st.row_ptr, st.col_idx, st.col_ptr,
+                                                 st.row_idx, wl.scale, dQ, dK, dV, stream), max(args.steps, 5))
+
+    # end to end through the C ABI from pinned host buffers
+    pin = [t.pin_memory() for t in (hQ, hK, hV, hdO)]
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (O, rm, rd, dQ, dK, dV)]
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_l2(l2)
+        e2e_ev[i][0].record(stream)
+        for d_, h_ in zip((Q, K, V, dO), pin):
+            d_.copy_(h_, non_blocking=True)
+        step(*args_dev)
+        for h_, d_ in zip(outs_h, (O, rm, rd, dQ, dK, dV)):
+            h_.copy_(d_, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), world) / args.steps
+
+    flops = alg_flops(wl, nnzb)
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    peaks = load_peaks()
+    kern = {k: {"launches": n, "ms_per_launch": ms / max(n, 1)} for k, (n, ms) in prof.items()}
+    dom = max(prof.items(), key=lambda kv: kv[1][1]) if prof else None
+    roofline = None
+    if dom:
+        name, (n, ms) = dom
+        kf = kernel_flops(name, wl, nnzb)
+        avg_ms = ms / n
+        achieved = kf / (avg_ms * 1e-3) / 1e12 if kf else None
+        roofline = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
+                    "unit": "TFLOP/s", "frac": (achieved / peaks["bf16"]) if achieved else None,
+                    "traffic": None, "peak_source": peaks["source"] + " bf16 burst",
+                    "flop_per_launch": kf, "ms_per_launch": avg_ms}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "heads": wl.heads, "seq": wl.seq,
+                   "head_dim": wl.head_dim, "block": BLOCK, "mask": wl.mask, "radius": wl.radius,
+                   "nnzb": nnzb, "density": round(nnzb / wl.nb ** 2, 4), "l2": "flushed before every step",
+                   "parallelism": f"replicas x{world}"},
+        "ms_fwd": round(ms_fwd, 4), "ms_bwd": round(ms_bwd, 4),
+        "pct_of_bf16_peak": round(100 * value / world / peaks["bf16"], 2),
+        "alg_gflop_per_step": flops / 1e9,
+        "kernels": kern,
+        "gpu_launches": sum(n for n, _ in prof.values()),
+        "roofline": roofline,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk.summary(),
+    }
+    if args.sdpa:
+        line["sdpa"] = sdpa_comparators(Q, K, V, dO, bm, l2, stream, dev, args)
+    return line
+
+
+def sdpa_comparators(Q, K, V, dO, bm, l2, stream, dev, args):
+    """Dense masked SDPA (boolean element mask) and unmasked dense SDPA on the same GPU, fwd+bwd ms."""
+    F = torch.nn.functional
+    em = torch.from_numpy(np.repeat(np.repeat(bm, BLOCK, 0), BLOCK, 1)).to(dev)
+    res = {}
+    for name, mask in (("masked", em), ("dense", None)):
+        def fb():
+            q, k, v = (t.detach().requires_grad_() for t in (Q, K, V))
+            o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask)
+            o.backward(dO)
+        try:
+            for _ in range(2):
+                fb()
+            ts = []
+            for _ in range(5):
+                flush_l2(l2)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fb()
+                b.record()
+                torch.cuda.synchronize(dev)
+                ts.append(a.elapsed_time(b))
+            res[f"sdpa_{name}_fwd_bwd_ms"] = round(statistics.median(ts), 4)
+        except Exception as e:  # report and continue
+            res[f"sdpa_{name}_fwd_bwd_ms"] = f"failed: {type(e).__name__}: {str(e)[:100]}"
+    return res
+
+
+def cpu_baseline(wl, budget_s):
+    """The fp64 oracle on the host cores over a bounded sample: whole heads of the workload, fwd+bwd."""
+    import oracle
+
+    bm = wl.block_mask()
+    nnzb = int(bm.sum())
+    hQ, hK, hV, hdO = wl.inputs(seed=0)
+    heads, t0 = 0, time.perf_counter()
+    while True:
+        b, h = divmod(heads, wl.heads)
+        b %= wl.batch
+        oracle.attn_fwd_bwd_head(hQ[b, h].double().numpy(), hK[b, h].double().numpy(), hV[b, h].double().numpy(),
+                                 hdO[b, h].double().numpy(), bm, wl.scale)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or heads >= wl.batch * wl.heads:
+            break
+    flops = 14 * BLOCK * BLOCK * wl.head_dim * nnzb * heads
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} of {wl.batch * wl.heads} (batch, head) slices of {wl.name}, fwd+bwd, "
+                      f"dense fp64 numpy, {el:.1f} s", "seconds": el, "heads": heads}
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="global_s8192", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sdpa", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time dense masked / unmasked SDPA on the same GPU")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    wl = inputs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        # the CPU oracle stands as the reference arm; rank 0 alone runs it.
+        # One step = the oracle's fwd+bwd on one (batch, head) slice of the workload.
+        if rank != 0:
+            return
+        import oracle
+
+        bm = wl.block_mask()
+        nnzb = int(bm.sum())
+        hQ, hK, hV, hdO = wl.inputs(seed=0)
+        times = []
+        for i in range(args.warmup + args.steps):
+            b, h = divmod(i % (wl.batch * wl.heads), wl.heads)
+            t0 = time.perf_counter()
+            oracle.attn_fwd_bwd_head(*(t[b, h].double().numpy() for t in (hQ, hK, hV, hdO)), bm, wl.scale)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        sec = statistics.median(times)
+        flops_head = 14 * BLOCK * BLOCK * wl.head_dim * nnzb
+        v = flops_head / sec / 1e12
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        sample = f"one (batch, head) slice of {wl.name} per step, fwd+bwd, dense fp64 numpy, median {sec:.2f} s"
+        line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(sec * 1e3 * wl.batch * wl.heads, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": wl.name, "batch": wl.batch, "heads": wl.heads, "seq": wl.seq,
+                           "head_dim": wl.head_dim, "block": BLOCK, "mask": wl.mask, "nnzb": nnzb},
+                "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    # CPU oracle baseline first, on rank 0 at N=1, before any GPU work
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if world > 1:
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+        dev = torch.device("cuda", local)
+    else:
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+    line = run_ours(args, rank, world, dev)
+    if cpu is not None:
+        line["cpu_baseline"] = {k: (round(v, 6) if isinstance(v, float) else v) for k, v in cpu.items()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+"""Block-sparse attention over BSR-128 block masks on GB300 (sm_103a).
+
+A thin ctypes binding over the C-ABI library ``libbsrattn.so`` (declared in
+``include/bsr_attn.h``).  The functions below only marshal arguments: torch
+tensors become bsr_tensor descriptors and device pointers, the current torch
+stream becomes the ``stream`` argument, and a non-OK status raises
+``BsrError``.  Every step of the computation runs in the library's CUDA
+kernels; if the library is missing, calls fail loudly (there is no fallback).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libbsrattn.so")
+
+BSR_F32, BSR_BF16 = 0, 1
+STATUS_NAMES = {0: "BSR_OK", 1: "BSR_ERR_INVALID_ARG", 2: "BSR_ERR_UNSUPPORTED", 3: "BSR_ERR_CUDA",
+                4: "BSR_ERR_TIMEOUT", 5: "BSR_ERR_DEVICE_CHECK"}
+
+# Every symbol include/bsr_attn.h declares.
+EXPORTS = ("bsr_attn_fwd", "bsr_attn_bwd", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
+           "bsr_last_error", "bsr_profile_enable", "bsr_profile_collect")
+
+
+class BsrError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class bsr_tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("heads", ctypes.c_int32), ("seq", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class bsr_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_float)]
+
+
+_lib_handle = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libbsrattn.so and declares its prototypes (raises if it was not built)."""
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                           "(block_sparse_attention_bsr_gb300/_build.py); there is no CPU fallback")
+    lib = ctypes.CDLL(path)
+    P, I32, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    T = ctypes.POINTER(bsr_tensor)
+    lib.bsr_attn_fwd.argtypes = [T, T, T, P, P, I32, I32, F32, T, P, P, P]
+    lib.bsr_attn_bwd.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
+    lib.bsr_build_bsc.argtypes = [P, P, I32, I32, P, P]
+    lib.bsr_validate.argtypes = [P, P, I32, I32]
+    lib.bsr_attn_check.argtypes = [P]
+    lib.bsr_last_error.argtypes = []
+    lib.bsr_last_error.restype = ctypes.c_char_p
+    lib.bsr_profile_enable.argtypes = [I32]
+    lib.bsr_profile_enable.restype = None
+    lib.bsr_profile_collect.argtypes = [ctypes.POINTER(bsr_kernel_time), I32]
+    lib.bsr_profile_collect.restype = I32
+    for name in ("bsr_attn_fwd", "bsr_attn_bwd", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
+        getattr(lib, name).restype = I32
+    _lib_handle = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = load_library().bsr_last_error().decode(errors="replace")
+        raise BsrError(status, msg)
+
+
+def _desc(t) -> bsr_tensor:
+    import torch
+
+    if t.dtype == torch.float32:
+        dt = BSR_F32
+    elif t.dtype == torch.bfloat16:
+        dt = BSR_BF16
+    else:
+        raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+    if t.dim() != 4 or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError("dense operands must be contiguous CUDA tensors [batch, heads, seq, head_dim]")
+    b, h, s, d = t.shape
+    return bsr_tensor(t.data_ptr(), dt, b, h, s, d)
+
+
+def _dev_ptr(t, dtype_name: str) -> int:
+    if not t.is_cuda or not t.is_contiguous() or str(t.dtype) != dtype_name:
+        raise ValueError(f"expected a contiguous CUDA {dtype_name} tensor, got {t.dtype} on {t.device}")
+    return t.data_ptr()
+
+
+def _stream(stream, like) -> int:
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream(like.device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def bsr_attn_fwd(Q, K, V, row_ptr, col_idx, n_brows: int, block: int, scale: float, O, row_max, row_denom,
+                 stream=None) -> None:
+    """Forward block-sparse attention: writes O, row_max, row_denom (see include/bsr_attn.h)."""
+    lib = load_library()
+    q, k, v, o = (_desc(t) for t in (Q, K, V, O))
+    _check(lib.bsr_attn_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                            _dev_ptr(row_ptr, "torch.int32"), _dev_ptr(col_idx, "torch.int32"),
+                            int(n_brows), int(block), float(scale), ctypes.byref(o),
+                            _dev_ptr(row_max, "torch.float32"), _dev_ptr(row_denom, "torch.float32"),
+                            _stream(stream, Q)))
+
+
+def bsr_attn_bwd(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx, scale: float,
+                 dQ, dK, dV, stream=None) -> None:
+    """Backward block-sparse attention: writes dQ, dK, dV (see include/bsr_attn.h)."""
+    lib = load_library()
+    q, k, v, o, do, dq, dk, dv = (_desc(t) for t in (Q, K, V, O, dO, dQ, dK, dV))
+    i32 = "torch.int32"
+    _check(lib.bsr_attn_bwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(o), ctypes.byref(do),
+                            _dev_ptr(row_max, "torch.float32"), _dev_ptr(row_denom, "torch.float32"),
+                            _dev_ptr(row_ptr, i32), _dev_ptr(col_idx, i32), _dev_ptr(col_ptr, i32),
+                            _dev_ptr(row_idx, i32), float(scale),
+                            ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), _stream(stream, Q)))
+
+
+def _host_i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def bsr_validate(row_ptr_h, col_idx_h, n_brows: int, n_bcols: int) -> None:
+    """Checks host BSR lists; raises BsrError with the library's message if they are malformed."""
+    rp, ci = _host_i32(row_ptr_h), _host_i32(col_idx_h)
+    if len(rp) != n_brows + 1:
+        raise BsrError(1, f"row_ptr has {len(rp)} entries, expected n_brows + 1 = {n_brows + 1}")
+    _check(load_library().bsr_validate(rp.ctypes.data, ci.ctypes.data if ci.size else None, n_brows, n_bcols))
+
+
+def bsr_build_bsc(row_ptr_h, col_idx_h, n_brows: int, n_bcols: int):
+    """Host BSC transpose: returns (col_ptr int32 [n_bcols+1], row_idx int32 [nnzb])."""
+    rp, ci = _host_i32(row_ptr_h), _host_i32(col_idx_h)
+    if len(rp) != n_brows + 1:
+        raise BsrError(1, f"row_ptr has {len(rp)} entries, expected n_brows + 1 = {n_brows + 1}")
+    nnzb = int(rp[-1]) if len(rp) else 0
+    col_ptr = np.zeros(n_bcols + 1, dtype=np.int32)
+    row_idx = np.zeros(max(nnzb, 1), dtype=np.int32)
+    _check(load_library().bsr_build_bsc(rp.ctypes.data, ci.ctypes.data if ci.size else None, n_brows, n_bcols,
+                                        col_ptr.ctypes.data, row_idx.ctypes.data))
+    return col_ptr, row_idx[:nnzb]
+
+
+def bsr_attn_check(stream=None) -> None:
+    """Synchronises the stream and raises if a kernel reported a timeout or a failed index check."""
+    import torch
+
+    s = torch.cuda.current_stream().cuda_stream if stream is None else _stream(stream, None)
+    _check(load_library().bsr_attn_check(s))
+
+
+def profile_enable(on: bool = True) -> None:
+    load_library().bsr_profile_enable(1 if on else 0)
+
+
+def profile_collect() -> dict:
+    """{kernel name: (launches, total ms)} since the last collect (events on the launching stream)."""
+    buf = (bsr_kernel_time * 64)()
+    n = load_library().bsr_profile_collect(buf, 64)
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n)}
+
+
+class Structure:
+    """Device copies of one BSR block mask and its BSC transpose (built by bsr_build_bsc)."""
+
+    def __init__(self, row_ptr_h, col_idx_h, n_bcols: int, device):
+        import torch
+
+        rp, ci = _host_i32(row_ptr_h), _host_i32(col_idx_h)
+        self.n_brows = len(rp) - 1
+        self.n_bcols = n_bcols
+        bsr_validate(rp, ci, self.n_brows, n_bcols)
+        cp, ri = bsr_build_bsc(rp, ci, self.n_brows, n_bcols)
+        self.host = dict(row_ptr=rp, col_idx=ci, col_ptr=cp, row_idx=ri)
+        # an empty index array still gets one element so its device pointer is valid
+        self.dev = {k: torch.from_numpy(v if v.size else np.zeros(1, np.int32)).to(device)
+                    for k, v in self.host.items()}
+        self.nnzb = int(rp[-1])
+
+    @property
+    def row_ptr(self):
+        return self.dev["row_ptr"]
+
+    @property
+    def col_idx(self):
+        return self.dev["col_idx"]
+
+    @property
+    def col_ptr(self):
+        return self.dev["col_ptr"]
+
+    @property
+    def row_idx(self):
+        return self.dev["row_idx"]

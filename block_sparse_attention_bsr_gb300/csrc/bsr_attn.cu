@@ -1,0 +1,256 @@
+// C-ABI front end: argument checks, scratch, the device status word, kernel
+// timing and dispatch to the attention kernels.
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+
+namespace bsr {
+
+namespace {
+thread_local std::string g_error;
+
+// Device status word: set by kernels whose bounded waits give up or whose
+// index checks fail; read and cleared by bsr_attn_check.
+__device__ int g_status;
+
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static std::mutex mu;
+  static std::vector<int*> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  if ((int)cache.size() <= dev) cache.resize(dev + 1, nullptr);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    cache[dev] = (int*)p;
+  }
+  return cache[dev];
+}
+
+// ------------------------------------------------------------ profiling --
+struct TimedLaunch {
+  std::string name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<TimedLaunch> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+bsr_status fail(bsr_status status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return status;
+}
+
+LaunchTimer::LaunchTimer(const char* name, cudaStream_t stream) : slot_(-1), stream_(stream) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof_on) return;
+  TimedLaunch t{name, take_event(), take_event()};
+  cudaEventRecord(t.start, stream);
+  g_prof.push_back(t);
+  slot_ = (int)g_prof.size() - 1;
+}
+
+LaunchTimer::~LaunchTimer() {
+  if (slot_ < 0) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (slot_ < (int)g_prof.size()) cudaEventRecord(g_prof[slot_].stop, stream_);
+}
+
+bsr_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return BSR_OK;
+}
+
+namespace {
+
+bsr_status check_tensor(const bsr_tensor* t, const char* name, const bsr_tensor* ref) {
+  if (!t) return fail(BSR_ERR_INVALID_ARG, "%s: null descriptor", name);
+  if (!t->data) return fail(BSR_ERR_INVALID_ARG, "%s: null data pointer", name);
+  if (t->dtype != BSR_F32 && t->dtype != BSR_BF16)
+    return fail(BSR_ERR_UNSUPPORTED, "%s: dtype %d not supported (BSR_F32 or BSR_BF16)", name, t->dtype);
+  if (t->batch < 1 || t->heads < 1 || t->seq < 1)
+    return fail(BSR_ERR_INVALID_ARG, "%s: non-positive shape [%d, %d, %d, %d]", name, t->batch, t->heads, t->seq,
+                t->head_dim);
+  if (t->head_dim != 64 && t->head_dim != 128 && t->head_dim != 256 && t->head_dim != 512)
+    return fail(BSR_ERR_UNSUPPORTED, "%s: head_dim %d not supported (64, 128, 256 or 512)", name, t->head_dim);
+  if (ref && (t->batch != ref->batch || t->heads != ref->heads || t->seq != ref->seq || t->head_dim != ref->head_dim))
+    return fail(BSR_ERR_INVALID_ARG, "%s: shape [%d, %d, %d, %d] differs from Q [%d, %d, %d, %d]", name, t->batch,
+                t->heads, t->seq, t->head_dim, ref->batch, ref->heads, ref->seq, ref->head_dim);
+  if (ref && t->dtype != ref->dtype)
+    return fail(BSR_ERR_UNSUPPORTED, "%s: dtype %d differs from Q's %d (mixed operands are not converted)", name,
+                t->dtype, ref->dtype);
+  return BSR_OK;
+}
+
+bsr_status make_dims(const bsr_tensor* Q, float scale, Dims* d) {
+  if ((long long)Q->batch * Q->heads > (1LL << 30))
+    return fail(BSR_ERR_INVALID_ARG, "batch * heads = %lld too large", (long long)Q->batch * Q->heads);
+  if (Q->seq % 128 != 0) return fail(BSR_ERR_INVALID_ARG, "seq %d is not a multiple of the block size 128", Q->seq);
+  if (!isfinite(scale)) return fail(BSR_ERR_INVALID_ARG, "scale is not finite");
+  d->BH = Q->batch * Q->heads;
+  d->S = Q->seq;
+  d->D = Q->head_dim;
+  d->nb = Q->seq / 128;
+  d->dtype = Q->dtype;
+  d->scale = scale;
+  return BSR_OK;
+}
+
+}  // namespace
+}  // namespace bsr
+
+using namespace bsr;
+
+extern "C" const char* bsr_last_error(void) { return g_error.c_str(); }
+
+extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                                   const int32_t* row_ptr, const int32_t* col_idx, int32_t n_brows,
+                                   int32_t block, float scale,
+                                   bsr_tensor* O, float* row_max, float* row_denom, void* stream) {
+  bsr_status st;
+  if (block != 128) return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd: block %d not supported (128)", block);
+  if ((st = check_tensor(Q, "Q", nullptr)) || (st = check_tensor(K, "K", Q)) || (st = check_tensor(V, "V", Q)) ||
+      (st = check_tensor(O, "O", Q)))
+    return st;
+  if (!row_ptr || !col_idx || !row_max || !row_denom)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_attn_fwd: null row_ptr / col_idx / row_max / row_denom");
+  FwdArgs a{};
+  if ((st = make_dims(Q, scale, &a.d))) return st;
+  if (n_brows != a.d.nb)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_attn_fwd: n_brows %d but seq %d / 128 = %d", n_brows, Q->seq, a.d.nb);
+  a.Q = Q->data;
+  a.K = K->data;
+  a.V = V->data;
+  a.O = O->data;
+  a.row_max = row_max;
+  a.row_denom = row_denom;
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.status = status_ptr();
+  if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
+  cudaStream_t s = (cudaStream_t)stream;
+  return launch_fwd_simt(a, s);
+}
+
+extern "C" bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                                   const bsr_tensor* O, const bsr_tensor* dO,
+                                   const float* row_max, const float* row_denom,
+                                   const int32_t* row_ptr, const int32_t* col_idx,
+                                   const int32_t* col_ptr, const int32_t* row_idx,
+                                   float scale,
+                                   bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream) {
+  bsr_status st;
+  if ((st = check_tensor(Q, "Q", nullptr)) || (st = check_tensor(K, "K", Q)) || (st = check_tensor(V, "V", Q)) ||
+      (st = check_tensor(O, "O", Q)) || (st = check_tensor(dO, "dO", Q)) || (st = check_tensor(dQ, "dQ", Q)) ||
+      (st = check_tensor(dK, "dK", Q)) || (st = check_tensor(dV, "dV", Q)))
+    return st;
+  if (!row_max || !row_denom || !row_ptr || !col_idx || !col_ptr || !row_idx)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_attn_bwd: null statistics or structure array");
+  BwdArgs a{};
+  if ((st = make_dims(Q, scale, &a.d))) return st;
+  a.Q = Q->data;
+  a.K = K->data;
+  a.V = V->data;
+  a.O = O->data;
+  a.dO = dO->data;
+  a.row_max = row_max;
+  a.row_denom = row_denom;
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.col_ptr = col_ptr;
+  a.row_idx = row_idx;
+  a.dQ = dQ->data;
+  a.dK = dK->data;
+  a.dV = dV->data;
+  a.status = status_ptr();
+  if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_bwd: no CUDA device");
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t delta_bytes = sizeof(float) * (size_t)a.d.BH * a.d.S;
+  cudaError_t e = cudaMallocAsync((void**)&a.delta, delta_bytes, s);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaMallocAsync(%zu): %s", delta_bytes, cudaGetErrorString(e));
+  st = launch_delta(a, s);
+  if (st == BSR_OK) st = launch_dq_simt(a, s);
+  if (st == BSR_OK) st = launch_dkdv_simt(a, s);
+  e = cudaFreeAsync(a.delta, s);
+  if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaFreeAsync: %s", cudaGetErrorString(e));
+  return st;
+}
+
+extern "C" bsr_status bsr_attn_check(void* stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_check: %s", cudaGetErrorString(e));
+  int* p = status_ptr();
+  if (!p) return fail(BSR_ERR_CUDA, "bsr_attn_check: no CUDA device");
+  int v = 0, zero = 0;
+  e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_check: %s", cudaGetErrorString(e));
+  if (v == kStatusTimeout) return fail(BSR_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (v == kStatusDeviceCheck) return fail(BSR_ERR_DEVICE_CHECK, "a device-side index check failed (block index out of range)");
+  if (v != 0) return fail(BSR_ERR_CUDA, "unknown device status %d", v);
+  return BSR_OK;
+}
+
+extern "C" void bsr_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = on != 0;
+}
+
+extern "C" int32_t bsr_profile_collect(bsr_kernel_time* out, int32_t max_entries) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  std::vector<bsr_kernel_time> agg;
+  for (auto& t : g_prof) {
+    float ms = 0.f;
+    cudaEventSynchronize(t.stop);
+    cudaEventElapsedTime(&ms, t.start, t.stop);
+    size_t k = 0;
+    for (; k < agg.size(); ++k)
+      if (t.name == agg[k].name) break;
+    if (k == agg.size()) {
+      bsr_kernel_time z{};
+      strncpy(z.name, t.name.c_str(), sizeof(z.name) - 1);
+      agg.push_back(z);
+    }
+    agg[k].launches += 1;
+    agg[k].total_ms += ms;
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  g_prof.clear();
+  int32_t n = 0;
+  for (auto& a : agg) {
+    if (n >= max_entries) break;
+    if (out) out[n] = a;
+    ++n;
+  }
+  return n;
+}

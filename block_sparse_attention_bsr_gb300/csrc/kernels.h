@@ -1,0 +1,78 @@
+// Kernel-side declarations: argument blocks and launchers for the attention
+// kernels.  Shared by the C-ABI front end and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace bsr {
+
+// Device status word values (mirrors bsr_status).
+enum : int { kStatusOk = 0, kStatusTimeout = BSR_ERR_TIMEOUT, kStatusDeviceCheck = BSR_ERR_DEVICE_CHECK };
+
+struct Dims {
+  int BH;      // batch * heads
+  int S;       // sequence length (rows per head)
+  int D;       // head_dim
+  int nb;      // S / 128 block rows (= block columns)
+  int dtype;   // bsr_dtype
+  float scale;
+};
+
+struct FwdArgs {
+  Dims d;
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* O;
+  float* row_max;
+  float* row_denom;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  int* status;
+};
+
+struct BwdArgs {
+  Dims d;
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* O;
+  const void* dO;
+  const float* row_max;
+  const float* row_denom;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  const int32_t* col_ptr;
+  const int32_t* row_idx;
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* delta;  // [BH * S] scratch: D_i = dO_i . O_i
+  int* status;
+};
+
+// RAII bracket that records a pair of CUDA events around one kernel launch
+// when profiling is enabled (bsr_profile_enable).
+class LaunchTimer {
+ public:
+  LaunchTimer(const char* name, cudaStream_t stream);
+  ~LaunchTimer();
+
+ private:
+  int slot_;
+  cudaStream_t stream_;
+};
+
+// Returns a status for the last launch on this thread (cudaGetLastError).
+bsr_status check_launch(const char* what);
+
+// Portable SIMT kernels (every head_dim and dtype).
+bsr_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
+bsr_status launch_delta(const BwdArgs& a, cudaStream_t s);
+bsr_status launch_dq_simt(const BwdArgs& a, cudaStream_t s);
+bsr_status launch_dkdv_simt(const BwdArgs& a, cudaStream_t s);
+
+}  // namespace bsr

@@ -1,0 +1,170 @@
+/*
+ * bsr_attn.h -- C ABI of the GB300 (sm_103a) block-sparse attention library.
+ *
+ * Block-sparse attention computes softmax(scale * Q K^T) V over the stored
+ * 128 x 128 blocks of a block mask given in BSR form (block-row pointers and
+ * block-column indices); every score outside a stored block is removed.  The
+ * forward pass also returns the fp32 row statistics, and the backward pass
+ * computes dQ by walking block rows and dK / dV by walking block columns of
+ * a BSC transpose built on the host, so that every output tile has exactly
+ * one writer and no atomics are used.
+ *
+ * Sources: "trnsparse 0.7.0 -> 0.9.0" diff (CHANGELOG [0.8.0], native path:
+ * static-structure kernels, attn_fwd_static / attn_bwd_static; CHANGELOG
+ * [0.9.0], one writer per output tile, bf16 operands with fp32 accumulation
+ * and fp32 statistics) and "trnsparse 0.4.1 -> 0.6.0" diff (CHANGELOG
+ * [0.5.0] delta identity; [0.5.1] dQ row-first and dK/dV column-first
+ * kernels, host-built BSC view, returned row_max / row_denom; [0.6.0]
+ * head_dim 256 and 512 by 128-wide chunks of the QK^T contraction).
+ *
+ * Conventions shared by every entry point:
+ *  - Dense tensors are [batch, heads, seq, head_dim], contiguous, row-major,
+ *    described by a bsr_tensor whose `data` is a DEVICE pointer.  All dense
+ *    tensors of one call have the same shape and dtype.  Supported:
+ *    head_dim in {64, 128, 256, 512}; dtype BSR_F32 or BSR_BF16;
+ *    seq = n_brows * 128; batch, heads >= 1.
+ *  - Statistics row_max / row_denom are fp32 DEVICE arrays [batch, heads, seq].
+ *    row_max is the maximum of the scaled scores scale * q.k of the row over
+ *    its stored blocks (natural-log units) and row_denom the sum of
+ *    exp(scale * q.k - row_max) over the same scores.  A block row with no
+ *    stored block gets O = 0, row_max = -inf, row_denom = 0.
+ *  - The mask is shared by every (batch, head).  row_ptr / col_idx /
+ *    col_ptr / row_idx passed to the kernels are int32 DEVICE arrays; columns
+ *    ascend without repeats inside a row (bsr_validate checks this on host).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *    asynchronous on it.  The caller owns every buffer; the library allocates
+ *    only stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *  - Every function returns a bsr_status; nothing throws across the ABI and
+ *    there is no fallback path.  bsr_last_error() gives a message for the
+ *    last failure on the calling thread.
+ */
+#ifndef BSR_ATTN_H
+#define BSR_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { BSR_F32 = 0, BSR_BF16 = 1 } bsr_dtype;
+
+typedef enum {
+  BSR_OK = 0,
+  BSR_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad structure */
+  BSR_ERR_UNSUPPORTED = 2,   /* head_dim / dtype / block outside the supported set */
+  BSR_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+  BSR_ERR_TIMEOUT = 4,       /* a bounded device-side wait gave up (reported by bsr_attn_check) */
+  BSR_ERR_DEVICE_CHECK = 5   /* a device-side bounds check failed (reported by bsr_attn_check) */
+} bsr_status;
+
+typedef struct {
+  void* data;        /* device pointer to [batch, heads, seq, head_dim] elements */
+  int32_t dtype;     /* bsr_dtype */
+  int32_t batch;
+  int32_t heads;
+  int32_t seq;
+  int32_t head_dim;
+} bsr_tensor;
+
+/*
+ * Forward pass ("trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.8.0]:
+ * attn_fwd_static, one launch with the softmax statistics kept on chip, no
+ * K/V gather and no per-block score round trip through HBM).
+ *
+ *   O[i]         = sum_j P[i,j] V[j],   P = softmax over stored j of scale * Q[i].K[j]
+ *   row_max[i]   = max over stored j of scale * Q[i].K[j]
+ *   row_denom[i] = sum over stored j of exp(scale * Q[i].K[j] - row_max[i])
+ *
+ * Q, K, V, O: dense tensors (device), O written in the operands' dtype.
+ * row_ptr: int32 [n_brows + 1] (device); col_idx: int32 [row_ptr[n_brows]] (device).
+ * block must be 128.  scale is usually 1/sqrt(head_dim).
+ * Errors: BSR_ERR_INVALID_ARG for null pointers or mismatched shapes,
+ * BSR_ERR_UNSUPPORTED for block != 128, head_dim or dtype outside the set,
+ * BSR_ERR_CUDA when a launch fails.  Nothing is written on error.
+ */
+bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                        const int32_t* row_ptr, const int32_t* col_idx, int32_t n_brows,
+                        int32_t block, float scale,
+                        bsr_tensor* O, float* row_max, float* row_denom, void* stream);
+
+/*
+ * Backward pass ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.5.0] delta
+ * identity D_i = dO_i . O_i; [0.5.1] _attn_bwd_dq_kernel row-first and
+ * _attn_bwd_dkdv_kernel column-first over the host-built BSC view, no
+ * atomic scatter; "trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.8.0]
+ * attn_bwd_static).
+ *
+ *   P = exp(scale * Q K^T - row_max) / row_denom on stored blocks,
+ *   dV = P^T dO;  dS = P * (dO V^T - D);  dQ = scale dS K;  dK = scale dS^T Q.
+ *
+ * Q, K, V, O, dO: dense inputs (device); O, row_max, row_denom from
+ * bsr_attn_fwd with the same scale.  row_ptr / col_idx: the BSR lists;
+ * col_ptr: int32 [n_bcols + 1] and row_idx: int32 [nnzb], the BSC transpose
+ * from bsr_build_bsc (rows ascending inside a column); all device arrays.
+ * `scale` must equal the forward's (the signature carries it explicitly).
+ * dQ, dK, dV: dense outputs (device), every element written (tiles of empty
+ * block columns / rows are written as zeros).
+ * Scratch: one fp32 [batch, heads, seq] delta array, stream-ordered.
+ * Errors as for bsr_attn_fwd.
+ */
+bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                        const bsr_tensor* O, const bsr_tensor* dO,
+                        const float* row_max, const float* row_denom,
+                        const int32_t* row_ptr, const int32_t* col_idx,
+                        const int32_t* col_ptr, const int32_t* row_idx,
+                        float scale,
+                        bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream);
+
+/*
+ * Host helper: BSC transpose of a BSR block structure ("trnsparse 0.4.1 ->
+ * 0.6.0" diff, CHANGELOG [0.5.1], _attn_bwd_gather, host-side BSC
+ * construction).  All pointers are HOST arrays owned by the caller:
+ * row_ptr_h [n_brows+1], col_idx_h [nnzb] in; col_ptr_h [n_bcols+1],
+ * row_idx_h [nnzb] out.  Block rows ascend inside each block column.
+ * Returns BSR_ERR_INVALID_ARG (and writes nothing) when the BSR lists fail
+ * bsr_validate.
+ */
+bsr_status bsr_build_bsc(const int32_t* row_ptr_h, const int32_t* col_idx_h,
+                         int32_t n_brows, int32_t n_bcols,
+                         int32_t* col_ptr_h, int32_t* row_idx_h);
+
+/*
+ * Host helper: checks BSR lists (HOST arrays): row_ptr[0] = 0, row_ptr
+ * non-decreasing, every col_idx in [0, n_bcols), strictly ascending inside a
+ * row (no duplicates).  Returns BSR_OK or BSR_ERR_INVALID_ARG with a message.
+ */
+bsr_status bsr_validate(const int32_t* row_ptr_h, const int32_t* col_idx_h,
+                        int32_t n_brows, int32_t n_bcols);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word that
+ * the kernels set when a bounded wait gives up (BSR_ERR_TIMEOUT) or a device
+ * bounds check fails (BSR_ERR_DEVICE_CHECK).  BSR_OK when neither happened.
+ */
+bsr_status bsr_attn_check(void* stream);
+
+/* Message for the last non-OK status returned on the calling thread. */
+const char* bsr_last_error(void);
+
+/*
+ * Kernel timing for benchmarks.  While enabled, every kernel the library
+ * launches is bracketed by CUDA events recorded on its launching stream.
+ * bsr_profile_collect synchronises those events and returns, per kernel name,
+ * the number of launches and their summed duration in ms since the last
+ * collect, then clears the record.  Returns the number of entries written.
+ */
+typedef struct {
+  char name[48];
+  int32_t launches;
+  float total_ms;
+} bsr_kernel_time;
+
+void bsr_profile_enable(int32_t on);
+int32_t bsr_profile_collect(bsr_kernel_time* out, int32_t max_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSR_ATTN_H */

@@ -1,0 +1,93 @@
+"""Helpers for the GPU-vs-oracle parity tests (the CUDA path is called through the C ABI)."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import block_sparse_attention_bsr_gb300 as bsr
+import oracle
+
+# Tolerances.  fp32 operands: max-abs 1e-4 on O / dQ / dK / dV and 1e-5
+# relative-to-max on the statistics.  bf16 operands: 2e-2 relative-to-max on
+# the outputs and gradients against the oracle run on the bf16-rounded inputs,
+# 1e-4 relative-to-max on the fp32 statistics.
+TOL = {
+    "f32": dict(out_abs=1e-4, out_rel=None, stat_rel=1e-5),
+    "bf16": dict(out_abs=None, out_rel=2e-2, stat_rel=1e-4),
+}
+
+
+def run_gpu(Q, K, V, dO, bm, scale, device="cuda", backward=True):
+    """Runs forward (+ backward) through the C ABI on `device`; returns CPU float64 numpy arrays."""
+    dev = torch.device(device)
+    rp, ci = _bsr(bm)
+    st = bsr.Structure(rp, ci, bm.shape[1], dev)
+    q, k, v, do = (t.to(dev).contiguous() for t in (Q, K, V, dO))
+    O = torch.empty_like(q)
+    rm = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
+    rd = torch.empty_like(rm)
+    bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, 128, scale, O, rm, rd)
+    out = dict(O=O, row_max=rm, row_denom=rd)
+    if backward:
+        dQ, dK, dV = (torch.empty_like(q) for _ in range(3))
+        bsr.bsr_attn_bwd(q, k, v, O, do, rm, rd, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, scale,
+                         dQ, dK, dV)
+        out.update(dQ=dQ, dK=dK, dV=dV)
+    bsr.bsr_attn_check()
+    return {n: t.double().cpu().numpy() for n, t in out.items()}
+
+
+def _bsr(bm):
+    from block_sparse_attention_bsr_gb300 import inputs
+
+    return inputs.bsr_from_block_mask(bm)
+
+
+def oracle_heads(Q, K, V, dO, bm, scale, heads, backward=True):
+    """Oracle results for selected (batch, head) pairs: {name: [len(heads), S, ...]}."""
+    res = {n: [] for n in ("O", "row_max", "row_denom", "dQ", "dK", "dV")}
+    for b, h in heads:
+        args = [t[b, h].double().numpy() for t in (Q, K, V, dO)]
+        if backward:
+            o, rm, rd, dq, dk, dv = oracle.attn_fwd_bwd_head(*args, bm, scale)
+            res["dQ"].append(dq)
+            res["dK"].append(dk)
+            res["dV"].append(dv)
+        else:
+            o4, rm4, rd4 = oracle.attn_fwd(*(a[None, None] for a in args[:3]), bm, scale)
+            o, rm, rd = o4[0, 0], rm4[0, 0], rd4[0, 0]
+        res["O"].append(o)
+        res["row_max"].append(rm)
+        res["row_denom"].append(rd)
+    return {n: np.stack(v) for n, v in res.items() if v}
+
+
+def compare(got: dict, ref: dict, dtype: str, heads=None, what="") -> dict:
+    """Asserts parity within TOL[dtype]; returns the measured errors."""
+    tol = TOL[dtype]
+    errs = {}
+    for name, r in ref.items():
+        g = got[name]
+        if heads is not None:
+            g = np.stack([g[b, h] for b, h in heads])
+        else:
+            g = g.reshape(r.shape)
+        if name in ("row_max", "row_denom"):
+            fin = np.isfinite(r)
+            assert np.array_equal(fin, np.isfinite(g)), f"{what} {name}: -inf pattern differs"
+            denom = max(np.abs(r[fin]).max(), 1e-30) if fin.any() else 1.0
+            err = float(np.abs(g[fin] - r[fin]).max() / denom) if fin.any() else 0.0
+            errs[name] = err
+            assert err <= tol["stat_rel"], f"{what} {name}: rel-to-max error {err:.3e} > {tol['stat_rel']}"
+            continue
+        diff = np.abs(g - r)
+        if tol["out_abs"] is not None:
+            err = float(diff.max())
+            errs[name] = err
+            assert err <= tol["out_abs"], f"{what} {name}: max-abs error {err:.3e} > {tol['out_abs']}"
+        else:
+            err = float(diff.max() / max(np.abs(r).max(), 1e-30))
+            errs[name] = err
+            assert err <= tol["out_rel"], f"{what} {name}: rel-to-max error {err:.3e} > {tol['out_rel']}"
+    return errs
