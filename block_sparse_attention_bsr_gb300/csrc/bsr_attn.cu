@@ -161,13 +161,13 @@ extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, con
   return launch_fwd_simt(a, s);
 }
 
-extern "C" bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
-                                   const bsr_tensor* O, const bsr_tensor* dO,
-                                   const float* row_max, const float* row_denom,
-                                   const int32_t* row_ptr, const int32_t* col_idx,
-                                   const int32_t* col_ptr, const int32_t* row_idx,
-                                   float scale,
-                                   bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream) {
+namespace bsr {
+
+bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V, const bsr_tensor* O,
+                          const bsr_tensor* dO, const float* row_max, const float* row_denom,
+                          const int32_t* row_ptr, const int32_t* col_idx, const int32_t* col_ptr,
+                          const int32_t* row_idx, float scale, bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV,
+                          BwdArgs* out) {
   bsr_status st;
   if ((st = check_tensor(Q, "Q", nullptr)) || (st = check_tensor(K, "K", Q)) || (st = check_tensor(V, "V", Q)) ||
       (st = check_tensor(O, "O", Q)) || (st = check_tensor(dO, "dO", Q)) || (st = check_tensor(dQ, "dQ", Q)) ||
@@ -193,13 +193,35 @@ extern "C" bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, con
   a.dV = dV->data;
   a.status = status_ptr();
   if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_bwd: no CUDA device");
+  *out = a;
+  return BSR_OK;
+}
+
+bsr_status run_bwd(const BwdArgs& a, cudaStream_t s) {
+  bsr_status st = launch_delta(a, s);
+  if (st == BSR_OK) st = launch_dq_simt(a, s);
+  if (st == BSR_OK) st = launch_dkdv_simt(a, s);
+  return st;
+}
+
+}  // namespace bsr
+
+extern "C" bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                                   const bsr_tensor* O, const bsr_tensor* dO,
+                                   const float* row_max, const float* row_denom,
+                                   const int32_t* row_ptr, const int32_t* col_idx,
+                                   const int32_t* col_ptr, const int32_t* row_idx,
+                                   float scale,
+                                   bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream) {
+  BwdArgs a{};
+  bsr_status st = build_bwd_args(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx, scale,
+                                 dQ, dK, dV, &a);
+  if (st != BSR_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   const size_t delta_bytes = sizeof(float) * (size_t)a.d.BH * a.d.S;
   cudaError_t e = cudaMallocAsync((void**)&a.delta, delta_bytes, s);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaMallocAsync(%zu): %s", delta_bytes, cudaGetErrorString(e));
-  st = launch_delta(a, s);
-  if (st == BSR_OK) st = launch_dq_simt(a, s);
-  if (st == BSR_OK) st = launch_dkdv_simt(a, s);
+  st = run_bwd(a, s);
   e = cudaFreeAsync(a.delta, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaFreeAsync: %s", cudaGetErrorString(e));
   return st;

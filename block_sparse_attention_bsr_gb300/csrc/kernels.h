@@ -66,6 +66,17 @@ class LaunchTimer {
   cudaStream_t stream_;
 };
 
+// Validates the backward arguments and fills *out (delta left null).
+bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V, const bsr_tensor* O,
+                          const bsr_tensor* dO, const float* row_max, const float* row_denom,
+                          const int32_t* row_ptr, const int32_t* col_idx, const int32_t* col_ptr,
+                          const int32_t* row_idx, float scale, bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV,
+                          BwdArgs* out);
+
+// Launches the backward kernels (delta, dQ, dK/dV) on `s`; a.delta must
+// point at BH * S floats of device scratch.
+bsr_status run_bwd(const BwdArgs& a, cudaStream_t s);
+
 // Returns a status for the last launch on this thread (cudaGetLastError).
 bsr_status check_launch(const char* what);
 
@@ -74,5 +85,10 @@ bsr_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
 bsr_status launch_delta(const BwdArgs& a, cudaStream_t s);
 bsr_status launch_dq_simt(const BwdArgs& a, cudaStream_t s);
 bsr_status launch_dkdv_simt(const BwdArgs& a, cudaStream_t s);
+
+// Tensor-core (tcgen05 / TMA) kernels.  `order` (device, optional) maps the
+// CTA's x index to a block row.
+bool tc_fwd_supported(const Dims& d);
+bsr_status launch_fwd_tc(const FwdArgs& a, const int32_t* order, cudaStream_t s);
 
 }  // namespace bsr
