@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "BSR_OK", 1: "BSR_ERR_INVALID_ARG", 2: "BSR_ERR_UNSUPPORTED",
                 4: "BSR_ERR_TIMEOUT", 5: "BSR_ERR_DEVICE_CHECK"}
 
 # Every symbol include/bsr_attn.h declares.
-EXPORTS = ("bsr_attn_fwd", "bsr_attn_bwd", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
+EXPORTS = ("bsr_attn_fwd", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
            "bsr_last_error", "bsr_profile_enable", "bsr_profile_collect")
 
 
@@ -58,6 +58,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     T = ctypes.POINTER(bsr_tensor)
     lib.bsr_attn_fwd.argtypes = [T, T, T, P, P, I32, I32, F32, T, P, P, P]
     lib.bsr_attn_bwd.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
+    lib.bsr_attn_bwd_noalloc.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_build_bsc.argtypes = [P, P, I32, I32, P, P]
     lib.bsr_validate.argtypes = [P, P, I32, I32]
     lib.bsr_attn_check.argtypes = [P]
@@ -67,7 +68,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsr_profile_enable.restype = None
     lib.bsr_profile_collect.argtypes = [ctypes.POINTER(bsr_kernel_time), I32]
     lib.bsr_profile_collect.restype = I32
-    for name in ("bsr_attn_fwd", "bsr_attn_bwd", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
+    for name in ("bsr_attn_fwd", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
         getattr(lib, name).restype = I32
     _lib_handle = lib
     return lib
@@ -133,6 +134,25 @@ def bsr_attn_bwd(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, 
                             _dev_ptr(row_ptr, i32), _dev_ptr(col_idx, i32), _dev_ptr(col_ptr, i32),
                             _dev_ptr(row_idx, i32), float(scale),
                             ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), _stream(stream, Q)))
+
+
+def bsr_attn_bwd_noalloc(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx, scale: float,
+                         dQ, dK, dV, stream=None) -> None:
+    """Backward pass that allocates no device memory (static scratch; see include/bsr_attn.h).
+
+    For callers that cannot allocate: another allocator owns the device
+    memory, or the hot path must not call the CUDA allocator.  Limited to
+    batch * heads * seq <= 1,048,576; calls that overlap on the GPU race.
+    """
+    lib = load_library()
+    q, k, v, o, do, dq, dk, dv = (_desc(t) for t in (Q, K, V, O, dO, dQ, dK, dV))
+    i32 = "torch.int32"
+    _check(lib.bsr_attn_bwd_noalloc(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(o),
+                                    ctypes.byref(do), _dev_ptr(row_max, "torch.float32"),
+                                    _dev_ptr(row_denom, "torch.float32"), _dev_ptr(row_ptr, i32),
+                                    _dev_ptr(col_idx, i32), _dev_ptr(col_ptr, i32), _dev_ptr(row_idx, i32),
+                                    float(scale), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                    _stream(stream, Q)))
 
 
 def _host_i32(a) -> np.ndarray:

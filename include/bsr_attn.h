@@ -117,6 +117,29 @@ bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tens
                         bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream);
 
 /*
+ * Backward pass that allocates nothing.  The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory, either
+ * because another allocator already owns the device's memory (a framework's
+ * caching allocator, a serving runtime's pools) or because their hot path
+ * must not call into the CUDA allocator.  Same arguments, results and errors
+ * as bsr_attn_bwd, but the delta scratch comes from a fixed array in the
+ * library's static device memory (4 MiB per GPU that loads the library,
+ * held until the process exits) instead of cudaMallocAsync.
+ * Limits: batch * heads * seq <= 1,048,576, else BSR_ERR_INVALID_ARG.
+ * All calls share the array: calls whose kernels overlap on the GPU race, so
+ * order them on one stream.  The first call on a device (with that device
+ * current) looks up the array's device address; make it before any stream
+ * capture.
+ */
+bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                                const bsr_tensor* O, const bsr_tensor* dO,
+                                const float* row_max, const float* row_denom,
+                                const int32_t* row_ptr, const int32_t* col_idx,
+                                const int32_t* col_ptr, const int32_t* row_idx,
+                                float scale,
+                                bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream);
+
+/*
  * Host helper: BSC transpose of a BSR block structure ("trnsparse 0.4.1 ->
  * 0.6.0" diff, CHANGELOG [0.5.1], _attn_bwd_gather, host-side BSC
  * construction).  All pointers are HOST arrays owned by the caller:
