@@ -158,6 +158,7 @@ extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, con
   a.status = status_ptr();
   if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
   cudaStream_t s = (cudaStream_t)stream;
+  if (tc_fwd_supported(a.d)) return launch_fwd_tc(a, nullptr, s);
   return launch_fwd_simt(a, s);
 }
 
