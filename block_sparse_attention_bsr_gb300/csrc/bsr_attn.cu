@@ -200,7 +200,9 @@ bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
 
 bsr_status run_bwd(const BwdArgs& a, cudaStream_t s) {
   bsr_status st = launch_delta(a, s);
-  if (st == BSR_OK) st = launch_dq_simt(a, s);
+  if (st != BSR_OK) return st;
+  if (tc_bwd_supported(a.d)) return launch_bwd_tc(a, s);
+  st = launch_dq_simt(a, s);
   if (st == BSR_OK) st = launch_dkdv_simt(a, s);
   return st;
 }

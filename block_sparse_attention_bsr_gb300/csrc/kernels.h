@@ -90,5 +90,7 @@ bsr_status launch_dkdv_simt(const BwdArgs& a, cudaStream_t s);
 // CTA's x index to a block row.
 bool tc_fwd_supported(const Dims& d);
 bsr_status launch_fwd_tc(const FwdArgs& a, const int32_t* order, cudaStream_t s);
+bool tc_bwd_supported(const Dims& d);
+bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
 
 }  // namespace bsr
