@@ -158,8 +158,17 @@ extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, con
   a.status = status_ptr();
   if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
   cudaStream_t s = (cudaStream_t)stream;
-  if (tc_fwd_supported(a.d)) return launch_fwd_tc(a, nullptr, s);
-  return launch_fwd_simt(a, s);
+  if (!tc_fwd_supported(a.d)) return launch_fwd_simt(a, s);
+  int32_t* order = nullptr;
+  cudaError_t e = cudaMallocAsync((void**)&order, sizeof(int32_t) * a.d.nb, s);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaMallocAsync: %s", cudaGetErrorString(e));
+  a.order = order;
+  PlanArgs p{row_ptr, row_ptr, order, order, a.d.nb};
+  st = launch_plan(p, 1, s);
+  if (st == BSR_OK) st = launch_fwd_tc(a, order, s);
+  e = cudaFreeAsync(order, s);
+  if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaFreeAsync: %s", cudaGetErrorString(e));
+  return st;
 }
 
 namespace bsr {
@@ -201,7 +210,11 @@ bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
 bsr_status run_bwd(const BwdArgs& a, cudaStream_t s) {
   bsr_status st = launch_delta(a, s);
   if (st != BSR_OK) return st;
-  if (tc_bwd_supported(a.d)) return launch_bwd_tc(a, s);
+  if (tc_bwd_supported(a.d)) {
+    PlanArgs p{a.row_ptr, a.col_ptr, a.row_order, a.col_order, a.d.nb};
+    if ((st = launch_plan(p, 2, s)) != BSR_OK) return st;
+    return launch_bwd_tc(a, s);
+  }
   st = launch_dq_simt(a, s);
   if (st == BSR_OK) st = launch_dkdv_simt(a, s);
   return st;
@@ -221,9 +234,14 @@ extern "C" bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, con
                                  dQ, dK, dV, &a);
   if (st != BSR_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t delta_bytes = sizeof(float) * (size_t)a.d.BH * a.d.S;
-  cudaError_t e = cudaMallocAsync((void**)&a.delta, delta_bytes, s);
-  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaMallocAsync(%zu): %s", delta_bytes, cudaGetErrorString(e));
+  const size_t rows = (size_t)a.d.BH * a.d.S;
+  const size_t scratch_bytes = 2 * sizeof(float) * rows + 2 * sizeof(int32_t) * a.d.nb;
+  cudaError_t e = cudaMallocAsync((void**)&a.delta, scratch_bytes, s);
+  if (e != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaMallocAsync(%zu): %s", scratch_bytes, cudaGetErrorString(e));
+  a.lse2 = a.delta + rows;
+  a.row_order = (int32_t*)(a.lse2 + rows);
+  a.col_order = a.row_order + a.d.nb;
   st = run_bwd(a, s);
   e = cudaFreeAsync(a.delta, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaFreeAsync: %s", cudaGetErrorString(e));

@@ -1,23 +1,24 @@
 // Backward pass that allocates nothing, for callers that cannot allocate
 // device memory.
 //
-// bsr_attn_bwd takes its one piece of scratch (the fp32 delta array,
-// D_i = dO_i . O_i, one value per query row) from cudaMallocAsync on the
-// caller's stream.  Some callers cannot allow that: their device memory is
+// bsr_attn_bwd takes its scratch (two fp32 values per query row: the delta
+// D_i = dO_i . O_i and the row's base-2 log-sum-exp) from cudaMallocAsync
+// on the caller's stream.  Some callers cannot allow that: their device memory is
 // already fully reserved by another allocator (a framework's caching
 // allocator that holds the whole device, or a serving runtime that carves
 // all memory into its own pools), or their hot path is not allowed to call
 // into the CUDA allocator at all.  bsr_attn_bwd_noalloc runs the same
-// kernels but takes the delta scratch from a fixed-size array in the
-// library's static device memory instead.
+// kernels but takes that scratch from a fixed-size array in the library's
+// static device memory instead.
 //
 // Limits and rules:
-//  * The array holds kNoAllocMaxRows floats (4 MiB), so batch * heads * seq
-//    must not exceed 1,048,576 (e.g. 128 heads at seq 8192); larger calls are
-//    rejected with BSR_ERR_INVALID_ARG.  Every GPU that loads the library
-//    keeps the 4 MiB reserved until the process exits.
+//  * The array holds 2 * kNoAllocMaxRows floats plus two work-order lists of
+//    up to kNoAllocMaxRows / 128 ints (8 MiB + 64 KiB), so batch * heads *
+//    seq must not exceed 1,048,576 (e.g. 128 heads at seq 8192); larger calls
+//    are rejected with BSR_ERR_INVALID_ARG.  Every GPU that loads the library
+//    keeps the array reserved until the process exits.
 //  * All calls share the one array.  The delta kernel overwrites every entry
-//    it later reads, so nothing has to start at zero, but two calls whose
+//    that is later read, so nothing has to start at zero, but two calls whose
 //    kernels overlap on the GPU (different streams, or different host
 //    threads on the same device) race on the array: order them.
 //  * The device address of the array is looked up once per device, on the
@@ -35,7 +36,9 @@ namespace {
 
 constexpr size_t kNoAllocMaxRows = size_t(1) << 20;
 
-static __device__ __align__(256) float g_noalloc_delta[kNoAllocMaxRows];
+constexpr size_t kNoAllocMaxLines = kNoAllocMaxRows / 128;
+
+static __device__ __align__(256) float g_noalloc_delta[2 * kNoAllocMaxRows + 2 * kNoAllocMaxLines];
 
 constexpr int kMaxDevices = 64;
 
@@ -83,5 +86,8 @@ extern "C" bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor
                 "use bsr_attn_bwd",
                 rows, kNoAllocMaxRows);
   if ((st = noalloc_scratch(&a.delta)) != BSR_OK) return st;
+  a.lse2 = a.delta + rows;
+  a.row_order = (int32_t*)(a.lse2 + rows);  // rows <= kNoAllocMaxRows, so nb <= kNoAllocMaxLines
+  a.col_order = a.row_order + a.d.nb;
   return run_bwd(a, (cudaStream_t)stream);
 }

@@ -31,6 +31,7 @@ struct FwdArgs {
   float* row_denom;
   const int32_t* row_ptr;
   const int32_t* col_idx;
+  const int32_t* order;  // [nb] block rows longest first (plan_kernel), or null
   int* status;
 };
 
@@ -51,8 +52,24 @@ struct BwdArgs {
   void* dK;
   void* dV;
   float* delta;  // [BH * S] scratch: D_i = dO_i . O_i
+  float* lse2;   // [BH * S] scratch: row_max * log2(e) + log2(row_denom)
+  int32_t* row_order;  // [nb] scratch: block rows longest first
+  int32_t* col_order;  // [nb] scratch: block columns longest first
   int* status;
 };
+
+// Planner inputs: one or two prefix-offset lists of n lines each.
+struct PlanArgs {
+  const int32_t* ptr0;
+  const int32_t* ptr1;
+  int32_t* order0;
+  int32_t* order1;
+  int n;
+};
+
+// Sorts the lines of `lists` (1 or 2) prefix-offset lists by length, longest
+// first, into the order arrays.
+bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s);
 
 // RAII bracket that records a pair of CUDA events around one kernel launch
 // when profiling is enabled (bsr_profile_enable).
@@ -73,8 +90,9 @@ bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
                           const int32_t* row_idx, float scale, bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV,
                           BwdArgs* out);
 
-// Launches the backward kernels (delta, dQ, dK/dV) on `s`; a.delta must
-// point at BH * S floats of device scratch.
+// Launches the backward kernels (plan, delta, dQ, dK/dV) on `s`; a.delta and
+// a.lse2 must each point at BH * S floats of 16-byte aligned device scratch,
+// a.row_order and a.col_order at nb ints each.
 bsr_status run_bwd(const BwdArgs& a, cudaStream_t s);
 
 // Returns a status for the last launch on this thread (cudaGetLastError).
@@ -90,6 +108,7 @@ bsr_status launch_dkdv_simt(const BwdArgs& a, cudaStream_t s);
 // CTA's x index to a block row.
 bool tc_fwd_supported(const Dims& d);
 bsr_status launch_fwd_tc(const FwdArgs& a, const int32_t* order, cudaStream_t s);
+bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s);  // head_dim 64 / 128, P in TMEM
 bool tc_bwd_supported(const Dims& d);
 bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
 

@@ -91,8 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = (Bars*)(sm + C::kBarOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.y;
-  const int m = order ? order[blockIdx.x] : (int)blockIdx.x;
+  const int bh = blockIdx.x % a.d.BH;
+  const int m = order[blockIdx.x / a.d.BH];
   const int S = a.d.S;
   const int j0 = a.row_ptr[m];
   const int nblk = a.row_ptr[m + 1] - j0;
@@ -330,7 +330,7 @@ bsr_status launch_fwd(const FwdArgs& a, const TensorMaps& tm, const int32_t* ord
   auto kern = fwd_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "fwd_tc: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
-  dim3 grid(a.d.nb, a.d.BH);
+  dim3 grid(a.d.nb * a.d.BH);
   LaunchTimer timer("fwd_tc", s);
   kern<<<grid, kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a, order);
   return check_launch("fwd_tc launch");
@@ -341,6 +341,7 @@ bsr_status launch_fwd(const FwdArgs& a, const TensorMaps& tm, const int32_t* ord
 bool tc_fwd_supported(const Dims& d) { return d.dtype == BSR_BF16 && (d.D == 64 || d.D == 128 || d.D == 256); }
 
 bsr_status launch_fwd_tc(const FwdArgs& a, const int32_t* order, cudaStream_t s) {
+  if (a.d.D <= 128) return launch_fwd_tc2(a, s);
   TensorMaps tm;
   bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
   if (st != BSR_OK) return st;

@@ -1,0 +1,366 @@
+// Tensor-core forward pass for bf16 operands with head_dim 64 / 128 on
+// sm_103a, with P kept in tensor memory.
+//
+// Same walk as the head_dim-256 kernel in tc_fwd.cu (one CTA per block row m
+// of one (batch, head); the row's stored blocks j in [row_ptr[m],
+// row_ptr[m+1]) are visited in order and the K / V tiles of block column
+// col_idx[j] come straight from HBM by TMA; "trnsparse 0.7.0 -> 0.9.0" diff,
+// CHANGELOG [0.8.0], attn_fwd_static), with three changes that keep the
+// tensor pipe fed:
+//   * P goes back to tensor memory as bf16 and the P.V MMA reads its A
+//     operand from there (no shared-memory round trip for P);
+//   * two softmax warpgroups split the 128 columns of each score tile; the
+//     row maximum is combined through shared memory;
+//   * S is double-buffered in TMEM, so S_{j+1} = Q K_{j+1}^T runs while the
+//     softmax of block j is computed.
+//
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2..9 two softmax warpgroups; thread (warp w, lane l) owns
+// query row 32 (w % 4) + l (its TMEM lane), warpgroup g = (w - 2) / 4 owns
+// columns [64 g, 64 g + 64) of the scores and half of O's columns.
+// TMEM columns: S buffers at 0 and 128, O at 256 (D columns), P at 384
+// (64 columns of bf16 pairs).  All waits are bounded (see sm100.cuh).
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tc_common.h"
+
+namespace bsr {
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 320;
+constexpr int kSoftmax = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256, kColP = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: stale max may lag by 2^8
+
+template <int D>
+struct Fwd2Cfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kKStages = D == 64 ? 4 : 3;
+  static constexpr int kVStages = D == 64 ? 4 : 2;
+  static constexpr int kRedOff = kTile * (1 + kKStages + kVStages);
+  static constexpr int kBarOff = kRedOff + 2 * 2 * 128 * 4;  // [parity][half][row] maxima
+  static constexpr int kSmem = kBarOff + 256 + 1024;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t pv_done;
+  uint64_t final_mma;
+  uint64_t red_full[2];  // both warpgroups' partial row values written (by parity)
+  uint64_t k_full[4];
+  uint64_t k_empty[4];
+  uint64_t v_full[4];
+  uint64_t v_empty[4];
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* b, int* status) {
+  bool ok = mbar_wait(bar, parity, &b->abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < 200000000ull) {
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
+  using C = Fwd2Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = sm;
+  uint8_t* sK = sQ + C::kTile;
+  uint8_t* sV = sK + C::kKStages * C::kTile;
+  float* sRed = (float*)(sm + C::kRedOff);
+  Bars* bars = (Bars*)(sm + C::kBarOff);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.x % a.d.BH;
+  const int m = a.order[blockIdx.x / a.d.BH];
+  const int S = a.d.S;
+  const int j0 = a.row_ptr[m];
+  const int nblk = a.row_ptr[m + 1] - j0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], kSoftmax);
+    }
+    mbar_init(&bars->p_full, kSoftmax);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->final_mma, 1);
+    mbar_init(&bars->red_full[0], kSoftmax);
+    mbar_init(&bars->red_full[1], kSoftmax);
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  volatile int* ab = &bars->abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0 && nblk > 0) {
+      // ------------------------------------------------------ producer --
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int qrow = bh * S + m * 128;
+      mbar_arrive_expect_tx(&bars->q_full, C::kTile);
+      for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(sQ + b * 16384, &tmQ, b * 64, qrow, &bars->q_full);
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < nblk; ++i) {
+        int n = a.col_idx[j0 + i];
+        if (n < 0 || n >= a.d.nb) {
+          atomicExch(a.status, kStatusDeviceCheck);
+          n = 0;
+        }
+        const int krow = bh * S + n * 128;
+        const int ks = i % C::kKStages, vs = i % C::kVStages;
+        if (!(ok = mbar_wait(&bars->k_empty[ks], ((i / C::kKStages) & 1) ^ 1, ab, a.status))) break;
+        mbar_arrive_expect_tx(&bars->k_full[ks], C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_2d(sK + ks * C::kTile + b * 16384, &tmK, b * 64, krow, &bars->k_full[ks]);
+        k_issued = i + 1;
+        if (!(ok = mbar_wait(&bars->v_empty[vs], ((i / C::kVStages) & 1) ^ 1, ab, a.status))) break;
+        mbar_arrive_expect_tx(&bars->v_full[vs], C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_2d(sV + vs * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[vs]);
+        v_issued = i + 1;
+      }
+      // drain: every copy issued must have landed before the CTA exits
+      drain_wait(&bars->q_full, 0);
+      for (int i = (k_issued > C::kKStages ? k_issued - C::kKStages : 0); i < k_issued; ++i)
+        drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1);
+      for (int i = (v_issued > C::kVStages ? v_issued - C::kVStages : 0); i < v_issued; ++i)
+        drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nblk > 0) {
+      // ----------------------------------------------------------- MMA --
+      const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
+      const uint32_t idPV = instr_desc(1, 0, 1, D, 128);
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      bool ok = mbar_wait(&bars->q_full, 0, ab, a.status);
+      auto issue_s = [&](int i) -> bool {
+        const int ks = i % C::kKStages;
+        const int b = i & 1;
+        if (!mbar_wait(&bars->k_full[ks], (i / C::kKStages) & 1, ab, a.status)) return false;
+        if (!mbar_wait(&bars->s_free[b], ((i >> 1) & 1) ^ 1, ab, a.status)) return false;
+        tc_fence_after();
+        const uint32_t kb = aK + ks * C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + b * 128, smem_desc(aQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
+        }
+        mma_commit(&bars->k_empty[ks]);
+        mma_commit(&bars->s_full[b]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int i = 0; ok && i < nblk; ++i) {
+        if (i + 1 < nblk && !(ok = issue_s(i + 1))) break;
+        const int vs = i % C::kVStages;
+        if (!(ok = mbar_wait(&bars->p_full, i & 1, ab, a.status))) break;
+        if (!(ok = mbar_wait(&bars->v_full[vs], (i / C::kVStages) & 1, ab, a.status))) break;
+        tc_fence_after();
+        const uint32_t vb = aV + vs * C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8, smem_desc(vb + kk * 2048, 16384, 1024), idPV,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->v_empty[vs]);
+        mma_commit(&bars->pv_done);
+      }
+      mma_commit(&bars->final_mma);
+      drain_wait(&bars->final_mma, 0);
+    }
+  } else {
+    // -------------------------------------------------------- softmax --
+    const int g = (warp - 2) / 4;  // column half
+    const int wl = warp % 4;
+    const int r = wl * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
+    const float sl2 = a.d.scale * kLog2e;
+    float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+      const int b = i & 1;
+      if (!(ok = warp_wait(&bars->s_full[b], (i >> 1) & 1, bars, a.status))) break;
+      tc_fence_after();
+      float t[64];
+      {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tmem + lane_base + b * 128 + g * 64, v0);
+        tmem_ld32(tmem + lane_base + b * 128 + g * 64 + 32, v1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          t[k] = __uint_as_float(v0[k]) * sl2;
+          t[32 + k] = __uint_as_float(v1[k]) * sl2;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[b]);
+      float mx = t[0];
+#pragma unroll
+      for (int k = 1; k < 64; ++k) mx = fmaxf(mx, t[k]);
+      // combine the two column halves of the row through shared memory (two
+      // buffers by block parity: no thread runs more than one block ahead,
+      // since each exchange waits for all 256 softmax threads)
+      float* red = sRed + (i & 1) * 256;
+      red[g * 128 + r] = mx;
+      mbar_arrive(&bars->red_full[i & 1]);
+      if (!(ok = warp_wait(&bars->red_full[i & 1], (i >> 1) & 1, bars, a.status))) break;
+      mx = fmaxf(mx, red[(g ^ 1) * 128 + r]);
+      m_true = fmaxf(m_true, mx);
+      if (i > 0) {
+        // PV of the previous block must be done before O is rescaled or P overwritten
+        if (!(ok = warp_wait(&bars->pv_done, (i - 1) & 1, bars, a.status))) break;
+        tc_fence_after();
+        const bool need = mx - m_ref > kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = fmaxf(m_ref, mx);
+          const float alpha = ex2(m_ref - m_new);
+          l *= alpha;
+          m_ref = m_new;
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t v[32];
+            const uint32_t ta = tmem + lane_base + kColO + g * (D / 2) + c * 32;
+            tmem_ld32(ta, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tmem_st32(ta, v);
+          }
+        }
+      } else {
+        m_ref = mx;
+      }
+      float sum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float p0 = ex2(t[2 * k] - m_ref), p1 = ex2(t[2 * k + 1] - m_ref);
+        sum += p0 + p1;
+        pk[k] = pack_bf16x2(p0, p1);
+      }
+      l += sum;
+      tmem_st32(tmem + lane_base + kColP + g * 32, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+    }
+    // ------------------------------------------------------- epilogue --
+    const size_t grow = (size_t)bh * S + (size_t)m * 128 + r;
+    __nv_bfloat16* orow = (__nv_bfloat16*)a.O + grow * D + g * (D / 2);
+    if (nblk == 0) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < D / 16; ++c) ((uint4*)orow)[c] = z;
+      if (g == 0) {
+        a.row_max[grow] = -INFINITY;
+        a.row_denom[grow] = 0.f;
+      }
+    } else if (ok) {
+      // total row sum: the two halves' partial sums share the reference max
+      float* red = sRed + (nblk & 1) * 256;
+      red[g * 128 + r] = l;
+      mbar_arrive(&bars->red_full[nblk & 1]);
+      ok = warp_wait(&bars->red_full[nblk & 1], (nblk >> 1) & 1, bars, a.status);
+      if (ok) l += red[(g ^ 1) * 128 + r];
+      if (ok) ok = warp_wait(&bars->pv_done, (nblk - 1) & 1, bars, a.status);
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kColO + g * (D / 2) + c * 32, v);
+          tmem_wait_ld();
+          uint4* dst = (uint4*)(orow + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
+            o.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
+            o.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
+            o.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
+            dst[q] = o;
+          }
+        }
+        if (g == 0) {
+          a.row_max[grow] = m_true * kLn2;
+          a.row_denom[grow] = l * ex2(m_ref - m_true);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D>
+bsr_status launch(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
+  using C = Fwd2Cfg<D>;
+  auto kern = fwd_tc2_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "fwd_tc: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
+  LaunchTimer timer("fwd_tc", s);
+  kern<<<dim3(a.d.nb * a.d.BH), kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
+  return check_launch("fwd_tc launch");
+}
+
+}  // namespace
+
+bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s) {
+  TensorMaps tm;
+  bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
+  if (st != BSR_OK) return st;
+  switch (a.d.D) {
+    case 64: return launch<64>(a, tm, s);
+    case 128: return launch<128>(a, tm, s);
+    default: return fail(BSR_ERR_UNSUPPORTED, "fwd_tc2: head_dim %d", a.d.D);
+  }
+}
+
+}  // namespace bsr

@@ -105,7 +105,8 @@ bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tens
  * `scale` must equal the forward's (the signature carries it explicitly).
  * dQ, dK, dV: dense outputs (device), every element written (tiles of empty
  * block columns / rows are written as zeros).
- * Scratch: one fp32 [batch, heads, seq] delta array, stream-ordered.
+ * Scratch: two fp32 [batch, heads, seq] arrays (delta, base-2 log-sum-exp),
+ * stream-ordered.
  * Errors as for bsr_attn_fwd.
  */
 bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
@@ -122,9 +123,10 @@ bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tens
  * because another allocator already owns the device's memory (a framework's
  * caching allocator, a serving runtime's pools) or because their hot path
  * must not call into the CUDA allocator.  Same arguments, results and errors
- * as bsr_attn_bwd, but the delta scratch comes from a fixed array in the
- * library's static device memory (4 MiB per GPU that loads the library,
- * held until the process exits) instead of cudaMallocAsync.
+ * as bsr_attn_bwd, but its scratch (delta and log-sum-exp per row) comes
+ * from a fixed array in the library's static device memory (8 MiB per GPU
+ * that loads the library, held until the process exits) instead of
+ * cudaMallocAsync.
  * Limits: batch * heads * seq <= 1,048,576, else BSR_ERR_INVALID_ARG.
  * All calls share the array: calls whose kernels overlap on the GPU race, so
  * order them on one stream.  The first call on a device (with that device
