@@ -84,6 +84,18 @@ LaunchTimer::~LaunchTimer() {
   if (slot_ < (int)g_prof.size()) cudaEventRecord(g_prof[slot_].stop, stream_);
 }
 
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::mutex mu;
+  static std::vector<int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+  if (!cache[dev] && cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    cache[dev] = 0;
+  return cache[dev];
+}
+
 bsr_status check_launch(const char* what) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -159,14 +171,26 @@ extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, con
   if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
   cudaStream_t s = (cudaStream_t)stream;
   if (!tc_fwd_supported(a.d)) return launch_fwd_simt(a, s);
-  int32_t* order = nullptr;
-  cudaError_t e = cudaMallocAsync((void**)&order, sizeof(int32_t) * a.d.nb, s);
+  const int G = tc_grid(a.d);
+  if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cannot query the SM count");
+  const bool persistent = a.d.D <= 128;  // the head_dim-256 kernel keeps one CTA per row
+  const size_t plan_bytes = sizeof(int32_t) * plan_words(a.d.nb, G, a.d.BH);
+  const size_t part_bytes = persistent ? fwd_part_bytes(a.d.D) * plan_tiles(a.d.nb, G, a.d.BH) : 0;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, plan_bytes + part_bytes, s);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaMallocAsync: %s", cudaGetErrorString(e));
-  a.order = order;
-  PlanArgs p{row_ptr, row_ptr, order, order, a.d.nb};
+  a.plan = (int32_t*)scratch;
+  a.part = persistent ? (float*)((char*)scratch + plan_bytes) : nullptr;
+  PlanArgs p{};
+  p.list[0] = PlanList{row_ptr, a.plan};
+  p.n = a.d.nb;
+  p.G = G;
+  p.BH = a.d.BH;
+  p.allow_split = persistent ? 1 : 0;
+  p.status = a.status;
   st = launch_plan(p, 1, s);
-  if (st == BSR_OK) st = launch_fwd_tc(a, order, s);
-  e = cudaFreeAsync(order, s);
+  if (st == BSR_OK) st = launch_fwd_tc(a, s);
+  e = cudaFreeAsync(scratch, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaFreeAsync: %s", cudaGetErrorString(e));
   return st;
 }
@@ -207,11 +231,38 @@ bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
   return BSR_OK;
 }
 
-bsr_status run_bwd(const BwdArgs& a, cudaStream_t s) {
+size_t bwd_scratch_bytes(const Dims& d, int G, bool split) {
+  const size_t rows = (size_t)d.BH * d.S;
+  size_t bytes = 2 * sizeof(float) * rows;
+  bytes += 2 * sizeof(int32_t) * plan_words(d.nb, G, d.BH);
+  if (split) bytes += 3 * sizeof(float) * (size_t)128 * d.D * plan_tiles(d.nb, G, d.BH);
+  return bytes;
+}
+
+void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split) {
+  const size_t rows = (size_t)a->d.BH * a->d.S;
+  a->delta = (float*)base;
+  a->lse2 = a->delta + rows;
+  a->row_plan = (int32_t*)(a->lse2 + rows);
+  a->col_plan = a->row_plan + plan_words(a->d.nb, G, a->d.BH);
+  float* part = (float*)(a->col_plan + plan_words(a->d.nb, G, a->d.BH));
+  const size_t tiles = plan_tiles(a->d.nb, G, a->d.BH);
+  a->part_q = split ? part : nullptr;
+  a->part_kv = split ? part + (size_t)128 * a->d.D * tiles : nullptr;
+}
+
+bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split) {
   bsr_status st = launch_delta(a, s);
   if (st != BSR_OK) return st;
   if (tc_bwd_supported(a.d)) {
-    PlanArgs p{a.row_ptr, a.col_ptr, a.row_order, a.col_order, a.d.nb};
+    PlanArgs p{};
+    p.list[0] = PlanList{a.row_ptr, a.row_plan};
+    p.list[1] = PlanList{a.col_ptr, a.col_plan};
+    p.n = a.d.nb;
+    p.G = tc_grid(a.d);
+    p.BH = a.d.BH;
+    p.allow_split = split ? 1 : 0;
+    p.status = a.status;
     if ((st = launch_plan(p, 2, s)) != BSR_OK) return st;
     return launch_bwd_tc(a, s);
   }
@@ -234,16 +285,16 @@ extern "C" bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, con
                                  dQ, dK, dV, &a);
   if (st != BSR_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t rows = (size_t)a.d.BH * a.d.S;
-  const size_t scratch_bytes = 2 * sizeof(float) * rows + 2 * sizeof(int32_t) * a.d.nb;
-  cudaError_t e = cudaMallocAsync((void**)&a.delta, scratch_bytes, s);
+  const int G = tc_grid(a.d);
+  if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_bwd: cannot query the SM count");
+  const size_t scratch_bytes = bwd_scratch_bytes(a.d, G, true);
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, scratch_bytes, s);
   if (e != cudaSuccess)
     return fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaMallocAsync(%zu): %s", scratch_bytes, cudaGetErrorString(e));
-  a.lse2 = a.delta + rows;
-  a.row_order = (int32_t*)(a.lse2 + rows);
-  a.col_order = a.row_order + a.d.nb;
-  st = run_bwd(a, s);
-  e = cudaFreeAsync(a.delta, s);
+  bwd_scratch_carve(&a, scratch, G, true);
+  st = run_bwd(a, s, true);
+  e = cudaFreeAsync(scratch, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaFreeAsync: %s", cudaGetErrorString(e));
   return st;
 }

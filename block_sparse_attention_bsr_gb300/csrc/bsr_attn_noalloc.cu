@@ -12,11 +12,13 @@
 // static device memory instead.
 //
 // Limits and rules:
-//  * The array holds 2 * kNoAllocMaxRows floats plus two work-order lists of
-//    up to kNoAllocMaxRows / 128 ints (8 MiB + 64 KiB), so batch * heads *
-//    seq must not exceed 1,048,576 (e.g. 128 heads at seq 8192); larger calls
-//    are rejected with BSR_ERR_INVALID_ARG.  Every GPU that loads the library
+//  * The array holds 2 * kNoAllocMaxRows floats plus kNoAllocPlanWords ints
+//    for the two work lists (8.5 MiB in all), so batch * heads * seq must not
+//    exceed 1,048,576 (e.g. 128 heads at seq 8192); larger calls are
+//    rejected with BSR_ERR_INVALID_ARG.  Every GPU that loads the library
 //    keeps the array reserved until the process exits.
+//  * Long block rows / columns are not split into chunks here (that needs
+//    partial-result buffers); the work is still spread longest first.
 //  * All calls share the one array.  The delta kernel overwrites every entry
 //    that is later read, so nothing has to start at zero, but two calls whose
 //    kernels overlap on the GPU (different streams, or different host
@@ -36,9 +38,9 @@ namespace {
 
 constexpr size_t kNoAllocMaxRows = size_t(1) << 20;
 
-constexpr size_t kNoAllocMaxLines = kNoAllocMaxRows / 128;
+constexpr size_t kNoAllocPlanWords = size_t(1) << 17;
 
-static __device__ __align__(256) float g_noalloc_delta[2 * kNoAllocMaxRows + 2 * kNoAllocMaxLines];
+static __device__ __align__(256) float g_noalloc_delta[2 * kNoAllocMaxRows + kNoAllocPlanWords];
 
 constexpr int kMaxDevices = 64;
 
@@ -85,9 +87,12 @@ extern "C" bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor
                 "bsr_attn_bwd_noalloc: batch * heads * seq = %zu exceeds the static scratch of %zu rows; "
                 "use bsr_attn_bwd",
                 rows, kNoAllocMaxRows);
-  if ((st = noalloc_scratch(&a.delta)) != BSR_OK) return st;
-  a.lse2 = a.delta + rows;
-  a.row_order = (int32_t*)(a.lse2 + rows);  // rows <= kNoAllocMaxRows, so nb <= kNoAllocMaxLines
-  a.col_order = a.row_order + a.d.nb;
-  return run_bwd(a, (cudaStream_t)stream);
+  const int G = tc_grid(a.d);
+  if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_bwd_noalloc: cannot query the SM count");
+  if (bwd_scratch_bytes(a.d, G, false) > sizeof(g_noalloc_delta))
+    return fail(BSR_ERR_INVALID_ARG, "bsr_attn_bwd_noalloc: the work lists need more than the static scratch");
+  float* base = nullptr;
+  if ((st = noalloc_scratch(&base)) != BSR_OK) return st;
+  bwd_scratch_carve(&a, base, G, false);
+  return run_bwd(a, (cudaStream_t)stream, false);
 }

@@ -31,7 +31,8 @@ struct FwdArgs {
   float* row_denom;
   const int32_t* row_ptr;
   const int32_t* col_idx;
-  const int32_t* order;  // [nb] block rows longest first (plan_kernel), or null
+  int32_t* plan;          // block-row plan (plan.cu)
+  float* part;            // partial results of split rows: O (128 x D) and 3 x 128 stats per tile
   int* status;
 };
 
@@ -53,22 +54,87 @@ struct BwdArgs {
   void* dV;
   float* delta;  // [BH * S] scratch: D_i = dO_i . O_i
   float* lse2;   // [BH * S] scratch: row_max * log2(e) + log2(row_denom)
-  int32_t* row_order;  // [nb] scratch: block rows longest first
-  int32_t* col_order;  // [nb] scratch: block columns longest first
+  int32_t* row_plan;   // block-row plan (dQ walk)
+  int32_t* col_plan;   // block-column plan (dK/dV walk)
+  float* part_q;       // partial dQ of split rows (128 x D per tile)
+  float* part_kv;      // partial dK, dV of split columns (2 x 128 x D per tile)
   int* status;
 };
 
-// Planner inputs: one or two prefix-offset lists of n lines each.
-struct PlanArgs {
-  const int32_t* ptr0;
-  const int32_t* ptr1;
-  int32_t* order0;
-  int32_t* order1;
-  int n;
+// One work item as the planner writes it (see sched.cuh / plan.cu).
+struct PlanItem {
+  int32_t line;   // block row or block column
+  int32_t first;  // offset of its first entry in col_idx / row_idx
+  int32_t n;      // stored blocks in the item
+  int32_t slot;   // -1: the whole line; else the partial-result slot of this chunk
 };
 
-// Sorts the lines of `lists` (1 or 2) prefix-offset lists by length, longest
-// first, into the order arrays.
+// Layout of one plan in device scratch (int32 units, 16-byte aligned base):
+//   header[4]                  items, work-queue counter, split lines, L
+//   items[cap_items]           PlanItem, longest first
+//   slot_line[cap_slots]       split line of each partial slot
+//   line_base[cap_lines]       first slot of each split line
+//   line_chunks[cap_lines]     chunks of each split line
+//   counters[cap_lines*BH*2]   arrivals per (split line, head, column half)
+// Bounds: L >= nnzb * BH / G, so split lines <= G / BH and slots < 2 G / BH.
+struct PlanLayout {
+  int32_t* header;
+  PlanItem* items;
+  int32_t* slot_line;
+  int32_t* line_base;
+  int32_t* line_chunks;
+  int32_t* counters;
+  int cap_items, cap_slots, cap_lines;
+};
+
+__host__ __device__ inline void plan_caps(int n, int G, int BH, int* items, int* slots, int* lines) {
+  *items = n + 2 * G + 2;
+  *slots = 2 * G / BH + 2;
+  *lines = G / BH + 2;
+}
+
+// int32 words one plan occupies (a multiple of 4).
+__host__ __device__ inline size_t plan_words(int n, int G, int BH) {
+  int ci, cs, cl;
+  plan_caps(n, G, BH, &ci, &cs, &cl);
+  size_t w = 4 + 4 * (size_t)ci + cs + 2 * (size_t)cl + 2 * (size_t)cl * BH;
+  return (w + 3) & ~(size_t)3;
+}
+
+__host__ __device__ inline PlanLayout plan_layout(int32_t* base, int n, int G, int BH) {
+  PlanLayout l;
+  plan_caps(n, G, BH, &l.cap_items, &l.cap_slots, &l.cap_lines);
+  l.header = base;
+  l.items = (PlanItem*)(base + 4);
+  l.slot_line = base + 4 + 4 * (size_t)l.cap_items;
+  l.line_base = l.slot_line + l.cap_slots;
+  l.line_chunks = l.line_base + l.cap_lines;
+  l.counters = l.line_chunks + l.cap_lines;
+  return l;
+}
+
+// Partial-result tiles a split plan may need: cap_slots * BH.
+__host__ __device__ inline size_t plan_tiles(int n, int G, int BH) {
+  int ci, cs, cl;
+  plan_caps(n, G, BH, &ci, &cs, &cl);
+  return (size_t)cs * BH;
+}
+
+struct PlanList {
+  const int32_t* ptr;  // [n + 1] prefix offsets (row_ptr or col_ptr)
+  int32_t* plan;       // plan_words(n, G, BH) int32 of scratch
+};
+
+struct PlanArgs {
+  PlanList list[2];
+  int n;            // lines per list (block rows = block columns)
+  int G;            // persistent CTAs of the kernels that read the plan
+  int BH;
+  int allow_split;  // 0: every line is one item (no partial results)
+  int* status;
+};
+
+// Builds `lists` (1 or 2) plans.
 bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s);
 
 // RAII bracket that records a pair of CUDA events around one kernel launch
@@ -83,17 +149,25 @@ class LaunchTimer {
   cudaStream_t stream_;
 };
 
-// Validates the backward arguments and fills *out (delta left null).
+// Validates the backward arguments and fills *out (scratch pointers left null).
 bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V, const bsr_tensor* O,
                           const bsr_tensor* dO, const float* row_max, const float* row_denom,
                           const int32_t* row_ptr, const int32_t* col_idx, const int32_t* col_ptr,
                           const int32_t* row_idx, float scale, bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV,
                           BwdArgs* out);
 
-// Launches the backward kernels (plan, delta, dQ, dK/dV) on `s`; a.delta and
-// a.lse2 must each point at BH * S floats of 16-byte aligned device scratch,
-// a.row_order and a.col_order at nb ints each.
-bsr_status run_bwd(const BwdArgs& a, cudaStream_t s);
+// Backward scratch: a.delta and a.lse2 (BH * S floats each, 16-byte
+// aligned), the block-row and block-column plans (plan_words ints each) and,
+// with split plans, the partial-result tiles of dQ (128 x D floats each) and
+// dK / dV (2 x 128 x D floats each), plan_tiles of each.
+size_t bwd_scratch_bytes(const Dims& d, int G, bool split);
+// Carves a scratch block of bwd_scratch_bytes at `base` into a's arrays.
+void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split);
+// Launches delta, plan, dQ and dK/dV on `s` (scratch carved already).
+bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split);
+
+// Number of SMs of the current device (cached per device); 0 on error.
+int sm_count();
 
 // Returns a status for the last launch on this thread (cudaGetLastError).
 bsr_status check_launch(const char* what);
@@ -104,12 +178,16 @@ bsr_status launch_delta(const BwdArgs& a, cudaStream_t s);
 bsr_status launch_dq_simt(const BwdArgs& a, cudaStream_t s);
 bsr_status launch_dkdv_simt(const BwdArgs& a, cudaStream_t s);
 
-// Tensor-core (tcgen05 / TMA) kernels.  `order` (device, optional) maps the
-// CTA's x index to a block row.
+// Tensor-core (tcgen05 / TMA) kernels; a.plan (and a.part for head_dim <=
+// 128) must hold the block-row plan built by launch_plan.
 bool tc_fwd_supported(const Dims& d);
-bsr_status launch_fwd_tc(const FwdArgs& a, const int32_t* order, cudaStream_t s);
+bsr_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
 bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s);  // head_dim 64 / 128, P in TMEM
 bool tc_bwd_supported(const Dims& d);
+// Persistent grid of the tensor-core kernels: min(SMs, lines * BH); 0 on error.
+int tc_grid(const Dims& d);
+// Bytes of one forward partial-result tile (split rows), head_dim 64 / 128.
+size_t fwd_part_bytes(int D);
 bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
 
 }  // namespace bsr

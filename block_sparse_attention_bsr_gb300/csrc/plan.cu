@@ -1,16 +1,20 @@
-// Work ordering for the attention kernels: block rows (or block columns)
-// sorted by their number of stored blocks, longest first.
+// Work lists for the persistent attention kernels.
 //
-// The pages split output tiles between cores "balanced by stored blocks"
-// with one writer per tile ("trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG
-// [0.9.0]).  Here the same balance comes from the launch order: the CTA with
-// linear index c handles line order[c / BH] of head c % BH, so the longest
-// lines of every head start in the first wave and the short ones fill in
-// behind them.  Each output tile is still written by exactly one CTA.
-//
-// One CTA per list: a counting sort by count (descending).  Lines with the
-// same count may come out in any order; that changes only the schedule, never
-// a result.
+// For each list (block rows for the forward and dQ walks, block columns for
+// the dK/dV walk) the planner
+//   * splits every line longer than L stored blocks into ceil(len / L)
+//     chunks of nearly equal length, L = max(8, ceil(nnzb * BH / G)) (G =
+//     persistent CTAs), so that no single item is longer than the average
+//     share of one CTA;
+//   * sorts the items by length, longest first (a counting sort: items of
+//     equal length may come out in any order, which changes the schedule but
+//     never a result);
+//   * gives each chunk of a split line a partial-result slot, and zeroes the
+//     per-(line, head, column half) arrival counters used by the last-arriver
+//     merge, and the work-queue counter.
+// Balancing the work by stored blocks with one writer per output tile
+// follows "trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.9.0].
+// Plan layout (int32): see PlanLayout in kernels.h.
 
 #include "kernels.h"
 
@@ -19,34 +23,112 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// ptr: [n + 1] prefix offsets; order: [n] out.  hist: n + 1 ints of shared memory.
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
-  extern __shared__ int hist[];
-  const int* ptr = blockIdx.x == 0 ? p.ptr0 : p.ptr1;
-  int* order = blockIdx.x == 0 ? p.order0 : p.order1;
-  const int n = p.n;
-  for (int v = threadIdx.x; v <= n; v += blockDim.x) hist[v] = 0;
+__device__ __forceinline__ int line_len(const int32_t* ptr, int i, int n) {
+  int c = ptr[i + 1] - ptr[i];
+  return c < 0 ? 0 : (c > n ? n : c);
+}
+
+// Block-wide exclusive scan of hist[0..n] taken from the top value down:
+// afterwards hist[v] = number of items with length > v.
+__device__ void scan_desc(int* hist, int n, int* warp_sums) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int len = n + 1;
+  const int seg = (len + nt - 1) / nt;
+  // thread tid owns reversed positions [tid * seg, tid * seg + seg): values n - p
+  int local = 0;
+  for (int p = tid * seg; p < tid * seg + seg && p < len; ++p) local += hist[n - p];
+  // inclusive warp scan of the per-thread sums
+  const int lane = tid % 32, w = tid / 32;
+  int x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[w] = x;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    int c = ptr[i + 1] - ptr[i];
-    c = c < 0 ? 0 : (c > n ? n : c);
-    atomicAdd(&hist[c], 1);
+  if (w == 0) {
+    int v = lane < nt / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    warp_sums[lane] = v;  // inclusive over warps
   }
   __syncthreads();
-  // exclusive scan from the largest count down: start[v] = #lines with count > v
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int v = n; v >= 0; --v) {
-      const int h = hist[v];
-      hist[v] = run;
-      run += h;
+  int run = x - local + (w > 0 ? warp_sums[w - 1] : 0);  // exclusive prefix of this thread
+  for (int p = tid * seg; p < tid * seg + seg && p < len; ++p) {
+    const int h = hist[n - p];
+    hist[n - p] = run;
+    run += h;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
+  extern __shared__ int hist[];  // [n + 1]
+  __shared__ int warp_sums[32];
+  __shared__ int counts[3];      // items, split lines, slots
+  const PlanList& L = p.list[blockIdx.x];
+  const int n = p.n;
+  const int32_t* ptr = L.ptr;
+  PlanLayout lay = plan_layout(L.plan, n, p.G, p.BH);
+
+  for (int v = threadIdx.x; v <= n; v += blockDim.x) hist[v] = 0;
+  if (threadIdx.x < 3) counts[threadIdx.x] = 0;
+  __syncthreads();
+
+  const long long nnzb = ptr[n] > 0 ? ptr[n] : 0;
+  long long lim = (nnzb * p.BH + p.G - 1) / p.G;
+  if (lim < 8) lim = 8;
+  const int Lmax = p.allow_split ? (int)(lim < n ? lim : n) : n;
+
+  // pass 1: histogram of chunk lengths; slots and split-line indices
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int len = line_len(ptr, i, n);
+    const int nc = len > Lmax ? (len + Lmax - 1) / Lmax : 1;
+    for (int c = 0; c < nc; ++c) atomicAdd(&hist[len / nc + (c < len % nc ? 1 : 0)], 1);
+    atomicAdd(&counts[0], nc);
+  }
+  __syncthreads();
+  scan_desc(hist, n, warp_sums);
+
+  // pass 2: place the items
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int len = line_len(ptr, i, n);
+    const int nc = len > Lmax ? (len + Lmax - 1) / Lmax : 1;
+    int base = -1;
+    if (nc > 1) {
+      const int sl = atomicAdd(&counts[1], 1);
+      base = atomicAdd(&counts[2], nc);
+      if (sl < lay.cap_lines && base + nc <= lay.cap_slots) {
+        lay.line_base[sl] = base;
+        lay.line_chunks[sl] = nc;
+        for (int c = 0; c < nc; ++c) lay.slot_line[base + c] = sl;
+      } else {
+        atomicExch(p.status, kStatusDeviceCheck);
+        base = -1;
+      }
+    }
+    int off = ptr[i];
+    for (int c = 0; c < nc; ++c) {
+      const int clen = len / nc + (c < len % nc ? 1 : 0);
+      const int pos = atomicAdd(&hist[clen], 1);
+      if (pos < lay.cap_items) lay.items[pos] = PlanItem{i, off, clen, base < 0 ? -1 : base + c};
+      off += clen;
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    int c = ptr[i + 1] - ptr[i];
-    c = c < 0 ? 0 : (c > n ? n : c);
-    order[atomicAdd(&hist[c], 1)] = i;
+  const int nsl = counts[1] < lay.cap_lines ? counts[1] : lay.cap_lines;
+  for (int x = threadIdx.x; x < nsl * p.BH * 2; x += blockDim.x) lay.counters[x] = 0;
+  if (threadIdx.x == 0) {
+    const int items = counts[0] <= lay.cap_items ? counts[0] : 0;
+    if (counts[0] > lay.cap_items) atomicExch(p.status, kStatusDeviceCheck);
+    lay.header[0] = items;
+    lay.header[1] = 0;  // work-queue counter
+    lay.header[2] = nsl;
+    lay.header[3] = Lmax;
   }
 }
 

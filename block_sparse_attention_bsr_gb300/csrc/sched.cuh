@@ -1,0 +1,119 @@
+// Persistent work distribution shared by the tensor-core kernels.
+//
+// The grid holds one CTA per SM.  The planner (plan.cu) lists the work items
+// of one kernel -- a block row (forward, dQ) or block column (dK/dV), or a
+// chunk of one when the line is long -- sorted longest first, and every item
+// is done once per (batch, head): work index k stands for item k / BH of head
+// k % BH.  CTAs take work indices from a global counter, so an SM that drew a
+// long item takes fewer short ones after it (longest-processing-time-first
+// list scheduling; the pages balance their two cores "by stored blocks",
+// "trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.9.0]).
+//
+// Inside a CTA the producer thread draws the indices and hands them to the
+// MMA thread and the elementwise warps through a small ring in shared memory
+// (full / empty mbarriers), so all roles walk the same sequence.  A cursor
+// points at one stored block of one item and advances block by block.
+#pragma once
+
+#include <stdint.h>
+
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace bsr {
+
+constexpr int kRing = 4;
+
+struct RingSmem {
+  int32_t k[kRing];
+  uint64_t full[kRing];
+  uint64_t empty[kRing];
+};
+
+struct Cursor {
+  int t;       // position in the CTA's item sequence
+  int q;       // non-empty items started so far (per-item barrier phases)
+  int g;       // blocks visited so far (per-block barrier phases)
+  int i;       // block within the item
+  int n;       // blocks in the item
+  int line;
+  int bh;
+  int first;
+  int slot;
+  bool done;
+};
+
+struct Walk {
+  const PlanItem* items;
+  int BH;
+  int total;  // items * BH
+
+  __device__ __forceinline__ void decode(int k, Cursor& c) const {
+    const PlanItem it = items[k / BH];
+    c.bh = k % BH;
+    c.line = it.line;
+    c.first = it.first;
+    c.n = it.n;
+    c.slot = it.slot;
+  }
+};
+
+// Producer side: draws the next work index into ring slot t % kRing once all
+// consumers released it; -1 marks the end.  Returns false on a timeout.
+__device__ __forceinline__ bool ring_put(RingSmem* ring, int t, int* queue, int total, int* k_out,
+                                         volatile int* abort_flag, int* status) {
+  const int s = t % kRing;
+  if (!sm100::mbar_wait(&ring->empty[s], ((t / kRing) & 1) ^ 1, abort_flag, status)) return false;
+  int k = atomicAdd(queue, 1);
+  if (k >= total) k = -1;
+  ring->k[s] = k;
+  sm100::mbar_arrive(&ring->full[s]);
+  *k_out = k;
+  return true;
+}
+
+// Consumer side: waits for ring slot t % kRing and returns its work index.
+__device__ __forceinline__ bool ring_get(RingSmem* ring, int t, int* k_out, volatile int* abort_flag,
+                                         int* status) {
+  const int s = t % kRing;
+  if (!sm100::mbar_wait(&ring->full[s], (t / kRing) & 1, abort_flag, status)) return false;
+  *k_out = *(volatile int32_t*)&ring->k[s];
+  return true;
+}
+
+__device__ __forceinline__ void ring_release(RingSmem* ring, int t) { sm100::mbar_arrive(&ring->empty[t % kRing]); }
+
+// Sync of the 128 threads of one warpgroup on an mbarrier of count 128
+// (bounded; `phase` counts the syncs this thread has done on `bar`).
+__device__ __forceinline__ bool group_sync(uint64_t* bar, int& phase, volatile int* abort_flag, int* status) {
+  sm100::mbar_arrive(bar);
+  const bool ok = sm100::mbar_wait(bar, phase & 1, abort_flag, status);
+  ++phase;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Last-arriver merge of a split line.  Each chunk's warpgroup has written its
+// partial result; this publishes it and tells whether this warpgroup is the
+// last of the line's chunks (for this head and column half) to arrive, in
+// which case it sums all the chunks' partials into the output.  `r` is the
+// thread's row in the warpgroup (0..127).
+__device__ __forceinline__ bool merge_arrive(const PlanLayout& lay, int slot, int bh, int BH, int hg, int r,
+                                             volatile int* flag, uint64_t* bar, int& phase,
+                                             volatile int* abort_flag, int* status, bool* last) {
+  __threadfence();
+  if (!group_sync(bar, phase, abort_flag, status)) return false;
+  if (r == 0) {
+    const int sl = lay.slot_line[slot];
+    const int old = atomicAdd(&lay.counters[(sl * BH + bh) * 2 + hg], 1);
+    *flag = (old == lay.line_chunks[sl] - 1) ? 1 : 0;
+  }
+  if (!group_sync(bar, phase, abort_flag, status)) return false;
+  *last = *flag != 0;
+  if (*last) __threadfence();
+  return true;
+}
+
+// Reads 4 floats of another CTA's partial result (L2, bypassing L1).
+__device__ __forceinline__ float4 ld_partial(const float* p) { return __ldcg((const float4*)p); }
+
+}  // namespace bsr

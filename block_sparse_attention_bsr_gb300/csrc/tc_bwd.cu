@@ -37,6 +37,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "sched.cuh"
 #include "sm100.cuh"
 #include "tc_common.h"
 
@@ -132,20 +133,24 @@ struct DqCfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr int kBarOff = kTile * (2 + 2 * kStages);
-  static constexpr int kSmem = kBarOff + 256 + 1024;
+  static constexpr int kSmem = kBarOff + 512 + 1024;
 };
 
 struct DqBars {
   uint64_t qd_full;
+  uint64_t qd_empty;
   uint64_t sdp_full;
   uint64_t sdp_free;
   uint64_t ds_full;
   uint64_t dq_done;
   uint64_t final_mma;
+  uint64_t wg_sync[2];
   uint64_t k_full[4];
   uint64_t k_empty[4];
   uint64_t v_full[4];
   uint64_t v_empty[4];
+  RingSmem ring;
+  int merge_flag[2];
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -165,24 +170,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.x % a.d.BH;
-  const int m = a.row_order[blockIdx.x / a.d.BH];
   const int S = a.d.S;
-  const int j0 = a.row_ptr[m];
-  const int nblk = a.row_ptr[m + 1] - j0;
+  const PlanLayout lay = plan_layout(a.row_plan, a.d.nb, (int)gridDim.x, a.d.BH);
+  const Walk walk{lay.items, a.d.BH, lay.header[0] * a.d.BH};
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->qd_full, 1);
+    mbar_init(&bars->qd_empty, 1);
     mbar_init(&bars->sdp_full, 1);
     mbar_init(&bars->sdp_free, kEw);
     mbar_init(&bars->ds_full, kEw);
     mbar_init(&bars->dq_done, 1);
     mbar_init(&bars->final_mma, 1);
+    mbar_init(&bars->wg_sync[0], 128);
+    mbar_init(&bars->wg_sync[1], 128);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bars->ring.full[i], 1);
+      mbar_init(&bars->ring.empty[i], 1 + kEw / 32);  // MMA thread + elementwise warps
     }
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -196,56 +206,106 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   volatile int* ab = &bars->abort_flag;
+  RingSmem* ring = &bars->ring;
 
   if (warp == 0) {
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       // ------------------------------------------------------ producer --
-      const int qrow = bh * S + m * 128;
-      mbar_arrive_expect_tx(&bars->qd_full, 2 * C::kTile);
-      for (int b = 0; b < C::kBoxes; ++b) {
-        tma_load_2d(sQ + b * 16384, &tmQ, b * 64, qrow, &bars->qd_full);
-        tma_load_2d(sdO + b * 16384, &tmdO, b * 64, qrow, &bars->qd_full);
-      }
-      int issued = 0;
-      for (int i = 0; i < nblk; ++i) {
-        int n = a.col_idx[j0 + i];
-        if (n < 0 || n >= a.d.nb) {
-          atomicExch(a.status, kStatusDeviceCheck);
-          n = 0;
+      int g = 0, q = 0;
+      bool ok = true;
+      for (int t = 0; ok; ++t) {
+        int k;
+        if (!(ok = ring_put(ring, t, lay.header + 1, walk.total, &k, ab, a.status)) || k < 0) break;
+        Cursor cur;
+        walk.decode(k, cur);
+        if (cur.n == 0) continue;
+        // Q, dO of a new item: the previous item's S / dP MMAs must be done
+        if (!(ok = mbar_wait(&bars->qd_empty, (q & 1) ^ 1, ab, a.status))) break;
+        const int qrow = cur.bh * S + cur.line * 128;
+        mbar_arrive_expect_tx(&bars->qd_full, 2 * C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b) {
+          tma_load_2d(sQ + b * 16384, &tmQ, b * 64, qrow, &bars->qd_full);
+          tma_load_2d(sdO + b * 16384, &tmdO, b * 64, qrow, &bars->qd_full);
         }
-        const int krow = bh * S + n * 128;
-        const int st = i % C::kStages;
-        const uint32_t use = i / C::kStages;
-        if (!mbar_wait(&bars->k_empty[st], (use & 1) ^ 1, ab, a.status)) break;
-        mbar_arrive_expect_tx(&bars->k_full[st], C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(sK + st * C::kTile + b * 16384, &tmK, b * 64, krow, &bars->k_full[st]);
-        issued = 2 * i + 1;
-        if (!mbar_wait(&bars->v_empty[st], (use & 1) ^ 1, ab, a.status)) break;
-        mbar_arrive_expect_tx(&bars->v_full[st], C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(sV + st * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[st]);
-        issued = 2 * i + 2;
+        ++q;
+        for (int i = 0; i < cur.n; ++i, ++g) {
+          int n = a.col_idx[cur.first + i];
+          if (n < 0 || n >= a.d.nb) {
+            atomicExch(a.status, kStatusDeviceCheck);
+            n = 0;
+          }
+          const int krow = cur.bh * S + n * 128;
+          const int st = g % C::kStages;
+          const uint32_t use = g / C::kStages;
+          if (!(ok = mbar_wait(&bars->k_empty[st], (use & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->k_full[st], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(sK + st * C::kTile + b * 16384, &tmK, b * 64, krow, &bars->k_full[st]);
+          if (!(ok = mbar_wait(&bars->v_empty[st], (use & 1) ^ 1, ab, a.status))) {
+            ++g;  // this block's K was issued, its V was not
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->v_full[st], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(sV + st * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[st]);
+        }
       }
-      drain_wait(&bars->qd_full, 0);
-      for (int t = (issued > 2 * C::kStages ? issued - 2 * C::kStages : 0); t < issued; ++t) {
-        const int i = t / 2, st = i % C::kStages;
-        drain_wait((t & 1) ? &bars->v_full[st] : &bars->k_full[st], (i / C::kStages) & 1);
+      // drain: every copy issued must land before the CTA exits
+      if (q > 0) drain_wait(&bars->qd_full, (q - 1) & 1);
+      for (int i = (g > C::kStages ? g - C::kStages : 0); i < g; ++i) {
+        drain_wait(&bars->k_full[i % C::kStages], (i / C::kStages) & 1);
+        drain_wait(&bars->v_full[i % C::kStages], (i / C::kStages) & 1);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       // ----------------------------------------------------------- MMA --
+      // S / dP of block g+1 (cursor A) are issued before dQ of block g
+      // (cursor B), so they run while the elementwise pass of block g
+      // computes dS.  A draws items from the ring; B follows and releases
+      // each item once it is past it.
       const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
       const uint32_t idDQ = instr_desc(1, 0, 1, D, 128);
       const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO), aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(&bars->qd_full, 0, ab, a.status);
-      auto issue_sdp = [&](int i) -> bool {
-        const int st = i % C::kStages;
-        const uint32_t use = i / C::kStages;
+      bool ok = true;
+      auto seek_a = [&](Cursor& c) {
+        while (true) {
+          int k;
+          if (!(ok = ring_get(ring, c.t, &k, ab, a.status)) || k < 0) {
+            c.done = true;
+            return;
+          }
+          walk.decode(k, c);
+          if (c.n > 0) {
+            c.i = 0;
+            return;
+          }
+          ++c.t;
+        }
+      };
+      auto seek_b = [&](Cursor& c) {
+        while (true) {
+          const int k = *(volatile int32_t*)&ring->k[c.t % kRing];
+          if (k < 0) {
+            c.done = true;
+            return;
+          }
+          walk.decode(k, c);
+          if (c.n > 0) {
+            c.i = 0;
+            return;
+          }
+          ring_release(ring, c.t);
+          ++c.t;
+        }
+      };
+      auto issue_sdp = [&](const Cursor& c) -> bool {
+        const int st = c.g % C::kStages;
+        const uint32_t use = c.g / C::kStages;
+        if (c.i == 0 && !mbar_wait(&bars->qd_full, c.q & 1, ab, a.status)) return false;
         if (!mbar_wait(&bars->k_full[st], use & 1, ab, a.status)) return false;
         if (!mbar_wait(&bars->v_full[st], use & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->sdp_free, (i & 1) ^ 1, ab, a.status)) return false;
+        if (!mbar_wait(&bars->sdp_free, (c.g & 1) ^ 1, ab, a.status)) return false;
         tc_fence_after();
         const uint32_t kb = aK + st * C::kTile, vb = aV + st * C::kTile;
 #pragma unroll
@@ -260,62 +320,146 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars->v_empty[st]);
         mma_commit(&bars->sdp_full);
+        if (c.i == c.n - 1) mma_commit(&bars->qd_empty);
         return true;
       };
-      if (ok) ok = issue_sdp(0);
-      for (int i = 0; ok && i < nblk; ++i) {
-        if (i + 1 < nblk && !(ok = issue_sdp(i + 1))) break;
-        const int st = i % C::kStages;
-        if (!(ok = mbar_wait(&bars->ds_full, i & 1, ab, a.status))) break;
+      auto next_a = [&](Cursor& c) {
+        ++c.g;
+        if (++c.i == c.n) {
+          ++c.q;
+          ++c.t;
+          seek_a(c);
+        }
+      };
+      Cursor A{0, 0, 0, 0, 0, 0, 0, 0, 0, false};
+      seek_a(A);
+      Cursor B = A;
+      if (ok && !A.done) {
+        if ((ok = issue_sdp(A))) next_a(A);
+      }
+      while (ok && !B.done) {
+        if (!A.done) {
+          if (!(ok = issue_sdp(A))) break;
+          next_a(A);
+          if (!ok) break;
+        }
+        const int st = B.g % C::kStages;
+        if (!(ok = mbar_wait(&bars->ds_full, B.g & 1, ab, a.status))) break;
         tc_fence_after();
         const uint32_t kb = aK + st * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ts(tmem + kColDQ, tmem + kColDS + kk * 8, smem_desc(kb + kk * 2048, 16384, 1024), idDQ,
-                      (i > 0 || kk > 0) ? 1u : 0u);
+                      (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->k_empty[st]);
         mma_commit(&bars->dq_done);
+        ++B.g;
+        if (++B.i == B.n) {
+          ring_release(ring, B.t);
+          ++B.q;
+          ++B.t;
+          seek_b(B);
+        }
       }
       mma_commit(&bars->final_mma);
       drain_wait(&bars->final_mma, 0);
     }
   } else {
     // ---------------------------------------------------- elementwise --
-    const int g = (warp - 2) / 4;  // column half
+    const int hg = (warp - 2) / 4;  // column half
     const int wl = warp % 4;
     const int r = wl * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
-    const size_t grow = (size_t)bh * S + (size_t)m * 128 + r;
-    __nv_bfloat16* dqrow = (__nv_bfloat16*)a.dQ + grow * D + g * (D / 2);
-    if (nblk == 0) {
-      zero_cols<D / 2>(dqrow);
-    } else {
-      const float sl2 = a.d.scale * kLog2e;
-      const float lse2 = a.lse2[grow];
-      const float dl = a.delta[grow];
-      bool ok = true;
-      for (int i = 0; i < nblk; ++i) {
-        if (!(ok = warp_wait(&bars->sdp_full, i & 1, ab, a.status))) break;
-        tc_fence_after();
-        float s[64], dp[64];
-        tmem_ld64(tmem + lane_base + kColS + g * 64, s);
-        tmem_ld64(tmem + lane_base + kColDP + g * 64, dp);
-        tc_fence_before();
-        mbar_arrive(&bars->sdp_free);
+    const float sl2 = a.d.scale * kLog2e;
+    int g = 0, sync_phase = 0;
+    bool ok = true;
+    for (int t = 0; ok; ++t) {
+      int k = -1;
+      if (lane == 0) ok = ring_get(ring, t, &k, ab, a.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      k = __shfl_sync(0xffffffffu, k, 0);
+      if (!ok || k < 0) break;
+      Cursor cur;
+      walk.decode(k, cur);
+      const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
+      __nv_bfloat16* dqrow = (__nv_bfloat16*)a.dQ + grow * D + hg * (D / 2);
+      if (cur.n == 0) {
+        zero_cols<D / 2>(dqrow);
+      } else {
+        const float lse2 = a.lse2[grow];
+        const float dl = a.delta[grow];
+        for (int i = 0; i < cur.n; ++i, ++g) {
+          if (!(ok = warp_wait(&bars->sdp_full, g & 1, ab, a.status))) break;
+          tc_fence_after();
+          float s[64], dp[64];
+          tmem_ld64(tmem + lane_base + kColS + hg * 64, s);
+          tmem_ld64(tmem + lane_base + kColDP + hg * 64, dp);
+          tc_fence_before();
+          mbar_arrive(&bars->sdp_free);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) s[k] = ex2(fmaf(s[k], sl2, -lse2)) * (dp[k] - dl);
-        if (i > 0 && !(ok = warp_wait(&bars->dq_done, (i - 1) & 1, ab, a.status))) break;
+          for (int j = 0; j < 64; ++j) s[j] = ex2(fmaf(s[j], sl2, -lse2)) * (dp[j] - dl);
+          if (g > 0 && !(ok = warp_wait(&bars->dq_done, (g - 1) & 1, ab, a.status))) break;
+          tc_fence_after();
+          tmem_st_bf16x64(tmem + lane_base + kColDS + hg * 32, s);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->ds_full);
+        }
+        if (!ok) break;
+        if (!(ok = warp_wait(&bars->dq_done, (g - 1) & 1, ab, a.status))) break;
         tc_fence_after();
-        tmem_st_bf16x64(tmem + lane_base + kColDS + g * 32, s);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->ds_full);
+        if (cur.slot < 0) {
+          store_acc_cols<D / 2>(tmem + lane_base + kColDQ + hg * (D / 2), dqrow, a.d.scale);
+        } else {
+          // chunk of a split row: publish the fp32 partial, the last chunk merges
+          float* prow = a.part_q + ((size_t)(cur.slot * a.d.BH + cur.bh) * 128 + r) * D + hg * (D / 2);
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kColDQ + hg * (D / 2) + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              ((float4*)(prow + c * 32))[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                          __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+          bool last = false;
+          if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
+                                  sync_phase, ab, a.status, &last)))
+            break;
+          if (last) {
+            const int sl = lay.slot_line[cur.slot];
+            const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
+#pragma unroll 1
+            for (int c = 0; c < D / 64; ++c) {
+              float acc[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+              for (int ch = 0; ch < nc; ++ch) {
+                const float* src =
+                    a.part_q + ((size_t)((base + ch) * a.d.BH + cur.bh) * 128 + r) * D + hg * (D / 2) + c * 32;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 x = ld_partial(src + 4 * j);
+                  acc[4 * j] += x.x;
+                  acc[4 * j + 1] += x.y;
+                  acc[4 * j + 2] += x.z;
+                  acc[4 * j + 3] += x.w;
+                }
+              }
+              uint4* dst = (uint4*)(dqrow + c * 32);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(pack_bf16x2(acc[8 * j] * a.d.scale, acc[8 * j + 1] * a.d.scale),
+                                    pack_bf16x2(acc[8 * j + 2] * a.d.scale, acc[8 * j + 3] * a.d.scale),
+                                    pack_bf16x2(acc[8 * j + 4] * a.d.scale, acc[8 * j + 5] * a.d.scale),
+                                    pack_bf16x2(acc[8 * j + 6] * a.d.scale, acc[8 * j + 7] * a.d.scale));
+            }
+          }
+        }
       }
-      if (ok) ok = warp_wait(&bars->dq_done, (nblk - 1) & 1, ab, a.status);
-      if (ok) {
-        tc_fence_after();
-        store_acc_cols<D / 2>(tmem + lane_base + kColDQ + g * (D / 2), dqrow, a.d.scale);
-      }
+      __syncwarp();
+      if (lane == 0) ring_release(ring, t);
     }
   }
 
@@ -333,24 +477,73 @@ struct DkvCfg {
   static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr int kOp = 128 * 128 * 2;  // dS^T tile
   static constexpr int kBarOff = kTile * (2 + 2 * kStages) + kOp;
-  static constexpr int kSmem = kBarOff + 256 + 1024;
+  static constexpr int kSmem = kBarOff + 512 + 1024;
 };
 
 struct DkvBars {
   uint64_t kv_full;
+  uint64_t kv_empty;
   uint64_t st_full;
   uint64_t st_free;
   uint64_t pds_full;
   uint64_t pt_free;
   uint64_t dst_free;
   uint64_t final_mma;
+  uint64_t wg_sync[2];
   uint64_t q_full[4];
   uint64_t q_empty[4];
   uint64_t do_full[4];
   uint64_t do_empty[4];
+  RingSmem ring;
+  int merge_flag[2];
   uint32_t tmem_slot;
   int abort_flag;
 };
+
+// Writes NC fp32 TMEM columns of this lane to dst (global, 16-byte aligned).
+template <int NC>
+__device__ __forceinline__ void store_acc_f32(uint32_t taddr, float* dst) {
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c * 32, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      ((float4*)(dst + c * 32))[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+  }
+}
+
+// Sums NC fp32 columns over `nc` partial rows spaced `stride` floats apart
+// (from src) and stores them as bf16 times `mul` at dst.
+template <int NC>
+__device__ __forceinline__ void merge_rows(const float* src, size_t stride, int nc, __nv_bfloat16* dst, float mul) {
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    float acc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    for (int ch = 0; ch < nc; ++ch) {
+      const float* p = src + ch * stride + c * 32;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = ld_partial(p + 4 * j);
+        acc[4 * j] += x.x;
+        acc[4 * j + 1] += x.y;
+        acc[4 * j + 2] += x.z;
+        acc[4 * j + 3] += x.w;
+      }
+    }
+    uint4* d = (uint4*)(dst + c * 32);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      d[j] = make_uint4(pack_bf16x2(acc[8 * j] * mul, acc[8 * j + 1] * mul),
+                        pack_bf16x2(acc[8 * j + 2] * mul, acc[8 * j + 3] * mul),
+                        pack_bf16x2(acc[8 * j + 4] * mul, acc[8 * j + 5] * mul),
+                        pack_bf16x2(acc[8 * j + 6] * mul, acc[8 * j + 7] * mul));
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -370,25 +563,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.x % a.d.BH;
-  const int n = a.col_order[blockIdx.x / a.d.BH];
   const int S = a.d.S;
-  const int t0 = a.col_ptr[n];
-  const int nblk = a.col_ptr[n + 1] - t0;
+  const PlanLayout lay = plan_layout(a.col_plan, a.d.nb, (int)gridDim.x, a.d.BH);
+  const Walk walk{lay.items, a.d.BH, lay.header[0] * a.d.BH};
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
     mbar_init(&bars->st_full, 1);
     mbar_init(&bars->st_free, kEw);
     mbar_init(&bars->pds_full, kEw);
     mbar_init(&bars->pt_free, 1);
     mbar_init(&bars->dst_free, 1);
     mbar_init(&bars->final_mma, 1);
+    mbar_init(&bars->wg_sync[0], 128);
+    mbar_init(&bars->wg_sync[1], 128);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->do_full[i], 1);
       mbar_init(&bars->do_empty[i], 1);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bars->ring.full[i], 1);
+      mbar_init(&bars->ring.empty[i], 1 + kEw / 32);
     }
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -402,57 +600,111 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   volatile int* ab = &bars->abort_flag;
+  RingSmem* ring = &bars->ring;
 
   if (warp == 0) {
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       // ------------------------------------------------------ producer --
-      const int krow = bh * S + n * 128;
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTile);
-      for (int b = 0; b < C::kBoxes; ++b) {
-        tma_load_2d(sK + b * 16384, &tmK, b * 64, krow, &bars->kv_full);
-        tma_load_2d(sV + b * 16384, &tmV, b * 64, krow, &bars->kv_full);
-      }
-      int issued = 0;
-      for (int i = 0; i < nblk; ++i) {
-        int m = a.row_idx[t0 + i];
-        if (m < 0 || m >= a.d.nb) {
-          atomicExch(a.status, kStatusDeviceCheck);
-          m = 0;
+      int g = 0, q = 0;
+      bool ok = true;
+      for (int t = 0; ok; ++t) {
+        int k;
+        if (!(ok = ring_put(ring, t, lay.header + 1, walk.total, &k, ab, a.status)) || k < 0) break;
+        Cursor cur;
+        walk.decode(k, cur);
+        if (cur.n == 0) continue;
+        // K, V of a new item: the previous item's S^T / dP^T must be done
+        if (!(ok = mbar_wait(&bars->kv_empty, (q & 1) ^ 1, ab, a.status))) break;
+        const int krow = cur.bh * S + cur.line * 128;
+        mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b) {
+          tma_load_2d(sK + b * 16384, &tmK, b * 64, krow, &bars->kv_full);
+          tma_load_2d(sV + b * 16384, &tmV, b * 64, krow, &bars->kv_full);
         }
-        const int qrow = bh * S + m * 128;
-        const int st = i % C::kStages;
-        const uint32_t use = i / C::kStages;
-        if (!mbar_wait(&bars->q_empty[st], (use & 1) ^ 1, ab, a.status)) break;
-        mbar_arrive_expect_tx(&bars->q_full[st], C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(sQ + st * C::kTile + b * 16384, &tmQ, b * 64, qrow, &bars->q_full[st]);
-        issued = 2 * i + 1;
-        if (!mbar_wait(&bars->do_empty[st], (use & 1) ^ 1, ab, a.status)) break;
-        mbar_arrive_expect_tx(&bars->do_full[st], C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(sdO + st * C::kTile + b * 16384, &tmdO, b * 64, qrow, &bars->do_full[st]);
-        issued = 2 * i + 2;
+        ++q;
+        for (int i = 0; i < cur.n; ++i, ++g) {
+          int m = a.row_idx[cur.first + i];
+          if (m < 0 || m >= a.d.nb) {
+            atomicExch(a.status, kStatusDeviceCheck);
+            m = 0;
+          }
+          const int qrow = cur.bh * S + m * 128;
+          const int st = g % C::kStages;
+          const uint32_t use = g / C::kStages;
+          if (!(ok = mbar_wait(&bars->q_empty[st], (use & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->q_full[st], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(sQ + st * C::kTile + b * 16384, &tmQ, b * 64, qrow, &bars->q_full[st]);
+          if (!(ok = mbar_wait(&bars->do_empty[st], (use & 1) ^ 1, ab, a.status))) {
+            ++g;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->do_full[st], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(sdO + st * C::kTile + b * 16384, &tmdO, b * 64, qrow, &bars->do_full[st]);
+        }
       }
-      drain_wait(&bars->kv_full, 0);
-      for (int t = (issued > 2 * C::kStages ? issued - 2 * C::kStages : 0); t < issued; ++t) {
-        const int i = t / 2, st = i % C::kStages;
-        drain_wait((t & 1) ? &bars->do_full[st] : &bars->q_full[st], (i / C::kStages) & 1);
+      if (q > 0) drain_wait(&bars->kv_full, (q - 1) & 1);
+      for (int i = (g > C::kStages ? g - C::kStages : 0); i < g; ++i) {
+        drain_wait(&bars->q_full[i % C::kStages], (i / C::kStages) & 1);
+        drain_wait(&bars->do_full[i % C::kStages], (i / C::kStages) & 1);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       // ----------------------------------------------------------- MMA --
-      // Per block i: S^T_i and dP^T_i land before the elementwise pass; the
+      // Per block g: S^T_g and dP^T_g land before the elementwise pass; the
       // elementwise pass reads both and releases them (st_free), so
-      // S^T_{i+1} is issued while it computes; P^T_i comes back over the
-      // dP^T columns, so dP^T_{i+1} waits for dV_i to finish (pt_free).
+      // S^T_{g+1} (cursor A) is issued while it computes; P^T_g comes back
+      // over the dP^T columns, so dP^T_{g+1} waits for dV_g (pt_free).
       const uint32_t idST = instr_desc(1, 0, 0, 128, 128);
       const uint32_t idG = instr_desc(1, 0, 1, D, 128);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
       const uint32_t aDST = smem_u32(sDST);
-      auto issue_st = [&](int i) -> bool {
-        const int st = i % C::kStages;
-        if (!mbar_wait(&bars->q_full[st], (i / C::kStages) & 1, ab, a.status)) return false;
+      bool ok = true;
+      auto seek_a = [&](Cursor& c) {
+        while (true) {
+          int k;
+          if (!(ok = ring_get(ring, c.t, &k, ab, a.status)) || k < 0) {
+            c.done = true;
+            return;
+          }
+          walk.decode(k, c);
+          if (c.n > 0) {
+            c.i = 0;
+            return;
+          }
+          ++c.t;
+        }
+      };
+      auto seek_b = [&](Cursor& c) {
+        while (true) {
+          const int k = *(volatile int32_t*)&ring->k[c.t % kRing];
+          if (k < 0) {
+            c.done = true;
+            return;
+          }
+          walk.decode(k, c);
+          if (c.n > 0) {
+            c.i = 0;
+            return;
+          }
+          ring_release(ring, c.t);
+          ++c.t;
+        }
+      };
+      auto next_a = [&](Cursor& c) {
+        ++c.g;
+        if (++c.i == c.n) {
+          ++c.q;
+          ++c.t;
+          seek_a(c);
+        }
+      };
+      auto issue_st = [&](const Cursor& c) -> bool {
+        const int st = c.g % C::kStages;
+        if (c.i == 0 && !mbar_wait(&bars->kv_full, c.q & 1, ab, a.status)) return false;
+        if (!mbar_wait(&bars->q_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
         tc_fence_after();
         const uint32_t qb = aQ + st * C::kTile;
 #pragma unroll
@@ -462,9 +714,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      auto issue_dpt = [&](int i) -> bool {
-        const int st = i % C::kStages;
-        if (!mbar_wait(&bars->do_full[st], (i / C::kStages) & 1, ab, a.status)) return false;
+      auto issue_dpt = [&](const Cursor& c) -> bool {
+        const int st = c.g % C::kStages;
+        if (!mbar_wait(&bars->do_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
         tc_fence_after();
         const uint32_t gb = adO + st * C::kTile;
 #pragma unroll
@@ -473,36 +725,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + kColDPT, smem_desc(aV + off, 16, 1024), smem_desc(gb + off, 16, 1024), idST, kk > 0);
         }
         mma_commit(&bars->st_full);
+        if (c.i == c.n - 1) mma_commit(&bars->kv_empty);
         return true;
       };
-      bool ok = mbar_wait(&bars->kv_full, 0, ab, a.status);
-      if (ok) ok = issue_st(0) && issue_dpt(0);
-      for (int i = 0; ok && i < nblk; ++i) {
-        const int st = i % C::kStages;
-        if (i + 1 < nblk) {
-          if (!(ok = mbar_wait(&bars->st_free, i & 1, ab, a.status))) break;
-          if (!(ok = issue_st(i + 1))) break;
+      Cursor A{0, 0, 0, 0, 0, 0, 0, 0, 0, false};
+      seek_a(A);
+      Cursor B = A;
+      if (ok && !A.done) {
+        if ((ok = issue_st(A) && issue_dpt(A))) next_a(A);
+      }
+      while (ok && !B.done) {
+        const int st = B.g % C::kStages;
+        if (!A.done) {
+          if (!(ok = mbar_wait(&bars->st_free, B.g & 1, ab, a.status))) break;
+          if (!(ok = issue_st(A))) break;
         }
-        if (!(ok = mbar_wait(&bars->pds_full, i & 1, ab, a.status))) break;
+        if (!(ok = mbar_wait(&bars->pds_full, B.g & 1, ab, a.status))) break;
         tc_fence_after();
         const uint32_t qb = aQ + st * C::kTile, gb = adO + st * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ts(tmem + kColDV, tmem + kColDPT + kk * 8 + (kk >= 4 ? 32 : 0),
-                      smem_desc(gb + kk * 2048, 16384, 1024), idG, (i > 0 || kk > 0) ? 1u : 0u);
+                      smem_desc(gb + kk * 2048, 16384, 1024), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->pt_free);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16_ss(tmem + kColDK, smem_desc(aDST + off, 16, 1024), smem_desc(qb + kk * 2048, 16384, 1024), idG,
-                      (i > 0 || kk > 0) ? 1u : 0u);
+                      (B.i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars->q_empty[st]);
         mma_commit(&bars->do_empty[st]);
         mma_commit(&bars->dst_free);
-        if (i + 1 < nblk) {
-          if (!(ok = mbar_wait(&bars->pt_free, i & 1, ab, a.status))) break;
-          if (!(ok = issue_dpt(i + 1))) break;
+        if (!A.done) {
+          if (!(ok = mbar_wait(&bars->pt_free, B.g & 1, ab, a.status))) break;
+          if (!(ok = issue_dpt(A))) break;
+          next_a(A);
+          if (!ok) break;
+        }
+        ++B.g;
+        if (++B.i == B.n) {
+          ring_release(ring, B.t);
+          ++B.q;
+          ++B.t;
+          seek_b(B);
         }
       }
       mma_commit(&bars->final_mma);
@@ -510,62 +776,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------- elementwise --
-    const int g = (warp - 2) / 4;  // query half of the tile
+    const int hg = (warp - 2) / 4;  // query half of the tile
     const int wl = warp % 4;
-    const int r = wl * 32 + lane;  // key row of the tile
+    const int r = wl * 32 + lane;   // key row of the tile
     const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
-    const size_t grow = (size_t)bh * S + (size_t)n * 128 + r;
-    __nv_bfloat16* dkrow = (__nv_bfloat16*)a.dK + grow * D + g * (D / 2);
-    __nv_bfloat16* dvrow = (__nv_bfloat16*)a.dV + grow * D + g * (D / 2);
-    if (nblk == 0) {
-      zero_cols<D / 2>(dkrow);
-      zero_cols<D / 2>(dvrow);
-    } else {
-      const float sl2 = a.d.scale * kLog2e;
-      const uint32_t aDST = smem_u32(sDST);
-      bool ok = true;
-      for (int i = 0; i < nblk; ++i) {
-        int m = a.row_idx[t0 + i];
-        m = (m < 0 || m >= a.d.nb) ? 0 : m;
-        const size_t q0 = (size_t)bh * S + (size_t)m * 128 + g * 64;
-        const float4* lse4 = (const float4*)(a.lse2 + q0);
-        const float4* dl4 = (const float4*)(a.delta + q0);
-        if (!(ok = warp_wait(&bars->st_full, i & 1, ab, a.status))) break;
-        tc_fence_after();
-        float s[64], dp[64];
-        tmem_ld64(tmem + lane_base + kColST + g * 64, s);
-        tmem_ld64(tmem + lane_base + kColDPT + g * 64, dp);
-        tc_fence_before();
-        mbar_arrive(&bars->st_free);
+    const float sl2 = a.d.scale * kLog2e;
+    const uint32_t aDST = smem_u32(sDST);
+    int g = 0, sync_phase = 0;
+    bool ok = true;
+    for (int t = 0; ok; ++t) {
+      int k = -1;
+      if (lane == 0) ok = ring_get(ring, t, &k, ab, a.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      k = __shfl_sync(0xffffffffu, k, 0);
+      if (!ok || k < 0) break;
+      Cursor cur;
+      walk.decode(k, cur);
+      const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
+      __nv_bfloat16* dkrow = (__nv_bfloat16*)a.dK + grow * D + hg * (D / 2);
+      __nv_bfloat16* dvrow = (__nv_bfloat16*)a.dV + grow * D + hg * (D / 2);
+      if (cur.n == 0) {
+        zero_cols<D / 2>(dkrow);
+        zero_cols<D / 2>(dvrow);
+      } else {
+        for (int i = 0; i < cur.n; ++i, ++g) {
+          int m = a.row_idx[cur.first + i];
+          m = (m < 0 || m >= a.d.nb) ? 0 : m;
+          const size_t q0 = (size_t)cur.bh * S + (size_t)m * 128 + hg * 64;
+          const float4* lse4 = (const float4*)(a.lse2 + q0);
+          const float4* dl4 = (const float4*)(a.delta + q0);
+          if (!(ok = warp_wait(&bars->st_full, g & 1, ab, a.status))) break;
+          tc_fence_after();
+          float s[64], dp[64];
+          tmem_ld64(tmem + lane_base + kColST + hg * 64, s);
+          tmem_ld64(tmem + lane_base + kColDPT + hg * 64, dp);
+          tc_fence_before();
+          mbar_arrive(&bars->st_free);
 #pragma unroll
-        for (int k4 = 0; k4 < 16; ++k4) {
-          const float4 l = __ldg(lse4 + k4), d = __ldg(dl4 + k4);
-          s[4 * k4 + 0] = ex2(fmaf(s[4 * k4 + 0], sl2, -l.x));
-          s[4 * k4 + 1] = ex2(fmaf(s[4 * k4 + 1], sl2, -l.y));
-          s[4 * k4 + 2] = ex2(fmaf(s[4 * k4 + 2], sl2, -l.z));
-          s[4 * k4 + 3] = ex2(fmaf(s[4 * k4 + 3], sl2, -l.w));
-          dp[4 * k4 + 0] = s[4 * k4 + 0] * (dp[4 * k4 + 0] - d.x);
-          dp[4 * k4 + 1] = s[4 * k4 + 1] * (dp[4 * k4 + 1] - d.y);
-          dp[4 * k4 + 2] = s[4 * k4 + 2] * (dp[4 * k4 + 2] - d.z);
-          dp[4 * k4 + 3] = s[4 * k4 + 3] * (dp[4 * k4 + 3] - d.w);
+          for (int k4 = 0; k4 < 16; ++k4) {
+            const float4 l = __ldg(lse4 + k4), d = __ldg(dl4 + k4);
+            s[4 * k4 + 0] = ex2(fmaf(s[4 * k4 + 0], sl2, -l.x));
+            s[4 * k4 + 1] = ex2(fmaf(s[4 * k4 + 1], sl2, -l.y));
+            s[4 * k4 + 2] = ex2(fmaf(s[4 * k4 + 2], sl2, -l.z));
+            s[4 * k4 + 3] = ex2(fmaf(s[4 * k4 + 3], sl2, -l.w));
+            dp[4 * k4 + 0] = s[4 * k4 + 0] * (dp[4 * k4 + 0] - d.x);
+            dp[4 * k4 + 1] = s[4 * k4 + 1] * (dp[4 * k4 + 1] - d.y);
+            dp[4 * k4 + 2] = s[4 * k4 + 2] * (dp[4 * k4 + 2] - d.z);
+            dp[4 * k4 + 3] = s[4 * k4 + 3] * (dp[4 * k4 + 3] - d.w);
+          }
+          // P^T over this warpgroup's own dP^T columns (already read above;
+          // dV of the previous block finished before dP^T of this one began)
+          tmem_st_bf16x64(tmem + lane_base + kColDPT + hg * 64, s);
+          if (g > 0 && !(ok = warp_wait(&bars->dst_free, (g - 1) & 1, ab, a.status))) break;
+          st_row_chunk(aDST, r, 2 * hg, dp);
+          st_row_chunk(aDST, r, 2 * hg + 1, dp + 32);
+          tmem_wait_st();
+          tc_fence_before();
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->pds_full);
         }
-        // P^T over this warpgroup's own dP^T columns (already read above;
-        // dV of the previous block finished before dP^T of this one began)
-        tmem_st_bf16x64(tmem + lane_base + kColDPT + g * 64, s);
-        if (i > 0 && !(ok = warp_wait(&bars->dst_free, (i - 1) & 1, ab, a.status))) break;
-        st_row_chunk(aDST, r, 2 * g, dp);
-        st_row_chunk(aDST, r, 2 * g + 1, dp + 32);
-        tmem_wait_st();
-        tc_fence_before();
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->pds_full);
-      }
-      if (ok) ok = warp_wait(&bars->dst_free, (nblk - 1) & 1, ab, a.status);
-      if (ok) {
+        if (!ok) break;
+        if (!(ok = warp_wait(&bars->dst_free, (g - 1) & 1, ab, a.status))) break;
         tc_fence_after();
-        store_acc_cols<D / 2>(tmem + lane_base + kColDV + g * (D / 2), dvrow, 1.f);
-        store_acc_cols<D / 2>(tmem + lane_base + kColDK + g * (D / 2), dkrow, a.d.scale);
+        if (cur.slot < 0) {
+          store_acc_cols<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), dvrow, 1.f);
+          store_acc_cols<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), dkrow, a.d.scale);
+        } else {
+          // chunk of a split column: publish the fp32 partials, the last chunk merges
+          const size_t tile = (size_t)cur.slot * a.d.BH + cur.bh;
+          float* pv = a.part_kv + ((tile * 2 + 0) * 128 + r) * D + hg * (D / 2);
+          float* pk = a.part_kv + ((tile * 2 + 1) * 128 + r) * D + hg * (D / 2);
+          store_acc_f32<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), pv);
+          store_acc_f32<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), pk);
+          bool last = false;
+          if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
+                                  sync_phase, ab, a.status, &last)))
+            break;
+          if (last) {
+            const int sl = lay.slot_line[cur.slot];
+            const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
+            const size_t t0 = (size_t)base * a.d.BH + cur.bh;
+            const size_t stride = (size_t)a.d.BH * 2 * 128 * D;  // next slot, same head
+            merge_rows<D / 2>(a.part_kv + ((t0 * 2 + 0) * 128 + r) * D + hg * (D / 2), stride, nc, dvrow, 1.f);
+            merge_rows<D / 2>(a.part_kv + ((t0 * 2 + 1) * 128 + r) * D + hg * (D / 2), stride, nc, dkrow,
+                              a.d.scale);
+          }
+        }
       }
+      __syncwarp();
+      if (lane == 0) ring_release(ring, t);
     }
   }
 
@@ -576,14 +875,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, cudaStream_t s) {
+bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, int grid, cudaStream_t s) {
   {
     auto kern = dq_tc_kernel<D>;
     const int smem = DqCfg<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_tc: cudaFuncSetAttribute(%d): %s", smem, cudaGetErrorString(e));
     LaunchTimer timer("dq_tc", s);
-    kern<<<dim3(a.d.nb * a.d.BH), kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
+    kern<<<grid, kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
     bsr_status st = check_launch("dq_tc launch");
     if (st != BSR_OK) return st;
   }
@@ -594,7 +893,7 @@ bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap&
     if (e != cudaSuccess)
       return fail(BSR_ERR_CUDA, "dkdv_tc: cudaFuncSetAttribute(%d): %s", smem, cudaGetErrorString(e));
     LaunchTimer timer("dkdv_tc", s);
-    kern<<<dim3(a.d.nb * a.d.BH), kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
+    kern<<<grid, kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
     return check_launch("dkdv_tc launch");
   }
 }
@@ -603,17 +902,25 @@ bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap&
 
 bool tc_bwd_supported(const Dims& d) { return d.dtype == BSR_BF16 && (d.D == 64 || d.D == 128); }
 
+int tc_grid(const Dims& d) {
+  const int sms = sm_count();
+  const int total = d.nb * d.BH;
+  return sms <= 0 ? 0 : (total < sms ? total : sms);
+}
+
 bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   if ((((uintptr_t)a.lse2) | ((uintptr_t)a.delta)) & 15)
     return fail(BSR_ERR_INVALID_ARG, "bwd_tc: scratch arrays must be 16-byte aligned");
+  const int grid = tc_grid(a.d);
+  if (grid <= 0) return fail(BSR_ERR_CUDA, "bwd_tc: cannot query the SM count");
   TensorMaps tm;
   bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
   if (st != BSR_OK) return st;
   CUtensorMap tmdO;
   if ((st = make_tensor_map(a.d, a.dO, &tmdO, "dO")) != BSR_OK) return st;
   switch (a.d.D) {
-    case 64: return launch_bwd<64>(a, tm, tmdO, s);
-    case 128: return launch_bwd<128>(a, tm, tmdO, s);
+    case 64: return launch_bwd<64>(a, tm, tmdO, grid, s);
+    case 128: return launch_bwd<128>(a, tm, tmdO, grid, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "bwd_tc: head_dim %d", a.d.D);
   }
 }

@@ -80,7 +80,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, FwdArgs a, const int32_t* __restrict__ order) {
+                  const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int bh = blockIdx.x % a.d.BH;
-  const int m = order[blockIdx.x / a.d.BH];
+  // unsplit plan: item e is block row items[e].line, rows longest first
+  const int m = ((const PlanItem*)(a.plan + 4))[blockIdx.x / a.d.BH].line;
   const int S = a.d.S;
   const int j0 = a.row_ptr[m];
   const int nblk = a.row_ptr[m + 1] - j0;
@@ -325,14 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-bsr_status launch_fwd(const FwdArgs& a, const TensorMaps& tm, const int32_t* order, cudaStream_t s) {
+bsr_status launch_fwd(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
   using C = FwdCfg<D>;
   auto kern = fwd_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "fwd_tc: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
   dim3 grid(a.d.nb * a.d.BH);
   LaunchTimer timer("fwd_tc", s);
-  kern<<<grid, kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a, order);
+  kern<<<grid, kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
   return check_launch("fwd_tc launch");
 }
 
@@ -340,15 +341,15 @@ bsr_status launch_fwd(const FwdArgs& a, const TensorMaps& tm, const int32_t* ord
 
 bool tc_fwd_supported(const Dims& d) { return d.dtype == BSR_BF16 && (d.D == 64 || d.D == 128 || d.D == 256); }
 
-bsr_status launch_fwd_tc(const FwdArgs& a, const int32_t* order, cudaStream_t s) {
+bsr_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   if (a.d.D <= 128) return launch_fwd_tc2(a, s);
   TensorMaps tm;
   bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
   if (st != BSR_OK) return st;
   switch (a.d.D) {
-    case 64: return launch_fwd<64>(a, tm, order, s);
-    case 128: return launch_fwd<128>(a, tm, order, s);
-    case 256: return launch_fwd<256>(a, tm, order, s);
+    case 64: return launch_fwd<64>(a, tm, s);
+    case 128: return launch_fwd<128>(a, tm, s);
+    case 256: return launch_fwd<256>(a, tm, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "fwd_tc: head_dim %d", a.d.D);
   }
 }

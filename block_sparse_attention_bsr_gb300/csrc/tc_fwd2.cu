@@ -1,12 +1,15 @@
 // Tensor-core forward pass for bf16 operands with head_dim 64 / 128 on
 // sm_103a, with P kept in tensor memory.
 //
-// Same walk as the head_dim-256 kernel in tc_fwd.cu (one CTA per block row m
-// of one (batch, head); the row's stored blocks j in [row_ptr[m],
+// Same walk as the head_dim-256 kernel in tc_fwd.cu (for each block row m
+// of one (batch, head) the row's stored blocks j in [row_ptr[m],
 // row_ptr[m+1]) are visited in order and the K / V tiles of block column
 // col_idx[j] come straight from HBM by TMA; "trnsparse 0.7.0 -> 0.9.0" diff,
-// CHANGELOG [0.8.0], attn_fwd_static), with three changes that keep the
+// CHANGELOG [0.8.0], attn_fwd_static), with four changes that keep the
 // tensor pipe fed:
+//   * persistent CTAs, one per SM, walk the (row, head) work list longest
+//     row first (sched.cuh), prefetching the next row's tiles while the
+//     current one finishes;
 //   * P goes back to tensor memory as bf16 and the P.V MMA reads its A
 //     operand from there (no shared-memory round trip for P);
 //   * two softmax warpgroups split the 128 columns of each score tile; the
@@ -26,6 +29,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "sched.cuh"
 #include "sm100.cuh"
 #include "tc_common.h"
 
@@ -50,24 +54,36 @@ struct Fwd2Cfg {
   static constexpr int kVStages = D == 64 ? 4 : 2;
   static constexpr int kRedOff = kTile * (1 + kKStages + kVStages);
   static constexpr int kBarOff = kRedOff + 2 * 2 * 128 * 4;  // [parity][half][row] maxima
-  static constexpr int kSmem = kBarOff + 256 + 1024;
+  static constexpr int kSmem = kBarOff + 512 + 1024;
 };
 
 struct Bars {
   uint64_t q_full;
+  uint64_t q_empty;
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t pv_done;
   uint64_t final_mma;
   uint64_t red_full[2];  // both warpgroups' partial row values written (by parity)
+  uint64_t wg_sync[2];
   uint64_t k_full[4];
   uint64_t k_empty[4];
   uint64_t v_full[4];
   uint64_t v_empty[4];
+  RingSmem ring;
+  int merge_flag[2];
   uint32_t tmem_slot;
   int abort_flag;
 };
+
+// Partial result of one chunk of a split row (fp32): O (128 x D, relative to
+// the chunk's reference max) then, per column half and row, the chunk's
+// reference max, row sum and true max (log2 units) and a pad.
+template <int D>
+__host__ __device__ constexpr size_t fwd_part_floats() {
+  return (size_t)128 * D + 2 * 128 * 4;
+}
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* b, int* status) {
   bool ok = mbar_wait(bar, parity, &b->abort_flag, status);
@@ -94,14 +110,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = (Bars*)(sm + C::kBarOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.x % a.d.BH;
-  const int m = a.order[blockIdx.x / a.d.BH];
   const int S = a.d.S;
-  const int j0 = a.row_ptr[m];
-  const int nblk = a.row_ptr[m + 1] - j0;
+  const PlanLayout lay = plan_layout(a.plan, a.d.nb, (int)gridDim.x, a.d.BH);
+  const Walk walk{lay.items, a.d.BH, lay.header[0] * a.d.BH};
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], kSoftmax);
@@ -111,6 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->red_full[0], kSoftmax);
     mbar_init(&bars->red_full[1], kSoftmax);
+    mbar_init(&bars->wg_sync[0], 128);
+    mbar_init(&bars->wg_sync[1], 128);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bars->ring.full[i], 1);
+      mbar_init(&bars->ring.empty[i], 1 + kSoftmax / 32);
+    }
     for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -131,54 +152,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   volatile int* ab = &bars->abort_flag;
+  RingSmem* ring = &bars->ring;
 
   if (warp == 0) {
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       // ------------------------------------------------------ producer --
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const int qrow = bh * S + m * 128;
-      mbar_arrive_expect_tx(&bars->q_full, C::kTile);
-      for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(sQ + b * 16384, &tmQ, b * 64, qrow, &bars->q_full);
-      int k_issued = 0, v_issued = 0;
+      int kg = 0, vg = 0, q = 0, g = 0;
       bool ok = true;
-      for (int i = 0; ok && i < nblk; ++i) {
-        int n = a.col_idx[j0 + i];
-        if (n < 0 || n >= a.d.nb) {
-          atomicExch(a.status, kStatusDeviceCheck);
-          n = 0;
+      for (int t = 0; ok; ++t) {
+        int k;
+        if (!(ok = ring_put(ring, t, lay.header + 1, walk.total, &k, ab, a.status)) || k < 0) break;
+        Cursor cur;
+        walk.decode(k, cur);
+        if (cur.n == 0) continue;
+        // Q of a new item: the previous item's S MMAs must be done
+        if (!(ok = mbar_wait(&bars->q_empty, (q & 1) ^ 1, ab, a.status))) break;
+        const int qrow = cur.bh * S + cur.line * 128;
+        mbar_arrive_expect_tx(&bars->q_full, C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(sQ + b * 16384, &tmQ, b * 64, qrow, &bars->q_full);
+        ++q;
+        for (int j = 0; j < cur.n; ++j, ++g) {
+          int n = a.col_idx[cur.first + j];
+          if (n < 0 || n >= a.d.nb) {
+            atomicExch(a.status, kStatusDeviceCheck);
+            n = 0;
+          }
+          const int krow = cur.bh * S + n * 128;
+          const int ks = g % C::kKStages, vs = g % C::kVStages;
+          if (!(ok = mbar_wait(&bars->k_empty[ks], ((g / C::kKStages) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->k_full[ks], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(sK + ks * C::kTile + b * 16384, &tmK, b * 64, krow, &bars->k_full[ks]);
+          kg = g + 1;
+          if (!(ok = mbar_wait(&bars->v_empty[vs], ((g / C::kVStages) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->v_full[vs], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(sV + vs * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[vs]);
+          vg = g + 1;
         }
-        const int krow = bh * S + n * 128;
-        const int ks = i % C::kKStages, vs = i % C::kVStages;
-        if (!(ok = mbar_wait(&bars->k_empty[ks], ((i / C::kKStages) & 1) ^ 1, ab, a.status))) break;
-        mbar_arrive_expect_tx(&bars->k_full[ks], C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(sK + ks * C::kTile + b * 16384, &tmK, b * 64, krow, &bars->k_full[ks]);
-        k_issued = i + 1;
-        if (!(ok = mbar_wait(&bars->v_empty[vs], ((i / C::kVStages) & 1) ^ 1, ab, a.status))) break;
-        mbar_arrive_expect_tx(&bars->v_full[vs], C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(sV + vs * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[vs]);
-        v_issued = i + 1;
       }
       // drain: every copy issued must have landed before the CTA exits
-      drain_wait(&bars->q_full, 0);
-      for (int i = (k_issued > C::kKStages ? k_issued - C::kKStages : 0); i < k_issued; ++i)
+      if (q > 0) drain_wait(&bars->q_full, (q - 1) & 1);
+      for (int i = (kg > C::kKStages ? kg - C::kKStages : 0); i < kg; ++i)
         drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1);
-      for (int i = (v_issued > C::kVStages ? v_issued - C::kVStages : 0); i < v_issued; ++i)
+      for (int i = (vg > C::kVStages ? vg - C::kVStages : 0); i < vg; ++i)
         drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       // ----------------------------------------------------------- MMA --
+      // S of block g+1 (other TMEM buffer) is issued before P.V of block g.
       const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
       const uint32_t idPV = instr_desc(1, 0, 1, D, 128);
       const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(&bars->q_full, 0, ab, a.status);
-      auto issue_s = [&](int i) -> bool {
+      auto issue_s = [&](const Cursor& c) -> bool {
+        const int i = c.g;
         const int ks = i % C::kKStages;
         const int b = i & 1;
+        if (c.i == 0 && !mbar_wait(&bars->q_full, c.q & 1, ab, a.status)) return false;
         if (!mbar_wait(&bars->k_full[ks], (i / C::kKStages) & 1, ab, a.status)) return false;
         if (!mbar_wait(&bars->s_free[b], ((i >> 1) & 1) ^ 1, ab, a.status)) return false;
         tc_fence_after();
@@ -190,11 +224,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars->k_empty[ks]);
         mma_commit(&bars->s_full[b]);
+        if (c.i == c.n - 1) mma_commit(&bars->q_empty);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int i = 0; ok && i < nblk; ++i) {
-        if (i + 1 < nblk && !(ok = issue_s(i + 1))) break;
+      bool ok = true;
+      auto seek_a = [&](Cursor& c) {
+        while (true) {
+          int k;
+          if (!(ok = ring_get(ring, c.t, &k, ab, a.status)) || k < 0) {
+            c.done = true;
+            return;
+          }
+          walk.decode(k, c);
+          if (c.n > 0) {
+            c.i = 0;
+            return;
+          }
+          ++c.t;
+        }
+      };
+      auto seek_b = [&](Cursor& c) {
+        while (true) {
+          const int k = *(volatile int32_t*)&ring->k[c.t % kRing];
+          if (k < 0) {
+            c.done = true;
+            return;
+          }
+          walk.decode(k, c);
+          if (c.n > 0) {
+            c.i = 0;
+            return;
+          }
+          ring_release(ring, c.t);
+          ++c.t;
+        }
+      };
+      auto next_a = [&](Cursor& c) {
+        ++c.g;
+        if (++c.i == c.n) {
+          ++c.q;
+          ++c.t;
+          seek_a(c);
+        }
+      };
+      Cursor A{0, 0, 0, 0, 0, 0, 0, 0, 0, false};
+      seek_a(A);
+      Cursor B = A;
+      if (ok && !A.done) {
+        if ((ok = issue_s(A))) next_a(A);
+      }
+      while (ok && !B.done) {
+        if (!A.done) {
+          if (!(ok = issue_s(A))) break;
+          next_a(A);
+          if (!ok) break;
+        }
+        const int i = B.g;
         const int vs = i % C::kVStages;
         if (!(ok = mbar_wait(&bars->p_full, i & 1, ab, a.status))) break;
         if (!(ok = mbar_wait(&bars->v_full[vs], (i / C::kVStages) & 1, ab, a.status))) break;
@@ -203,115 +288,146 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8, smem_desc(vb + kk * 2048, 16384, 1024), idPV,
-                      (i > 0 || kk > 0) ? 1u : 0u);
+                      (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->v_empty[vs]);
         mma_commit(&bars->pv_done);
+        ++B.g;
+        if (++B.i == B.n) {
+          ring_release(ring, B.t);
+          ++B.q;
+          ++B.t;
+          seek_b(B);
+        }
       }
       mma_commit(&bars->final_mma);
       drain_wait(&bars->final_mma, 0);
     }
   } else {
     // -------------------------------------------------------- softmax --
-    const int g = (warp - 2) / 4;  // column half
+    const int hg = (warp - 2) / 4;  // column half
     const int wl = warp % 4;
     const int r = wl * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
     const float sl2 = a.d.scale * kLog2e;
-    float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+    int g = 0;  // blocks processed by this CTA
+    int x = 0;  // exchanges through sRed (both warpgroups take part in each)
+    int sync_phase = 0;
     bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
-      const int b = i & 1;
-      if (!(ok = warp_wait(&bars->s_full[b], (i >> 1) & 1, bars, a.status))) break;
-      tc_fence_after();
-      float t[64];
-      {
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tmem + lane_base + b * 128 + g * 64, v0);
-        tmem_ld32(tmem + lane_base + b * 128 + g * 64 + 32, v1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          t[k] = __uint_as_float(v0[k]) * sl2;
-          t[32 + k] = __uint_as_float(v1[k]) * sl2;
+    // Combines a per-row value of the two column halves through shared
+    // memory (two buffers by exchange parity: no thread gets more than one
+    // exchange ahead, since each waits for all 256 softmax threads).
+    auto exchange = [&](float v, float* other) -> bool {
+      float* red = sRed + (x & 1) * 256;
+      red[hg * 128 + r] = v;
+      mbar_arrive(&bars->red_full[x & 1]);
+      const bool good = warp_wait(&bars->red_full[x & 1], (x >> 1) & 1, bars, a.status);
+      if (good) *other = red[(hg ^ 1) * 128 + r];
+      ++x;
+      return good;
+    };
+    for (int t = 0; ok; ++t) {
+      int k = -1;
+      if (lane == 0) ok = ring_get(ring, t, &k, ab, a.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      k = __shfl_sync(0xffffffffu, k, 0);
+      if (!ok || k < 0) break;
+      Cursor cur;
+      walk.decode(k, cur);
+      const int nblk = cur.n;
+      const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
+      __nv_bfloat16* orow = (__nv_bfloat16*)a.O + grow * D + hg * (D / 2);
+      if (nblk == 0) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < D / 16; ++c) ((uint4*)orow)[c] = z;
+        if (hg == 0) {
+          a.row_max[grow] = -INFINITY;
+          a.row_denom[grow] = 0.f;
         }
+        __syncwarp();
+        if (lane == 0) ring_release(ring, t);
+        continue;
       }
-      tc_fence_before();
-      mbar_arrive(&bars->s_free[b]);
-      float mx = t[0];
-#pragma unroll
-      for (int k = 1; k < 64; ++k) mx = fmaxf(mx, t[k]);
-      // combine the two column halves of the row through shared memory (two
-      // buffers by block parity: no thread runs more than one block ahead,
-      // since each exchange waits for all 256 softmax threads)
-      float* red = sRed + (i & 1) * 256;
-      red[g * 128 + r] = mx;
-      mbar_arrive(&bars->red_full[i & 1]);
-      if (!(ok = warp_wait(&bars->red_full[i & 1], (i >> 1) & 1, bars, a.status))) break;
-      mx = fmaxf(mx, red[(g ^ 1) * 128 + r]);
-      m_true = fmaxf(m_true, mx);
-      if (i > 0) {
-        // PV of the previous block must be done before O is rescaled or P overwritten
-        if (!(ok = warp_wait(&bars->pv_done, (i - 1) & 1, bars, a.status))) break;
+      float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+      for (int i = 0; i < nblk; ++i, ++g) {
+        const int b = g & 1;
+        if (!(ok = warp_wait(&bars->s_full[b], (g >> 1) & 1, bars, a.status))) break;
         tc_fence_after();
-        const bool need = mx - m_ref > kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = fmaxf(m_ref, mx);
-          const float alpha = ex2(m_ref - m_new);
-          l *= alpha;
-          m_ref = m_new;
-#pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t v[32];
-            const uint32_t ta = tmem + lane_base + kColO + g * (D / 2) + c * 32;
-            tmem_ld32(ta, v);
-            tmem_wait_ld();
+        float tt[64];
+        {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tmem + lane_base + b * 128 + hg * 64, v0);
+          tmem_ld32(tmem + lane_base + b * 128 + hg * 64 + 32, v1);
+          tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st32(ta, v);
+          for (int k = 0; k < 32; ++k) {
+            tt[k] = __uint_as_float(v0[k]) * sl2;
+            tt[32 + k] = __uint_as_float(v1[k]) * sl2;
           }
         }
-      } else {
-        m_ref = mx;
-      }
-      float sum = 0.f;
-      uint32_t pk[32];
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[b]);
+        float mx = tt[0];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float p0 = ex2(t[2 * k] - m_ref), p1 = ex2(t[2 * k + 1] - m_ref);
-        sum += p0 + p1;
-        pk[k] = pack_bf16x2(p0, p1);
+        for (int k = 1; k < 64; ++k) mx = fmaxf(mx, tt[k]);
+        float mo;
+        if (!(ok = exchange(mx, &mo))) break;
+        mx = fmaxf(mx, mo);
+        m_true = fmaxf(m_true, mx);
+        // P.V of the previous block (this row's or the previous row's) must
+        // be done before O is rescaled or P is overwritten
+        if (g > 0) {
+          if (!(ok = warp_wait(&bars->pv_done, (g - 1) & 1, bars, a.status))) break;
+          tc_fence_after();
+        }
+        if (i > 0) {
+          const bool need = mx - m_ref > kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(m_ref, mx);
+            const float alpha = ex2(m_ref - m_new);
+            l *= alpha;
+            m_ref = m_new;
+#pragma unroll 1
+            for (int c = 0; c < D / 64; ++c) {
+              uint32_t v[32];
+              const uint32_t ta = tmem + lane_base + kColO + hg * (D / 2) + c * 32;
+              tmem_ld32(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+              tmem_st32(ta, v);
+            }
+          }
+        } else {
+          m_ref = mx;
+        }
+        float sum = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p0 = ex2(tt[2 * k] - m_ref), p1 = ex2(tt[2 * k + 1] - m_ref);
+          sum += p0 + p1;
+          pk[k] = pack_bf16x2(p0, p1);
+        }
+        l += sum;
+        tmem_st32(tmem + lane_base + kColP + hg * 32, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);
       }
-      l += sum;
-      tmem_st32(tmem + lane_base + kColP + g * 32, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full);
-    }
-    // ------------------------------------------------------- epilogue --
-    const size_t grow = (size_t)bh * S + (size_t)m * 128 + r;
-    __nv_bfloat16* orow = (__nv_bfloat16*)a.O + grow * D + g * (D / 2);
-    if (nblk == 0) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int c = 0; c < D / 16; ++c) ((uint4*)orow)[c] = z;
-      if (g == 0) {
-        a.row_max[grow] = -INFINITY;
-        a.row_denom[grow] = 0.f;
-      }
-    } else if (ok) {
+      if (!ok) break;
+      // ----------------------------------------------------- epilogue --
       // total row sum: the two halves' partial sums share the reference max
-      float* red = sRed + (nblk & 1) * 256;
-      red[g * 128 + r] = l;
-      mbar_arrive(&bars->red_full[nblk & 1]);
-      ok = warp_wait(&bars->red_full[nblk & 1], (nblk >> 1) & 1, bars, a.status);
-      if (ok) l += red[(g ^ 1) * 128 + r];
-      if (ok) ok = warp_wait(&bars->pv_done, (nblk - 1) & 1, bars, a.status);
-      if (ok) {
-        tc_fence_after();
+      float lo;
+      if (!(ok = exchange(l, &lo))) break;
+      l += lo;
+      if (!(ok = warp_wait(&bars->pv_done, (g - 1) & 1, bars, a.status))) break;
+      tc_fence_after();
+      if (cur.slot < 0) {
         const float inv = 1.f / l;
 #pragma unroll 1
         for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kColO + g * (D / 2) + c * 32, v);
+          tmem_ld32(tmem + lane_base + kColO + hg * (D / 2) + c * 32, v);
           tmem_wait_ld();
           uint4* dst = (uint4*)(orow + c * 32);
 #pragma unroll
@@ -324,11 +440,79 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[q] = o;
           }
         }
-        if (g == 0) {
+        if (hg == 0) {
           a.row_max[grow] = m_true * kLn2;
           a.row_denom[grow] = l * ex2(m_ref - m_true);
         }
+      } else {
+        // chunk of a split row: publish O (relative to m_ref) and the row's
+        // statistics; the last chunk to arrive combines them:
+        //   M = max m_true_c,  w_c = 2^(m_ref_c - M),  l = sum l_c w_c,
+        //   O = sum w_c O_c / l
+        constexpr size_t kPart = fwd_part_floats<D>();
+        float* tile = a.part + ((size_t)cur.slot * a.d.BH + cur.bh) * kPart;
+        float* prow = tile + (size_t)r * D + hg * (D / 2);
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kColO + hg * (D / 2) + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ((float4*)(prow + c * 32))[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+        *(float4*)(tile + 128 * D + (hg * 128 + r) * 4) = make_float4(m_ref, l, m_true, 0.f);
+        bool last = false;
+        if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
+                                sync_phase, ab, a.status, &last)))
+          break;
+        if (last) {
+          const int sl = lay.slot_line[cur.slot];
+          const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
+          const float* t0 = a.part + ((size_t)base * a.d.BH + cur.bh) * kPart;
+          const size_t stride = (size_t)a.d.BH * kPart;  // next chunk, same head
+          float M = -INFINITY;
+          for (int ch = 0; ch < nc; ++ch) M = fmaxf(M, ld_partial(t0 + ch * stride + 128 * D + (hg * 128 + r) * 4).z);
+          float lsum = 0.f;
+          for (int ch = 0; ch < nc; ++ch) {
+            const float4 st = ld_partial(t0 + ch * stride + 128 * D + (hg * 128 + r) * 4);
+            lsum += st.y * ex2(st.x - M);
+          }
+          const float inv = 1.f / lsum;
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+            for (int ch = 0; ch < nc; ++ch) {
+              const float* src = t0 + ch * stride;
+              const float w = ex2(ld_partial(src + 128 * D + (hg * 128 + r) * 4).x - M) * inv;
+              const float* p = src + (size_t)r * D + hg * (D / 2) + c * 32;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 x4 = ld_partial(p + 4 * j);
+                acc[4 * j] = fmaf(w, x4.x, acc[4 * j]);
+                acc[4 * j + 1] = fmaf(w, x4.y, acc[4 * j + 1]);
+                acc[4 * j + 2] = fmaf(w, x4.z, acc[4 * j + 2]);
+                acc[4 * j + 3] = fmaf(w, x4.w, acc[4 * j + 3]);
+              }
+            }
+            uint4* dst = (uint4*)(orow + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(pack_bf16x2(acc[8 * j], acc[8 * j + 1]), pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
+                                  pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
+                                  pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+          }
+          if (hg == 0) {
+            a.row_max[grow] = M * kLn2;
+            a.row_denom[grow] = lsum;
+          }
+        }
       }
+      __syncwarp();
+      if (lane == 0) ring_release(ring, t);
     }
   }
 
@@ -345,12 +529,18 @@ bsr_status launch(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess)
     return fail(BSR_ERR_CUDA, "fwd_tc: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
+  const int grid = tc_grid(a.d);
+  if (grid <= 0) return fail(BSR_ERR_CUDA, "fwd_tc: cannot query the SM count");
   LaunchTimer timer("fwd_tc", s);
-  kern<<<dim3(a.d.nb * a.d.BH), kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
+  kern<<<grid, kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
   return check_launch("fwd_tc launch");
 }
 
 }  // namespace
+
+size_t fwd_part_bytes(int D) {
+  return sizeof(float) * (D == 64 ? fwd_part_floats<64>() : fwd_part_floats<128>());
+}
 
 bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s) {
   TensorMaps tm;

@@ -123,10 +123,11 @@ bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tens
  * because another allocator already owns the device's memory (a framework's
  * caching allocator, a serving runtime's pools) or because their hot path
  * must not call into the CUDA allocator.  Same arguments, results and errors
- * as bsr_attn_bwd, but its scratch (delta and log-sum-exp per row) comes
- * from a fixed array in the library's static device memory (8 MiB per GPU
- * that loads the library, held until the process exits) instead of
- * cudaMallocAsync.
+ * as bsr_attn_bwd, but its scratch (delta and log-sum-exp per row, and the
+ * two work lists) comes from a fixed array in the library's static device
+ * memory (8.5 MiB per GPU that loads the library, held until the process
+ * exits) instead of cudaMallocAsync.  Long block rows / columns are not
+ * split into chunks on this path (that would need partial-result buffers).
  * Limits: batch * heads * seq <= 1,048,576, else BSR_ERR_INVALID_ARG.
  * All calls share the array: calls whose kernels overlap on the GPU race, so
  * order them on one stream.  The first call on a device (with that device
