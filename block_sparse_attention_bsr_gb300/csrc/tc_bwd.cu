@@ -131,8 +131,11 @@ template <int D>
 struct DqCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTile = 128 * D * 2;
-  static constexpr int kStages = D == 64 ? 4 : 2;
-  static constexpr int kBarOff = kTile * (2 + 2 * kStages);
+  // K_g is held until dQ_g (the last MMA of block g) and is needed again
+  // right after it, so it gets one stage more than V.
+  static constexpr int kKStages = D == 64 ? 4 : 3;
+  static constexpr int kVStages = D == 64 ? 4 : 2;
+  static constexpr int kBarOff = kTile * (2 + kKStages + kVStages);
   static constexpr int kSmem = kBarOff + 512 + 1024;
 };
 
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = sm;
   uint8_t* sdO = sQ + C::kTile;
   uint8_t* sK = sdO + C::kTile;
-  uint8_t* sV = sK + C::kStages * C::kTile;
+  uint8_t* sV = sK + C::kKStages * C::kTile;
   DqBars* bars = (DqBars*)(sm + C::kBarOff);
   constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
 
@@ -184,9 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->wg_sync[0], 128);
     mbar_init(&bars->wg_sync[1], 128);
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ producer --
-      int g = 0, q = 0;
+      int g = 0, q = 0, kg = 0, vg = 0;
       bool ok = true;
       for (int t = 0; ok; ++t) {
         int k;
@@ -235,27 +240,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             n = 0;
           }
           const int krow = cur.bh * S + n * 128;
-          const int st = g % C::kStages;
-          const uint32_t use = g / C::kStages;
-          if (!(ok = mbar_wait(&bars->k_empty[st], (use & 1) ^ 1, ab, a.status))) break;
-          mbar_arrive_expect_tx(&bars->k_full[st], C::kTile);
+          const int ks = g % C::kKStages, vs = g % C::kVStages;
+          if (!(ok = mbar_wait(&bars->k_empty[ks], ((g / C::kKStages) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->k_full[ks], C::kTile);
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_2d(sK + st * C::kTile + b * 16384, &tmK, b * 64, krow, &bars->k_full[st]);
-          if (!(ok = mbar_wait(&bars->v_empty[st], (use & 1) ^ 1, ab, a.status))) {
-            ++g;  // this block's K was issued, its V was not
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->v_full[st], C::kTile);
+            tma_load_2d(sK + ks * C::kTile + b * 16384, &tmK, b * 64, krow, &bars->k_full[ks]);
+          kg = g + 1;
+          if (!(ok = mbar_wait(&bars->v_empty[vs], ((g / C::kVStages) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->v_full[vs], C::kTile);
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_2d(sV + st * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[st]);
+            tma_load_2d(sV + vs * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[vs]);
+          vg = g + 1;
         }
       }
       // drain: every copy issued must land before the CTA exits
       if (q > 0) drain_wait(&bars->qd_full, (q - 1) & 1);
-      for (int i = (g > C::kStages ? g - C::kStages : 0); i < g; ++i) {
-        drain_wait(&bars->k_full[i % C::kStages], (i / C::kStages) & 1);
-        drain_wait(&bars->v_full[i % C::kStages], (i / C::kStages) & 1);
-      }
+      for (int i = (kg > C::kKStages ? kg - C::kKStages : 0); i < kg; ++i)
+        drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1);
+      for (int i = (vg > C::kVStages ? vg - C::kVStages : 0); i < vg; ++i)
+        drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -300,14 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto issue_sdp = [&](const Cursor& c) -> bool {
-        const int st = c.g % C::kStages;
-        const uint32_t use = c.g / C::kStages;
+        const int ks = c.g % C::kKStages, vs = c.g % C::kVStages;
         if (c.i == 0 && !mbar_wait(&bars->qd_full, c.q & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->k_full[st], use & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->v_full[st], use & 1, ab, a.status)) return false;
+        if (!mbar_wait(&bars->k_full[ks], (c.g / C::kKStages) & 1, ab, a.status)) return false;
+        if (!mbar_wait(&bars->v_full[vs], (c.g / C::kVStages) & 1, ab, a.status)) return false;
         if (!mbar_wait(&bars->sdp_free, (c.g & 1) ^ 1, ab, a.status)) return false;
         tc_fence_after();
-        const uint32_t kb = aK + st * C::kTile, vb = aV + st * C::kTile;
+        const uint32_t kb = aK + ks * C::kTile, vb = aV + vs * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16_ss(tmem + kColDP, smem_desc(adO + off, 16, 1024), smem_desc(vb + off, 16, 1024), idS, kk > 0);
         }
-        mma_commit(&bars->v_empty[st]);
+        mma_commit(&bars->v_empty[vs]);
         mma_commit(&bars->sdp_full);
         if (c.i == c.n - 1) mma_commit(&bars->qd_empty);
         return true;
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           next_a(A);
           if (!ok) break;
         }
-        const int st = B.g % C::kStages;
+        const int st = B.g % C::kKStages;
         if (!(ok = mbar_wait(&bars->ds_full, B.g & 1, ab, a.status))) break;
         tc_fence_after();
         const uint32_t kb = aK + st * C::kTile;
@@ -396,8 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld64(tmem + lane_base + kColDP + hg * 64, dp);
           tc_fence_before();
           mbar_arrive(&bars->sdp_free);
+          const float2 sc = make_float2(sl2, sl2), nl = make_float2(-lse2, -lse2), nd = make_float2(-dl, -dl);
 #pragma unroll
-          for (int j = 0; j < 64; ++j) s[j] = ex2(fmaf(s[j], sl2, -lse2)) * (dp[j] - dl);
+          for (int j = 0; j < 32; ++j) {
+            const float2 x = fma2(make_float2(s[2 * j], s[2 * j + 1]), sc, nl);
+            const float2 y = mul2(make_float2(ex2(x.x), ex2(x.y)), add2(make_float2(dp[2 * j], dp[2 * j + 1]), nd));
+            s[2 * j] = y.x;
+            s[2 * j + 1] = y.y;
+          }
           if (g > 0 && !(ok = warp_wait(&bars->dq_done, (g - 1) & 1, ab, a.status))) break;
           tc_fence_after();
           tmem_st_bf16x64(tmem + lane_base + kColDS + hg * 32, s);
@@ -476,8 +484,13 @@ struct DkvCfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr int kOp = 128 * 128 * 2;  // dS^T tile
-  static constexpr int kBarOff = kTile * (2 + 2 * kStages) + kOp;
-  static constexpr int kSmem = kBarOff + 512 + 1024;
+  static constexpr int kStatOff = kTile * (2 + 2 * kStages) + kOp;
+  static constexpr int kStat = 2 * 128 * 4;  // lse2 and delta of one block row's 128 queries
+  static constexpr int kBarOff = kStatOff + kStages * kStat;
+  // The dynamic shared memory base is 1024-byte aligned (checked at run
+  // time), so this kernel, which needs almost all of the 227 KB, keeps no
+  // alignment slack.
+  static constexpr int kSmem = kBarOff + 384;
 };
 
 struct DkvBars {
@@ -485,7 +498,8 @@ struct DkvBars {
   uint64_t kv_empty;
   uint64_t st_full;
   uint64_t st_free;
-  uint64_t pds_full;
+  uint64_t pt_ready;
+  uint64_t ds_ready;
   uint64_t pt_free;
   uint64_t dst_free;
   uint64_t final_mma;
@@ -551,12 +565,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, BwdArgs a) {
   using C = DkvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  if (smem_u32(smem_raw) & 1023) {  // no slack for re-alignment: refuse (uniform, before any barrier)
+    if (threadIdx.x == 0) atomicExch(a.status, kStatusDeviceCheck);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   uint8_t* sK = sm;
   uint8_t* sV = sK + C::kTile;
   uint8_t* sQ = sV + C::kTile;
   uint8_t* sdO = sQ + C::kStages * C::kTile;
   uint8_t* sDST = sdO + C::kStages * C::kTile;
+  float* sStat = (float*)(sm + C::kStatOff);  // [stage][lse2 | delta][128]
   DkvBars* bars = (DkvBars*)(sm + C::kBarOff);
   // P^T (bf16) is written over the dP^T columns each warpgroup has read:
   // queries [0, 64) at column 128, queries [64, 128) at column 192.
@@ -572,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->kv_empty, 1);
     mbar_init(&bars->st_full, 1);
     mbar_init(&bars->st_free, kEw);
-    mbar_init(&bars->pds_full, kEw);
+    mbar_init(&bars->pt_ready, kEw);
+    mbar_init(&bars->ds_ready, kEw);
     mbar_init(&bars->pt_free, 1);
     mbar_init(&bars->dst_free, 1);
     mbar_init(&bars->final_mma, 1);
@@ -632,9 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = g % C::kStages;
           const uint32_t use = g / C::kStages;
           if (!(ok = mbar_wait(&bars->q_empty[st], (use & 1) ^ 1, ab, a.status))) break;
-          mbar_arrive_expect_tx(&bars->q_full[st], C::kTile);
+          mbar_arrive_expect_tx(&bars->q_full[st], C::kTile + C::kStat);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_2d(sQ + st * C::kTile + b * 16384, &tmQ, b * 64, qrow, &bars->q_full[st]);
+          bulk_load(sStat + st * 256, a.lse2 + qrow, 512, &bars->q_full[st]);
+          bulk_load(sStat + st * 256 + 128, a.delta + qrow, 512, &bars->q_full[st]);
           if (!(ok = mbar_wait(&bars->do_empty[st], (use & 1) ^ 1, ab, a.status))) {
             ++g;
             break;
@@ -656,7 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Per block g: S^T_g and dP^T_g land before the elementwise pass; the
       // elementwise pass reads both and releases them (st_free), so
       // S^T_{g+1} (cursor A) is issued while it computes; P^T_g comes back
-      // over the dP^T columns, so dP^T_{g+1} waits for dV_g (pt_free).
+      // over the dP^T columns (pt_ready) and dV_g starts while dS^T_g is
+      // still being computed; dP^T_{g+1} waits for dV_g (pt_free).
       const uint32_t idST = instr_desc(1, 0, 0, 128, 128);
       const uint32_t idG = instr_desc(1, 0, 1, D, 128);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
@@ -740,14 +763,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(&bars->st_free, B.g & 1, ab, a.status))) break;
           if (!(ok = issue_st(A))) break;
         }
-        if (!(ok = mbar_wait(&bars->pds_full, B.g & 1, ab, a.status))) break;
-        tc_fence_after();
         const uint32_t qb = aQ + st * C::kTile, gb = adO + st * C::kTile;
+        // dV as soon as P^T is in TMEM (its completion frees the dP^T columns
+        // for the next block); dK once dS^T is in shared memory
+        if (!(ok = mbar_wait(&bars->pt_ready, B.g & 1, ab, a.status))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ts(tmem + kColDV, tmem + kColDPT + kk * 8 + (kk >= 4 ? 32 : 0),
                       smem_desc(gb + kk * 2048, 16384, 1024), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->do_empty[st]);
         mma_commit(&bars->pt_free);
+        if (!(ok = mbar_wait(&bars->ds_ready, B.g & 1, ab, a.status))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -755,7 +783,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (B.i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars->q_empty[st]);
-        mma_commit(&bars->do_empty[st]);
         mma_commit(&bars->dst_free);
         if (!A.done) {
           if (!(ok = mbar_wait(&bars->pt_free, B.g & 1, ab, a.status))) break;
@@ -800,11 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         zero_cols<D / 2>(dvrow);
       } else {
         for (int i = 0; i < cur.n; ++i, ++g) {
-          int m = a.row_idx[cur.first + i];
-          m = (m < 0 || m >= a.d.nb) ? 0 : m;
-          const size_t q0 = (size_t)cur.bh * S + (size_t)m * 128 + hg * 64;
-          const float4* lse4 = (const float4*)(a.lse2 + q0);
-          const float4* dl4 = (const float4*)(a.delta + q0);
+          const int st = g % C::kStages;
           if (!(ok = warp_wait(&bars->st_full, g & 1, ab, a.status))) break;
           tc_fence_after();
           float s[64], dp[64];
@@ -812,28 +835,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld64(tmem + lane_base + kColDPT + hg * 64, dp);
           tc_fence_before();
           mbar_arrive(&bars->st_free);
+          // statistics of this block row's queries, brought in with Q (q_full
+          // completed before S^T_g was issued)
+          const float* lse = sStat + st * 256 + hg * 64;
+          const float* dl = lse + 128;
+          const float2 sc = make_float2(sl2, sl2);
 #pragma unroll
-          for (int k4 = 0; k4 < 16; ++k4) {
-            const float4 l = __ldg(lse4 + k4), d = __ldg(dl4 + k4);
-            s[4 * k4 + 0] = ex2(fmaf(s[4 * k4 + 0], sl2, -l.x));
-            s[4 * k4 + 1] = ex2(fmaf(s[4 * k4 + 1], sl2, -l.y));
-            s[4 * k4 + 2] = ex2(fmaf(s[4 * k4 + 2], sl2, -l.z));
-            s[4 * k4 + 3] = ex2(fmaf(s[4 * k4 + 3], sl2, -l.w));
-            dp[4 * k4 + 0] = s[4 * k4 + 0] * (dp[4 * k4 + 0] - d.x);
-            dp[4 * k4 + 1] = s[4 * k4 + 1] * (dp[4 * k4 + 1] - d.y);
-            dp[4 * k4 + 2] = s[4 * k4 + 2] * (dp[4 * k4 + 2] - d.z);
-            dp[4 * k4 + 3] = s[4 * k4 + 3] * (dp[4 * k4 + 3] - d.w);
+          for (int k = 0; k < 32; ++k) {
+            const float2 l2 = *(const float2*)(lse + 2 * k);
+            const float2 x = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc, make_float2(-l2.x, -l2.y));
+            s[2 * k] = ex2(x.x);
+            s[2 * k + 1] = ex2(x.y);
           }
           // P^T over this warpgroup's own dP^T columns (already read above;
           // dV of the previous block finished before dP^T of this one began)
           tmem_st_bf16x64(tmem + lane_base + kColDPT + hg * 64, s);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->pt_ready);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float2 d2 = *(const float2*)(dl + 2 * k);
+            const float2 x = mul2(make_float2(s[2 * k], s[2 * k + 1]),
+                                  add2(make_float2(dp[2 * k], dp[2 * k + 1]), make_float2(-d2.x, -d2.y)));
+            dp[2 * k] = x.x;
+            dp[2 * k + 1] = x.y;
+          }
           if (g > 0 && !(ok = warp_wait(&bars->dst_free, (g - 1) & 1, ab, a.status))) break;
           st_row_chunk(aDST, r, 2 * hg, dp);
           st_row_chunk(aDST, r, 2 * hg + 1, dp + 32);
-          tmem_wait_st();
-          tc_fence_before();
           fence_proxy_async_smem();
-          mbar_arrive(&bars->pds_full);
+          mbar_arrive(&bars->ds_ready);
         }
         if (!ok) break;
         if (!(ok = warp_wait(&bars->dst_free, (g - 1) & 1, ab, a.status))) break;

@@ -17,8 +17,9 @@
 //   * S is double-buffered in TMEM, so S_{j+1} = Q K_{j+1}^T runs while the
 //     softmax of block j is computed.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
-// issuer, warps 2..9 two softmax warpgroups; thread (warp w, lane l) owns
+// Warp roles (352 threads): warp 0 TMA producer of Q and K, warp 10 TMA
+// producer of V, warp 1 TMEM owner and MMA issuer, warps 2..9 two softmax
+// warpgroups; thread (warp w, lane l) owns
 // query row 32 (w % 4) + l (its TMEM lane), warpgroup g = (w - 2) / 4 owns
 // columns [64 g, 64 g + 64) of the scores and half of O's columns.
 // TMEM columns: S buffers at 0 and 128, O at 256 (D columns), P at 384
@@ -38,7 +39,8 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;  // producer, MMA, 8 softmax warps, V producer
+constexpr int kWarpV = 10;
 constexpr int kSoftmax = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256, kColP = 384;
@@ -83,6 +85,20 @@ struct Bars {
 template <int D>
 __host__ __device__ constexpr size_t fwd_part_floats() {
   return (size_t)128 * D + 2 * 128 * 4;
+}
+
+// 2^x on the FMA pipe, for x <= 8: x = n + f with n = floor(x), f in [0, 1);
+// 2^f ~= 1 + f (c1 + f (c2 + f c3)), a cubic fitted to 2^f on [0, 1] by
+// iteratively reweighted least squares on the relative error (max relative
+// error 8.6e-5, well below the 2^-9 of the bf16 P it feeds); 2^n is added
+// to the exponent bits.  Arguments below -126 are clamped (the result there
+// is far below anything a bf16 P can hold next to the row maximum's 1).
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fmaxf(x, -126.f);
+  const float n = floorf(x);
+  const float f = x - n;
+  const float p = fmaf(fmaf(fmaf(0.0770655f, f, 0.22764668f), f, 0.6951164f), f, 1.f);
+  return __int_as_float(__float_as_int(p) + ((int)n << 23));
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* b, int* status) {
@@ -130,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->wg_sync[1], 128);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&bars->ring.full[i], 1);
-      mbar_init(&bars->ring.empty[i], 1 + kSoftmax / 32);
+      mbar_init(&bars->ring.empty[i], 2 + kSoftmax / 32);  // MMA, softmax warps, V producer
     }
     for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
@@ -160,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int kg = 0, vg = 0, q = 0, g = 0;
+      int kg = 0, q = 0, g = 0;
       bool ok = true;
       for (int t = 0; ok; ++t) {
         int k;
@@ -181,23 +197,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             n = 0;
           }
           const int krow = cur.bh * S + n * 128;
-          const int ks = g % C::kKStages, vs = g % C::kVStages;
+          const int ks = g % C::kKStages;
           if (!(ok = mbar_wait(&bars->k_empty[ks], ((g / C::kKStages) & 1) ^ 1, ab, a.status))) break;
           mbar_arrive_expect_tx(&bars->k_full[ks], C::kTile);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_2d(sK + ks * C::kTile + b * 16384, &tmK, b * 64, krow, &bars->k_full[ks]);
           kg = g + 1;
-          if (!(ok = mbar_wait(&bars->v_empty[vs], ((g / C::kVStages) & 1) ^ 1, ab, a.status))) break;
-          mbar_arrive_expect_tx(&bars->v_full[vs], C::kTile);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_2d(sV + vs * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[vs]);
-          vg = g + 1;
         }
       }
       // drain: every copy issued must have landed before the CTA exits
       if (q > 0) drain_wait(&bars->q_full, (q - 1) & 1);
       for (int i = (kg > C::kKStages ? kg - C::kKStages : 0); i < kg; ++i)
         drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1);
+    }
+  } else if (warp == kWarpV) {
+    if (lane == 0) {
+      // ---------------------------------------------------- V producer --
+      // V runs on its own thread so that K (needed first, by S) is never
+      // held back behind a V stage that is still in use by P.V.
+      int vg = 0, g = 0;
+      bool ok = true;
+      for (int t = 0; ok; ++t) {
+        int k;
+        if (!(ok = ring_get(ring, t, &k, ab, a.status)) || k < 0) break;
+        Cursor cur;
+        walk.decode(k, cur);
+        for (int j = 0; j < cur.n; ++j, ++g) {
+          int n = a.col_idx[cur.first + j];
+          n = (n < 0 || n >= a.d.nb) ? 0 : n;
+          const int krow = cur.bh * S + n * 128;
+          const int vs = g % C::kVStages;
+          if (!(ok = mbar_wait(&bars->v_empty[vs], ((g / C::kVStages) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->v_full[vs], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(sV + vs * C::kTile + b * 16384, &tmV, b * 64, krow, &bars->v_full[vs]);
+          vg = g + 1;
+        }
+        if (ok) ring_release(ring, t);
+      }
       for (int i = (vg > C::kVStages ? vg - C::kVStages : 0); i < vg; ++i)
         drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1);
     }
@@ -302,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars->final_mma);
       drain_wait(&bars->final_mma, 0);
     }
-  } else {
+  } else if (warp < kWarpV) {
     // -------------------------------------------------------- softmax --
     const int hg = (warp - 2) / 4;  // column half
     const int wl = warp % 4;
@@ -358,57 +395,79 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_base + b * 128 + hg * 64, v0);
           tmem_ld32(tmem + lane_base + b * 128 + hg * 64 + 32, v1);
           tmem_wait_ld();
+          const float2 sc = make_float2(sl2, sl2);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            tt[k] = __uint_as_float(v0[k]) * sl2;
-            tt[32 + k] = __uint_as_float(v1[k]) * sl2;
+          for (int k = 0; k < 16; ++k) {
+            const float2 x0 = mul2(make_float2(__uint_as_float(v0[2 * k]), __uint_as_float(v0[2 * k + 1])), sc);
+            const float2 x1 = mul2(make_float2(__uint_as_float(v1[2 * k]), __uint_as_float(v1[2 * k + 1])), sc);
+            tt[2 * k] = x0.x;
+            tt[2 * k + 1] = x0.y;
+            tt[32 + 2 * k] = x1.x;
+            tt[32 + 2 * k + 1] = x1.y;
           }
         }
         tc_fence_before();
         mbar_arrive(&bars->s_free[b]);
-        float mx = tt[0];
+        // row maximum of this half: eight independent chains, then a tree
+        float m8[8];
 #pragma unroll
-        for (int k = 1; k < 64; ++k) mx = fmaxf(mx, tt[k]);
+        for (int k = 0; k < 8; ++k) m8[k] = tt[k];
+#pragma unroll
+        for (int k = 8; k < 64; ++k) m8[k & 7] = fmaxf(m8[k & 7], tt[k]);
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         float mo;
         if (!(ok = exchange(mx, &mo))) break;
         mx = fmaxf(mx, mo);
         m_true = fmaxf(m_true, mx);
+        // The reference max depends only on the scores, so it is settled
+        // (and the exponentials computed) before waiting for the previous
+        // block's P.V; only the O rescale and the P store have to wait.
+        float alpha = 1.f;
+        bool rescale = false;
+        if (i > 0) {
+          const bool need = mx - m_ref > kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(m_ref, mx);
+            alpha = ex2(m_ref - m_new);
+            l *= alpha;
+            m_ref = m_new;
+            rescale = true;
+          }
+        } else {
+          m_ref = mx;
+        }
+        float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+        uint32_t pk[32];
+        const float2 nm = make_float2(-m_ref, -m_ref);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 x = add2(make_float2(tt[2 * k], tt[2 * k + 1]), nm);
+          // one pair in four on the FMA pipe, the rest on MUFU (ex2)
+          const float2 p = (k & 3) == 3 ? make_float2(exp2_poly(x.x), exp2_poly(x.y)) : make_float2(ex2(x.x), ex2(x.y));
+          sum4[k & 3] = add2(sum4[k & 3], p);
+          pk[k] = pack_bf16x2(p.x, p.y);
+        }
+        l += (sum4[0].x + sum4[0].y + sum4[1].x + sum4[1].y) + (sum4[2].x + sum4[2].y + sum4[3].x + sum4[3].y);
         // P.V of the previous block (this row's or the previous row's) must
         // be done before O is rescaled or P is overwritten
         if (g > 0) {
           if (!(ok = warp_wait(&bars->pv_done, (g - 1) & 1, bars, a.status))) break;
           tc_fence_after();
         }
-        if (i > 0) {
-          const bool need = mx - m_ref > kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            const float m_new = fmaxf(m_ref, mx);
-            const float alpha = ex2(m_ref - m_new);
-            l *= alpha;
-            m_ref = m_new;
+        if (rescale) {
 #pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {
-              uint32_t v[32];
-              const uint32_t ta = tmem + lane_base + kColO + hg * (D / 2) + c * 32;
-              tmem_ld32(ta, v);
-              tmem_wait_ld();
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t v[32];
+            const uint32_t ta = tmem + lane_base + kColO + hg * (D / 2) + c * 32;
+            tmem_ld32(ta, v);
+            tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-              tmem_st32(ta, v);
-            }
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tmem_st32(ta, v);
           }
-        } else {
-          m_ref = mx;
         }
-        float sum = 0.f;
-        uint32_t pk[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float p0 = ex2(tt[2 * k] - m_ref), p1 = ex2(tt[2 * k + 1] - m_ref);
-          sum += p0 + p1;
-          pk[k] = pack_bf16x2(p0, p1);
-        }
-        l += sum;
         tmem_st32(tmem + lane_base + kColP + hg * 32, pk);
         tmem_wait_st();
         tc_fence_before();
