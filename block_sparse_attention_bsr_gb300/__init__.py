@@ -142,7 +142,7 @@ def bsr_attn_bwd_noalloc(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, c
 
     For callers that cannot allocate: another allocator owns the device
     memory, or the hot path must not call the CUDA allocator.  Limited to
-    batch * heads * seq <= 1,048,576 (8.5 MiB of static device memory);
+    batch * heads * seq <= 1,048,576 (9 MiB of static device memory);
     calls that overlap on the GPU race.
     """
     lib = load_library()

@@ -180,6 +180,7 @@ extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, con
   cudaError_t e = cudaMallocAsync(&scratch, plan_bytes + part_bytes, s);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaMallocAsync: %s", cudaGetErrorString(e));
   a.plan = (int32_t*)scratch;
+  a.G = G;
   a.part = persistent ? (float*)((char*)scratch + plan_bytes) : nullptr;
   PlanArgs p{};
   p.list[0] = PlanList{row_ptr, a.plan};

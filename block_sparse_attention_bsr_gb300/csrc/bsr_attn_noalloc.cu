@@ -13,7 +13,7 @@
 //
 // Limits and rules:
 //  * The array holds 2 * kNoAllocMaxRows floats plus kNoAllocPlanWords ints
-//    for the two work lists (8.5 MiB in all), so batch * heads * seq must not
+//    for the two work lists (9 MiB in all), so batch * heads * seq must not
 //    exceed 1,048,576 (e.g. 128 heads at seq 8192); larger calls are
 //    rejected with BSR_ERR_INVALID_ARG.  Every GPU that loads the library
 //    keeps the array reserved until the process exits.
@@ -38,7 +38,7 @@ namespace {
 
 constexpr size_t kNoAllocMaxRows = size_t(1) << 20;
 
-constexpr size_t kNoAllocPlanWords = size_t(1) << 17;
+constexpr size_t kNoAllocPlanWords = size_t(1) << 18;
 
 static __device__ __align__(256) float g_noalloc_delta[2 * kNoAllocMaxRows + kNoAllocPlanWords];
 

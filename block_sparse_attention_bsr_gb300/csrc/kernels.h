@@ -32,6 +32,7 @@ struct FwdArgs {
   const int32_t* row_ptr;
   const int32_t* col_idx;
   int32_t* plan;          // block-row plan (plan.cu)
+  int G;                  // persistent CTAs the plan was built for
   float* part;            // partial results of split rows: O (128 x D) and 3 x 128 stats per tile
   int* status;
 };
@@ -70,21 +71,30 @@ struct PlanItem {
 };
 
 // Layout of one plan in device scratch (int32 units, 16-byte aligned base):
-//   header[4]                  items, work-queue counter, split lines, L
+//   header[4]                  items, work-queue counter, split lines, buckets
 //   items[cap_items]           PlanItem, longest first
+//   buckets[cap_buckets]       PlanBucket, one per item length, longest first
 //   slot_line[cap_slots]       split line of each partial slot
 //   line_base[cap_lines]       first slot of each split line
 //   line_chunks[cap_lines]     chunks of each split line
 //   counters[cap_lines*BH*2]   arrivals per (split line, head, column half)
 // Bounds: L >= nnzb * BH / G, so split lines <= G / BH and slots < 2 G / BH.
+struct PlanBucket {
+  int32_t work;   // first work index of the bucket (items before it times BH)
+  int32_t start;  // first item of the bucket
+  int32_t count;  // items in the bucket (all of one length)
+  int32_t len;
+};
+
 struct PlanLayout {
   int32_t* header;
   PlanItem* items;
+  PlanBucket* buckets;
   int32_t* slot_line;
   int32_t* line_base;
   int32_t* line_chunks;
   int32_t* counters;
-  int cap_items, cap_slots, cap_lines;
+  int cap_items, cap_slots, cap_lines, cap_buckets;
 };
 
 __host__ __device__ inline void plan_caps(int n, int G, int BH, int* items, int* slots, int* lines) {
@@ -97,16 +107,18 @@ __host__ __device__ inline void plan_caps(int n, int G, int BH, int* items, int*
 __host__ __device__ inline size_t plan_words(int n, int G, int BH) {
   int ci, cs, cl;
   plan_caps(n, G, BH, &ci, &cs, &cl);
-  size_t w = 4 + 4 * (size_t)ci + cs + 2 * (size_t)cl + 2 * (size_t)cl * BH;
+  size_t w = 4 + 4 * (size_t)ci + 4 * (size_t)(n + 1) + cs + 2 * (size_t)cl + 2 * (size_t)cl * BH;
   return (w + 3) & ~(size_t)3;
 }
 
 __host__ __device__ inline PlanLayout plan_layout(int32_t* base, int n, int G, int BH) {
   PlanLayout l;
   plan_caps(n, G, BH, &l.cap_items, &l.cap_slots, &l.cap_lines);
+  l.cap_buckets = n + 1;
   l.header = base;
   l.items = (PlanItem*)(base + 4);
-  l.slot_line = base + 4 + 4 * (size_t)l.cap_items;
+  l.buckets = (PlanBucket*)(base + 4 + 4 * (size_t)l.cap_items);
+  l.slot_line = (int32_t*)(l.buckets + l.cap_buckets);
   l.line_base = l.slot_line + l.cap_slots;
   l.line_chunks = l.line_base + l.cap_lines;
   l.counters = l.line_chunks + l.cap_lines;

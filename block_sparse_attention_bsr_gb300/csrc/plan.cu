@@ -6,9 +6,11 @@
 //     chunks of nearly equal length, L = max(8, ceil(nnzb * BH / G)) (G =
 //     persistent CTAs), so that no single item is longer than the average
 //     share of one CTA;
-//   * sorts the items by length, longest first (a counting sort: items of
-//     equal length may come out in any order, which changes the schedule but
-//     never a result);
+//   * sorts the items by length, longest first, lines ascending inside a
+//     length (a counting sort; the order changes the schedule, never a
+//     result), and records one bucket per length; the kernels read work
+//     index k of a bucket as head k / count, item k % count of the bucket
+//     (see sched.cuh);
 //   * gives each chunk of a split line a partial-result slot, and zeroes the
 //     per-(line, head, column half) arrival counters used by the last-arriver
 //     merge, and the work-queue counter.
@@ -67,11 +69,14 @@ __device__ void scan_desc(int* hist, int n, int* warp_sums) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
-  extern __shared__ int hist[];  // [n + 1]
+  extern __shared__ int sm_plan[];  // hist[n + 1], count[n + 1], len[n]
   __shared__ int warp_sums[32];
-  __shared__ int counts[3];      // items, split lines, slots
+  __shared__ int counts[3];         // items, split lines, slots
   const PlanList& L = p.list[blockIdx.x];
   const int n = p.n;
+  int* hist = sm_plan;
+  int* count = sm_plan + (n + 1);
+  int* lens = sm_plan + 2 * (n + 1);
   const int32_t* ptr = L.ptr;
   PlanLayout lay = plan_layout(L.plan, n, p.G, p.BH);
 
@@ -84,19 +89,34 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   if (lim < 8) lim = 8;
   const int Lmax = p.allow_split ? (int)(lim < n ? lim : n) : n;
 
-  // pass 1: histogram of chunk lengths; slots and split-line indices
+  // pass 1: histogram of chunk lengths
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int len = line_len(ptr, i, n);
+    lens[i] = len;
     const int nc = len > Lmax ? (len + Lmax - 1) / Lmax : 1;
     for (int c = 0; c < nc; ++c) atomicAdd(&hist[len / nc + (c < len % nc ? 1 : 0)], 1);
     atomicAdd(&counts[0], nc);
   }
   __syncthreads();
-  scan_desc(hist, n, warp_sums);
+  for (int v = threadIdx.x; v <= n; v += blockDim.x) count[v] = hist[v];
+  __syncthreads();
+  scan_desc(hist, n, warp_sums);  // hist[v] = first item of length v
+  // bucket table, longest first
+  if (threadIdx.x == 0) {
+    int nbk = 0;
+    for (int v = n; v >= 0; --v) {
+      if (count[v] == 0) continue;
+      lay.buckets[nbk] = PlanBucket{hist[v] * p.BH, hist[v], count[v], v};
+      ++nbk;
+    }
+    lay.header[3] = nbk;
+  }
 
-  // pass 2: place the items
+  // pass 2: place the items; inside a length bucket lines ascend (stable),
+  // so CTAs that start together work on neighbouring lines
+  const bool stable = n <= 2048;  // O(n^2 / threads) shared-memory reads
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int len = line_len(ptr, i, n);
+    const int len = lens[i];
     const int nc = len > Lmax ? (len + Lmax - 1) / Lmax : 1;
     int base = -1;
     if (nc > 1) {
@@ -114,7 +134,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
     int off = ptr[i];
     for (int c = 0; c < nc; ++c) {
       const int clen = len / nc + (c < len % nc ? 1 : 0);
-      const int pos = atomicAdd(&hist[clen], 1);
+      int pos;
+      if (stable) {
+        // items of length clen that come before (line i, chunk c) in line order
+        int before = 0;
+        for (int j = 0; j < i; ++j) {
+          const int lj = lens[j];
+          const int ncj = lj > Lmax ? (lj + Lmax - 1) / Lmax : 1;
+          const int bj = lj / ncj, rj = lj % ncj;
+          before += (clen == bj + 1 ? rj : 0) + (clen == bj ? ncj - rj : 0);
+        }
+        for (int c2 = 0; c2 < c; ++c2) before += (len / nc + (c2 < len % nc ? 1 : 0)) == clen ? 1 : 0;
+        pos = hist[clen] + before;
+      } else {
+        pos = atomicAdd(&hist[clen], 1);
+      }
       if (pos < lay.cap_items) lay.items[pos] = PlanItem{i, off, clen, base < 0 ? -1 : base + c};
       off += clen;
     }
@@ -128,14 +162,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
     lay.header[0] = items;
     lay.header[1] = 0;  // work-queue counter
     lay.header[2] = nsl;
-    lay.header[3] = Lmax;
   }
 }
 
 }  // namespace
 
 bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
-  const size_t smem = sizeof(int) * (size_t)(p.n + 1);
+  const size_t smem = sizeof(int) * (3 * (size_t)p.n + 2);
   if (smem > 200 * 1024) return fail(BSR_ERR_UNSUPPORTED, "plan: %d block rows exceed the planner's limit", p.n);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -45,18 +45,35 @@ struct Cursor {
 
 struct Walk {
   const PlanItem* items;
+  const PlanBucket* buckets;
+  int nbuckets;
   int BH;
   int total;  // items * BH
 
+  // Work index k -> (item, head).  Buckets of equal-length items come
+  // longest first; inside a bucket the heads are the slow index and the
+  // lines (ascending) the fast one, so CTAs working at the same time share a
+  // head and neighbouring lines, whose K / V / Q / dO tiles overlap in L2.
   __device__ __forceinline__ void decode(int k, Cursor& c) const {
-    const PlanItem it = items[k / BH];
-    c.bh = k % BH;
+    int lo = 0, hi = nbuckets - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (buckets[mid].work <= k) lo = mid; else hi = mid - 1;
+    }
+    const PlanBucket b = buckets[lo];
+    const int kp = k - b.work;
+    const PlanItem it = items[b.start + kp % b.count];
+    c.bh = kp / b.count;
     c.line = it.line;
     c.first = it.first;
     c.n = it.n;
     c.slot = it.slot;
   }
 };
+
+__device__ __forceinline__ Walk make_walk(const PlanLayout& lay, int BH) {
+  return Walk{lay.items, lay.buckets, lay.header[3], BH, lay.header[0] * BH};
+}
 
 // Producer side: draws the next work index into ring slot t % kRing once all
 // consumers released it; -1 marks the end.  Returns false on a timeout.

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
   const PlanLayout lay = plan_layout(a.row_plan, a.d.nb, (int)gridDim.x, a.d.BH);
-  const Walk walk{lay.items, a.d.BH, lay.header[0] * a.d.BH};
+  const Walk walk = make_walk(lay, a.d.BH);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->qd_full, 1);
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
   const PlanLayout lay = plan_layout(a.col_plan, a.d.nb, (int)gridDim.x, a.d.BH);
-  const Walk walk{lay.items, a.d.BH, lay.header[0] * a.d.BH};
+  const Walk walk = make_walk(lay, a.d.BH);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);

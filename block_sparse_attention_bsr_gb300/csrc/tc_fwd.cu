@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "sched.cuh"
 #include "sm100.cuh"
 #include "tc_common.h"
 
@@ -91,9 +92,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = (Bars*)(sm + C::kBarOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.x % a.d.BH;
-  // unsplit plan: item e is block row items[e].line, rows longest first
-  const int m = ((const PlanItem*)(a.plan + 4))[blockIdx.x / a.d.BH].line;
+  // unsplit plan: work index blockIdx.x is one (block row, head)
+  Cursor work;
+  make_walk(plan_layout(a.plan, a.d.nb, a.G, a.d.BH), a.d.BH).decode(blockIdx.x, work);
+  const int bh = work.bh;
+  const int m = work.line;
   const int S = a.d.S;
   const int j0 = a.row_ptr[m];
   const int nblk = a.row_ptr[m + 1] - j0;

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
   const PlanLayout lay = plan_layout(a.plan, a.d.nb, (int)gridDim.x, a.d.BH);
-  const Walk walk{lay.items, a.d.BH, lay.header[0] * a.d.BH};
+  const Walk walk = make_walk(lay, a.d.BH);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);

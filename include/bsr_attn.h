@@ -125,7 +125,7 @@ bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tens
  * must not call into the CUDA allocator.  Same arguments, results and errors
  * as bsr_attn_bwd, but its scratch (delta and log-sum-exp per row, and the
  * two work lists) comes from a fixed array in the library's static device
- * memory (8.5 MiB per GPU that loads the library, held until the process
+ * memory (9 MiB per GPU that loads the library, held until the process
  * exits) instead of cudaMallocAsync.  Long block rows / columns are not
  * split into chunks on this path (that would need partial-result buffers).
  * Limits: batch * heads * seq <= 1,048,576, else BSR_ERR_INVALID_ARG.
