@@ -261,8 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {
       // ----------------------------------------------------------- MMA --
+      // The whole warp walks the schedule (descriptor arithmetic stays
+      // warp-uniform); one elected lane issues the MMAs and commits.
+      const uint32_t leader = elect_one();
       // S / dP of block g+1 (cursor A) are issued before dQ of block g
       // (cursor B), so they run while the elementwise pass of block g
       // computes dS.  A draws items from the ring; B follows and releases
@@ -274,7 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto seek_a = [&](Cursor& c) {
         while (true) {
           int k;
-          if (!(ok = ring_get(ring, c.t, &k, ab, a.status)) || k < 0) {
+          int kk0 = -1;
+          bool good = true;
+          if (lane == 0) good = ring_get(ring, c.t, &kk0, ab, a.status);
+          ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+          k = __shfl_sync(0xffffffffu, kk0, 0);
+          if (!ok || k < 0) {
             c.done = true;
             return;
           }
@@ -298,31 +306,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             c.i = 0;
             return;
           }
-          ring_release(ring, c.t);
+          __syncwarp();
+          if (lane == 0) ring_release(ring, c.t);
           ++c.t;
         }
       };
       auto issue_sdp = [&](const Cursor& c) -> bool {
         const int ks = c.g % C::kKStages, vs = c.g % C::kVStages;
-        if (c.i == 0 && !mbar_wait(&bars->qd_full, c.q & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->k_full[ks], (c.g / C::kKStages) & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->v_full[vs], (c.g / C::kVStages) & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->sdp_free, (c.g & 1) ^ 1, ab, a.status)) return false;
+        if (c.i == 0 && !warp_wait(&bars->qd_full, c.q & 1, ab, a.status)) return false;
+        if (!warp_wait(&bars->k_full[ks], (c.g / C::kKStages) & 1, ab, a.status)) return false;
+        if (!warp_wait(&bars->v_full[vs], (c.g / C::kVStages) & 1, ab, a.status)) return false;
+        if (!warp_wait(&bars->sdp_free, (c.g & 1) ^ 1, ab, a.status)) return false;
         tc_fence_after();
         const uint32_t kb = aK + ks * C::kTile, vb = aV + vs * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColS, smem_desc(aQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
+          mma_bf16_ss_by(leader, tmem + kColS, smem_desc(aQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDP, smem_desc(adO + off, 16, 1024), smem_desc(vb + off, 16, 1024), idS, kk > 0);
+          mma_bf16_ss_by(leader, tmem + kColDP, smem_desc(adO + off, 16, 1024), smem_desc(vb + off, 16, 1024), idS, kk > 0);
         }
-        mma_commit(&bars->v_empty[vs]);
-        mma_commit(&bars->sdp_full);
-        if (c.i == c.n - 1) mma_commit(&bars->qd_empty);
+        mma_commit_by(leader, &bars->v_empty[vs]);
+        mma_commit_by(leader, &bars->sdp_full);
+        if (c.i == c.n - 1) mma_commit_by(leader, &bars->qd_empty);
         return true;
       };
       auto next_a = [&](Cursor& c) {
@@ -346,25 +355,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         const int st = B.g % C::kKStages;
-        if (!(ok = mbar_wait(&bars->ds_full, B.g & 1, ab, a.status))) break;
+        if (!(ok = warp_wait(&bars->ds_full, B.g & 1, ab, a.status))) break;
         tc_fence_after();
         const uint32_t kb = aK + st * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + kColDQ, tmem + kColDS + kk * 8, smem_desc(kb + kk * 2048, 16384, 1024), idDQ,
+          mma_bf16_ts_by(leader, tmem + kColDQ, tmem + kColDS + kk * 8, smem_desc(kb + kk * 2048, 16384, 1024), idDQ,
                       (B.i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->k_empty[st]);
-        mma_commit(&bars->dq_done);
+        mma_commit_by(leader, &bars->k_empty[st]);
+        mma_commit_by(leader, &bars->dq_done);
         ++B.g;
         if (++B.i == B.n) {
-          ring_release(ring, B.t);
+          __syncwarp();
+          if (lane == 0) ring_release(ring, B.t);
           ++B.q;
           ++B.t;
           seek_b(B);
         }
       }
-      mma_commit(&bars->final_mma);
-      drain_wait(&bars->final_mma, 0);
+      mma_commit_by(leader, &bars->final_mma);
+      if (leader) drain_wait(&bars->final_mma, 0);
+      __syncwarp();
     }
   } else {
     // ---------------------------------------------------- elementwise --
@@ -673,8 +684,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {
       // ----------------------------------------------------------- MMA --
+      // The whole warp walks the schedule (descriptor arithmetic stays
+      // warp-uniform); one elected lane issues the MMAs and commits.
+      const uint32_t leader = elect_one();
       // Per block g: S^T_g and dP^T_g land before the elementwise pass; the
       // elementwise pass reads both and releases them (st_free), so
       // S^T_{g+1} (cursor A) is issued while it computes; P^T_g comes back
@@ -688,7 +702,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto seek_a = [&](Cursor& c) {
         while (true) {
           int k;
-          if (!(ok = ring_get(ring, c.t, &k, ab, a.status)) || k < 0) {
+          int kk0 = -1;
+          bool good = true;
+          if (lane == 0) good = ring_get(ring, c.t, &kk0, ab, a.status);
+          ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+          k = __shfl_sync(0xffffffffu, kk0, 0);
+          if (!ok || k < 0) {
             c.done = true;
             return;
           }
@@ -712,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             c.i = 0;
             return;
           }
-          ring_release(ring, c.t);
+          __syncwarp();
+          if (lane == 0) ring_release(ring, c.t);
           ++c.t;
         }
       };
@@ -726,29 +746,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_st = [&](const Cursor& c) -> bool {
         const int st = c.g % C::kStages;
-        if (c.i == 0 && !mbar_wait(&bars->kv_full, c.q & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->q_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
+        if (c.i == 0 && !warp_wait(&bars->kv_full, c.q & 1, ab, a.status)) return false;
+        if (!warp_wait(&bars->q_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
         tc_fence_after();
         const uint32_t qb = aQ + st * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColST, smem_desc(aK + off, 16, 1024), smem_desc(qb + off, 16, 1024), idST, kk > 0);
+          mma_bf16_ss_by(leader, tmem + kColST, smem_desc(aK + off, 16, 1024), smem_desc(qb + off, 16, 1024), idST, kk > 0);
         }
         return true;
       };
       auto issue_dpt = [&](const Cursor& c) -> bool {
         const int st = c.g % C::kStages;
-        if (!mbar_wait(&bars->do_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
+        if (!warp_wait(&bars->do_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
         tc_fence_after();
         const uint32_t gb = adO + st * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDPT, smem_desc(aV + off, 16, 1024), smem_desc(gb + off, 16, 1024), idST, kk > 0);
+          mma_bf16_ss_by(leader, tmem + kColDPT, smem_desc(aV + off, 16, 1024), smem_desc(gb + off, 16, 1024), idST, kk > 0);
         }
-        mma_commit(&bars->st_full);
-        if (c.i == c.n - 1) mma_commit(&bars->kv_empty);
+        mma_commit_by(leader, &bars->st_full);
+        if (c.i == c.n - 1) mma_commit_by(leader, &bars->kv_empty);
         return true;
       };
       Cursor A{0, 0, 0, 0, 0, 0, 0, 0, 0, false};
@@ -760,46 +780,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && !B.done) {
         const int st = B.g % C::kStages;
         if (!A.done) {
-          if (!(ok = mbar_wait(&bars->st_free, B.g & 1, ab, a.status))) break;
+          if (!(ok = warp_wait(&bars->st_free, B.g & 1, ab, a.status))) break;
           if (!(ok = issue_st(A))) break;
         }
         const uint32_t qb = aQ + st * C::kTile, gb = adO + st * C::kTile;
         // dV as soon as P^T is in TMEM (its completion frees the dP^T columns
         // for the next block); dK once dS^T is in shared memory
-        if (!(ok = mbar_wait(&bars->pt_ready, B.g & 1, ab, a.status))) break;
+        if (!(ok = warp_wait(&bars->pt_ready, B.g & 1, ab, a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + kColDV, tmem + kColDPT + kk * 8 + (kk >= 4 ? 32 : 0),
+          mma_bf16_ts_by(leader, tmem + kColDV, tmem + kColDPT + kk * 8 + (kk >= 4 ? 32 : 0),
                       smem_desc(gb + kk * 2048, 16384, 1024), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->do_empty[st]);
-        mma_commit(&bars->pt_free);
-        if (!(ok = mbar_wait(&bars->ds_ready, B.g & 1, ab, a.status))) break;
+        mma_commit_by(leader, &bars->do_empty[st]);
+        mma_commit_by(leader, &bars->pt_free);
+        if (!(ok = warp_wait(&bars->ds_ready, B.g & 1, ab, a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDK, smem_desc(aDST + off, 16, 1024), smem_desc(qb + kk * 2048, 16384, 1024), idG,
+          mma_bf16_ss_by(leader, tmem + kColDK, smem_desc(aDST + off, 16, 1024), smem_desc(qb + kk * 2048, 16384, 1024), idG,
                       (B.i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bars->q_empty[st]);
-        mma_commit(&bars->dst_free);
+        mma_commit_by(leader, &bars->q_empty[st]);
+        mma_commit_by(leader, &bars->dst_free);
         if (!A.done) {
-          if (!(ok = mbar_wait(&bars->pt_free, B.g & 1, ab, a.status))) break;
+          if (!(ok = warp_wait(&bars->pt_free, B.g & 1, ab, a.status))) break;
           if (!(ok = issue_dpt(A))) break;
           next_a(A);
           if (!ok) break;
         }
         ++B.g;
         if (++B.i == B.n) {
-          ring_release(ring, B.t);
+          __syncwarp();
+          if (lane == 0) ring_release(ring, B.t);
           ++B.q;
           ++B.t;
           seek_b(B);
         }
       }
-      mma_commit(&bars->final_mma);
-      drain_wait(&bars->final_mma, 0);
+      mma_commit_by(leader, &bars->final_mma);
+      if (leader) drain_wait(&bars->final_mma, 0);
+      __syncwarp();
     }
   } else {
     // ---------------------------------------------------- elementwise --

@@ -5,25 +5,33 @@
 // of one (batch, head) the row's stored blocks j in [row_ptr[m],
 // row_ptr[m+1]) are visited in order and the K / V tiles of block column
 // col_idx[j] come straight from HBM by TMA; "trnsparse 0.7.0 -> 0.9.0" diff,
-// CHANGELOG [0.8.0], attn_fwd_static), with four changes that keep the
+// CHANGELOG [0.8.0], attn_fwd_static), with these changes that keep the
 // tensor pipe fed:
-//   * persistent CTAs, one per SM, walk the (row, head) work list longest
-//     row first (sched.cuh), prefetching the next row's tiles while the
-//     current one finishes;
-//   * P goes back to tensor memory as bf16 and the P.V MMA reads its A
-//     operand from there (no shared-memory round trip for P);
-//   * two softmax warpgroups split the 128 columns of each score tile; the
-//     row maximum is combined through shared memory;
-//   * S is double-buffered in TMEM, so S_{j+1} = Q K_{j+1}^T runs while the
-//     softmax of block j is computed.
+//   * persistent CTAs, one per SM, take (row, head) work items longest row
+//     first from a queue (sched.cuh) and prefetch the next item's Q (two Q
+//     buffers) and K / V tiles while the current one finishes;
+//   * the 128 keys of every block are split into two halves of 64, and each
+//     half has its own softmax warpgroup with its own online-softmax state
+//     (running reference max, row sum) and its own O accumulator
+//     O_h = sum_j P_hj V_hj.  The halves never talk to each other inside a
+//     row; once per row the two partial results are combined exactly like
+//     two chunks of a split row:  R = max(m_0, m_1),
+//     O = (2^(m_0 - R) O_0 + 2^(m_1 - R) O_1) / (2^(m_0 - R) l_0 + 2^(m_1 - R) l_1);
+//   * P goes back to tensor memory as bf16 (two buffers) and the P.V MMA
+//     reads its A operand from there;
+//   * S has one TMEM buffer, released as soon as both warpgroups have
+//     loaded their halves into registers, so S_{j+1} = Q K_{j+1}^T runs
+//     while the softmax of block j is computed and the MMA thread never
+//     waits for its own P.V.
 //
 // Warp roles (352 threads): warp 0 TMA producer of Q and K, warp 10 TMA
 // producer of V, warp 1 TMEM owner and MMA issuer, warps 2..9 two softmax
-// warpgroups; thread (warp w, lane l) owns
-// query row 32 (w % 4) + l (its TMEM lane), warpgroup g = (w - 2) / 4 owns
-// columns [64 g, 64 g + 64) of the scores and half of O's columns.
-// TMEM columns: S buffers at 0 and 128, O at 256 (D columns), P at 384
-// (64 columns of bf16 pairs).  All waits are bounded (see sm100.cuh).
+// warpgroups; thread (warp w, lane l) owns query row 32 (w % 4) + l (its
+// TMEM lane), warpgroup h = (w - 2) / 4 owns keys [64 h, 64 h + 64) of each
+// block and, in the final combine, output columns [h D / 2, h D / 2 + D / 2).
+// TMEM columns: S at 0 (half h at +64 h), bf16 P of block j at
+// 128 + 64 (j % 2) (half h at +32 h), O_0 at 256, O_1 at 256 + D.  All waits
+// are bounded (see sm100.cuh).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -43,7 +51,7 @@ constexpr int kThreads = 352;  // producer, MMA, 8 softmax warps, V producer
 constexpr int kWarpV = 10;
 constexpr int kSoftmax = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256, kColP = 384;
+constexpr uint32_t kColP = 128, kColO = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: stale max may lag by 2^8
@@ -52,22 +60,30 @@ template <int D>
 struct Fwd2Cfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTile = 128 * D * 2;
+  static constexpr int kQStages = 2;
   static constexpr int kKStages = D == 64 ? 4 : 3;
   static constexpr int kVStages = D == 64 ? 4 : 2;
-  static constexpr int kRedOff = kTile * (1 + kKStages + kVStages);
-  static constexpr int kBarOff = kRedOff + 2 * 2 * 128 * 4;  // [parity][half][row] maxima
-  static constexpr int kSmem = kBarOff + 512 + 1024;
+  static constexpr int kRedOff = kTile * (kQStages + kKStages + kVStages);
+  // per row: m_ref_0, l_0, m_ref_1, l_1, m_true_1 (the row statistics are
+  // written by warpgroup 0, which needs the other half's true maximum)
+  static constexpr int kRedFloats = 5 * 128;
+  static constexpr int kBarOff = kRedOff + kRedFloats * 4;
+  // The dynamic shared memory base is 1024-byte aligned (checked at run
+  // time); with head_dim 128 the tiles take almost all of the 227 KB, so no
+  // alignment slack is kept.
+  static constexpr int kSmem = kBarOff + 512;
 };
 
 struct Bars {
-  uint64_t q_full;
-  uint64_t q_empty;
-  uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t s_full;
+  uint64_t s_free;      // both warpgroups have loaded S into registers
+  uint64_t p_full[2];   // by key half: P_h of the current block is in TMEM
+  uint64_t pv_done[2];  // by key half: P_h V_h of a block done (half 1 also covers half 0)
   uint64_t final_mma;
-  uint64_t red_full[2];  // both warpgroups' partial row values written (by parity)
+  uint64_t red_full;   // both warpgroups' row statistics written
+  uint64_t red_empty;  // both warpgroups have read them
   uint64_t wg_sync[2];
   uint64_t k_full[4];
   uint64_t k_empty[4];
@@ -78,27 +94,36 @@ struct Bars {
   uint32_t tmem_slot;
   int abort_flag;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block overflows its shared-memory slot");
 
 // Partial result of one chunk of a split row (fp32): O (128 x D, relative to
 // the chunk's reference max) then, per column half and row, the chunk's
-// reference max, row sum and true max (log2 units) and a pad.
+// reference max, row sum and an upper bound of the row's maximum (the true
+// maximum in half 0, whose merge writes the row statistics; log2 units) and
+// a pad.
 template <int D>
 __host__ __device__ constexpr size_t fwd_part_floats() {
   return (size_t)128 * D + 2 * 128 * 4;
 }
 
-// 2^x on the FMA pipe, for x <= 8: x = n + f with n = floor(x), f in [0, 1);
-// 2^f ~= 1 + f (c1 + f (c2 + f c3)), a cubic fitted to 2^f on [0, 1] by
-// iteratively reweighted least squares on the relative error (max relative
-// error 8.6e-5, well below the 2^-9 of the bf16 P it feeds); 2^n is added
-// to the exponent bits.  Arguments below -126 are clamped (the result there
-// is far below anything a bf16 P can hold next to the row maximum's 1).
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -126.f);
-  const float n = floorf(x);
-  const float f = x - n;
-  const float p = fmaf(fmaf(fmaf(0.0770655f, f, 0.22764668f), f, 0.6951164f), f, 1.f);
-  return __int_as_float(__float_as_int(p) + ((int)n << 23));
+// Largest (or, for a negative scale, smallest) of 64 raw scores: eight
+// chains of three-input max, then a tree.
+template <bool kMax>
+__device__ __forceinline__ float extreme64(const float (&v)[64]) {
+  float c[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float* x = v + 8 * j;
+    if (kMax) {
+      c[j] = max3f(max3f(max3f(x[0], x[1], x[2]), x[3], x[4]), x[5], x[6]);
+      c[j] = fmaxf(c[j], x[7]);
+    } else {
+      c[j] = min3f(min3f(min3f(x[0], x[1], x[2]), x[3], x[4]), x[5], x[6]);
+      c[j] = fminf(c[j], x[7]);
+    }
+  }
+  if (kMax) return max3f(max3f(c[0], c[1], c[2]), max3f(c[3], c[4], c[5]), fmaxf(c[6], c[7]));
+  return min3f(min3f(c[0], c[1], c[2]), min3f(c[3], c[4], c[5]), fminf(c[6], c[7]));
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* b, int* status) {
@@ -118,9 +143,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
   using C = Fwd2Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  if (smem_u32(smem_raw) & 1023) {  // no slack for re-alignment: refuse (uniform, before any barrier)
+    if (threadIdx.x == 0) atomicExch(a.status, kStatusDeviceCheck);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   uint8_t* sQ = sm;
-  uint8_t* sK = sQ + C::kTile;
+  uint8_t* sK = sQ + C::kQStages * C::kTile;
   uint8_t* sV = sK + C::kKStages * C::kTile;
   float* sRed = (float*)(sm + C::kRedOff);
   Bars* bars = (Bars*)(sm + C::kBarOff);
@@ -131,19 +160,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Walk walk = make_walk(lay, a.d.BH);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], kSoftmax);
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->pv_done[i], 1);
+      mbar_init(&bars->wg_sync[i], 128);
     }
-    mbar_init(&bars->p_full, kSoftmax);
-    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, kSoftmax);
     mbar_init(&bars->final_mma, 1);
-    mbar_init(&bars->red_full[0], kSoftmax);
-    mbar_init(&bars->red_full[1], kSoftmax);
-    mbar_init(&bars->wg_sync[0], 128);
-    mbar_init(&bars->wg_sync[1], 128);
+    mbar_init(&bars->red_full, kSoftmax);
+    mbar_init(&bars->red_empty, kSoftmax);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&bars->ring.full[i], 1);
       mbar_init(&bars->ring.empty[i], 2 + kSoftmax / 32);  // MMA, softmax warps, V producer
@@ -184,11 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         Cursor cur;
         walk.decode(k, cur);
         if (cur.n == 0) continue;
-        // Q of a new item: the previous item's S MMAs must be done
-        if (!(ok = mbar_wait(&bars->q_empty, (q & 1) ^ 1, ab, a.status))) break;
+        // Q of item q goes to buffer q % 2 once item q - 2's S MMAs are done
+        const int qb = q & 1;
+        if (!(ok = mbar_wait(&bars->q_empty[qb], ((q >> 1) & 1) ^ 1, ab, a.status))) break;
         const int qrow = cur.bh * S + cur.line * 128;
-        mbar_arrive_expect_tx(&bars->q_full, C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(sQ + b * 16384, &tmQ, b * 64, qrow, &bars->q_full);
+        mbar_arrive_expect_tx(&bars->q_full[qb], C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_2d(sQ + qb * C::kTile + b * 16384, &tmQ, b * 64, qrow, &bars->q_full[qb]);
         ++q;
         for (int j = 0; j < cur.n; ++j, ++g) {
           int n = a.col_idx[cur.first + j];
@@ -206,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // drain: every copy issued must have landed before the CTA exits
-      if (q > 0) drain_wait(&bars->q_full, (q - 1) & 1);
+      for (int i = (q > 2 ? q - 2 : 0); i < q; ++i) drain_wait(&bars->q_full[i & 1], (i >> 1) & 1);
       for (int i = (kg > C::kKStages ? kg - C::kKStages : 0); i < kg; ++i)
         drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1);
     }
@@ -239,129 +269,145 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ----------------------------------------------------------- MMA --
-      // S of block g+1 (other TMEM buffer) is issued before P.V of block g.
-      const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
-      const uint32_t idPV = instr_desc(1, 0, 1, D, 128);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      auto issue_s = [&](const Cursor& c) -> bool {
-        const int i = c.g;
-        const int ks = i % C::kKStages;
-        const int b = i & 1;
-        if (c.i == 0 && !mbar_wait(&bars->q_full, c.q & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->k_full[ks], (i / C::kKStages) & 1, ab, a.status)) return false;
-        if (!mbar_wait(&bars->s_free[b], ((i >> 1) & 1) ^ 1, ab, a.status)) return false;
-        tc_fence_after();
-        const uint32_t kb = aK + ks * C::kTile;
+    // ------------------------------------------------------------- MMA --
+    // The whole warp walks the schedule (so the descriptor arithmetic stays
+    // warp-uniform); one elected lane issues the MMAs and commits.
+    // S of block g+1 is issued (as soon as the softmax has taken S of block
+    // g) before P.V of block g.
+    const uint32_t leader = elect_one();
+    const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
+    const uint32_t idPV = instr_desc(1, 0, 1, D, 128);
+    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+    auto issue_s = [&](const Cursor& c) -> bool {
+      const int i = c.g;
+      const int ks = i % C::kKStages;
+      const int qb = c.q & 1;
+      if (c.i == 0 && !warp_wait(&bars->q_full[qb], (c.q >> 1) & 1, bars, a.status)) return false;
+      if (!warp_wait(&bars->k_full[ks], (i / C::kKStages) & 1, bars, a.status)) return false;
+      if (!warp_wait(&bars->s_free, (i & 1) ^ 1, bars, a.status)) return false;
+      tc_fence_after();
+      const uint32_t kb = aK + ks * C::kTile;
+      const uint32_t qa = aQ + qb * C::kTile;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + b * 128, smem_desc(aQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
-        }
-        mma_commit(&bars->k_empty[ks]);
-        mma_commit(&bars->s_full[b]);
-        if (c.i == c.n - 1) mma_commit(&bars->q_empty);
-        return true;
-      };
-      bool ok = true;
-      auto seek_a = [&](Cursor& c) {
-        while (true) {
-          int k;
-          if (!(ok = ring_get(ring, c.t, &k, ab, a.status)) || k < 0) {
-            c.done = true;
-            return;
-          }
-          walk.decode(k, c);
-          if (c.n > 0) {
-            c.i = 0;
-            return;
-          }
-          ++c.t;
-        }
-      };
-      auto seek_b = [&](Cursor& c) {
-        while (true) {
-          const int k = *(volatile int32_t*)&ring->k[c.t % kRing];
-          if (k < 0) {
-            c.done = true;
-            return;
-          }
-          walk.decode(k, c);
-          if (c.n > 0) {
-            c.i = 0;
-            return;
-          }
-          ring_release(ring, c.t);
-          ++c.t;
-        }
-      };
-      auto next_a = [&](Cursor& c) {
-        ++c.g;
-        if (++c.i == c.n) {
-          ++c.q;
-          ++c.t;
-          seek_a(c);
-        }
-      };
-      Cursor A{0, 0, 0, 0, 0, 0, 0, 0, 0, false};
-      seek_a(A);
-      Cursor B = A;
-      if (ok && !A.done) {
-        if ((ok = issue_s(A))) next_a(A);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16_ss_by(leader, tmem, smem_desc(qa + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
       }
-      while (ok && !B.done) {
-        if (!A.done) {
-          if (!(ok = issue_s(A))) break;
-          next_a(A);
-          if (!ok) break;
+      mma_commit_by(leader, &bars->k_empty[ks]);
+      mma_commit_by(leader, &bars->s_full);
+      if (c.i == c.n - 1) mma_commit_by(leader, &bars->q_empty[qb]);
+      __syncwarp();
+      return true;
+    };
+    bool ok = true;
+    auto get = [&](int t, int* k) -> bool {
+      int kk = -1;
+      bool good = true;
+      if (lane == 0) good = ring_get(ring, t, &kk, ab, a.status);
+      good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+      *k = __shfl_sync(0xffffffffu, kk, 0);
+      return good;
+    };
+    auto seek_a = [&](Cursor& c) {
+      while (true) {
+        int k;
+        if (!(ok = get(c.t, &k)) || k < 0) {
+          c.done = true;
+          return;
         }
-        const int i = B.g;
-        const int vs = i % C::kVStages;
-        if (!(ok = mbar_wait(&bars->p_full, i & 1, ab, a.status))) break;
-        if (!(ok = mbar_wait(&bars->v_full[vs], (i / C::kVStages) & 1, ab, a.status))) break;
-        tc_fence_after();
-        const uint32_t vb = aV + vs * C::kTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8, smem_desc(vb + kk * 2048, 16384, 1024), idPV,
-                      (B.i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->v_empty[vs]);
-        mma_commit(&bars->pv_done);
-        ++B.g;
-        if (++B.i == B.n) {
-          ring_release(ring, B.t);
-          ++B.q;
-          ++B.t;
-          seek_b(B);
+        walk.decode(k, c);
+        if (c.n > 0) {
+          c.i = 0;
+          return;
         }
+        ++c.t;
       }
-      mma_commit(&bars->final_mma);
-      drain_wait(&bars->final_mma, 0);
+    };
+    auto seek_b = [&](Cursor& c) {
+      while (true) {
+        const int k = *(volatile int32_t*)&ring->k[c.t % kRing];
+        if (k < 0) {
+          c.done = true;
+          return;
+        }
+        walk.decode(k, c);
+        if (c.n > 0) {
+          c.i = 0;
+          return;
+        }
+        __syncwarp();
+        if (lane == 0) ring_release(ring, c.t);
+        ++c.t;
+      }
+    };
+    auto next_a = [&](Cursor& c) {
+      ++c.g;
+      if (++c.i == c.n) {
+        ++c.q;
+        ++c.t;
+        seek_a(c);
+      }
+    };
+    Cursor A{0, 0, 0, 0, 0, 0, 0, 0, 0, false};
+    seek_a(A);
+    Cursor B = A;
+    if (ok && !A.done) {
+      if ((ok = issue_s(A))) next_a(A);
     }
+    while (ok && !B.done) {
+      if (!A.done) {
+        if (!(ok = issue_s(A))) break;
+        next_a(A);
+        if (!ok) break;
+      }
+      const int i = B.g;
+      const int vs = i % C::kVStages;
+      const int b = i & 1;
+      if (!(ok = warp_wait(&bars->v_full[vs], (i / C::kVStages) & 1, bars, a.status))) break;
+      // The first block of a row overwrites both accumulators, which both
+      // warpgroups read while combining the previous row: wait for both.
+      if (!(ok = warp_wait(&bars->p_full[0], i & 1, bars, a.status))) break;
+      if (B.i == 0 && !(ok = warp_wait(&bars->p_full[1], i & 1, bars, a.status))) break;
+      tc_fence_after();
+      const uint32_t vb = aV + vs * C::kTile;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1 && B.i > 0) {
+          if (!(ok = warp_wait(&bars->p_full[1], i & 1, bars, a.status))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ts_by(leader, tmem + kColO + h * D, tmem + kColP + b * 64 + h * 32 + kk * 8,
+                         smem_desc(vb + (4 * h + kk) * 2048, 16384, 1024), idPV, (B.i > 0 || kk > 0) ? 1u : 0u);
+        if (h == 1) mma_commit_by(leader, &bars->v_empty[vs]);
+        mma_commit_by(leader, &bars->pv_done[h]);
+      }
+      __syncwarp();
+      if (!ok) break;
+      ++B.g;
+      if (++B.i == B.n) {
+        if (lane == 0) ring_release(ring, B.t);
+        ++B.q;
+        ++B.t;
+        seek_b(B);
+      }
+    }
+    mma_commit_by(leader, &bars->final_mma);
+    if (leader) drain_wait(&bars->final_mma, 0);
+    __syncwarp();
   } else if (warp < kWarpV) {
     // -------------------------------------------------------- softmax --
-    const int hg = (warp - 2) / 4;  // column half
+    const int hg = (warp - 2) / 4;  // key half of every block
     const int wl = warp % 4;
     const int r = wl * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
+    const uint32_t colO = kColO + hg * D;  // this half's accumulator
     const float sl2 = a.d.scale * kLog2e;
     int g = 0;  // blocks processed by this CTA
-    int x = 0;  // exchanges through sRed (both warpgroups take part in each)
+    int x = 0;  // row-statistics exchanges (one per non-empty item)
     int sync_phase = 0;
     bool ok = true;
-    // Combines a per-row value of the two column halves through shared
-    // memory (two buffers by exchange parity: no thread gets more than one
-    // exchange ahead, since each waits for all 256 softmax threads).
-    auto exchange = [&](float v, float* other) -> bool {
-      float* red = sRed + (x & 1) * 256;
-      red[hg * 128 + r] = v;
-      mbar_arrive(&bars->red_full[x & 1]);
-      const bool good = warp_wait(&bars->red_full[x & 1], (x >> 1) & 1, bars, a.status);
-      if (good) *other = red[(hg ^ 1) * 128 + r];
-      ++x;
-      return good;
-    };
     for (int t = 0; ok; ++t) {
       int k = -1;
       if (lane == 0) ok = ring_get(ring, t, &k, ab, a.status);
@@ -387,42 +433,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
       for (int i = 0; i < nblk; ++i, ++g) {
         const int b = g & 1;
-        if (!(ok = warp_wait(&bars->s_full[b], (g >> 1) & 1, bars, a.status))) break;
+        if (!(ok = warp_wait(&bars->s_full, g & 1, bars, a.status))) break;
         tc_fence_after();
-        float tt[64];
+        float tt[64];  // raw scores of this half
         {
           uint32_t v0[32], v1[32];
-          tmem_ld32(tmem + lane_base + b * 128 + hg * 64, v0);
-          tmem_ld32(tmem + lane_base + b * 128 + hg * 64 + 32, v1);
+          tmem_ld32(tmem + lane_base + hg * 64, v0);
+          tmem_ld32(tmem + lane_base + hg * 64 + 32, v1);
           tmem_wait_ld();
-          const float2 sc = make_float2(sl2, sl2);
+          tc_fence_before();
+          mbar_arrive(&bars->s_free);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 x0 = mul2(make_float2(__uint_as_float(v0[2 * k]), __uint_as_float(v0[2 * k + 1])), sc);
-            const float2 x1 = mul2(make_float2(__uint_as_float(v1[2 * k]), __uint_as_float(v1[2 * k + 1])), sc);
-            tt[2 * k] = x0.x;
-            tt[2 * k + 1] = x0.y;
-            tt[32 + 2 * k] = x1.x;
-            tt[32 + 2 * k + 1] = x1.y;
+          for (int k = 0; k < 32; ++k) {
+            tt[k] = __uint_as_float(v0[k]);
+            tt[32 + k] = __uint_as_float(v1[k]);
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[b]);
-        // row maximum of this half: eight independent chains, then a tree
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = tt[k];
-#pragma unroll
-        for (int k = 8; k < 64; ++k) m8[k & 7] = fmaxf(m8[k & 7], tt[k]);
-        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        float mo;
-        if (!(ok = exchange(mx, &mo))) break;
-        mx = fmaxf(mx, mo);
+        // row maximum of this half in log2 units (the scale is applied to
+        // the extreme raw score, not to every score)
+        const float mx = (sl2 >= 0.f ? extreme64<true>(tt) : extreme64<false>(tt)) * sl2;
         m_true = fmaxf(m_true, mx);
-        // The reference max depends only on the scores, so it is settled
-        // (and the exponentials computed) before waiting for the previous
-        // block's P.V; only the O rescale and the P store have to wait.
         float alpha = 1.f;
         bool rescale = false;
         if (i > 0) {
@@ -440,27 +470,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
         uint32_t pk[32];
-        const float2 nm = make_float2(-m_ref, -m_ref);
+        const float2 sc = make_float2(sl2, sl2), nm = make_float2(-m_ref, -m_ref);
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float2 x = add2(make_float2(tt[2 * k], tt[2 * k + 1]), nm);
-          // one pair in four on the FMA pipe, the rest on MUFU (ex2)
-          const float2 p = (k & 3) == 3 ? make_float2(exp2_poly(x.x), exp2_poly(x.y)) : make_float2(ex2(x.x), ex2(x.y));
+          // x = s * scale * log2(e) - m_ref in one rounding, then 2^x on MUFU
+          const float2 x = fma2(make_float2(tt[2 * k], tt[2 * k + 1]), sc, nm);
+          const float2 p = make_float2(ex2(x.x), ex2(x.y));
           sum4[k & 3] = add2(sum4[k & 3], p);
           pk[k] = pack_bf16x2(p.x, p.y);
         }
         l += (sum4[0].x + sum4[0].y + sum4[1].x + sum4[1].y) + (sum4[2].x + sum4[2].y + sum4[3].x + sum4[3].y);
-        // P.V of the previous block (this row's or the previous row's) must
-        // be done before O is rescaled or P is overwritten
+        // The previous block's P_h V_h must be done before O_h is rescaled
+        // and before P_h of this block overwrites the P buffer of the block
+        // before that; it also keeps this warpgroup at most one block ahead
+        // of the MMA thread's p_full wait.
         if (g > 0) {
-          if (!(ok = warp_wait(&bars->pv_done, (g - 1) & 1, bars, a.status))) break;
+          if (!(ok = warp_wait(&bars->pv_done[hg], (g - 1) & 1, bars, a.status))) break;
           tc_fence_after();
         }
         if (rescale) {
 #pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
-            const uint32_t ta = tmem + lane_base + kColO + hg * (D / 2) + c * 32;
+            const uint32_t ta = tmem + lane_base + colO + c * 32;
             tmem_ld32(ta, v);
             tmem_wait_ld();
 #pragma unroll
@@ -468,60 +500,93 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(ta, v);
           }
         }
-        tmem_st32(tmem + lane_base + kColP + hg * 32, pk);
+        tmem_st32(tmem + lane_base + kColP + b * 64 + hg * 32, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full);
+        mbar_arrive(&bars->p_full[hg]);
       }
       if (!ok) break;
       // ----------------------------------------------------- epilogue --
-      // total row sum: the two halves' partial sums share the reference max
-      float lo;
-      if (!(ok = exchange(l, &lo))) break;
-      l += lo;
-      if (!(ok = warp_wait(&bars->pv_done, (g - 1) & 1, bars, a.status))) break;
+      // exchange (m_ref, l) of the two halves (and half 1's true max)
+      if (x > 0 && !(ok = warp_wait(&bars->red_empty, (x - 1) & 1, bars, a.status))) break;
+      sRed[(2 * hg) * 128 + r] = m_ref;
+      sRed[(2 * hg + 1) * 128 + r] = l;
+      if (hg == 1) sRed[4 * 128 + r] = m_true;
+      mbar_arrive(&bars->red_full);
+      if (!(ok = warp_wait(&bars->red_full, x & 1, bars, a.status))) break;
+      const float m0 = sRed[r], l0 = sRed[128 + r], m1 = sRed[256 + r], l1 = sRed[384 + r];
+      const float mt1 = sRed[512 + r];
+      mbar_arrive(&bars->red_empty);
+      ++x;
+      const float R = fmaxf(m0, m1);
+      const float c0 = ex2(m0 - R), c1 = ex2(m1 - R);
+      const float L = l0 * c0 + l1 * c1;
+      // both halves' last P.V (pv_done[1] also covers half 0)
+      if (!(ok = warp_wait(&bars->pv_done[1], (g - 1) & 1, bars, a.status))) break;
       tc_fence_after();
+      const uint32_t t0 = tmem + lane_base + kColO + hg * (D / 2);
       if (cur.slot < 0) {
-        const float inv = 1.f / l;
+        const float inv = 1.f / L;
+        const float2 w = make_float2(c0 * inv, c1 * inv);
 #pragma unroll 1
         for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kColO + hg * (D / 2) + c * 32, v);
+          uint32_t u[32], v[32];
+          tmem_ld32(t0 + c * 32, u);
+          tmem_ld32(t0 + D + c * 32, v);
           tmem_wait_ld();
           uint4* dst = (uint4*)(orow + c * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
-            o.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
-            o.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
-            o.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
-            dst[q] = o;
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = q * 8 + 2 * e;
+              const float2 y = fma2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])),
+                                    make_float2(w.x, w.x),
+                                    mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                         make_float2(w.y, w.y)));
+              o[e] = pack_bf16x2(y.x, y.y);
+            }
+            dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
         if (hg == 0) {
-          a.row_max[grow] = m_true * kLn2;
-          a.row_denom[grow] = l * ex2(m_ref - m_true);
+          const float M = fmaxf(m_true, mt1);
+          a.row_max[grow] = M * kLn2;
+          a.row_denom[grow] = L * ex2(R - M);
         }
       } else {
-        // chunk of a split row: publish O (relative to m_ref) and the row's
-        // statistics; the last chunk to arrive combines them:
-        //   M = max m_true_c,  w_c = 2^(m_ref_c - M),  l = sum l_c w_c,
-        //   O = sum w_c O_c / l
+        // chunk of a split row: publish this half's columns of
+        // c0 O_0 + c1 O_1 (relative to R) and the chunk's statistics; the
+        // last chunk to arrive combines them:
+        //   M = max_c Z_c,  w_c = 2^(R_c - M),  l = sum_c L_c w_c,
+        //   O = sum_c w_c O_c / l
+        // with Z_c the chunk's true max in half 0 (whose merge writes the row
+        // statistics) and R_c in half 1 (any common bound works there).
         constexpr size_t kPart = fwd_part_floats<D>();
         float* tile = a.part + ((size_t)cur.slot * a.d.BH + cur.bh) * kPart;
         float* prow = tile + (size_t)r * D + hg * (D / 2);
 #pragma unroll 1
         for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kColO + hg * (D / 2) + c * 32, v);
+          uint32_t u[32], v[32];
+          tmem_ld32(t0 + c * 32, u);
+          tmem_ld32(t0 + D + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            ((float4*)(prow + c * 32))[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          for (int j = 0; j < 8; ++j) {
+            const float2 y0 = fma2(make_float2(__uint_as_float(u[4 * j]), __uint_as_float(u[4 * j + 1])),
+                                   make_float2(c0, c0),
+                                   mul2(make_float2(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1])),
+                                        make_float2(c1, c1)));
+            const float2 y1 = fma2(make_float2(__uint_as_float(u[4 * j + 2]), __uint_as_float(u[4 * j + 3])),
+                                   make_float2(c0, c0),
+                                   mul2(make_float2(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])),
+                                        make_float2(c1, c1)));
+            ((float4*)(prow + c * 32))[j] = make_float4(y0.x, y0.y, y1.x, y1.y);
+          }
         }
-        *(float4*)(tile + 128 * D + (hg * 128 + r) * 4) = make_float4(m_ref, l, m_true, 0.f);
+        const float Z = hg == 0 ? fmaxf(m_true, mt1) : R;
+        *(float4*)(tile + 128 * D + (hg * 128 + r) * 4) = make_float4(R, L, Z, 0.f);
         bool last = false;
         if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
                                 sync_phase, ab, a.status, &last)))
@@ -529,13 +594,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last) {
           const int sl = lay.slot_line[cur.slot];
           const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
-          const float* t0 = a.part + ((size_t)base * a.d.BH + cur.bh) * kPart;
+          const float* p0 = a.part + ((size_t)base * a.d.BH + cur.bh) * kPart;
           const size_t stride = (size_t)a.d.BH * kPart;  // next chunk, same head
           float M = -INFINITY;
-          for (int ch = 0; ch < nc; ++ch) M = fmaxf(M, ld_partial(t0 + ch * stride + 128 * D + (hg * 128 + r) * 4).z);
+          for (int ch = 0; ch < nc; ++ch) M = fmaxf(M, ld_partial(p0 + ch * stride + 128 * D + (hg * 128 + r) * 4).z);
           float lsum = 0.f;
           for (int ch = 0; ch < nc; ++ch) {
-            const float4 st = ld_partial(t0 + ch * stride + 128 * D + (hg * 128 + r) * 4);
+            const float4 st = ld_partial(p0 + ch * stride + 128 * D + (hg * 128 + r) * 4);
             lsum += st.y * ex2(st.x - M);
           }
           const float inv = 1.f / lsum;
@@ -545,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[j] = 0.f;
             for (int ch = 0; ch < nc; ++ch) {
-              const float* src = t0 + ch * stride;
+              const float* src = p0 + ch * stride;
               const float w = ex2(ld_partial(src + 128 * D + (hg * 128 + r) * 4).x - M) * inv;
               const float* p = src + (size_t)r * D + hg * (D / 2) + c * 32;
 #pragma unroll
@@ -570,6 +635,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // this warp's reads of O_0 / O_1 are complete before its warpgroup's
+      // next P_h arrival lets the MMA overwrite them
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) ring_release(ring, t);
     }
