@@ -349,7 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((ok = issue_sdp(A))) next_a(A);
       }
       while (ok && !B.done) {
-        if (!A.done) {
+        // S / dP of the next block go first, unless that block starts an item
+        // whose Q / dO are still in flight: then dQ of this block goes first
+        // (its elementwise pass is done or nearly), so that the row's
+        // epilogue does not wait for the next row's loads.
+        const bool a_later = !A.done && A.i == 0 && !__all_sync(0xffffffffu, mbar_test_wait(&bars->qd_full, A.q & 1));
+        if (!A.done && !a_later) {
           if (!(ok = issue_sdp(A))) break;
           next_a(A);
           if (!ok) break;
@@ -364,6 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->k_empty[st]);
         mma_commit_by(leader, &bars->dq_done);
+        __syncwarp();
+        if (a_later) {
+          if (!(ok = issue_sdp(A))) break;
+          next_a(A);
+          if (!ok) break;
+        }
         ++B.g;
         if (++B.i == B.n) {
           __syncwarp();
@@ -507,8 +518,9 @@ struct DkvCfg {
 struct DkvBars {
   uint64_t kv_full;
   uint64_t kv_empty;
-  uint64_t st_full;
-  uint64_t st_free;
+  uint64_t st_full;   // S^T of the block in TMEM
+  uint64_t dpt_full;  // dP^T of the block in TMEM
+  uint64_t dpt_free;  // both warpgroups have loaded dP^T
   uint64_t pt_ready;
   uint64_t ds_ready;
   uint64_t pt_free;
@@ -588,8 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sDST = sdO + C::kStages * C::kTile;
   float* sStat = (float*)(sm + C::kStatOff);  // [stage][lse2 | delta][128]
   DkvBars* bars = (DkvBars*)(sm + C::kBarOff);
-  // P^T (bf16) is written over the dP^T columns each warpgroup has read:
-  // queries [0, 64) at column 128, queries [64, 128) at column 192.
+  // P^T (bf16) is written over the S^T columns each warpgroup has read:
+  // queries [0, 64) at column 0, queries [64, 128) at column 64.
   constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -601,7 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->kv_empty, 1);
     mbar_init(&bars->st_full, 1);
-    mbar_init(&bars->st_free, kEw);
+    mbar_init(&bars->dpt_full, 1);
+    mbar_init(&bars->dpt_free, kEw);
     mbar_init(&bars->pt_ready, kEw);
     mbar_init(&bars->ds_ready, kEw);
     mbar_init(&bars->pt_free, 1);
@@ -689,11 +702,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The whole warp walks the schedule (descriptor arithmetic stays
       // warp-uniform); one elected lane issues the MMAs and commits.
       const uint32_t leader = elect_one();
-      // Per block g: S^T_g and dP^T_g land before the elementwise pass; the
-      // elementwise pass reads both and releases them (st_free), so
-      // S^T_{g+1} (cursor A) is issued while it computes; P^T_g comes back
-      // over the dP^T columns (pt_ready) and dV_g starts while dS^T_g is
-      // still being computed; dP^T_{g+1} waits for dV_g (pt_free).
+      // Per block g the pipe runs dV_g, dK_g, S^T_{g+1}, dP^T_{g+1}:
+      //   * dV_g as soon as P^T_g is in TMEM (pt_ready; P^T lies over the
+      //     S^T columns), dK_g once dS^T_g is in shared memory (ds_ready);
+      //   * S^T_{g+1} overwrites P^T_g, so it waits for dV_g to complete
+      //     (pt_free), which happens while dK_g is still running;
+      //   * dP^T_{g+1} waits until the elementwise pass has loaded dP^T_g.
+      // The elementwise pass of block g+1 starts on S^T_{g+1} (exponentials,
+      // P^T) while dP^T_{g+1} is computed.
       const uint32_t idST = instr_desc(1, 0, 0, 128, 128);
       const uint32_t idG = instr_desc(1, 0, 1, D, 128);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
@@ -755,6 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16_ss_by(leader, tmem + kColST, smem_desc(aK + off, 16, 1024), smem_desc(qb + off, 16, 1024), idST, kk > 0);
         }
+        mma_commit_by(leader, &bars->st_full);
         return true;
       };
       auto issue_dpt = [&](const Cursor& c) -> bool {
@@ -767,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16_ss_by(leader, tmem + kColDPT, smem_desc(aV + off, 16, 1024), smem_desc(gb + off, 16, 1024), idST, kk > 0);
         }
-        mma_commit_by(leader, &bars->st_full);
+        mma_commit_by(leader, &bars->dpt_full);
         if (c.i == c.n - 1) mma_commit_by(leader, &bars->kv_empty);
         return true;
       };
@@ -779,19 +796,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       while (ok && !B.done) {
         const int st = B.g % C::kStages;
-        if (!A.done) {
-          if (!(ok = warp_wait(&bars->st_free, B.g & 1, ab, a.status))) break;
-          if (!(ok = issue_st(A))) break;
-        }
         const uint32_t qb = aQ + st * C::kTile, gb = adO + st * C::kTile;
-        // dV as soon as P^T is in TMEM (its completion frees the dP^T columns
-        // for the next block); dK once dS^T is in shared memory
         if (!(ok = warp_wait(&bars->pt_ready, B.g & 1, ab, a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts_by(leader, tmem + kColDV, tmem + kColDPT + kk * 8 + (kk >= 4 ? 32 : 0),
-                      smem_desc(gb + kk * 2048, 16384, 1024), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts_by(leader, tmem + kColDV, tmem + kColST + kk * 8 + (kk >= 4 ? 32 : 0),
+                         smem_desc(gb + kk * 2048, 16384, 1024), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->do_empty[st]);
         mma_commit_by(leader, &bars->pt_free);
         if (!(ok = warp_wait(&bars->ds_ready, B.g & 1, ab, a.status))) break;
@@ -799,17 +810,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColDK, smem_desc(aDST + off, 16, 1024), smem_desc(qb + kk * 2048, 16384, 1024), idG,
-                      (B.i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ss_by(leader, tmem + kColDK, smem_desc(aDST + off, 16, 1024), smem_desc(qb + kk * 2048, 16384, 1024),
+                         idG, (B.i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit_by(leader, &bars->q_empty[st]);
         mma_commit_by(leader, &bars->dst_free);
         if (!A.done) {
           if (!(ok = warp_wait(&bars->pt_free, B.g & 1, ab, a.status))) break;
+          if (!(ok = issue_st(A))) break;
+          if (!(ok = warp_wait(&bars->dpt_free, B.g & 1, ab, a.status))) break;
           if (!(ok = issue_dpt(A))) break;
           next_a(A);
           if (!ok) break;
         }
+        __syncwarp();
         ++B.g;
         if (++B.i == B.n) {
           __syncwarp();
@@ -854,9 +868,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           float s[64], dp[64];
           tmem_ld64(tmem + lane_base + kColST + hg * 64, s);
-          tmem_ld64(tmem + lane_base + kColDPT + hg * 64, dp);
-          tc_fence_before();
-          mbar_arrive(&bars->st_free);
           // statistics of this block row's queries, brought in with Q (q_full
           // completed before S^T_g was issued)
           const float* lse = sStat + st * 256 + hg * 64;
@@ -869,12 +880,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             s[2 * k] = ex2(x.x);
             s[2 * k + 1] = ex2(x.y);
           }
-          // P^T over this warpgroup's own dP^T columns (already read above;
-          // dV of the previous block finished before dP^T of this one began)
-          tmem_st_bf16x64(tmem + lane_base + kColDPT + hg * 64, s);
+          // P^T over this warpgroup's own S^T columns (already read above;
+          // dV of the previous block finished before S^T of this one began)
+          tmem_st_bf16x64(tmem + lane_base + kColST + hg * 64, s);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->pt_ready);
+          if (!(ok = warp_wait(&bars->dpt_full, g & 1, ab, a.status))) break;
+          tc_fence_after();
+          tmem_ld64(tmem + lane_base + kColDPT + hg * 64, dp);
+          tc_fence_before();
+          mbar_arrive(&bars->dpt_free);
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             const float2 d2 = *(const float2*)(dl + 2 * k);
