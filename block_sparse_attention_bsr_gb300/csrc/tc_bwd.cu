@@ -144,8 +144,10 @@ struct DqBars {
   uint64_t qd_empty;
   uint64_t sdp_full;
   uint64_t sdp_free;
-  uint64_t ds_full;
-  uint64_t dq_done;
+  // by dS buffer, like dq_done: with two buffers the elementwise pass may run
+  // two blocks ahead of the MMA thread, so one barrier could alias phases
+  uint64_t ds_full[2];
+  uint64_t dq_done[2];  // by dS buffer: dQ of a block that read it is done
   uint64_t final_mma;
   uint64_t wg_sync[2];
   uint64_t k_full[4];
@@ -170,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = sdO + C::kTile;
   uint8_t* sV = sK + C::kKStages * C::kTile;
   DqBars* bars = (DqBars*)(sm + C::kBarOff);
+  // dS (bf16) of block g at column 384 + 64 (g % 2): two buffers, so the
+  // elementwise pass of block g waits only for dQ of block g - 2
   constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -182,8 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->qd_empty, 1);
     mbar_init(&bars->sdp_full, 1);
     mbar_init(&bars->sdp_free, kEw);
-    mbar_init(&bars->ds_full, kEw);
-    mbar_init(&bars->dq_done, 1);
+    mbar_init(&bars->ds_full[0], kEw);
+    mbar_init(&bars->ds_full[1], kEw);
+    mbar_init(&bars->dq_done[0], 1);
+    mbar_init(&bars->dq_done[1], 1);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->wg_sync[0], 128);
     mbar_init(&bars->wg_sync[1], 128);
@@ -360,15 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         const int st = B.g % C::kKStages;
-        if (!(ok = warp_wait(&bars->ds_full, B.g & 1, ab, a.status))) break;
+        if (!(ok = warp_wait(&bars->ds_full[B.g & 1], (B.g >> 1) & 1, ab, a.status))) break;
         tc_fence_after();
         const uint32_t kb = aK + st * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts_by(leader, tmem + kColDQ, tmem + kColDS + kk * 8, smem_desc(kb + kk * 2048, 16384, 1024), idDQ,
+          mma_bf16_ts_by(leader, tmem + kColDQ, tmem + kColDS + (B.g & 1) * 64 + kk * 8, smem_desc(kb + kk * 2048, 16384, 1024), idDQ,
                       (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->k_empty[st]);
-        mma_commit_by(leader, &bars->dq_done);
+        mma_commit_by(leader, &bars->dq_done[B.g & 1]);
         __syncwarp();
         if (a_later) {
           if (!(ok = issue_sdp(A))) break;
@@ -428,15 +434,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             s[2 * j] = y.x;
             s[2 * j + 1] = y.y;
           }
-          if (g > 0 && !(ok = warp_wait(&bars->dq_done, (g - 1) & 1, ab, a.status))) break;
+          if (g > 1 && !(ok = warp_wait(&bars->dq_done[g & 1], ((g - 2) >> 1) & 1, ab, a.status))) break;
           tc_fence_after();
-          tmem_st_bf16x64(tmem + lane_base + kColDS + hg * 32, s);
+          tmem_st_bf16x64(tmem + lane_base + kColDS + (g & 1) * 64 + hg * 32, s);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&bars->ds_full);
+          mbar_arrive(&bars->ds_full[g & 1]);
         }
         if (!ok) break;
-        if (!(ok = warp_wait(&bars->dq_done, (g - 1) & 1, ab, a.status))) break;
+        if (!(ok = warp_wait(&bars->dq_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ab, a.status))) break;
         tc_fence_after();
         if (cur.slot < 0) {
           store_acc_cols<D / 2>(tmem + lane_base + kColDQ + hg * (D / 2), dqrow, a.d.scale);
@@ -702,14 +708,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The whole warp walks the schedule (descriptor arithmetic stays
       // warp-uniform); one elected lane issues the MMAs and commits.
       const uint32_t leader = elect_one();
-      // Per block g the pipe runs dV_g, dK_g, S^T_{g+1}, dP^T_{g+1}:
+      // Per block g the pipe runs dV_g, S^T_{g+1}, dP^T_{g+1}, dK_g:
       //   * dV_g as soon as P^T_g is in TMEM (pt_ready; P^T lies over the
-      //     S^T columns), dK_g once dS^T_g is in shared memory (ds_ready);
+      //     S^T columns);
       //   * S^T_{g+1} overwrites P^T_g, so it waits for dV_g to complete
-      //     (pt_free), which happens while dK_g is still running;
-      //   * dP^T_{g+1} waits until the elementwise pass has loaded dP^T_g.
-      // The elementwise pass of block g+1 starts on S^T_{g+1} (exponentials,
-      // P^T) while dP^T_{g+1} is computed.
+      //     (pt_free) -- the elementwise pass is still computing dS^T_g;
+      //   * dP^T_{g+1} once the elementwise pass has loaded dP^T_g;
+      //   * dK_g once dS^T_g is in shared memory (ds_ready).
+      // So S^T_{g+1} and dP^T_{g+1} are ready by the time the elementwise
+      // pass finishes block g.
       const uint32_t idST = instr_desc(1, 0, 0, 128, 128);
       const uint32_t idG = instr_desc(1, 0, 1, D, 128);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
@@ -805,6 +812,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                          smem_desc(gb + kk * 2048, 16384, 1024), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->do_empty[st]);
         mma_commit_by(leader, &bars->pt_free);
+        auto issue_next = [&]() -> bool {
+          if (!warp_wait(&bars->pt_free, B.g & 1, ab, a.status)) return false;
+          if (!issue_st(A)) return false;
+          if (!warp_wait(&bars->dpt_free, B.g & 1, ab, a.status)) return false;
+          if (!issue_dpt(A)) return false;
+          next_a(A);
+          return ok;
+        };
+        // The next block's S^T / dP^T go before dK of this one, unless that
+        // block starts an item whose K / V are still in flight: then dK goes
+        // first, so that this item's epilogue does not wait for those loads.
+        const bool a_later = !A.done && A.i == 0 && !__all_sync(0xffffffffu, mbar_test_wait(&bars->kv_full, A.q & 1));
+        if (!A.done && !a_later && !(ok = issue_next())) break;
         if (!(ok = warp_wait(&bars->ds_ready, B.g & 1, ab, a.status))) break;
         tc_fence_after();
 #pragma unroll
@@ -815,14 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit_by(leader, &bars->q_empty[st]);
         mma_commit_by(leader, &bars->dst_free);
-        if (!A.done) {
-          if (!(ok = warp_wait(&bars->pt_free, B.g & 1, ab, a.status))) break;
-          if (!(ok = issue_st(A))) break;
-          if (!(ok = warp_wait(&bars->dpt_free, B.g & 1, ab, a.status))) break;
-          if (!(ok = issue_dpt(A))) break;
-          next_a(A);
-          if (!ok) break;
-        }
+        if (a_later && !(ok = issue_next())) break;
         __syncwarp();
         ++B.g;
         if (++B.i == B.n) {
