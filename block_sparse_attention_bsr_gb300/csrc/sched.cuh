@@ -133,4 +133,32 @@ __device__ __forceinline__ bool merge_arrive(const PlanLayout& lay, int slot, in
 // Reads 4 floats of another CTA's partial result (L2, bypassing L1).
 __device__ __forceinline__ float4 ld_partial(const float* p) { return __ldcg((const float4*)p); }
 
+// Partial tiles of split lines (fp32, 128 rows x D columns) are stored in
+// groups of four columns: element (r, c) at ((c / 4) * 128 + r) * 4 + c % 4,
+// so the 32 rows of a warp write and read one contiguous 512-byte run per
+// group instead of 32 scattered row segments.
+__device__ __forceinline__ float* part_group(float* tile, int cg, int r) { return tile + ((size_t)cg * 128 + r) * 4; }
+
+// Stores 32 fp32 values of row r, columns [4 cg0, 4 cg0 + 32), into a tile.
+__device__ __forceinline__ void part_store32(float* tile, int cg0, int r, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *(float4*)part_group(tile, cg0 + j, r) = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                         __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+}
+
+// acc += w * (row r, columns [4 cg0, 4 cg0 + 32) of a tile).
+__device__ __forceinline__ void part_accum32(const float* tile, int cg0, int r, float w, float (&acc)[32]) {
+  float4 x[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = ld_partial(part_group(const_cast<float*>(tile), cg0 + j, r));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    acc[4 * j] = fmaf(w, x[j].x, acc[4 * j]);
+    acc[4 * j + 1] = fmaf(w, x[j].y, acc[4 * j + 1]);
+    acc[4 * j + 2] = fmaf(w, x[j].z, acc[4 * j + 2]);
+    acc[4 * j + 3] = fmaf(w, x[j].w, acc[4 * j + 3]);
+  }
+}
+
 }  // namespace bsr

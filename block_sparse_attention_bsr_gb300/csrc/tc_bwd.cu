@@ -126,6 +126,40 @@ __device__ __forceinline__ void tmem_st_bf16x64(uint32_t taddr, const float (&x)
   tmem_st32(taddr, v);
 }
 
+// Writes NC fp32 TMEM columns of this lane (row r) into a partial tile,
+// starting at column group cg0 (see part_group).
+template <int NC>
+__device__ __forceinline__ void store_acc_part(uint32_t taddr, float* tile, int cg0, int r) {
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c * 32, v);
+    tmem_wait_ld();
+    part_store32(tile, cg0 + c * 8, r, v);
+  }
+}
+
+// Sums NC columns of row r (from column group cg0) over `nc` partial tiles
+// spaced `stride` floats apart and stores them as bf16 times `mul` at dst.
+template <int NC>
+__device__ __forceinline__ void merge_tiles(const float* tile0, size_t stride, int nc, int cg0, int r,
+                                            __nv_bfloat16* dst, float mul) {
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    float acc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    for (int ch = 0; ch < nc; ++ch) part_accum32(tile0 + ch * stride, cg0 + c * 8, r, 1.f, acc);
+    uint4* d = (uint4*)(dst + c * 32);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      d[j] = make_uint4(pack_bf16x2(acc[8 * j] * mul, acc[8 * j + 1] * mul),
+                        pack_bf16x2(acc[8 * j + 2] * mul, acc[8 * j + 3] * mul),
+                        pack_bf16x2(acc[8 * j + 4] * mul, acc[8 * j + 5] * mul),
+                        pack_bf16x2(acc[8 * j + 6] * mul, acc[8 * j + 7] * mul));
+  }
+}
+
 // =================================================================== dQ ====
 template <int D>
 struct DqCfg {
@@ -448,17 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_acc_cols<D / 2>(tmem + lane_base + kColDQ + hg * (D / 2), dqrow, a.d.scale);
         } else {
           // chunk of a split row: publish the fp32 partial, the last chunk merges
-          float* prow = a.part_q + ((size_t)(cur.slot * a.d.BH + cur.bh) * 128 + r) * D + hg * (D / 2);
-#pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kColDQ + hg * (D / 2) + c * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              ((float4*)(prow + c * 32))[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                          __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-          }
+          const size_t kTileF = (size_t)128 * D;
+          store_acc_part<D / 2>(tmem + lane_base + kColDQ + hg * (D / 2),
+                                a.part_q + (size_t)(cur.slot * a.d.BH + cur.bh) * kTileF, hg * (D / 8), r);
           bool last = false;
           if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
                                   sync_phase, ab, a.status, &last)))
@@ -466,31 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (last) {
             const int sl = lay.slot_line[cur.slot];
             const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
-#pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {
-              float acc[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-              for (int ch = 0; ch < nc; ++ch) {
-                const float* src =
-                    a.part_q + ((size_t)((base + ch) * a.d.BH + cur.bh) * 128 + r) * D + hg * (D / 2) + c * 32;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 x = ld_partial(src + 4 * j);
-                  acc[4 * j] += x.x;
-                  acc[4 * j + 1] += x.y;
-                  acc[4 * j + 2] += x.z;
-                  acc[4 * j + 3] += x.w;
-                }
-              }
-              uint4* dst = (uint4*)(dqrow + c * 32);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                dst[j] = make_uint4(pack_bf16x2(acc[8 * j] * a.d.scale, acc[8 * j + 1] * a.d.scale),
-                                    pack_bf16x2(acc[8 * j + 2] * a.d.scale, acc[8 * j + 3] * a.d.scale),
-                                    pack_bf16x2(acc[8 * j + 4] * a.d.scale, acc[8 * j + 5] * a.d.scale),
-                                    pack_bf16x2(acc[8 * j + 6] * a.d.scale, acc[8 * j + 7] * a.d.scale));
-            }
+            merge_tiles<D / 2>(a.part_q + (size_t)(base * a.d.BH + cur.bh) * kTileF, (size_t)a.d.BH * kTileF, nc,
+                               hg * (D / 8), r, dqrow, a.d.scale);
           }
         }
       }
@@ -542,51 +545,6 @@ struct DkvBars {
   uint32_t tmem_slot;
   int abort_flag;
 };
-
-// Writes NC fp32 TMEM columns of this lane to dst (global, 16-byte aligned).
-template <int NC>
-__device__ __forceinline__ void store_acc_f32(uint32_t taddr, float* dst) {
-#pragma unroll 1
-  for (int c = 0; c < NC / 32; ++c) {
-    uint32_t v[32];
-    tmem_ld32(taddr + c * 32, v);
-    tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      ((float4*)(dst + c * 32))[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-  }
-}
-
-// Sums NC fp32 columns over `nc` partial rows spaced `stride` floats apart
-// (from src) and stores them as bf16 times `mul` at dst.
-template <int NC>
-__device__ __forceinline__ void merge_rows(const float* src, size_t stride, int nc, __nv_bfloat16* dst, float mul) {
-#pragma unroll 1
-  for (int c = 0; c < NC / 32; ++c) {
-    float acc[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-    for (int ch = 0; ch < nc; ++ch) {
-      const float* p = src + ch * stride + c * 32;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 x = ld_partial(p + 4 * j);
-        acc[4 * j] += x.x;
-        acc[4 * j + 1] += x.y;
-        acc[4 * j + 2] += x.z;
-        acc[4 * j + 3] += x.w;
-      }
-    }
-    uint4* d = (uint4*)(dst + c * 32);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      d[j] = make_uint4(pack_bf16x2(acc[8 * j] * mul, acc[8 * j + 1] * mul),
-                        pack_bf16x2(acc[8 * j + 2] * mul, acc[8 * j + 3] * mul),
-                        pack_bf16x2(acc[8 * j + 4] * mul, acc[8 * j + 5] * mul),
-                        pack_bf16x2(acc[8 * j + 6] * mul, acc[8 * j + 7] * mul));
-  }
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -926,11 +884,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_acc_cols<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), dkrow, a.d.scale);
         } else {
           // chunk of a split column: publish the fp32 partials, the last chunk merges
+          const size_t kTileF = (size_t)128 * D;
           const size_t tile = (size_t)cur.slot * a.d.BH + cur.bh;
-          float* pv = a.part_kv + ((tile * 2 + 0) * 128 + r) * D + hg * (D / 2);
-          float* pk = a.part_kv + ((tile * 2 + 1) * 128 + r) * D + hg * (D / 2);
-          store_acc_f32<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), pv);
-          store_acc_f32<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), pk);
+          store_acc_part<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), a.part_kv + (tile * 2 + 0) * kTileF,
+                                hg * (D / 8), r);
+          store_acc_part<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), a.part_kv + (tile * 2 + 1) * kTileF,
+                                hg * (D / 8), r);
           bool last = false;
           if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
                                   sync_phase, ab, a.status, &last)))
@@ -939,10 +898,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sl = lay.slot_line[cur.slot];
             const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
             const size_t t0 = (size_t)base * a.d.BH + cur.bh;
-            const size_t stride = (size_t)a.d.BH * 2 * 128 * D;  // next slot, same head
-            merge_rows<D / 2>(a.part_kv + ((t0 * 2 + 0) * 128 + r) * D + hg * (D / 2), stride, nc, dvrow, 1.f);
-            merge_rows<D / 2>(a.part_kv + ((t0 * 2 + 1) * 128 + r) * D + hg * (D / 2), stride, nc, dkrow,
-                              a.d.scale);
+            const size_t stride = (size_t)a.d.BH * 2 * kTileF;  // next slot, same head
+            merge_tiles<D / 2>(a.part_kv + (t0 * 2 + 0) * kTileF, stride, nc, hg * (D / 8), r, dvrow, 1.f);
+            merge_tiles<D / 2>(a.part_kv + (t0 * 2 + 1) * kTileF, stride, nc, hg * (D / 8), r, dkrow, a.d.scale);
           }
         }
       }

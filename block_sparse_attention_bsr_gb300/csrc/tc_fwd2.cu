@@ -565,7 +565,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // statistics) and R_c in half 1 (any common bound works there).
         constexpr size_t kPart = fwd_part_floats<D>();
         float* tile = a.part + ((size_t)cur.slot * a.d.BH + cur.bh) * kPart;
-        float* prow = tile + (size_t)r * D + hg * (D / 2);
 #pragma unroll 1
         for (int c = 0; c < D / 64; ++c) {
           uint32_t u[32], v[32];
@@ -573,17 +572,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t0 + D + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float2 y0 = fma2(make_float2(__uint_as_float(u[4 * j]), __uint_as_float(u[4 * j + 1])),
-                                   make_float2(c0, c0),
-                                   mul2(make_float2(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1])),
-                                        make_float2(c1, c1)));
-            const float2 y1 = fma2(make_float2(__uint_as_float(u[4 * j + 2]), __uint_as_float(u[4 * j + 3])),
-                                   make_float2(c0, c0),
-                                   mul2(make_float2(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])),
-                                        make_float2(c1, c1)));
-            ((float4*)(prow + c * 32))[j] = make_float4(y0.x, y0.y, y1.x, y1.y);
+          for (int j = 0; j < 16; ++j) {
+            const float2 y = fma2(make_float2(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1])), make_float2(c0, c0),
+                                  mul2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                                       make_float2(c1, c1)));
+            u[2 * j] = __float_as_uint(y.x);
+            u[2 * j + 1] = __float_as_uint(y.y);
           }
+          part_store32(tile, hg * (D / 8) + c * 8, r, u);
         }
         const float Z = hg == 0 ? fmaxf(m_true, mt1) : R;
         *(float4*)(tile + 128 * D + (hg * 128 + r) * 4) = make_float4(R, L, Z, 0.f);
@@ -612,15 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ch = 0; ch < nc; ++ch) {
               const float* src = p0 + ch * stride;
               const float w = ex2(ld_partial(src + 128 * D + (hg * 128 + r) * 4).x - M) * inv;
-              const float* p = src + (size_t)r * D + hg * (D / 2) + c * 32;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 x4 = ld_partial(p + 4 * j);
-                acc[4 * j] = fmaf(w, x4.x, acc[4 * j]);
-                acc[4 * j + 1] = fmaf(w, x4.y, acc[4 * j + 1]);
-                acc[4 * j + 2] = fmaf(w, x4.z, acc[4 * j + 2]);
-                acc[4 * j + 3] = fmaf(w, x4.w, acc[4 * j + 3]);
-              }
+              part_accum32(src, hg * (D / 8) + c * 8, r, w, acc);
             }
             uint4* dst = (uint4*)(orow + c * 32);
 #pragma unroll
