@@ -389,11 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((ok = issue_sdp(A))) next_a(A);
       }
       while (ok && !B.done) {
-        // S / dP of the next block go first, unless that block starts an item
-        // whose Q / dO are still in flight: then dQ of this block goes first
-        // (its elementwise pass is done or nearly), so that the row's
-        // epilogue does not wait for the next row's loads.
-        const bool a_later = !A.done && A.i == 0 && !__all_sync(0xffffffffu, mbar_test_wait(&bars->qd_full, A.q & 1));
+        // S / dP of the next block go first, unless that block starts another
+        // item: then this row's last dQ goes first, so that the epilogue does
+        // not wait behind the next row's MMAs (or its Q / dO loads); the next
+        // S / dP run during the epilogue.
+        const bool a_later = !A.done && A.i == 0;
         if (!A.done && !a_later) {
           if (!(ok = issue_sdp(A))) break;
           next_a(A);
@@ -549,7 +549,8 @@ struct DkvBars {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, BwdArgs a) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                   const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV, BwdArgs a) {
   using C = DkvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // no slack for re-alignment: refuse (uniform, before any barrier)
@@ -779,9 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           return ok;
         };
         // The next block's S^T / dP^T go before dK of this one, unless that
-        // block starts an item whose K / V are still in flight: then dK goes
-        // first, so that this item's epilogue does not wait for those loads.
-        const bool a_later = !A.done && A.i == 0 && !__all_sync(0xffffffffu, mbar_test_wait(&bars->kv_full, A.q & 1));
+        // block starts another item: then this item's last dK goes first, so
+        // that its epilogue does not wait behind the next item's MMAs (or
+        // that item's K / V loads); the next S^T runs during the epilogue.
+        const bool a_later = !A.done && A.i == 0;
         if (!A.done && !a_later && !(ok = issue_next())) break;
         if (!(ok = warp_wait(&bars->ds_ready, B.g & 1, ab, a.status))) break;
         tc_fence_after();
@@ -880,8 +882,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(&bars->dst_free, (g - 1) & 1, ab, a.status))) break;
         tc_fence_after();
         if (cur.slot < 0) {
-          store_acc_cols<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), dvrow, 1.f);
-          store_acc_cols<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), dkrow, a.d.scale);
+          if constexpr (D == 128) {
+            // dV then dK of this key tile, each staged as bf16 in the dS^T
+            // tile (free: the item's last dK has completed) in the TMA box
+            // layout and written by one TMA store per warpgroup: its 64
+            // columns are one box
+            const int row0 = cur.bh * S + cur.line * 128;
+#pragma unroll 1
+            for (int w = 0; w < 2; ++w) {
+              const uint32_t tcol = (w == 0 ? kColDV : kColDK) + hg * 64;
+              const float mul = w == 0 ? 1.f : a.d.scale;
+#pragma unroll 1
+              for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + tcol + c * 32, v);
+                tmem_wait_ld();
+                float x[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * mul;
+                st_row_chunk(aDST, r, 2 * hg + c, x);
+              }
+              fence_proxy_async_smem();
+              if (!(ok = group_sync(&bars->wg_sync[hg], sync_phase, ab, a.status))) break;
+              if (r == 0) {
+                tma_store_2d(w == 0 ? &tmdV : &tmdK, hg * 64, row0, sDST + hg * 16384);
+                bulk_commit();
+                bulk_wait_read();
+              }
+              if (!(ok = group_sync(&bars->wg_sync[hg], sync_phase, ab, a.status))) break;
+            }
+          } else {
+            store_acc_cols<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), dvrow, 1.f);
+            store_acc_cols<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), dkrow, a.d.scale);
+          }
+          if (!ok) break;
         } else {
           // chunk of a split column: publish the fp32 partials, the last chunk merges
           const size_t kTileF = (size_t)128 * D;
@@ -907,6 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ring_release(ring, t);
     }
+    bulk_wait_all();  // TMA stores issued by this thread have completed
   }
 
   tc_fence_before();
@@ -916,7 +951,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, int grid, cudaStream_t s) {
+bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, const CUtensorMap& tmdK,
+                      const CUtensorMap& tmdV, int grid, cudaStream_t s) {
   {
     auto kern = dq_tc_kernel<D>;
     const int smem = DqCfg<D>::kSmem;
@@ -934,7 +970,7 @@ bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap&
     if (e != cudaSuccess)
       return fail(BSR_ERR_CUDA, "dkdv_tc: cudaFuncSetAttribute(%d): %s", smem, cudaGetErrorString(e));
     LaunchTimer timer("dkdv_tc", s);
-    kern<<<grid, kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
+    kern<<<grid, kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, tmdK, tmdV, a);
     return check_launch("dkdv_tc launch");
   }
 }
@@ -957,11 +993,13 @@ bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   TensorMaps tm;
   bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
   if (st != BSR_OK) return st;
-  CUtensorMap tmdO;
+  CUtensorMap tmdO, tmdK, tmdV;
   if ((st = make_tensor_map(a.d, a.dO, &tmdO, "dO")) != BSR_OK) return st;
+  if ((st = make_tensor_map(a.d, a.dK, &tmdK, "dK")) != BSR_OK) return st;
+  if ((st = make_tensor_map(a.d, a.dV, &tmdV, "dV")) != BSR_OK) return st;
   switch (a.d.D) {
-    case 64: return launch_bwd<64>(a, tm, tmdO, grid, s);
-    case 128: return launch_bwd<128>(a, tm, tmdO, grid, s);
+    case 64: return launch_bwd<64>(a, tm, tmdO, tmdK, tmdV, grid, s);
+    case 128: return launch_bwd<128>(a, tm, tmdO, tmdK, tmdV, grid, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "bwd_tc: head_dim %d", a.d.D);
   }
 }

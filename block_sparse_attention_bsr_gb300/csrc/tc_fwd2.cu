@@ -355,7 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((ok = issue_s(A))) next_a(A);
     }
     while (ok && !B.done) {
-      if (!A.done) {
+      // S of the next block goes first, unless that block starts another
+      // row: then this row's last P.V goes first, so that the row's
+      // epilogue does not wait behind the next row's S.
+      const bool a_later = !A.done && A.i == 0;
+      if (!A.done && !a_later) {
         if (!(ok = issue_s(A))) break;
         next_a(A);
         if (!ok) break;
@@ -385,6 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (!ok) break;
+      if (a_later) {
+        if (!(ok = issue_s(A))) break;
+        next_a(A);
+        if (!ok) break;
+      }
       ++B.g;
       if (++B.i == B.n) {
         if (lane == 0) ring_release(ring, B.t);
