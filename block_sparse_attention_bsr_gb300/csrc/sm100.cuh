@@ -301,6 +301,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Stores 16 words (32 bf16) at p (16-byte aligned): two 256-bit stores when
+// p is 32-byte aligned (each then fills whole 32-byte sectors), else four
+// 128-bit stores.
+__device__ __forceinline__ void st_global_64B(void* p, const uint32_t (&w)[16]) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"((char*)p + 32 * h),
+                   "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
+                   "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                   : "memory");
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) ((uint4*)p)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }

@@ -85,16 +85,10 @@ __device__ __forceinline__ void store_acc_cols(uint32_t taddr, __nv_bfloat16* gr
     uint32_t v[32];
     tmem_ld32(taddr + c * 32, v);
     tmem_wait_ld();
-    uint4* dst = (uint4*)(grow + c * 32);
+    uint32_t w[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 o;
-      o.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * mul, __uint_as_float(v[q * 8 + 1]) * mul);
-      o.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * mul, __uint_as_float(v[q * 8 + 3]) * mul);
-      o.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * mul, __uint_as_float(v[q * 8 + 5]) * mul);
-      o.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * mul, __uint_as_float(v[q * 8 + 7]) * mul);
-      dst[q] = o;
-    }
+    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
+    st_global_64B(grow + c * 32, w);
   }
 }
 
@@ -150,13 +144,10 @@ __device__ __forceinline__ void merge_tiles(const float* tile0, size_t stride, i
 #pragma unroll
     for (int j = 0; j < 32; ++j) acc[j] = 0.f;
     for (int ch = 0; ch < nc; ++ch) part_accum32(tile0 + ch * stride, cg0 + c * 8, r, 1.f, acc);
-    uint4* d = (uint4*)(dst + c * 32);
+    uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      d[j] = make_uint4(pack_bf16x2(acc[8 * j] * mul, acc[8 * j + 1] * mul),
-                        pack_bf16x2(acc[8 * j + 2] * mul, acc[8 * j + 3] * mul),
-                        pack_bf16x2(acc[8 * j + 4] * mul, acc[8 * j + 5] * mul),
-                        pack_bf16x2(acc[8 * j + 6] * mul, acc[8 * j + 7] * mul));
+    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(acc[2 * j] * mul, acc[2 * j + 1] * mul);
+    st_global_64B(dst + c * 32, w);
   }
 }
 

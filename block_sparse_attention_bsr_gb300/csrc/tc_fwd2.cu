@@ -543,21 +543,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t0 + c * 32, u);
           tmem_ld32(t0 + D + c * 32, v);
           tmem_wait_ld();
-          uint4* dst = (uint4*)(orow + c * 32);
+          uint32_t o[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = q * 8 + 2 * e;
-              const float2 y = fma2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])),
-                                    make_float2(w.x, w.x),
-                                    mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
-                                         make_float2(w.y, w.y)));
-              o[e] = pack_bf16x2(y.x, y.y);
-            }
-            dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int j = 0; j < 16; ++j) {
+            const float2 y = fma2(make_float2(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1])),
+                                  make_float2(w.x, w.x),
+                                  mul2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                                       make_float2(w.y, w.y)));
+            o[j] = pack_bf16x2(y.x, y.y);
           }
+          st_global_64B(orow + c * 32, o);
         }
         if (hg == 0) {
           const float M = fmaxf(m_true, mt1);
@@ -619,12 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float w = ex2(ld_partial(src + 128 * D + (hg * 128 + r) * 4).x - M) * inv;
               part_accum32(src, hg * (D / 8) + c * 8, r, w, acc);
             }
-            uint4* dst = (uint4*)(orow + c * 32);
+            uint32_t o[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_uint4(pack_bf16x2(acc[8 * j], acc[8 * j + 1]), pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
-                                  pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
-                                  pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+            for (int j = 0; j < 16; ++j) o[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+            st_global_64B(orow + c * 32, o);
           }
           if (hg == 0) {
             a.row_max[grow] = M * kLn2;
