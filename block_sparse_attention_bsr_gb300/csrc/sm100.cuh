@@ -163,6 +163,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// The same descriptor split into words for one operand tile: the low word
+// holds the start address (>> 4) and LBO, the high word SBO, the fixed
+// version bit and the swizzle mode.  A byte offset inside the tile adds
+// off >> 4 to the low word (the operand address stays below 256 KB, so the
+// 14-bit address field never carries), which keeps the per-MMA descriptor
+// arithmetic at one integer add.
+struct SDesc {
+  uint32_t lo, hi;
+  __device__ __forceinline__ SDesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+      : lo(((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16)),
+        hi(((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29)) {}
+  __device__ __forceinline__ uint64_t at(uint32_t off) const { return ((uint64_t)hi << 32) | (lo + (off >> 4)); }
+};
+
 // Instruction descriptor for kind::f16 / kind::tf32: fp32 accumulator,
 // operand format code `ab_fmt` (1 = bf16, 0 = f16 under kind::f16; 2 = tf32
 // under kind::tf32), A / B major-ness (0 = K-major, 1 = MN-major), N and M.

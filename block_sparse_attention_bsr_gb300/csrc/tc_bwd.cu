@@ -349,16 +349,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&bars->v_full[vs], (c.g / C::kVStages) & 1, ab, a.status)) return false;
         if (!warp_wait(&bars->sdp_free, (c.g & 1) ^ 1, ab, a.status)) return false;
         tc_fence_after();
-        const uint32_t kb = aK + ks * C::kTile, vb = aV + vs * C::kTile;
+        const SDesc dQ(aQ, 16, 1024), dO(adO, 16, 1024), dK(aK + ks * C::kTile, 16, 1024),
+            dV(aV + vs * C::kTile, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColS, smem_desc(aQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
+          mma_bf16_ss_by(leader, tmem + kColS, dQ.at(off), dK.at(off), idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColDP, smem_desc(adO + off, 16, 1024), smem_desc(vb + off, 16, 1024), idS, kk > 0);
+          mma_bf16_ss_by(leader, tmem + kColDP, dO.at(off), dV.at(off), idS, kk > 0);
         }
         mma_commit_by(leader, &bars->v_empty[vs]);
         mma_commit_by(leader, &bars->sdp_full);
@@ -393,11 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = B.g % C::kKStages;
         if (!(ok = warp_wait(&bars->ds_full[B.g & 1], (B.g >> 1) & 1, ab, a.status))) break;
         tc_fence_after();
-        const uint32_t kb = aK + st * C::kTile;
+        const SDesc dK(aK + st * C::kTile, 16384, 1024);
+        const uint32_t ds = tmem + kColDS + (B.g & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts_by(leader, tmem + kColDQ, tmem + kColDS + (B.g & 1) * 64 + kk * 8, smem_desc(kb + kk * 2048, 16384, 1024), idDQ,
-                      (B.i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts_by(leader, tmem + kColDQ, ds + kk * 8, dK.at(kk * 2048), idDQ, (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->k_empty[st]);
         mma_commit_by(leader, &bars->dq_done[B.g & 1]);
         __syncwarp();
@@ -670,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idST = instr_desc(1, 0, 0, 128, 128);
       const uint32_t idG = instr_desc(1, 0, 1, D, 128);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
-      const uint32_t aDST = smem_u32(sDST);
+      const SDesc dST(smem_u32(sDST), 16, 1024);
       bool ok = true;
       auto seek_a = [&](Cursor& c) {
         while (true) {
@@ -722,11 +723,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c.i == 0 && !warp_wait(&bars->kv_full, c.q & 1, ab, a.status)) return false;
         if (!warp_wait(&bars->q_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
         tc_fence_after();
-        const uint32_t qb = aQ + st * C::kTile;
+        const SDesc dK(aK, 16, 1024), dQ(aQ + st * C::kTile, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColST, smem_desc(aK + off, 16, 1024), smem_desc(qb + off, 16, 1024), idST, kk > 0);
+          mma_bf16_ss_by(leader, tmem + kColST, dK.at(off), dQ.at(off), idST, kk > 0);
         }
         mma_commit_by(leader, &bars->st_full);
         return true;
@@ -735,11 +736,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = c.g % C::kStages;
         if (!warp_wait(&bars->do_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
         tc_fence_after();
-        const uint32_t gb = adO + st * C::kTile;
+        const SDesc dV(aV, 16, 1024), dO(adO + st * C::kTile, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColDPT, smem_desc(aV + off, 16, 1024), smem_desc(gb + off, 16, 1024), idST, kk > 0);
+          mma_bf16_ss_by(leader, tmem + kColDPT, dV.at(off), dO.at(off), idST, kk > 0);
         }
         mma_commit_by(leader, &bars->dpt_full);
         if (c.i == c.n - 1) mma_commit_by(leader, &bars->kv_empty);
@@ -753,13 +754,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       while (ok && !B.done) {
         const int st = B.g % C::kStages;
-        const uint32_t qb = aQ + st * C::kTile, gb = adO + st * C::kTile;
+        const SDesc dQmn(aQ + st * C::kTile, 16384, 1024), dOmn(adO + st * C::kTile, 16384, 1024);
         if (!(ok = warp_wait(&bars->pt_ready, B.g & 1, ab, a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts_by(leader, tmem + kColDV, tmem + kColST + kk * 8 + (kk >= 4 ? 32 : 0),
-                         smem_desc(gb + kk * 2048, 16384, 1024), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts_by(leader, tmem + kColDV, tmem + kColST + kk * 8 + (kk >= 4 ? 32 : 0), dOmn.at(kk * 2048), idG,
+                         (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->do_empty[st]);
         mma_commit_by(leader, &bars->pt_free);
         auto issue_next = [&]() -> bool {
@@ -781,8 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColDK, smem_desc(aDST + off, 16, 1024), smem_desc(qb + kk * 2048, 16384, 1024),
-                         idG, (B.i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ss_by(leader, tmem + kColDK, dST.at(off), dQmn.at(kk * 2048), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit_by(leader, &bars->q_empty[st]);
         mma_commit_by(leader, &bars->dst_free);

@@ -286,12 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&bars->k_full[ks], (i / C::kKStages) & 1, bars, a.status)) return false;
       if (!warp_wait(&bars->s_free, (i & 1) ^ 1, bars, a.status)) return false;
       tc_fence_after();
-      const uint32_t kb = aK + ks * C::kTile;
-      const uint32_t qa = aQ + qb * C::kTile;
+      const SDesc dQ(aQ + qb * C::kTile, 16, 1024), dK(aK + ks * C::kTile, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_bf16_ss_by(leader, tmem, smem_desc(qa + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
+        mma_bf16_ss_by(leader, tmem, dQ.at(off), dK.at(off), idS, kk > 0);
       }
       mma_commit_by(leader, &bars->k_empty[ks]);
       mma_commit_by(leader, &bars->s_full);
@@ -373,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait(&bars->p_full[0], i & 1, bars, a.status))) break;
       if (B.i == 0 && !(ok = warp_wait(&bars->p_full[1], i & 1, bars, a.status))) break;
       tc_fence_after();
-      const uint32_t vb = aV + vs * C::kTile;
+      const SDesc dV(aV + vs * C::kTile, 16384, 1024);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (h == 1 && B.i > 0) {
@@ -383,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ts_by(leader, tmem + kColO + h * D, tmem + kColP + b * 64 + h * 32 + kk * 8,
-                         smem_desc(vb + (4 * h + kk) * 2048, 16384, 1024), idPV, (B.i > 0 || kk > 0) ? 1u : 0u);
+                         dV.at((4 * h + kk) * 2048), idPV, (B.i > 0 || kk > 0) ? 1u : 0u);
         if (h == 1) mma_commit_by(leader, &bars->v_empty[vs]);
         mma_commit_by(leader, &bars->pv_done[h]);
       }
