@@ -253,8 +253,7 @@ void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split) {
 }
 
 bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split) {
-  bsr_status st = launch_delta(a, s);
-  if (st != BSR_OK) return st;
+  bsr_status st;
   if (tc_bwd_supported(a.d)) {
     PlanArgs p{};
     p.list[0] = PlanList{a.row_ptr, a.row_plan};
@@ -264,9 +263,10 @@ bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split) {
     p.BH = a.d.BH;
     p.allow_split = split ? 1 : 0;
     p.status = a.status;
-    if ((st = launch_plan(p, 2, s)) != BSR_OK) return st;
+    if ((st = launch_delta_plan(a, p, 2, s)) != BSR_OK) return st;
     return launch_bwd_tc(a, s);
   }
+  if ((st = launch_delta(a, s)) != BSR_OK) return st;
   st = launch_dq_simt(a, s);
   if (st == BSR_OK) st = launch_dkdv_simt(a, s);
   return st;

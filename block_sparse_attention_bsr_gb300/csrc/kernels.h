@@ -148,6 +148,9 @@ struct PlanArgs {
 
 // Builds `lists` (1 or 2) plans.
 bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s);
+// Delta / lse2 and the plans of `p` in one launch where the plans are small
+// (else launch_delta then launch_plan).
+bsr_status launch_delta_plan(const BwdArgs& a, const PlanArgs& p, int lists, cudaStream_t s);
 
 // RAII bracket that records a pair of CUDA events around one kernel launch
 // when profiling is enabled (bsr_profile_enable).

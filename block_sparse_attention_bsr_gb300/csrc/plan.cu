@@ -18,6 +18,7 @@
 // follows "trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.9.0].
 // Plan layout (int32): see PlanLayout in kernels.h.
 
+#include "delta.cuh"
 #include "kernels.h"
 
 namespace bsr {
@@ -68,11 +69,12 @@ __device__ void scan_desc(int* hist, int n, int* warp_sums) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
-  extern __shared__ int sm_plan[];  // hist[n + 1], count[n + 1], len[n]
+// Builds list `li` of p with the whole CTA; sm_plan holds 3 n + 2 ints
+// (hist[n + 1], count[n + 1], len[n]).
+__device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   __shared__ int warp_sums[32];
   __shared__ int counts[3];         // items, split lines, slots
-  const PlanList& L = p.list[blockIdx.x];
+  const PlanList& L = p.list[li];
   const int n = p.n;
   int* hist = sm_plan;
   int* count = sm_plan + (n + 1);
@@ -165,6 +167,36 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   }
 }
 
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
+  extern __shared__ int sm_plan[];
+  plan_body(p, blockIdx.x, sm_plan);
+}
+
+// Delta / lse2 of the backward pass and its work lists in one launch: the
+// first `lists` CTAs build the plans while the others compute the per-row
+// statistics (the two are independent; both must be done before dQ and
+// dK / dV start).
+constexpr int kFusedThreads = 256;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kFusedThreads) delta_plan_kernel(BwdArgs a, PlanArgs p, int lists) {
+  extern __shared__ int sm_plan[];
+  if ((int)blockIdx.x < lists)
+    plan_body(p, blockIdx.x, sm_plan);
+  else
+    delta_rows<T, D, kFusedThreads>(a, (int)blockIdx.x - lists);
+}
+
+template <typename T, int D>
+bsr_status launch_fused(const BwdArgs& a, const PlanArgs& p, int lists, size_t smem, cudaStream_t s) {
+  const size_t rows = (size_t)a.d.BH * a.d.S;
+  constexpr size_t per = delta_rows_per_cta<D, kFusedThreads>();
+  const unsigned grid = (unsigned)(lists + (rows + per - 1) / per);
+  LaunchTimer timer("delta_plan", s);
+  delta_plan_kernel<T, D><<<grid, kFusedThreads, smem, s>>>(a, p, lists);
+  return check_launch("delta_plan launch");
+}
+
 }  // namespace
 
 bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
@@ -177,6 +209,20 @@ bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
   LaunchTimer timer("plan", s);
   plan_kernel<<<lists, kPlanThreads, smem, s>>>(p);
   return check_launch("plan launch");
+}
+
+bsr_status launch_delta_plan(const BwdArgs& a, const PlanArgs& p, int lists, cudaStream_t s) {
+  // fused only while the planner's shared memory and its O(n^2 / threads)
+  // stable placement stay small
+  const size_t smem = sizeof(int) * (3 * (size_t)p.n + 2);
+  const bool fuse = p.n <= 512 && a.d.dtype == BSR_BF16 && (a.d.D == 64 || a.d.D == 128);
+  if (!fuse) {
+    bsr_status st = launch_delta(a, s);
+    if (st != BSR_OK) return st;
+    return launch_plan(p, lists, s);
+  }
+  return a.d.D == 64 ? launch_fused<__nv_bfloat16, 64>(a, p, lists, smem, s)
+                     : launch_fused<__nv_bfloat16, 128>(a, p, lists, smem, s);
 }
 
 }  // namespace bsr

@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include "delta.cuh"
 #include "kernels.h"
 
 namespace bsr {
@@ -177,60 +178,9 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
 }
 
 // ------------------------------------------------------------------ delta --
-// D_i = dO_i . O_i (fp32) and the base-2 log-sum-exp of the row,
-// lse2_i = row_max_i log2(e) + log2(row_denom_i), one value each per query
-// row.  G lanes share a row, each reading 8 contiguous elements per step.
-template <typename T>
-__device__ __forceinline__ float dot8(const T* a, const T* b);
-template <>
-__device__ __forceinline__ float dot8<__nv_bfloat16>(const __nv_bfloat16* a, const __nv_bfloat16* b) {
-  const uint4 x = *(const uint4*)a, y = *(const uint4*)b;
-  const __nv_bfloat162* xa = (const __nv_bfloat162*)&x;
-  const __nv_bfloat162* ya = (const __nv_bfloat162*)&y;
-  float s = 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 u = __bfloat1622float2(xa[k]), v = __bfloat1622float2(ya[k]);
-    s = fmaf(u.x, v.x, s);
-    s = fmaf(u.y, v.y, s);
-  }
-  return s;
-}
-template <>
-__device__ __forceinline__ float dot8<float>(const float* a, const float* b) {
-  const float4 x0 = *(const float4*)a, x1 = *(const float4*)(a + 4);
-  const float4 y0 = *(const float4*)b, y1 = *(const float4*)(b + 4);
-  float s = x0.x * y0.x;
-  s = fmaf(x0.y, y0.y, s);
-  s = fmaf(x0.z, y0.z, s);
-  s = fmaf(x0.w, y0.w, s);
-  s = fmaf(x1.x, y1.x, s);
-  s = fmaf(x1.y, y1.y, s);
-  s = fmaf(x1.z, y1.z, s);
-  s = fmaf(x1.w, y1.w, s);
-  return s;
-}
-
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) delta_kernel(BwdArgs a) {
-  constexpr int CH = D / 8;              // 8-element chunks per row
-  constexpr int G = CH < 32 ? CH : 32;   // lanes per row
-  constexpr int RPW = 32 / G;            // rows per warp
-  const int lane = threadIdx.x % 32;
-  const size_t rows = (size_t)a.d.BH * a.d.S;
-  const size_t row = ((size_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * RPW + lane / G;
-  const bool valid = row < rows;
-  float s = 0.f;
-  if (valid) {
-    const T* o = (const T*)a.O + row * D;
-    const T* g = (const T*)a.dO + row * D;
-    for (int c = lane % G; c < CH; c += G) s += dot8<T>(o + c * 8, g + c * 8);
-  }
-  s = group_sum<G>(s);
-  if (valid && lane % G == 0) {
-    a.delta[row] = s;
-    a.lse2[row] = a.row_max[row] * 1.4426950408889634f + log2f(a.row_denom[row]);
-  }
+  delta_rows<T, D, kThreads>(a, blockIdx.x);
 }
 
 // --------------------------------------------------------------------- dQ --
@@ -438,8 +388,8 @@ template <typename T, int D>
 bsr_status delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   constexpr int G = D / 8 < 32 ? D / 8 : 32;
   const size_t rows = (size_t)a.d.BH * a.d.S;
-  const size_t rows_per_cta = (kThreads / 32) * (32 / G);
-  dim3 grid((unsigned)((rows + rows_per_cta - 1) / rows_per_cta));
+  (void)G;
+  dim3 grid((unsigned)((rows + delta_rows_per_cta<D, kThreads>() - 1) / delta_rows_per_cta<D, kThreads>()));
   return launch(delta_kernel<T, D>, grid, 0, s, "delta", &a);
 }
 
