@@ -42,6 +42,35 @@ def alg_flops(wl, nnzb, part="total"):
     return per * BLOCK * BLOCK * wl.head_dim * nnzb * wl.batch * wl.heads
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a
+# kernel on a workload, from one ncu capture, with the SHA-256 of the source
+# files the kernel was built from at the time; reported only while the
+# current sources still hash the same (otherwise the roofline's traffic is
+# null until the kernel is captured again).
+MEASURED_TRAFFIC = {
+    ("global_s8192", "dkdv_tc"): {"bytes": 206.2e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                  "sha256": "f7f9082229700749ab7254c23e7a605770cf23bc668e31e059f2d44c8c2ceafe"},
+    ("global_s8192", "dq_tc"): {"bytes": 181.0e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                "sha256": "f7f9082229700749ab7254c23e7a605770cf23bc668e31e059f2d44c8c2ceafe"},
+    ("global_s8192", "fwd_tc"): {"bytes": 136.6e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+                                 "sha256": "744ad6101477ec353834bcfe97f3a5032f76056547da2d919e97897440c01333"},
+}
+
+
+def measured_traffic(workload, kernel):
+    rec = MEASURED_TRAFFIC.get((workload, kernel))
+    if rec is None:
+        return None
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "block_sparse_attention_bsr_gb300", "csrc")
+    for f in rec["sources"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest() == rec["sha256"] else None
+
+
 def kernel_flops(name, wl, nnzb):
     for key, mult in FLOP_PER_BLOCK.items():
         if name.startswith(key):
@@ -209,7 +238,8 @@ def run_ours(args, rank, world, dev):
         achieved = kf / (avg_ms * 1e-3) / 1e12 if kf else None
         roofline = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
                     "unit": "TFLOP/s", "frac": (achieved / peaks["bf16"]) if achieved else None,
-                    "traffic": None, "peak_source": peaks["source"] + " bf16 burst",
+                    "traffic": measured_traffic(wl.name, name), "traffic_unit": "bytes per launch (ncu DRAM)",
+                    "peak_source": peaks["source"] + " bf16 burst",
                     "flop_per_launch": kf, "ms_per_launch": avg_ms}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -69,8 +69,19 @@ __device__ void scan_desc(int* hist, int n, int* warp_sums) {
   __syncthreads();
 }
 
-// Builds list `li` of p with the whole CTA; sm_plan holds 3 n + 2 ints
-// (hist[n + 1], count[n + 1], len[n]).
+// Chunking of a line of `len` blocks when no chunk may exceed Lmax: nc
+// chunks, the first r of length b + 1 and the others of length b.  Returned
+// as b, and r << 16 | nc (nc <= len / 8 + 1 < 2^16 for the lists the
+// planner accepts).
+__device__ __forceinline__ int chunking(int len, int Lmax, int* rn) {
+  const int nc = len > Lmax ? (len + Lmax - 1) / Lmax : 1;
+  *rn = ((len % nc) << 16) | nc;
+  return len / nc;
+}
+
+// Builds list `li` of p with the whole CTA; sm_plan holds 5 n + 2 ints
+// (hist[n + 1], count[n + 1], chunk length b[n], r << 16 | nc [n], first
+// block offset[n]).
 __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   __shared__ int warp_sums[32];
   __shared__ int counts[3];         // items, split lines, slots
@@ -78,7 +89,9 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   const int n = p.n;
   int* hist = sm_plan;
   int* count = sm_plan + (n + 1);
-  int* lens = sm_plan + 2 * (n + 1);
+  int* cb = sm_plan + 2 * (n + 1);
+  int* crn = cb + n;
+  int* offs = crn + n;
   const int32_t* ptr = L.ptr;
   PlanLayout lay = plan_layout(L.plan, n, p.G, p.BH);
 
@@ -91,12 +104,17 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   if (lim < 8) lim = 8;
   const int Lmax = p.allow_split ? (int)(lim < n ? lim : n) : n;
 
-  // pass 1: histogram of chunk lengths
+  // pass 1: chunking of every line and histogram of chunk lengths
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int len = line_len(ptr, i, n);
-    lens[i] = len;
-    const int nc = len > Lmax ? (len + Lmax - 1) / Lmax : 1;
-    for (int c = 0; c < nc; ++c) atomicAdd(&hist[len / nc + (c < len % nc ? 1 : 0)], 1);
+    offs[i] = ptr[i];
+    int rn;
+    const int bl = chunking(len, Lmax, &rn);
+    cb[i] = bl;
+    crn[i] = rn;
+    const int nc = rn & 0xFFFF, r = rn >> 16;
+    if (r > 0) atomicAdd(&hist[bl + 1], r);
+    atomicAdd(&hist[bl], nc - r);
     atomicAdd(&counts[0], nc);
   }
   __syncthreads();
@@ -118,8 +136,7 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   // so CTAs that start together work on neighbouring lines
   const bool stable = n <= 2048;  // O(n^2 / threads) shared-memory reads
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int len = lens[i];
-    const int nc = len > Lmax ? (len + Lmax - 1) / Lmax : 1;
+    const int bl = cb[i], nc = crn[i] & 0xFFFF, rl = crn[i] >> 16;
     int base = -1;
     if (nc > 1) {
       const int sl = atomicAdd(&counts[1], 1);
@@ -133,21 +150,22 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
         base = -1;
       }
     }
-    int off = ptr[i];
+    // items of length bl + 1 and bl of the lines before this one
+    int before_hi = 0, before_lo = 0;
+    if (stable) {
+      for (int j = 0; j < i; ++j) {
+        const int bj = cb[j], ncj = crn[j] & 0xFFFF, rj = crn[j] >> 16;
+        before_hi += (bj + 1 == bl + 1 ? rj : 0) + (bj == bl + 1 ? ncj - rj : 0);
+        before_lo += (bj + 1 == bl ? rj : 0) + (bj == bl ? ncj - rj : 0);
+      }
+    }
+    int off = offs[i];
     for (int c = 0; c < nc; ++c) {
-      const int clen = len / nc + (c < len % nc ? 1 : 0);
+      const bool hi = c < rl;
+      const int clen = bl + (hi ? 1 : 0);
       int pos;
       if (stable) {
-        // items of length clen that come before (line i, chunk c) in line order
-        int before = 0;
-        for (int j = 0; j < i; ++j) {
-          const int lj = lens[j];
-          const int ncj = lj > Lmax ? (lj + Lmax - 1) / Lmax : 1;
-          const int bj = lj / ncj, rj = lj % ncj;
-          before += (clen == bj + 1 ? rj : 0) + (clen == bj ? ncj - rj : 0);
-        }
-        for (int c2 = 0; c2 < c; ++c2) before += (len / nc + (c2 < len % nc ? 1 : 0)) == clen ? 1 : 0;
-        pos = hist[clen] + before;
+        pos = hist[clen] + (hi ? before_hi + c : before_lo + (c - rl));
       } else {
         pos = atomicAdd(&hist[clen], 1);
       }
@@ -200,7 +218,7 @@ bsr_status launch_fused(const BwdArgs& a, const PlanArgs& p, int lists, size_t s
 }  // namespace
 
 bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
-  const size_t smem = sizeof(int) * (3 * (size_t)p.n + 2);
+  const size_t smem = sizeof(int) * (5 * (size_t)p.n + 2);
   if (smem > 200 * 1024) return fail(BSR_ERR_UNSUPPORTED, "plan: %d block rows exceed the planner's limit", p.n);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -214,7 +232,7 @@ bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
 bsr_status launch_delta_plan(const BwdArgs& a, const PlanArgs& p, int lists, cudaStream_t s) {
   // fused only while the planner's shared memory and its O(n^2 / threads)
   // stable placement stay small
-  const size_t smem = sizeof(int) * (3 * (size_t)p.n + 2);
+  const size_t smem = sizeof(int) * (5 * (size_t)p.n + 2);
   const bool fuse = p.n <= 512 && a.d.dtype == BSR_BF16 && (a.d.D == 64 || a.d.D == 128);
   if (!fuse) {
     bsr_status st = launch_delta(a, s);
