@@ -171,12 +171,12 @@ def run_ours(args, rank, world, dev):
     bsr.bsr_attn_check()
 
     # device-resident timed region: per-step CUDA events, L2 flushed before each step
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    bsr.profile_collect()
-    bsr.profile_enable(True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+    def timed_steps(per_kernel):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        bsr.profile_collect()
+        bsr.profile_enable(per_kernel)
+        barrier(world)
+        torch.cuda.synchronize(dev)
         for i in range(args.steps):
             flush_l2(l2)
             evs[i][0].record(stream)
@@ -184,12 +184,18 @@ def run_ours(args, rank, world, dev):
             evs[i][1].record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
-    bsr.profile_enable(False)
-    prof = bsr.profile_collect()
-    bsr.bsr_attn_check()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = max_over_ranks(sum(step_ms), world)
-    ms_per_step = total_ms / args.steps
+        bsr.profile_enable(False)
+        prof = bsr.profile_collect()
+        bsr.bsr_attn_check()
+        return max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world) / args.steps, prof
+
+    # The headline pass records no events between the kernels of a step (each
+    # such record adds a few microseconds of idle GPU time); a second pass of
+    # the same K steps brackets every launch with events for the per-kernel
+    # durations the roofline uses.
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        ms_per_step, _ = timed_steps(False)
+        ms_per_step_instr, prof = timed_steps(True)
 
     # forward alone and backward alone (same protocol, untimed for the headline)
     def time_part(fn, reps):
@@ -250,6 +256,8 @@ def run_ours(args, rank, world, dev):
                    "nnzb": nnzb, "density": round(nnzb / wl.nb ** 2, 4), "l2": "flushed before every step",
                    "parallelism": f"replicas x{world}"},
         "ms_fwd": round(ms_fwd, 4), "ms_bwd": round(ms_bwd, 4),
+        "kernel_timing": {"pass": "second pass of the same K steps with CUDA events around every launch",
+                          "ms_per_step": round(ms_per_step_instr, 4)},
         "pct_of_bf16_peak": round(100 * value / world / peaks["bf16"], 2),
         "alg_gflop_per_step": flops / 1e9,
         "kernels": kern,

@@ -63,32 +63,34 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Writes 32 consecutive K-elements (bf16) of row r of a 128 x 128 K-major
-// operand tile with the 128-byte swizzle: K indices [32 c, 32 c + 32).
-__device__ __forceinline__ void st_row_chunk(uint32_t tile, int r, int c, const float* x) {
-  const uint32_t row = tile + (c >> 1) * 16384 + r * 128;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int u = (c & 1) * 4 + q;  // 16-byte unit inside the 128-byte row
-    st_shared_v4(row + ((u ^ (r & 7)) << 4), pack_bf16x2(x[q * 8 + 0], x[q * 8 + 1]),
-                 pack_bf16x2(x[q * 8 + 2], x[q * 8 + 3]), pack_bf16x2(x[q * 8 + 4], x[q * 8 + 5]),
-                 pack_bf16x2(x[q * 8 + 6], x[q * 8 + 7]));
-  }
-}
-
 // Stores NC fp32 TMEM columns of this thread's lane (from taddr) as bf16
-// times `mul` to global memory at grow.
+// times `mul` to global memory at grow: 64 columns per round, both 32-column
+// loads in flight before the one wait.
 template <int NC>
 __device__ __forceinline__ void store_acc_cols(uint32_t taddr, __nv_bfloat16* grow, float mul) {
+  static_assert(NC % 32 == 0, "whole 32-column loads");
 #pragma unroll 1
-  for (int c = 0; c < NC / 32; ++c) {
-    uint32_t v[32];
-    tmem_ld32(taddr + c * 32, v);
+  for (int c = 0; c < NC / 64; ++c) {
+    uint32_t v[32], u[32];
+    tmem_ld32(taddr + c * 64, v);
+    tmem_ld32(taddr + c * 64 + 32, u);
     tmem_wait_ld();
     uint32_t w[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
-    st_global_64B(grow + c * 32, w);
+    st_global_64B(grow + c * 64, w);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(u[2 * j]) * mul, __uint_as_float(u[2 * j + 1]) * mul);
+    st_global_64B(grow + c * 64 + 32, w);
+  }
+  if constexpr (NC % 64 != 0) {
+    uint32_t v[32];
+    tmem_ld32(taddr + NC - 32, v);
+    tmem_wait_ld();
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
+    st_global_64B(grow + NC - 32, w);
   }
 }
 
@@ -184,6 +186,7 @@ struct DqBars {
   uint32_t tmem_slot;
   int abort_flag;
 };
+static_assert(sizeof(DqBars) <= 512, "barrier block overflows its shared-memory slot");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -505,29 +508,36 @@ template <int D>
 struct DkvCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTile = 128 * D * 2;
-  static constexpr int kStages = D == 64 ? 4 : 2;
-  static constexpr int kOp = 128 * 128 * 2;  // dS^T tile
-  static constexpr int kStatOff = kTile * (2 + 2 * kStages) + kOp;
+  // Q_g is read by S^T_g and, last, by dK_g; Q of block g+kQStages can only
+  // load once dK_g is done, so Q gets one stage more than dO (read by dP^T_g
+  // and dV_g, both early in the block).
+  static constexpr int kQStages = D == 64 ? 4 : 3;
+  static constexpr int kOStages = D == 64 ? 4 : 2;
+  static constexpr int kStatStages = 2;
   static constexpr int kStat = 2 * 128 * 4;  // lse2 and delta of one block row's 128 queries
-  static constexpr int kBarOff = kStatOff + kStages * kStat;
+  static constexpr int kStatOff = kTile * (2 + kQStages + kOStages);
+  static constexpr int kBarOff = kStatOff + kStatStages * kStat;
   // The dynamic shared memory base is 1024-byte aligned (checked at run
   // time), so this kernel, which needs almost all of the 227 KB, keeps no
   // alignment slack.
-  static constexpr int kSmem = kBarOff + 384;
+  static constexpr int kSmem = kBarOff + 512;
 };
 
 struct DkvBars {
-  uint64_t kv_full;
-  uint64_t kv_empty;
+  uint64_t k_full;
+  uint64_t k_empty;  // the item's last S^T is done
+  uint64_t v_full;
+  uint64_t v_empty;  // the item's last dP^T is done
   uint64_t st_full;   // S^T of the block in TMEM
   uint64_t dpt_full;  // dP^T of the block in TMEM
-  uint64_t dpt_free;  // both warpgroups have loaded dP^T
-  uint64_t pt_ready;
-  uint64_t ds_ready;
-  uint64_t pt_free;
-  uint64_t dst_free;
+  uint64_t pt_ready;  // P^T (over the S^T columns) in TMEM
+  uint64_t ds_ready;  // dS^T (over the dP^T columns) in TMEM
+  uint64_t pt_free;   // dV of the block done: the S^T columns are free
+  uint64_t dk_done;   // dK of the block done: the dP^T columns are free
   uint64_t final_mma;
   uint64_t wg_sync[2];
+  uint64_t stat_full[2];   // lse2 / delta of the block in shared memory
+  uint64_t stat_empty[2];  // both warpgroups are done with them
   uint64_t q_full[4];
   uint64_t q_empty[4];
   uint64_t do_full[4];
@@ -537,12 +547,12 @@ struct DkvBars {
   uint32_t tmem_slot;
   int abort_flag;
 };
+static_assert(sizeof(DkvBars) <= 512, "barrier block overflows its shared-memory slot");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                   const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV, BwdArgs a) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, BwdArgs a) {
   using C = DkvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // no slack for re-alignment: refuse (uniform, before any barrier)
@@ -553,12 +563,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = sm;
   uint8_t* sV = sK + C::kTile;
   uint8_t* sQ = sV + C::kTile;
-  uint8_t* sdO = sQ + C::kStages * C::kTile;
-  uint8_t* sDST = sdO + C::kStages * C::kTile;
+  uint8_t* sdO = sQ + C::kQStages * C::kTile;
   float* sStat = (float*)(sm + C::kStatOff);  // [stage][lse2 | delta][128]
   DkvBars* bars = (DkvBars*)(sm + C::kBarOff);
-  // P^T (bf16) is written over the S^T columns each warpgroup has read:
-  // queries [0, 64) at column 0, queries [64, 128) at column 64.
+  // P^T (bf16) is written over the S^T columns and dS^T (bf16) over the dP^T
+  // columns each warpgroup has read: queries [0, 64) at column +0, queries
+  // [64, 128) at column +64.
   constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -567,21 +577,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Walk walk = make_walk(lay, a.d.BH);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->kv_full, 1);
-    mbar_init(&bars->kv_empty, 1);
+    mbar_init(&bars->k_full, 1);
+    mbar_init(&bars->k_empty, 1);
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->v_empty, 1);
     mbar_init(&bars->st_full, 1);
     mbar_init(&bars->dpt_full, 1);
-    mbar_init(&bars->dpt_free, kEw);
     mbar_init(&bars->pt_ready, kEw);
     mbar_init(&bars->ds_ready, kEw);
     mbar_init(&bars->pt_free, 1);
-    mbar_init(&bars->dst_free, 1);
+    mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->final_mma, 1);
-    mbar_init(&bars->wg_sync[0], 128);
-    mbar_init(&bars->wg_sync[1], 128);
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->wg_sync[i], 128);
+      mbar_init(&bars->stat_full[i], 1);
+      mbar_init(&bars->stat_empty[i], kEw);
+    }
+    for (int i = 0; i < C::kQStages; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
+    }
+    for (int i = 0; i < C::kOStages; ++i) {
       mbar_init(&bars->do_full[i], 1);
       mbar_init(&bars->do_empty[i], 1);
     }
@@ -606,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ producer --
-      int g = 0, q = 0;
+      int g = 0, q = 0, vq = 0, lq = 0, ls = 0, lo = 0;  // blocks, items (K), V; Q / stats / dO loads issued
       bool ok = true;
       for (int t = 0; ok; ++t) {
         int k;
@@ -614,14 +630,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         Cursor cur;
         walk.decode(k, cur);
         if (cur.n == 0) continue;
-        // K, V of a new item: the previous item's S^T / dP^T must be done
-        if (!(ok = mbar_wait(&bars->kv_empty, (q & 1) ^ 1, ab, a.status))) break;
+        // K of a new item once the previous item's last S^T is done; V
+        // (first needed by dP^T) once its last dP^T is done, after the
+        // first block's Q
+        if (!(ok = mbar_wait(&bars->k_empty, (q & 1) ^ 1, ab, a.status))) break;
         const int krow = cur.bh * S + cur.line * 128;
-        mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTile);
-        for (int b = 0; b < C::kBoxes; ++b) {
-          tma_load_2d(sK + b * 16384, &tmK, b * 64, krow, &bars->kv_full);
-          tma_load_2d(sV + b * 16384, &tmV, b * 64, krow, &bars->kv_full);
-        }
+        mbar_arrive_expect_tx(&bars->k_full, C::kTile);
+        for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(sK + b * 16384, &tmK, b * 64, krow, &bars->k_full);
         ++q;
         for (int i = 0; i < cur.n; ++i, ++g) {
           int m = a.row_idx[cur.first + i];
@@ -630,28 +645,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = 0;
           }
           const int qrow = cur.bh * S + m * 128;
-          const int st = g % C::kStages;
-          const uint32_t use = g / C::kStages;
-          if (!(ok = mbar_wait(&bars->q_empty[st], (use & 1) ^ 1, ab, a.status))) break;
-          mbar_arrive_expect_tx(&bars->q_full[st], C::kTile + C::kStat);
+          const int sq = g % C::kQStages, so = g % C::kOStages, ss = g % C::kStatStages;
+          if (!(ok = mbar_wait(&bars->q_empty[sq], ((g / C::kQStages) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->q_full[sq], C::kTile);
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_2d(sQ + st * C::kTile + b * 16384, &tmQ, b * 64, qrow, &bars->q_full[st]);
-          bulk_load(sStat + st * 256, a.lse2 + qrow, 512, &bars->q_full[st]);
-          bulk_load(sStat + st * 256 + 128, a.delta + qrow, 512, &bars->q_full[st]);
-          if (!(ok = mbar_wait(&bars->do_empty[st], (use & 1) ^ 1, ab, a.status))) {
-            ++g;
-            break;
+            tma_load_2d(sQ + sq * C::kTile + b * 16384, &tmQ, b * 64, qrow, &bars->q_full[sq]);
+          lq = g + 1;
+          if (!(ok = mbar_wait(&bars->stat_empty[ss], ((g / C::kStatStages) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->stat_full[ss], C::kStat);
+          bulk_load(sStat + ss * 256, a.lse2 + qrow, 512, &bars->stat_full[ss]);
+          bulk_load(sStat + ss * 256 + 128, a.delta + qrow, 512, &bars->stat_full[ss]);
+          ls = g + 1;
+          if (i == 0) {
+            if (!(ok = mbar_wait(&bars->v_empty, (vq & 1) ^ 1, ab, a.status))) break;
+            mbar_arrive_expect_tx(&bars->v_full, C::kTile);
+            for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(sV + b * 16384, &tmV, b * 64, krow, &bars->v_full);
+            ++vq;
           }
-          mbar_arrive_expect_tx(&bars->do_full[st], C::kTile);
+          if (!(ok = mbar_wait(&bars->do_empty[so], ((g / C::kOStages) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->do_full[so], C::kTile);
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_2d(sdO + st * C::kTile + b * 16384, &tmdO, b * 64, qrow, &bars->do_full[st]);
+            tma_load_2d(sdO + so * C::kTile + b * 16384, &tmdO, b * 64, qrow, &bars->do_full[so]);
+          lo = g + 1;
         }
       }
-      if (q > 0) drain_wait(&bars->kv_full, (q - 1) & 1);
-      for (int i = (g > C::kStages ? g - C::kStages : 0); i < g; ++i) {
-        drain_wait(&bars->q_full[i % C::kStages], (i / C::kStages) & 1);
-        drain_wait(&bars->do_full[i % C::kStages], (i / C::kStages) & 1);
-      }
+      // drain: every copy issued must land before the CTA exits
+      if (q > 0) drain_wait(&bars->k_full, (q - 1) & 1);
+      if (vq > 0) drain_wait(&bars->v_full, (vq - 1) & 1);
+      for (int i = (lq > C::kQStages ? lq - C::kQStages : 0); i < lq; ++i)
+        drain_wait(&bars->q_full[i % C::kQStages], (i / C::kQStages) & 1);
+      for (int i = (ls > C::kStatStages ? ls - C::kStatStages : 0); i < ls; ++i)
+        drain_wait(&bars->stat_full[i % C::kStatStages], (i / C::kStatStages) & 1);
+      for (int i = (lo > C::kOStages ? lo - C::kOStages : 0); i < lo; ++i)
+        drain_wait(&bars->do_full[i % C::kOStages], (i / C::kOStages) & 1);
     }
   } else if (warp == 1) {
     {
@@ -659,19 +685,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The whole warp walks the schedule (descriptor arithmetic stays
       // warp-uniform); one elected lane issues the MMAs and commits.
       const uint32_t leader = elect_one();
-      // Per block g the pipe runs dV_g, S^T_{g+1}, dP^T_{g+1}, dK_g:
-      //   * dV_g as soon as P^T_g is in TMEM (pt_ready; P^T lies over the
-      //     S^T columns);
-      //   * S^T_{g+1} overwrites P^T_g, so it waits for dV_g to complete
-      //     (pt_free) -- the elementwise pass is still computing dS^T_g;
-      //   * dP^T_{g+1} once the elementwise pass has loaded dP^T_g;
-      //   * dK_g once dS^T_g is in shared memory (ds_ready).
-      // So S^T_{g+1} and dP^T_{g+1} are ready by the time the elementwise
-      // pass finishes block g.
+      // Per block g the pipe runs dV_g, S^T_{g+1}, dK_g, dP^T_{g+1}:
+      //   * dV_g (A = P^T from TMEM) as soon as P^T_g is there (pt_ready);
+      //   * S^T_{g+1} overwrites P^T_g, so it waits for dV_g (pt_free);
+      //   * dK_g (A = dS^T from TMEM) once dS^T_g is there (ds_ready);
+      //   * dP^T_{g+1} overwrites dS^T_g, so it waits for dK_g (dk_done).
+      // S^T_{g+1} is ready when the elementwise pass finishes block g; Q of
+      // block g+3 loads as soon as dK_g is done.  When block g+1 starts
+      // another item, dK_g goes before S^T_{g+1}, so that this item's
+      // epilogue does not wait behind the next item's MMAs.
       const uint32_t idST = instr_desc(1, 0, 0, 128, 128);
       const uint32_t idG = instr_desc(1, 0, 1, D, 128);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
-      const SDesc dST(smem_u32(sDST), 16, 1024);
       bool ok = true;
       auto seek_a = [&](Cursor& c) {
         while (true) {
@@ -719,31 +744,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto issue_st = [&](const Cursor& c) -> bool {
-        const int st = c.g % C::kStages;
-        if (c.i == 0 && !warp_wait(&bars->kv_full, c.q & 1, ab, a.status)) return false;
-        if (!warp_wait(&bars->q_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
+        const int sq = c.g % C::kQStages;
+        if (c.i == 0 && !warp_wait(&bars->k_full, c.q & 1, ab, a.status)) return false;
+        if (!warp_wait(&bars->q_full[sq], (c.g / C::kQStages) & 1, ab, a.status)) return false;
         tc_fence_after();
-        const SDesc dK(aK, 16, 1024), dQ(aQ + st * C::kTile, 16, 1024);
+        const SDesc dK(aK, 16, 1024), dQ(aQ + sq * C::kTile, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16_ss_by(leader, tmem + kColST, dK.at(off), dQ.at(off), idST, kk > 0);
         }
         mma_commit_by(leader, &bars->st_full);
+        if (c.i == c.n - 1) mma_commit_by(leader, &bars->k_empty);
         return true;
       };
       auto issue_dpt = [&](const Cursor& c) -> bool {
-        const int st = c.g % C::kStages;
-        if (!warp_wait(&bars->do_full[st], (c.g / C::kStages) & 1, ab, a.status)) return false;
+        const int so = c.g % C::kOStages;
+        if (c.i == 0 && !warp_wait(&bars->v_full, c.q & 1, ab, a.status)) return false;
+        if (!warp_wait(&bars->do_full[so], (c.g / C::kOStages) & 1, ab, a.status)) return false;
         tc_fence_after();
-        const SDesc dV(aV, 16, 1024), dO(adO + st * C::kTile, 16, 1024);
+        const SDesc dV(aV, 16, 1024), dO(adO + so * C::kTile, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16_ss_by(leader, tmem + kColDPT, dV.at(off), dO.at(off), idST, kk > 0);
         }
         mma_commit_by(leader, &bars->dpt_full);
-        if (c.i == c.n - 1) mma_commit_by(leader, &bars->kv_empty);
+        if (c.i == c.n - 1) mma_commit_by(leader, &bars->v_empty);
         return true;
       };
       Cursor A{0, 0, 0, 0, 0, 0, 0, 0, 0, false};
@@ -753,40 +780,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((ok = issue_st(A) && issue_dpt(A))) next_a(A);
       }
       while (ok && !B.done) {
-        const int st = B.g % C::kStages;
-        const SDesc dQmn(aQ + st * C::kTile, 16384, 1024), dOmn(adO + st * C::kTile, 16384, 1024);
+        const int sq = B.g % C::kQStages, so = B.g % C::kOStages;
+        const SDesc dQmn(aQ + sq * C::kTile, 16384, 1024), dOmn(adO + so * C::kTile, 16384, 1024);
         if (!(ok = warp_wait(&bars->pt_ready, B.g & 1, ab, a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ts_by(leader, tmem + kColDV, tmem + kColST + kk * 8 + (kk >= 4 ? 32 : 0), dOmn.at(kk * 2048), idG,
                          (B.i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_by(leader, &bars->do_empty[st]);
+        mma_commit_by(leader, &bars->do_empty[so]);
         mma_commit_by(leader, &bars->pt_free);
-        auto issue_next = [&]() -> bool {
+        const bool a_first = !A.done && A.i == 0;  // the next block starts another item
+        auto issue_s = [&]() -> bool {
           if (!warp_wait(&bars->pt_free, B.g & 1, ab, a.status)) return false;
-          if (!issue_st(A)) return false;
-          if (!warp_wait(&bars->dpt_free, B.g & 1, ab, a.status)) return false;
-          if (!issue_dpt(A)) return false;
-          next_a(A);
-          return ok;
+          return issue_st(A);
         };
-        // The next block's S^T / dP^T go before dK of this one, unless that
-        // block starts another item: then this item's last dK goes first, so
-        // that its epilogue does not wait behind the next item's MMAs (or
-        // that item's K / V loads); the next S^T runs during the epilogue.
-        const bool a_later = !A.done && A.i == 0;
-        if (!A.done && !a_later && !(ok = issue_next())) break;
+        if (!A.done && !a_first && !(ok = issue_s())) break;
         if (!(ok = warp_wait(&bars->ds_ready, B.g & 1, ab, a.status))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColDK, dST.at(off), dQmn.at(kk * 2048), idG, (B.i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts_by(leader, tmem + kColDK, tmem + kColDPT + kk * 8 + (kk >= 4 ? 32 : 0), dQmn.at(kk * 2048), idG,
+                         (B.i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_by(leader, &bars->q_empty[sq]);
+        mma_commit_by(leader, &bars->dk_done);
+        if (!A.done) {
+          if (a_first && !(ok = issue_s())) break;
+          if (!(ok = warp_wait(&bars->dk_done, B.g & 1, ab, a.status))) break;
+          if (!(ok = issue_dpt(A))) break;
+          next_a(A);
+          if (!ok) break;
         }
-        mma_commit_by(leader, &bars->q_empty[st]);
-        mma_commit_by(leader, &bars->dst_free);
-        if (a_later && !(ok = issue_next())) break;
         __syncwarp();
         ++B.g;
         if (++B.i == B.n) {
@@ -808,7 +832,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wl * 32 + lane;   // key row of the tile
     const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
     const float sl2 = a.d.scale * kLog2e;
-    const uint32_t aDST = smem_u32(sDST);
     int g = 0, sync_phase = 0;
     bool ok = true;
     for (int t = 0; ok; ++t) {
@@ -827,14 +850,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         zero_cols<D / 2>(dvrow);
       } else {
         for (int i = 0; i < cur.n; ++i, ++g) {
-          const int st = g % C::kStages;
+          const int ss = g % C::kStatStages;
           if (!(ok = warp_wait(&bars->st_full, g & 1, ab, a.status))) break;
+          if (!(ok = warp_wait(&bars->stat_full[ss], (g / C::kStatStages) & 1, ab, a.status))) break;
           tc_fence_after();
           float s[64], dp[64];
           tmem_ld64(tmem + lane_base + kColST + hg * 64, s);
-          // statistics of this block row's queries, brought in with Q (q_full
-          // completed before S^T_g was issued)
-          const float* lse = sStat + st * 256 + hg * 64;
+          // statistics of this block row's queries (bulk-copied by the producer)
+          const float* lse = sStat + ss * 256 + hg * 64;
           const float* dl = lse + 128;
           const float2 sc = make_float2(sl2, sl2);
 #pragma unroll
@@ -853,8 +876,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = warp_wait(&bars->dpt_full, g & 1, ab, a.status))) break;
           tc_fence_after();
           tmem_ld64(tmem + lane_base + kColDPT + hg * 64, dp);
-          tc_fence_before();
-          mbar_arrive(&bars->dpt_free);
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             const float2 d2 = *(const float2*)(dl + 2 * k);
@@ -863,51 +884,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             dp[2 * k] = x.x;
             dp[2 * k + 1] = x.y;
           }
-          if (g > 0 && !(ok = warp_wait(&bars->dst_free, (g - 1) & 1, ab, a.status))) break;
-          st_row_chunk(aDST, r, 2 * hg, dp);
-          st_row_chunk(aDST, r, 2 * hg + 1, dp + 32);
-          fence_proxy_async_smem();
+          mbar_arrive(&bars->stat_empty[ss]);
+          // dS^T over this warpgroup's own dP^T columns (read above; dK of
+          // the previous block finished before dP^T of this one began)
+          tmem_st_bf16x64(tmem + lane_base + kColDPT + hg * 64, dp);
+          tmem_wait_st();
+          tc_fence_before();
           mbar_arrive(&bars->ds_ready);
         }
         if (!ok) break;
-        if (!(ok = warp_wait(&bars->dst_free, (g - 1) & 1, ab, a.status))) break;
-        tc_fence_after();
         if (cur.slot < 0) {
-          if constexpr (D == 128) {
-            // dV then dK of this key tile, each staged as bf16 in the dS^T
-            // tile (free: the item's last dK has completed) in the TMA box
-            // layout and written by one TMA store per warpgroup: its 64
-            // columns are one box
-            const int row0 = cur.bh * S + cur.line * 128;
-#pragma unroll 1
-            for (int w = 0; w < 2; ++w) {
-              const uint32_t tcol = (w == 0 ? kColDV : kColDK) + hg * 64;
-              const float mul = w == 0 ? 1.f : a.d.scale;
-#pragma unroll 1
-              for (int c = 0; c < 2; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + tcol + c * 32, v);
-                tmem_wait_ld();
-                float x[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * mul;
-                st_row_chunk(aDST, r, 2 * hg + c, x);
-              }
-              fence_proxy_async_smem();
-              if (!(ok = group_sync(&bars->wg_sync[hg], sync_phase, ab, a.status))) break;
-              if (r == 0) {
-                tma_store_2d(w == 0 ? &tmdV : &tmdK, hg * 64, row0, sDST + hg * 16384);
-                bulk_commit();
-                bulk_wait_read();
-              }
-              if (!(ok = group_sync(&bars->wg_sync[hg], sync_phase, ab, a.status))) break;
-            }
-          } else {
-            store_acc_cols<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), dvrow, 1.f);
-            store_acc_cols<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), dkrow, a.d.scale);
-          }
-          if (!ok) break;
+          // dV is final once the item's last dV is done (pt_free), while its
+          // last dK may still run
+          if (!(ok = warp_wait(&bars->pt_free, (g - 1) & 1, ab, a.status))) break;
+          tc_fence_after();
+          store_acc_cols<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), dvrow, 1.f);
+          if (!(ok = warp_wait(&bars->dk_done, (g - 1) & 1, ab, a.status))) break;
+          tc_fence_after();
+          store_acc_cols<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), dkrow, a.d.scale);
         } else {
+          if (!(ok = warp_wait(&bars->dk_done, (g - 1) & 1, ab, a.status))) break;
+          tc_fence_after();
           // chunk of a split column: publish the fp32 partials, the last chunk merges
           const size_t kTileF = (size_t)128 * D;
           const size_t tile = (size_t)cur.slot * a.d.BH + cur.bh;
@@ -932,7 +929,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ring_release(ring, t);
     }
-    bulk_wait_all();  // TMA stores issued by this thread have completed
   }
 
   tc_fence_before();
@@ -942,8 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, const CUtensorMap& tmdK,
-                      const CUtensorMap& tmdV, int grid, cudaStream_t s) {
+bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, int grid, cudaStream_t s) {
   {
     auto kern = dq_tc_kernel<D>;
     const int smem = DqCfg<D>::kSmem;
@@ -961,7 +956,7 @@ bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap&
     if (e != cudaSuccess)
       return fail(BSR_ERR_CUDA, "dkdv_tc: cudaFuncSetAttribute(%d): %s", smem, cudaGetErrorString(e));
     LaunchTimer timer("dkdv_tc", s);
-    kern<<<grid, kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, tmdK, tmdV, a);
+    kern<<<grid, kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
     return check_launch("dkdv_tc launch");
   }
 }
@@ -984,13 +979,11 @@ bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   TensorMaps tm;
   bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
   if (st != BSR_OK) return st;
-  CUtensorMap tmdO, tmdK, tmdV;
+  CUtensorMap tmdO;
   if ((st = make_tensor_map(a.d, a.dO, &tmdO, "dO")) != BSR_OK) return st;
-  if ((st = make_tensor_map(a.d, a.dK, &tmdK, "dK")) != BSR_OK) return st;
-  if ((st = make_tensor_map(a.d, a.dV, &tmdV, "dV")) != BSR_OK) return st;
   switch (a.d.D) {
-    case 64: return launch_bwd<64>(a, tm, tmdO, tmdK, tmdV, grid, s);
-    case 128: return launch_bwd<128>(a, tm, tmdO, tmdK, tmdV, grid, s);
+    case 64: return launch_bwd<64>(a, tm, tmdO, grid, s);
+    case 128: return launch_bwd<128>(a, tm, tmdO, grid, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "bwd_tc: head_dim %d", a.d.D);
   }
 }
