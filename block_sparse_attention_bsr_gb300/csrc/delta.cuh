@@ -63,12 +63,20 @@ __device__ __forceinline__ void delta_rows(const BwdArgs& a, int cta) {
   const int lane = threadIdx.x % 32;
   const size_t rows = (size_t)a.d.BH * a.d.S;
   const size_t row0 = ((size_t)cta * (kThreads / 32) + threadIdx.x / 32) * RPW * U + lane / G;
-  float s[U];
+  // the row statistics are loaded with the operands (one round trip to
+  // memory, not two), by the lane that writes the row's results
+  float s[U], rmax[U], rden[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     s[u] = 0.f;
+    rmax[u] = 0.f;
+    rden[u] = 1.f;
     const size_t row = row0 + (size_t)u * RPW;
     if (row < rows) {
+      if (lane % G == 0) {
+        rmax[u] = a.row_max[row];
+        rden[u] = a.row_denom[row];
+      }
       const T* o = (const T*)a.O + row * D;
       const T* g = (const T*)a.dO + row * D;
 #pragma unroll
@@ -83,7 +91,7 @@ __device__ __forceinline__ void delta_rows(const BwdArgs& a, int cta) {
     const size_t row = row0 + (size_t)u * RPW;
     if (row < rows && lane % G == 0) {
       a.delta[row] = t;
-      a.lse2[row] = a.row_max[row] * 1.4426950408889634f + log2f(a.row_denom[row]);
+      a.lse2[row] = rmax[u] * 1.4426950408889634f + log2f(rden[u]);
     }
   }
 }

@@ -79,9 +79,12 @@ __device__ __forceinline__ int chunking(int len, int Lmax, int* rn) {
   return len / nc;
 }
 
-// Builds list `li` of p with the whole CTA; sm_plan holds 5 n + 2 ints
-// (hist[n + 1], count[n + 1], chunk length b[n], r << 16 | nc [n], first
-// block offset[n]).
+// Shared-memory ints plan_body needs for n lines: hist, count, bucket rank
+// and the prefix offsets ([n + 1] each), chunk length b, r << 16 | nc and
+// first block offset ([n] each).
+__host__ __device__ constexpr size_t plan_smem_ints(int n) { return 4 * ((size_t)n + 1) + 3 * (size_t)n; }
+
+// Builds list `li` of p with the whole CTA in sm_plan (plan_smem_ints(n)).
 __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   __shared__ int warp_sums[32];
   __shared__ int counts[3];         // items, split lines, slots
@@ -89,13 +92,18 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   const int n = p.n;
   int* hist = sm_plan;
   int* count = sm_plan + (n + 1);
-  int* cb = sm_plan + 2 * (n + 1);
+  int* rank = sm_plan + 2 * (n + 1);
+  int* ptr = sm_plan + 3 * (n + 1);  // the list's prefix offsets, staged once
+  int* cb = sm_plan + 4 * (n + 1);
   int* crn = cb + n;
   int* offs = crn + n;
-  const int32_t* ptr = L.ptr;
   PlanLayout lay = plan_layout(L.plan, n, p.G, p.BH);
 
-  for (int v = threadIdx.x; v <= n; v += blockDim.x) hist[v] = 0;
+  // all offsets in one round trip to memory
+  for (int v = threadIdx.x; v <= n; v += blockDim.x) {
+    hist[v] = 0;
+    ptr[v] = L.ptr[v];
+  }
   if (threadIdx.x < 3) counts[threadIdx.x] = 0;
   __syncthreads();
 
@@ -118,19 +126,17 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
     atomicAdd(&counts[0], nc);
   }
   __syncthreads();
-  for (int v = threadIdx.x; v <= n; v += blockDim.x) count[v] = hist[v];
+  for (int v = threadIdx.x; v <= n; v += blockDim.x) {
+    count[v] = hist[v];
+    rank[v] = hist[v] > 0 ? 1 : 0;
+  }
   __syncthreads();
   scan_desc(hist, n, warp_sums);  // hist[v] = first item of length v
-  // bucket table, longest first
-  if (threadIdx.x == 0) {
-    int nbk = 0;
-    for (int v = n; v >= 0; --v) {
-      if (count[v] == 0) continue;
-      lay.buckets[nbk] = PlanBucket{hist[v] * p.BH, hist[v], count[v], v};
-      ++nbk;
-    }
-    lay.header[3] = nbk;
-  }
+  scan_desc(rank, n, warp_sums);  // rank[v] = bucket of length v (longest first)
+  // bucket table
+  for (int v = threadIdx.x; v <= n; v += blockDim.x)
+    if (count[v] > 0) lay.buckets[rank[v]] = PlanBucket{hist[v] * p.BH, hist[v], count[v], v};
+  if (threadIdx.x == 0) lay.header[3] = rank[0] + (count[0] > 0 ? 1 : 0);
 
   // pass 2: place the items; inside a length bucket lines ascend (stable),
   // so CTAs that start together work on neighbouring lines
@@ -217,22 +223,29 @@ bsr_status launch_fused(const BwdArgs& a, const PlanArgs& p, int lists, size_t s
 
 }  // namespace
 
+// Planner threads: enough for one line each (the loops stride past that),
+// a whole number of warps, at most the kernel's bound.
+static int plan_threads(int n) {
+  const int t = ((n + 1 + 31) / 32) * 32;
+  return t < 128 ? 128 : (t > kPlanThreads ? kPlanThreads : t);
+}
+
 bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
-  const size_t smem = sizeof(int) * (5 * (size_t)p.n + 2);
+  const size_t smem = sizeof(int) * plan_smem_ints(p.n);
   if (smem > 200 * 1024) return fail(BSR_ERR_UNSUPPORTED, "plan: %d block rows exceed the planner's limit", p.n);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "plan: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   }
   LaunchTimer timer("plan", s);
-  plan_kernel<<<lists, kPlanThreads, smem, s>>>(p);
+  plan_kernel<<<lists, plan_threads(p.n), smem, s>>>(p);
   return check_launch("plan launch");
 }
 
 bsr_status launch_delta_plan(const BwdArgs& a, const PlanArgs& p, int lists, cudaStream_t s) {
   // fused only while the planner's shared memory and its O(n^2 / threads)
   // stable placement stay small
-  const size_t smem = sizeof(int) * (5 * (size_t)p.n + 2);
+  const size_t smem = sizeof(int) * plan_smem_ints(p.n);
   const bool fuse = p.n <= 512 && a.d.dtype == BSR_BF16 && (a.d.D == 64 || a.d.D == 128);
   if (!fuse) {
     bsr_status st = launch_delta(a, s);

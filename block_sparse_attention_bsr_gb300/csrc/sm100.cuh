@@ -308,6 +308,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Loads 64 fp32 TMEM columns of this lane (two 32-column loads) and waits.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
+  uint32_t a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_wait_ld();
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    x[k] = __uint_as_float(a[k]);
+    x[32 + k] = __uint_as_float(b[k]);
+  }
+}
+
 // ------------------------------------------------------------- helpers --
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -101,19 +101,6 @@ __device__ __forceinline__ void zero_cols(__nv_bfloat16* grow) {
   for (int c = 0; c < NC / 8; ++c) ((uint4*)grow)[c] = z;
 }
 
-// Loads 64 fp32 TMEM columns of this lane (two 32-column loads) and waits.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
-  uint32_t a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-  tmem_wait_ld();
-#pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    x[k] = __uint_as_float(a[k]);
-    x[32 + k] = __uint_as_float(b[k]);
-  }
-}
-
 // Packs 64 fp32 values to bf16 pairs and stores them in 32 TMEM columns.
 __device__ __forceinline__ void tmem_st_bf16x64(uint32_t taddr, const float (&x)[64]) {
   uint32_t v[32];

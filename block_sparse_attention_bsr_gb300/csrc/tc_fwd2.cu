@@ -79,8 +79,8 @@ struct Bars {
   uint64_t q_empty[2];
   uint64_t s_full;
   uint64_t s_free;      // both warpgroups have loaded S into registers
-  uint64_t p_full[2];   // by key half: P_h of the current block is in TMEM
-  uint64_t pv_done[2];  // by key half: P_h V_h of a block done (half 1 also covers half 0)
+  uint64_t p_full[2][2];  // by P buffer b and key half h: P_h of block g (g % 2 = b) is in TMEM
+  uint64_t pv_done[2];    // by P buffer b: both halves' P.V of block g (g % 2 = b) are done
   uint64_t final_mma;
   uint64_t red_full;   // both warpgroups' row statistics written
   uint64_t red_empty;  // both warpgroups have read them
@@ -163,7 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
-      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_full[i][0], 128);
+      mbar_init(&bars->p_full[i][1], 128);
       mbar_init(&bars->pv_done[i], 1);
       mbar_init(&bars->wg_sync[i], 128);
     }
@@ -369,22 +370,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait(&bars->v_full[vs], (i / C::kVStages) & 1, bars, a.status))) break;
       // The first block of a row overwrites both accumulators, which both
       // warpgroups read while combining the previous row: wait for both.
-      if (!(ok = warp_wait(&bars->p_full[0], i & 1, bars, a.status))) break;
-      if (B.i == 0 && !(ok = warp_wait(&bars->p_full[1], i & 1, bars, a.status))) break;
+      if (!(ok = warp_wait(&bars->p_full[b][0], (i >> 1) & 1, bars, a.status))) break;
+      if (B.i == 0 && !(ok = warp_wait(&bars->p_full[b][1], (i >> 1) & 1, bars, a.status))) break;
       tc_fence_after();
       const SDesc dV(aV + vs * C::kTile, 16384, 1024);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (h == 1 && B.i > 0) {
-          if (!(ok = warp_wait(&bars->p_full[1], i & 1, bars, a.status))) break;
+          if (!(ok = warp_wait(&bars->p_full[b][1], (i >> 1) & 1, bars, a.status))) break;
           tc_fence_after();
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ts_by(leader, tmem + kColO + h * D, tmem + kColP + b * 64 + h * 32 + kk * 8,
                          dV.at((4 * h + kk) * 2048), idPV, (B.i > 0 || kk > 0) ? 1u : 0u);
-        if (h == 1) mma_commit_by(leader, &bars->v_empty[vs]);
-        mma_commit_by(leader, &bars->pv_done[h]);
+        if (h == 1) {
+          mma_commit_by(leader, &bars->v_empty[vs]);
+          mma_commit_by(leader, &bars->pv_done[b]);
+        }
       }
       __syncwarp();
       if (!ok) break;
@@ -488,15 +491,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[k] = pack_bf16x2(p.x, p.y);
         }
         l += (sum4[0].x + sum4[0].y + sum4[1].x + sum4[1].y) + (sum4[2].x + sum4[2].y + sum4[3].x + sum4[3].y);
-        // The previous block's P_h V_h must be done before O_h is rescaled
-        // and before P_h of this block overwrites the P buffer of the block
-        // before that; it also keeps this warpgroup at most one block ahead
-        // of the MMA thread's p_full wait.
-        if (g > 0) {
-          if (!(ok = warp_wait(&bars->pv_done[hg], (g - 1) & 1, bars, a.status))) break;
+        // P of this block goes to buffer b once P.V of block g - 2 (the
+        // buffer's previous use) is done; the MMA thread's p_full wait for
+        // block g - 2 came before that P.V, so this warpgroup's arrivals on
+        // p_full[b] never run two phases ahead of it.  O_h is rescaled only
+        // once P.V of block g - 1 is done as well.
+        if (g >= 2) {
+          if (!(ok = warp_wait(&bars->pv_done[b], ((g >> 1) - 1) & 1, bars, a.status))) break;
           tc_fence_after();
         }
         if (rescale) {
+          if (!(ok = warp_wait(&bars->pv_done[b ^ 1], ((g - 1) >> 1) & 1, bars, a.status))) break;
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
@@ -511,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tmem + lane_base + kColP + b * 64 + hg * 32, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[hg]);
+        mbar_arrive(&bars->p_full[b][hg]);
       }
       if (!ok) break;
       // ----------------------------------------------------- epilogue --
@@ -529,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float R = fmaxf(m0, m1);
       const float c0 = ex2(m0 - R), c1 = ex2(m1 - R);
       const float L = l0 * c0 + l1 * c1;
-      // both halves' last P.V (pv_done[1] also covers half 0)
-      if (!(ok = warp_wait(&bars->pv_done[1], (g - 1) & 1, bars, a.status))) break;
+      // both halves' last P.V
+      if (!(ok = warp_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, bars, a.status))) break;
       tc_fence_after();
       const uint32_t t0 = tmem + lane_base + kColO + hg * (D / 2);
       if (cur.slot < 0) {
