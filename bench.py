@@ -256,7 +256,9 @@ def run_ours(args, rank, world, dev):
                    "nnzb": nnzb, "density": round(nnzb / wl.nb ** 2, 4), "l2": "flushed before every step",
                    "parallelism": f"replicas x{world}"},
         "ms_fwd": round(ms_fwd, 4), "ms_bwd": round(ms_bwd, 4),
-        "kernel_timing": {"pass": "second pass of the same K steps with CUDA events around every launch",
+        "kernel_timing": {"pass": "second pass of the same K steps with CUDA events around every launch; "
+                                  "dQ and dK/dV run one after the other there (the headline pass overlaps them "
+                                  "on two streams)",
                           "ms_per_step": round(ms_per_step_instr, 4)},
         "pct_of_bf16_peak": round(100 * value / world / peaks["bf16"], 2),
         "alg_gflop_per_step": flops / 1e9,

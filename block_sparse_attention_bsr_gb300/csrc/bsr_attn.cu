@@ -69,6 +69,11 @@ bsr_status fail(bsr_status status, const char* fmt, ...) {
   return status;
 }
 
+bool profiling_launches() {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  return g_prof_on;
+}
+
 LaunchTimer::LaunchTimer(const char* name, cudaStream_t stream) : slot_(-1), stream_(stream) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (!g_prof_on) return;
@@ -94,6 +99,32 @@ int sm_count() {
   if (!cache[dev] && cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     cache[dev] = 0;
   return cache[dev];
+}
+
+// Per device: a second stream and a fork / join event pair, for kernels of
+// one call that may run side by side (created once, kept for the process).
+bsr_status side_stream(SideStream* out, std::unique_lock<std::mutex>* hold) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(BSR_ERR_CUDA, "side stream: cudaGetDevice failed");
+  static std::mutex mu;
+  static std::vector<SideStream> cache;
+  std::unique_lock<std::mutex> lock(mu);
+  if ((int)cache.size() <= dev) cache.resize(dev + 1);
+  SideStream& ss = cache[dev];
+  if (!ss.s) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess)
+      return fail(BSR_ERR_CUDA, "side stream: create failed: %s", cudaGetErrorString(cudaGetLastError()));
+    ss.s = st;
+    ss.fork = f;
+    ss.join = j;
+  }
+  *out = ss;
+  *hold = std::move(lock);  // the caller forks and joins under the lock
+  return BSR_OK;
 }
 
 bsr_status check_launch(const char* what) {

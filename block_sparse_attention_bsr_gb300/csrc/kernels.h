@@ -2,6 +2,8 @@
 // kernels.  Shared by the C-ABI front end and the kernel translation units.
 #pragma once
 
+#include <mutex>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -154,6 +156,11 @@ bsr_status launch_delta_plan(const BwdArgs& a, const PlanArgs& p, int lists, cud
 
 // RAII bracket that records a pair of CUDA events around one kernel launch
 // when profiling is enabled (bsr_profile_enable).
+// True while per-launch timing is on: kernels that normally overlap on two
+// streams then run one after the other, so that each launch's events bracket
+// that kernel alone.
+bool profiling_launches();
+
 class LaunchTimer {
  public:
   LaunchTimer(const char* name, cudaStream_t stream);
@@ -180,6 +187,15 @@ size_t bwd_scratch_bytes(const Dims& d, int G, bool split);
 void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split);
 // Launches delta, plan, dQ and dK/dV on `s` (scratch carved already).
 bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split);
+
+// A second stream of the current device with a fork / join event pair.
+// The fork and join must happen while *hold is held (calls from several host
+// threads share the pair).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+bsr_status side_stream(SideStream* out, std::unique_lock<std::mutex>* hold);
 
 // Number of SMs of the current device (cached per device); 0 on error.
 int sm_count();

@@ -924,28 +924,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// dQ and dK / dV read the same inputs and write different outputs, so they
+// run side by side: dK / dV on a second stream forked from `s` and joined
+// back into it.  Their CTAs never share an SM (each needs almost all of its
+// shared memory), so the second kernel's CTAs take the SMs the first one
+// leaves in its tail.
 template <int D>
 bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, int grid, cudaStream_t s) {
-  {
-    auto kern = dq_tc_kernel<D>;
-    const int smem = DqCfg<D>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_tc: cudaFuncSetAttribute(%d): %s", smem, cudaGetErrorString(e));
-    LaunchTimer timer("dq_tc", s);
-    kern<<<grid, kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
-    bsr_status st = check_launch("dq_tc launch");
-    if (st != BSR_OK) return st;
-  }
-  {
-    auto kern = dkdv_tc_kernel<D>;
-    const int smem = DkvCfg<D>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess)
-      return fail(BSR_ERR_CUDA, "dkdv_tc: cudaFuncSetAttribute(%d): %s", smem, cudaGetErrorString(e));
+  auto dq = dq_tc_kernel<D>;
+  auto dkdv = dkdv_tc_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmem);
+  if (e != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "dq_tc: cudaFuncSetAttribute(%d): %s", DqCfg<D>::kSmem, cudaGetErrorString(e));
+  e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<D>::kSmem);
+  if (e != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "dkdv_tc: cudaFuncSetAttribute(%d): %s", DkvCfg<D>::kSmem, cudaGetErrorString(e));
+  if (profiling_launches()) {  // one after the other, each timed alone
+    {
+      LaunchTimer timer("dq_tc", s);
+      dq<<<grid, kThreads, DqCfg<D>::kSmem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
+      bsr_status st = check_launch("dq_tc launch");
+      if (st != BSR_OK) return st;
+    }
     LaunchTimer timer("dkdv_tc", s);
-    kern<<<grid, kThreads, smem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
+    dkdv<<<grid, kThreads, DkvCfg<D>::kSmem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
     return check_launch("dkdv_tc launch");
   }
+  SideStream side;
+  std::unique_lock<std::mutex> hold;
+  bsr_status st = side_stream(&side, &hold);
+  if (st != BSR_OK) return st;
+  if ((e = cudaEventRecord(side.fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(side.s, side.fork, 0)) != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "bwd_tc: fork: %s", cudaGetErrorString(e));
+  dkdv<<<grid, kThreads, DkvCfg<D>::kSmem, side.s>>>(tm.q, tm.k, tm.v, tmdO, a);
+  st = check_launch("dkdv_tc launch");
+  if (st == BSR_OK) {
+    dq<<<grid, kThreads, DqCfg<D>::kSmem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
+    st = check_launch("dq_tc launch");
+  }
+  // join even after a failed launch, so `s` stays ordered after the side stream
+  if ((e = cudaEventRecord(side.join, side.s)) != cudaSuccess || (e = cudaStreamWaitEvent(s, side.join, 0)) != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "bwd_tc: join: %s", cudaGetErrorString(e));
+  return st;
 }
 
 }  // namespace
