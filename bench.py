@@ -48,12 +48,12 @@ def alg_flops(wl, nnzb, part="total"):
 # current sources still hash the same (otherwise the roofline's traffic is
 # null until the kernel is captured again).
 MEASURED_TRAFFIC = {
-    ("global_s8192", "dkdv_tc"): {"bytes": 206.2e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                  "sha256": "f7f9082229700749ab7254c23e7a605770cf23bc668e31e059f2d44c8c2ceafe"},
-    ("global_s8192", "dq_tc"): {"bytes": 181.0e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                "sha256": "f7f9082229700749ab7254c23e7a605770cf23bc668e31e059f2d44c8c2ceafe"},
-    ("global_s8192", "fwd_tc"): {"bytes": 136.6e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "744ad6101477ec353834bcfe97f3a5032f76056547da2d919e97897440c01333"},
+    ("global_s8192", "dkdv_tc"): {"bytes": 209.4e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                  "sha256": "9ae82b5b4c95aab3023746093e1ae7f4c79ee7672c07e9451a3769b864795fe1"},
+    ("global_s8192", "dq_tc"): {"bytes": 181.4e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                "sha256": "9ae82b5b4c95aab3023746093e1ae7f4c79ee7672c07e9451a3769b864795fe1"},
+    ("global_s8192", "fwd_tc"): {"bytes": 136.2e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+                                 "sha256": "f42c1790ba22eaebcc08235902cfc37b8e8647f5864f9f22332d830c1548b0c8"},
 }
 
 
