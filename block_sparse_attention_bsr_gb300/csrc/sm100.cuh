@@ -6,6 +6,9 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stddef.h>
+
+#include <cuda_bf16.h>
 
 namespace bsr {
 namespace sm100 {
@@ -342,6 +345,61 @@ __device__ __forceinline__ void st_global_64B(void* p, const uint32_t (&w)[16]) 
   } else {
 #pragma unroll
     for (int q = 0; q < 4; ++q) ((uint4*)p)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
+// Stores 64 bf16 (32 packed words w) of each of the warp's 32 consecutive
+// rows: lane l holds row l, which starts at `row` (its own pointer), rows
+// `ld` elements apart.  The four lanes of each group of four rows exchange
+// 32-byte chunks (a 4 x 4 block transpose in two shuffle steps: partner
+// lanes l ^ 2, then l ^ 1), so each 256-bit store writes 8 rows x 128
+// contiguous bytes instead of 32 rows x 32 bytes (a quarter of the
+// cache-line touches).  The whole warp calls it; `row` must be 32-byte
+// aligned and ld * 2 a multiple of 32 (otherwise rows are stored as they
+// are).  w is clobbered.
+__device__ __forceinline__ void st_rows64_bf16(uint32_t (&w)[32], __nv_bfloat16* row, size_t ld) {
+  const int q = threadIdx.x & 3;
+  const bool aligned = ((reinterpret_cast<uintptr_t>(row) & 31) == 0) && ((ld * 2) % 32 == 0);
+  if (!__all_sync(0xffffffffu, aligned)) {
+    uint32_t h[16];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) h[j] = w[16 * c + j];
+      st_global_64B(row + 32 * c, h);
+    }
+    return;
+  }
+  const bool b1 = (q & 2) != 0, b0 = (q & 1) != 0;
+  // chunk c of lane q = words 8 c .. 8 c + 7 = row q, columns 16 c .. 16 c + 15
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {  // chunks c and c + 2 with lane q ^ 2
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t lo = w[8 * c + j], hi = w[8 * (c + 2) + j];
+      const uint32_t r = __shfl_xor_sync(0xffffffffu, b1 ? lo : hi, 2);
+      w[8 * c + j] = b1 ? r : lo;
+      w[8 * (c + 2) + j] = b1 ? hi : r;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 4; c += 2) {  // chunks c and c + 1 with lane q ^ 1
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t lo = w[8 * c + j], hi = w[8 * (c + 1) + j];
+      const uint32_t r = __shfl_xor_sync(0xffffffffu, b0 ? lo : hi, 1);
+      w[8 * c + j] = b0 ? r : lo;
+      w[8 * (c + 1) + j] = b0 ? hi : r;
+    }
+  }
+  // lane q now holds, in words 8 k .. 8 k + 7, chunk q of row (l - q) + k
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __nv_bfloat16* p = row + (ptrdiff_t)(k - q) * (ptrdiff_t)ld + 16 * q;
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[8 * k]),
+                 "r"(w[8 * k + 1]), "r"(w[8 * k + 2]), "r"(w[8 * k + 3]), "r"(w[8 * k + 4]), "r"(w[8 * k + 5]),
+                 "r"(w[8 * k + 6]), "r"(w[8 * k + 7])
+                 : "memory");
   }
 }
 

@@ -64,10 +64,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Stores NC fp32 TMEM columns of this thread's lane (from taddr) as bf16
-// times `mul` to global memory at grow: 64 columns per round, both 32-column
-// loads in flight before the one wait.
+// times `mul` to global memory at grow (the warp's 32 lanes hold 32
+// consecutive rows, ld elements apart): 64 columns per round, both 32-column
+// loads in flight before the one wait, rows exchanged in groups of four so
+// the stores cover whole 128-byte lines (st_rows64_bf16).
 template <int NC>
-__device__ __forceinline__ void store_acc_cols(uint32_t taddr, __nv_bfloat16* grow, float mul) {
+__device__ __forceinline__ void store_acc_cols(uint32_t taddr, __nv_bfloat16* grow, float mul, size_t ld) {
   static_assert(NC % 32 == 0, "whole 32-column loads");
 #pragma unroll 1
   for (int c = 0; c < NC / 64; ++c) {
@@ -75,13 +77,13 @@ __device__ __forceinline__ void store_acc_cols(uint32_t taddr, __nv_bfloat16* gr
     tmem_ld32(taddr + c * 64, v);
     tmem_ld32(taddr + c * 64 + 32, u);
     tmem_wait_ld();
-    uint32_t w[16];
+    uint32_t w[32];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
-    st_global_64B(grow + c * 64, w);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(u[2 * j]) * mul, __uint_as_float(u[2 * j + 1]) * mul);
-    st_global_64B(grow + c * 64 + 32, w);
+    for (int j = 0; j < 16; ++j) {
+      w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
+      w[16 + j] = pack_bf16x2(__uint_as_float(u[2 * j]) * mul, __uint_as_float(u[2 * j + 1]) * mul);
+    }
+    st_rows64_bf16(w, grow + c * 64, ld);
   }
   if constexpr (NC % 64 != 0) {
     uint32_t v[32];
@@ -461,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(&bars->dq_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ab, a.status))) break;
         tc_fence_after();
         if (cur.slot < 0) {
-          store_acc_cols<D / 2>(tmem + lane_base + kColDQ + hg * (D / 2), dqrow, a.d.scale);
+          store_acc_cols<D / 2>(tmem + lane_base + kColDQ + hg * (D / 2), dqrow, a.d.scale, (size_t)D);
         } else {
           // chunk of a split row: publish the fp32 partial, the last chunk merges
           const size_t kTileF = (size_t)128 * D;
@@ -885,10 +887,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // last dK may still run
           if (!(ok = warp_wait(&bars->pt_free, (g - 1) & 1, ab, a.status))) break;
           tc_fence_after();
-          store_acc_cols<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), dvrow, 1.f);
+          store_acc_cols<D / 2>(tmem + lane_base + kColDV + hg * (D / 2), dvrow, 1.f, (size_t)D);
           if (!(ok = warp_wait(&bars->dk_done, (g - 1) & 1, ab, a.status))) break;
           tc_fence_after();
-          store_acc_cols<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), dkrow, a.d.scale);
+          store_acc_cols<D / 2>(tmem + lane_base + kColDK + hg * (D / 2), dkrow, a.d.scale, (size_t)D);
         } else {
           if (!(ok = warp_wait(&bars->dk_done, (g - 1) & 1, ab, a.status))) break;
           tc_fence_after();

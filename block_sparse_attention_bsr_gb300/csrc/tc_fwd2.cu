@@ -542,22 +542,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cur.slot < 0) {
         const float inv = 1.f / L;
         const float2 w = make_float2(c0 * inv, c1 * inv);
-#pragma unroll 1
+        // this half's D / 2 output columns as bf16, stored 64 at a time with
+        // the rows exchanged in groups of four (st_rows64_bf16)
+        uint32_t o[D / 4];
+#pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           uint32_t u[32], v[32];
           tmem_ld32(t0 + c * 32, u);
           tmem_ld32(t0 + D + c * 32, v);
           tmem_wait_ld();
-          uint32_t o[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float2 y = fma2(make_float2(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1])),
                                   make_float2(w.x, w.x),
                                   mul2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
                                        make_float2(w.y, w.y)));
-            o[j] = pack_bf16x2(y.x, y.y);
+            o[16 * c + j] = pack_bf16x2(y.x, y.y);
           }
-          st_global_64B(orow + c * 32, o);
+        }
+        if constexpr (D == 128) {
+          st_rows64_bf16(o, orow, (size_t)D);
+        } else {
+          st_global_64B(orow, o);
         }
         if (hg == 0) {
           const float M = fmaxf(m_true, mt1);
