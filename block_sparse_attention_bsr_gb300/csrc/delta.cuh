@@ -13,13 +13,27 @@ namespace bsr {
 // D_i = dO_i . O_i (fp32) and the base-2 log-sum-exp of the row,
 // lse2_i = row_max_i log2(e) + log2(row_denom_i), one value each per query
 // row.  G lanes share a row, each reading 8 contiguous elements per step.
+
+// 8 contiguous elements in registers, as loaded.
 template <typename T>
-__device__ __forceinline__ float dot8(const T* a, const T* b);
+struct Raw8;
 template <>
-__device__ __forceinline__ float dot8<__nv_bfloat16>(const __nv_bfloat16* a, const __nv_bfloat16* b) {
-  const uint4 x = *(const uint4*)a, y = *(const uint4*)b;
-  const __nv_bfloat162* xa = (const __nv_bfloat162*)&x;
-  const __nv_bfloat162* ya = (const __nv_bfloat162*)&y;
+struct Raw8<__nv_bfloat16> {
+  uint4 v;
+};
+template <>
+struct Raw8<float> {
+  float4 v0, v1;
+};
+
+__device__ __forceinline__ Raw8<__nv_bfloat16> ld8(const __nv_bfloat16* p) { return Raw8<__nv_bfloat16>{*(const uint4*)p}; }
+__device__ __forceinline__ Raw8<float> ld8(const float* p) {
+  return Raw8<float>{*(const float4*)p, *(const float4*)(p + 4)};
+}
+
+__device__ __forceinline__ float dot8(const Raw8<__nv_bfloat16>& a, const Raw8<__nv_bfloat16>& b) {
+  const __nv_bfloat162* xa = (const __nv_bfloat162*)&a.v;
+  const __nv_bfloat162* ya = (const __nv_bfloat162*)&b.v;
   float s = 0.f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -29,63 +43,70 @@ __device__ __forceinline__ float dot8<__nv_bfloat16>(const __nv_bfloat16* a, con
   }
   return s;
 }
-template <>
-__device__ __forceinline__ float dot8<float>(const float* a, const float* b) {
-  const float4 x0 = *(const float4*)a, x1 = *(const float4*)(a + 4);
-  const float4 y0 = *(const float4*)b, y1 = *(const float4*)(b + 4);
-  float s = x0.x * y0.x;
-  s = fmaf(x0.y, y0.y, s);
-  s = fmaf(x0.z, y0.z, s);
-  s = fmaf(x0.w, y0.w, s);
-  s = fmaf(x1.x, y1.x, s);
-  s = fmaf(x1.y, y1.y, s);
-  s = fmaf(x1.z, y1.z, s);
-  s = fmaf(x1.w, y1.w, s);
+__device__ __forceinline__ float dot8(const Raw8<float>& a, const Raw8<float>& b) {
+  float s = a.v0.x * b.v0.x;
+  s = fmaf(a.v0.y, b.v0.y, s);
+  s = fmaf(a.v0.z, b.v0.z, s);
+  s = fmaf(a.v0.w, b.v0.w, s);
+  s = fmaf(a.v1.x, b.v1.x, s);
+  s = fmaf(a.v1.y, b.v1.y, s);
+  s = fmaf(a.v1.z, b.v1.z, s);
+  s = fmaf(a.v1.w, b.v1.w, s);
   return s;
 }
 
-// Rows handled by one lane group in one pass: all their loads are issued
-// before any reduction, so enough bytes are in flight to keep HBM busy.
-constexpr int kDeltaUnroll = 4;
+// Lanes per row, 8-element chunks per lane and row, and rows per lane group
+// handled in one pass: all of a pass's loads are issued before any of them
+// is used, enough bytes in flight to keep HBM busy (about 128 bytes of
+// operands per lane, fewer rows when the rows are wide).
+template <typename T, int D>
+struct DeltaShape {
+  static constexpr int CH = D / 8;              // 8-element chunks per row
+  static constexpr int G = CH < 32 ? CH : 32;   // lanes per row
+  static constexpr int NCH = CH / G;            // chunks per lane and row
+  static constexpr int RPW = 32 / G;            // rows per warp and pass step
+  static constexpr int kBytes = 2 * NCH * 8 * (int)sizeof(T);  // per lane and row
+  static constexpr int U = kBytes <= 32 ? 4 : (kBytes <= 64 ? 2 : 1);
+};
 
-template <int D, int kThreads>
+template <typename T, int D, int kThreads>
 __host__ __device__ constexpr int delta_rows_per_cta() {
-  return (kThreads / 32) * (32 / (D / 8 < 32 ? D / 8 : 32)) * kDeltaUnroll;
+  return (kThreads / 32) * DeltaShape<T, D>::RPW * DeltaShape<T, D>::U;
 }
 
-// The rows of CTA `cta` (kThreads threads) of a delta pass.
+// The rows of CTA `cta` (kThreads threads) of a delta pass.  Row indices
+// past the end are clamped for the loads (so no load sits under a branch
+// and all of them are in flight together) and their results dropped.
 template <typename T, int D, int kThreads>
 __device__ __forceinline__ void delta_rows(const BwdArgs& a, int cta) {
-  constexpr int CH = D / 8;              // 8-element chunks per row
-  constexpr int G = CH < 32 ? CH : 32;   // lanes per row
-  constexpr int RPW = 32 / G;            // rows per warp and unroll step
-  constexpr int U = kDeltaUnroll;
+  using Sh = DeltaShape<T, D>;
+  constexpr int G = Sh::G, NCH = Sh::NCH, RPW = Sh::RPW, U = Sh::U;
+  static_assert(Sh::CH % G == 0, "whole chunks per lane");
   const int lane = threadIdx.x % 32;
   const size_t rows = (size_t)a.d.BH * a.d.S;
   const size_t row0 = ((size_t)cta * (kThreads / 32) + threadIdx.x / 32) * RPW * U + lane / G;
-  // the row statistics are loaded with the operands (one round trip to
-  // memory, not two), by the lane that writes the row's results
-  float s[U], rmax[U], rden[U];
+  Raw8<T> ov[U][NCH], gv[U][NCH];
+  float rmax[U], rden[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    s[u] = 0.f;
-    rmax[u] = 0.f;
-    rden[u] = 1.f;
     const size_t row = row0 + (size_t)u * RPW;
-    if (row < rows) {
-      if (lane % G == 0) {
-        rmax[u] = a.row_max[row];
-        rden[u] = a.row_denom[row];
-      }
-      const T* o = (const T*)a.O + row * D;
-      const T* g = (const T*)a.dO + row * D;
+    const size_t rr = row < rows ? row : rows - 1;
+    const T* o = (const T*)a.O + rr * D;
+    const T* g = (const T*)a.dO + rr * D;
 #pragma unroll
-      for (int c = lane % G; c < CH; c += G) s[u] += dot8<T>(o + c * 8, g + c * 8);
+    for (int k = 0; k < NCH; ++k) {
+      const int c = lane % G + k * G;
+      ov[u][k] = ld8(o + c * 8);
+      gv[u][k] = ld8(g + c * 8);
     }
+    rmax[u] = a.row_max[rr];
+    rden[u] = a.row_denom[rr];
   }
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    float t = s[u];
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) t += dot8(ov[u][k], gv[u][k]);
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
     const size_t row = row0 + (size_t)u * RPW;
@@ -94,6 +115,18 @@ __device__ __forceinline__ void delta_rows(const BwdArgs& a, int cta) {
       a.lse2[row] = rmax[u] * 1.4426950408889634f + log2f(rden[u]);
     }
   }
+}
+
+// A whole delta pass over the rows, in groups of delta_rows_per_cta rows:
+// CTA `first` of `stride` resident CTAs takes groups first, first + stride,
+// ... (a grid sized to what the SMs hold, so no CTA is launched for a single
+// round trip to memory).
+template <typename T, int D, int kThreads>
+__device__ __forceinline__ void delta_pass(const BwdArgs& a, int first, int stride) {
+  const size_t rows = (size_t)a.d.BH * a.d.S;
+  constexpr size_t per = delta_rows_per_cta<T, D, kThreads>();
+  const int groups = (int)((rows + per - 1) / per);
+  for (int c = first; c < groups; c += stride) delta_rows<T, D, kThreads>(a, c);
 }
 
 }  // namespace bsr

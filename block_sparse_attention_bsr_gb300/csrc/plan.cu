@@ -208,14 +208,23 @@ __global__ void __launch_bounds__(kFusedThreads) delta_plan_kernel(BwdArgs a, Pl
   if ((int)blockIdx.x < lists)
     plan_body(p, blockIdx.x, sm_plan);
   else
-    delta_rows<T, D, kFusedThreads>(a, (int)blockIdx.x - lists);
+    delta_pass<T, D, kFusedThreads>(a, (int)blockIdx.x - lists, (int)gridDim.x - lists);
 }
 
 template <typename T, int D>
 bsr_status launch_fused(const BwdArgs& a, const PlanArgs& p, int lists, size_t smem, cudaStream_t s) {
   const size_t rows = (size_t)a.d.BH * a.d.S;
-  constexpr size_t per = delta_rows_per_cta<D, kFusedThreads>();
-  const unsigned grid = (unsigned)(lists + (rows + per - 1) / per);
+  constexpr size_t per = delta_rows_per_cta<T, D, kFusedThreads>();
+  const size_t groups = (rows + per - 1) / per;
+  // delta CTAs: as many as the SMs hold at once (they loop over the groups)
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, delta_plan_kernel<T, D>, kFusedThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const size_t sms = (size_t)sm_count();
+  const size_t resident = sms > 0 ? sms * per_sm : groups;
+  const unsigned grid = (unsigned)(lists + (groups < resident ? groups : resident));
   LaunchTimer timer("delta_plan", s);
   delta_plan_kernel<T, D><<<grid, kFusedThreads, smem, s>>>(a, p, lists);
   return check_launch("delta_plan launch");

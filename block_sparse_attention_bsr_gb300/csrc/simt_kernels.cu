@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
 // ------------------------------------------------------------------ delta --
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) delta_kernel(BwdArgs a) {
-  delta_rows<T, D, kThreads>(a, blockIdx.x);
+  delta_pass<T, D, kThreads>(a, blockIdx.x, gridDim.x);
 }
 
 // --------------------------------------------------------------------- dQ --
@@ -389,7 +389,14 @@ bsr_status delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   constexpr int G = D / 8 < 32 ? D / 8 : 32;
   const size_t rows = (size_t)a.d.BH * a.d.S;
   (void)G;
-  dim3 grid((unsigned)((rows + delta_rows_per_cta<D, kThreads>() - 1) / delta_rows_per_cta<D, kThreads>()));
+  const size_t groups = (rows + delta_rows_per_cta<T, D, kThreads>() - 1) / delta_rows_per_cta<T, D, kThreads>();
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, delta_kernel<T, D>, kThreads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const size_t sms = (size_t)sm_count();
+  const size_t resident = sms > 0 ? sms * per_sm : groups;
+  dim3 grid((unsigned)(groups < resident ? groups : resident));
   return launch(delta_kernel<T, D>, grid, 0, s, "delta", &a);
 }
 
