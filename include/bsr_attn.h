@@ -19,7 +19,9 @@
  *
  * Conventions shared by every entry point:
  *  - Dense tensors are [batch, heads, seq, head_dim], contiguous, row-major,
- *    described by a bsr_tensor whose `data` is a DEVICE pointer.  All dense
+ *    described by a bsr_tensor whose `data` is a DEVICE pointer, 16-byte
+ *    aligned (inputs are read by TMA, outputs written with 16- and 32-byte
+ *    vector stores; a misaligned pointer is BSR_ERR_INVALID_ARG).  All dense
  *    tensors of one call have the same shape and dtype.  Supported:
  *    head_dim in {64, 128, 256, 512}; dtype BSR_F32 or BSR_BF16;
  *    seq = n_brows * 128; batch, heads >= 1.
@@ -59,7 +61,7 @@ typedef enum {
 } bsr_status;
 
 typedef struct {
-  void* data;        /* device pointer to [batch, heads, seq, head_dim] elements */
+  void* data;        /* device pointer (16-byte aligned) to [batch, heads, seq, head_dim] elements */
   int32_t dtype;     /* bsr_dtype */
   int32_t batch;
   int32_t heads;

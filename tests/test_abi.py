@@ -98,6 +98,8 @@ def _fwd(lib, Q=None, K=None, V=None, O=None, n_brows=2, block=128, scale=0.125,
     (dict(n_brows=3), 1, "n_brows"),
     (dict(Q=_fake(s=200), K=_fake(s=200), V=_fake(s=200), O=_fake(s=200)), 1, "multiple"),
     (dict(scale=float("nan")), 1, "scale"),
+    (dict(O=_fake(ptr=0x1002)), 1, "aligned"),
+    (dict(Q=_fake(ptr=0x1008)), 1, "aligned"),
 ])
 def test_fwd_rejects_bad_arguments_on_host(lib, kw, status, msg):
     # Every case fails in the host checks, before any CUDA call.

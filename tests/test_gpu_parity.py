@@ -154,3 +154,39 @@ def test_device_index_check_reports_error():
         bsr.bsr_attn_check()
     assert e.value.status == 5
     bsr.bsr_attn_check()  # the status word was cleared
+
+
+def test_backward_same_with_per_launch_timing():
+    # With per-launch timing on, dQ and dK/dV run one after the other on the
+    # caller's stream instead of side by side on two streams: same results.
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    bm = inputs.block_mask("global", 16, radius=2)
+    Q, K, V, dO = inputs.make_qkvdo(1, 4, 16 * 128, 128, "bf16", 1.0, 11)
+    a = run_gpu(Q, K, V, dO, bm, 0.09)
+    bsr.profile_enable(True)
+    try:
+        b = run_gpu(Q, K, V, dO, bm, 0.09)
+    finally:
+        bsr.profile_enable(False)
+        bsr.profile_collect()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_misaligned_output_is_rejected():
+    # Output views must be 16-byte aligned (vector stores in the epilogues):
+    # a view one element in is refused on the host, nothing is launched.
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    dev = torch.device("cuda")
+    q = torch.randn(1, 1, 256, 64, device=dev, dtype=torch.bfloat16)
+    row_ptr = torch.tensor([0, 1, 2], dtype=torch.int32, device=dev)
+    col_idx = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    buf = torch.empty(1 * 1 * 256 * 64 + 1, device=dev, dtype=torch.bfloat16)
+    O = buf[1:].view(1, 1, 256, 64)
+    rm = torch.empty(1, 1, 256, device=dev)
+    rd = torch.empty_like(rm)
+    with pytest.raises(bsr.BsrError) as e:
+        bsr.bsr_attn_fwd(q, q, q, row_ptr, col_idx, 2, 128, 0.125, O, rm, rd)
+    assert e.value.status == 1 and "aligned" in str(e.value)
