@@ -232,3 +232,56 @@ class Structure:
     @property
     def row_idx(self):
         return self.dev["row_idx"]
+
+
+_AUTOGRAD_FN = None
+
+
+def _autograd_fn():
+    """The torch.autograd.Function pairing bsr_attn_fwd with bsr_attn_bwd (built on first use)."""
+    global _AUTOGRAD_FN
+    if _AUTOGRAD_FN is not None:
+        return _AUTOGRAD_FN
+    import torch
+
+    class BlockSparseAttention(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, Q, K, V, structure, scale):
+            O = torch.empty_like(Q)
+            rm = torch.empty(Q.shape[:3], device=Q.device, dtype=torch.float32)
+            rd = torch.empty_like(rm)
+            bsr_attn_fwd(Q, K, V, structure.row_ptr, structure.col_idx, structure.n_brows, 128, scale, O, rm, rd)
+            ctx.save_for_backward(Q, K, V, O, rm, rd)
+            ctx.structure = structure
+            ctx.scale = scale
+            ctx.mark_non_differentiable(rm, rd)
+            return O, rm, rd
+
+        @staticmethod
+        def backward(ctx, dO, _drm, _drd):
+            Q, K, V, O, rm, rd = ctx.saved_tensors
+            st = ctx.structure
+            dO = dO.contiguous()
+            dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
+            bsr_attn_bwd(Q, K, V, O, dO, rm, rd, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, ctx.scale,
+                         dQ, dK, dV)
+            return dQ, dK, dV, None, None
+
+    _AUTOGRAD_FN = BlockSparseAttention
+    return _AUTOGRAD_FN
+
+
+def block_sparse_attention(Q, K, V, structure: "Structure", scale=None, return_stats: bool = False):
+    """softmax(scale * Q K^T over the stored 128 x 128 blocks) V, differentiable in Q, K and V.
+
+    Q, K, V: contiguous CUDA tensors [batch, heads, seq, head_dim] (bf16 or fp32,
+    16-byte aligned); `structure`: a Structure of the block mask on the same
+    device; scale defaults to 1 / sqrt(head_dim).  The forward and backward
+    passes are bsr_attn_fwd and bsr_attn_bwd on the current stream.  With
+    return_stats the fp32 row_max / row_denom statistics come back as well
+    (they carry no gradient).
+    """
+    if scale is None:
+        scale = 1.0 / float(Q.shape[-1]) ** 0.5
+    O, rm, rd = _autograd_fn().apply(Q, K, V, structure, float(scale))
+    return (O, rm, rd) if return_stats else O

@@ -118,3 +118,18 @@ def test_bwd_rejects_bad_arguments_on_host(lib):
     st = lib.bsr_attn_bwd(*(ctypes.byref(x) for x in t[:5]), P(1), P(2), P(3), P(0), P(5), P(6), 0.125,
                           *(ctypes.byref(x) for x in t[5:]), None)
     assert st == 1
+
+
+def test_autograd_wrapper_refuses_host_tensors():
+    # The wrapper only marshals arguments: host tensors are refused before
+    # anything reaches the library.
+    torch = pytest.importorskip("torch")
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    class _St:  # a structure stand-in: never dereferenced
+        row_ptr = col_idx = col_ptr = row_idx = None
+        n_brows = 2
+
+    x = torch.zeros(1, 1, 256, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        bsr.block_sparse_attention(x, x, x, _St())
