@@ -156,6 +156,26 @@ bsr_status launch_delta_plan(const BwdArgs& a, const PlanArgs& p, int lists, cud
 
 // RAII bracket that records a pair of CUDA events around one kernel launch
 // when profiling is enabled (bsr_profile_enable).
+// Launches `kern` on `s` as a programmatic dependent of the previous kernel
+// in the stream: it may start launching while that kernel finishes.  Every
+// kernel launched this way calls sm100::griddep_wait() before its first
+// access to global memory (the previous kernel may still be reading or
+// writing it, including stream-ordered scratch that is reused).
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+}
+
 // True while per-launch timing is on: kernels that normally overlap on two
 // streams then run one after the other, so that each launch's events bracket
 // that kernel alone.

@@ -20,6 +20,7 @@
 
 #include "delta.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace bsr {
 namespace {
@@ -192,6 +193,8 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
+  sm100::griddep_wait();  // may run as a programmatic dependent
+  sm100::griddep_launch_dependents();
   extern __shared__ int sm_plan[];
   plan_body(p, blockIdx.x, sm_plan);
 }
@@ -204,6 +207,8 @@ constexpr int kFusedThreads = 256;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kFusedThreads) delta_plan_kernel(BwdArgs a, PlanArgs p, int lists) {
+  sm100::griddep_wait();  // may run as a programmatic dependent
+  sm100::griddep_launch_dependents();
   extern __shared__ int sm_plan[];
   if ((int)blockIdx.x < lists)
     plan_body(p, blockIdx.x, sm_plan);
@@ -226,7 +231,8 @@ bsr_status launch_fused(const BwdArgs& a, const PlanArgs& p, int lists, size_t s
   const size_t resident = sms > 0 ? sms * per_sm : groups;
   const unsigned grid = (unsigned)(lists + (groups < resident ? groups : resident));
   LaunchTimer timer("delta_plan", s);
-  delta_plan_kernel<T, D><<<grid, kFusedThreads, smem, s>>>(a, p, lists);
+  const cudaError_t e = launch_dependent(delta_plan_kernel<T, D>, dim3(grid), dim3(kFusedThreads), smem, s, a, p, lists);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "delta_plan launch: %s", cudaGetErrorString(e));
   return check_launch("delta_plan launch");
 }
 
@@ -247,7 +253,8 @@ bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
     if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "plan: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   }
   LaunchTimer timer("plan", s);
-  plan_kernel<<<lists, plan_threads(p.n), smem, s>>>(p);
+  const cudaError_t e = launch_dependent(plan_kernel, dim3(lists), dim3(plan_threads(p.n)), smem, s, p);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "plan launch: %s", cudaGetErrorString(e));
   return check_launch("plan launch");
 }
 

@@ -130,6 +130,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// --------------------------------------------- programmatic dependent launch --
+// A kernel launched as a programmatic dependent of the previous kernel in its
+// stream may start before that kernel has finished; griddep_wait() blocks
+// until the previous grid has completed and its memory operations are
+// visible (a no-op for a kernel launched the ordinary way).
+// griddep_launch_dependents() lets the next kernel, if launched as a
+// programmatic dependent, start launching once every CTA of this grid has
+// executed it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- TMEM --
 // Allocates `ncols` (power of two, 32..512) TMEM columns; the whole warp must
 // call it.  The base address is written to *slot (shared memory).

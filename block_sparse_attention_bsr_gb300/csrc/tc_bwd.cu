@@ -181,6 +181,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, BwdArgs a) {
+  griddep_wait();  // may run as a programmatic dependent
+  griddep_launch_dependents();
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -542,6 +544,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, BwdArgs a) {
+  griddep_wait();  // may run as a programmatic dependent
+  griddep_launch_dependents();
   using C = DkvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // no slack for re-alignment: refuse (uniform, before any barrier)
@@ -961,8 +965,8 @@ bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap&
   dkdv<<<grid, kThreads, DkvCfg<D>::kSmem, side.s>>>(tm.q, tm.k, tm.v, tmdO, a);
   st = check_launch("dkdv_tc launch");
   if (st == BSR_OK) {
-    dq<<<grid, kThreads, DqCfg<D>::kSmem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
-    st = check_launch("dq_tc launch");
+    e = launch_dependent(dq, dim3(grid), dim3(kThreads), DqCfg<D>::kSmem, s, tm.q, tm.k, tm.v, tmdO, a);
+    st = e != cudaSuccess ? fail(BSR_ERR_CUDA, "dq_tc launch: %s", cudaGetErrorString(e)) : check_launch("dq_tc launch");
   }
   // join even after a failed launch, so `s` stays ordered after the side stream
   if ((e = cudaEventRecord(side.join, side.s)) != cudaSuccess || (e = cudaStreamWaitEvent(s, side.join, 0)) != cudaSuccess)

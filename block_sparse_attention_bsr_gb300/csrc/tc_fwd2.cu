@@ -141,6 +141,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
+  griddep_wait();  // may run as a programmatic dependent
+  griddep_launch_dependents();
   using C = Fwd2Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // no slack for re-alignment: refuse (uniform, before any barrier)
@@ -660,7 +662,8 @@ bsr_status launch(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
   const int grid = tc_grid(a.d);
   if (grid <= 0) return fail(BSR_ERR_CUDA, "fwd_tc: cannot query the SM count");
   LaunchTimer timer("fwd_tc", s);
-  kern<<<grid, kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
+  e = launch_dependent(kern, dim3(grid), dim3(kThreads), C::kSmem, s, tm.q, tm.k, tm.v, a);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "fwd_tc launch: %s", cudaGetErrorString(e));
   return check_launch("fwd_tc launch");
 }
 
