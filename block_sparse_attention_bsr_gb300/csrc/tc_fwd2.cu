@@ -141,11 +141,13 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
-  griddep_wait();  // may run as a programmatic dependent
+  // may run as a programmatic dependent: the prologue below touches only
+  // shared memory and TMEM; global memory waits for the previous grid
   griddep_launch_dependents();
   using C = Fwd2Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // no slack for re-alignment: refuse (uniform, before any barrier)
+    griddep_wait();
     if (threadIdx.x == 0) atomicExch(a.status, kStatusDeviceCheck);
     return;
   }
@@ -159,7 +161,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
   const PlanLayout lay = plan_layout(a.plan, a.d.nb, (int)gridDim.x, a.d.BH);
-  const Walk walk = make_walk(lay, a.d.BH);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -197,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();
+  const Walk walk = make_walk(lay, a.d.BH);
   const uint32_t tmem = bars->tmem_slot;
   volatile int* ab = &bars->abort_flag;
   RingSmem* ring = &bars->ring;
