@@ -79,7 +79,7 @@ struct Bars {
   uint64_t q_empty[2];
   uint64_t s_full;
   uint64_t s_free;      // both warpgroups have loaded S into registers
-  uint64_t p_full[2][2];  // by P buffer b and key half h: P_h of block g (g % 2 = b) is in TMEM
+  uint64_t p_full[2];     // by P buffer b: both halves' P of block g (g % 2 = b) are in TMEM
   uint64_t pv_done[2];    // by P buffer b: both halves' P.V of block g (g % 2 = b) are done
   uint64_t final_mma;
   uint64_t red_full;   // both warpgroups' row statistics written
@@ -166,8 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
-      mbar_init(&bars->p_full[i][0], 128);
-      mbar_init(&bars->p_full[i][1], 128);
+      mbar_init(&bars->p_full[i], kSoftmax);
       mbar_init(&bars->pv_done[i], 1);
       mbar_init(&bars->wg_sync[i], 128);
     }
@@ -373,18 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int vs = i % C::kVStages;
       const int b = i & 1;
       if (!(ok = warp_wait(&bars->v_full[vs], (i / C::kVStages) & 1, bars, a.status))) break;
-      // The first block of a row overwrites both accumulators, which both
-      // warpgroups read while combining the previous row: wait for both.
-      if (!(ok = warp_wait(&bars->p_full[b][0], (i >> 1) & 1, bars, a.status))) break;
-      if (B.i == 0 && !(ok = warp_wait(&bars->p_full[b][1], (i >> 1) & 1, bars, a.status))) break;
+      // both halves' P (the first block of a row also overwrites both
+      // accumulators, which both warpgroups read while combining the
+      // previous row)
+      if (!(ok = warp_wait(&bars->p_full[b], (i >> 1) & 1, bars, a.status))) break;
       tc_fence_after();
       const SDesc dV(aV + vs * C::kTile, 16384, 1024);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (h == 1 && B.i > 0) {
-          if (!(ok = warp_wait(&bars->p_full[b][1], (i >> 1) & 1, bars, a.status))) break;
-          tc_fence_after();
-        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ts_by(leader, tmem + kColO + h * D, tmem + kColP + b * 64 + h * 32 + kk * 8,
@@ -522,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tmem + lane_base + kColP + b * 64 + hg * 32, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[b][hg]);
+        mbar_arrive(&bars->p_full[b]);
       }
       if (!ok) break;
       // ----------------------------------------------------- epilogue --
