@@ -21,12 +21,17 @@
 //     reads its A operand from there;
 //   * S has one TMEM buffer, released as soon as both warpgroups have
 //     loaded their halves into registers, so S_{j+1} = Q K_{j+1}^T runs
-//     while the softmax of block j is computed and the MMA thread never
-//     waits for its own P.V.
+//     while the softmax of block j is computed;
+//   * two threads issue the MMAs, one the S and one the P.V of every block,
+//     each as soon as its operands are there (issue and commit cost a
+//     thread tens to a hundred cycles each, and each MMA thread waits on
+//     barriers that the other one does not need);
+//   * the producer keeps the work ring one item ahead of the item it loads,
+//     so the global work counter's round trip is off the item boundary.
 //
-// Warp roles (352 threads): warp 0 TMA producer of Q and K, warp 10 TMA
-// producer of V, warp 1 TMEM owner and MMA issuer, warps 2..9 two softmax
-// warpgroups; thread (warp w, lane l) owns query row 32 (w % 4) + l (its
+// Warp roles (384 threads): warp 0 TMA producer of Q and K, warp 10 TMA
+// producer of V, warp 1 TMEM owner and issuer of the S MMAs, warp 11 issuer
+// of the P.V MMAs, warps 2..9 two softmax warpgroups; thread (warp w, lane l) owns query row 32 (w % 4) + l (its
 // TMEM lane), warpgroup h = (w - 2) / 4 owns keys [64 h, 64 h + 64) of each
 // block and, in the final combine, output columns [h D / 2, h D / 2 + D / 2).
 // TMEM columns: S at 0 (half h at +64 h), bf16 P of block j at
@@ -47,8 +52,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 352;  // producer, MMA, 8 softmax warps, V producer
+constexpr int kThreads = 384;  // producer, S MMAs, 8 softmax warps, V producer, P.V MMAs
 constexpr int kWarpV = 10;
+constexpr int kWarpPV = 11;
 constexpr int kSoftmax = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColP = 128, kColO = 256;
@@ -81,7 +87,7 @@ struct Bars {
   uint64_t s_free;      // both warpgroups have loaded S into registers
   uint64_t p_full[2];     // by P buffer b: both halves' P of block g (g % 2 = b) are in TMEM
   uint64_t pv_done[2];    // by P buffer b: both halves' P.V of block g (g % 2 = b) are done
-  uint64_t final_mma;
+  uint64_t final_mma[2];  // by MMA thread (S, P.V): all its MMAs are done
   uint64_t red_full;   // both warpgroups' row statistics written
   uint64_t red_empty;  // both warpgroups have read them
   uint64_t wg_sync[2];
@@ -172,12 +178,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, kSoftmax);
-    mbar_init(&bars->final_mma, 1);
+    mbar_init(&bars->final_mma[0], 1);
+    mbar_init(&bars->final_mma[1], 1);
     mbar_init(&bars->red_full, kSoftmax);
     mbar_init(&bars->red_empty, kSoftmax);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&bars->ring.full[i], 1);
-      mbar_init(&bars->ring.empty[i], 2 + kSoftmax / 32);  // MMA, softmax warps, V producer
+      mbar_init(&bars->ring.empty[i], 3 + kSoftmax / 32);  // two MMA threads, softmax warps, V producer
     }
     for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
@@ -210,10 +217,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       int kg = 0, q = 0, g = 0;
+      int put = 0;         // ring slots published
+      bool ended = false;  // the slot that ends the walk is published
       bool ok = true;
+      auto publish = [&](int upto) -> bool {  // ring slots [put, upto)
+        for (; put < upto && !ended; ++put) {
+          int kk;
+          if (!ring_put(ring, put, lay.header + 1, walk.total, &kk, ab, a.status)) return false;
+          ended = kk < 0;
+        }
+        return true;
+      };
       for (int t = 0; ok; ++t) {
-        int k;
-        if (!(ok = ring_put(ring, t, lay.header + 1, walk.total, &k, ab, a.status)) || k < 0) break;
+        if (!(ok = publish(t + 1))) break;
+        const int k = *(volatile int32_t*)&ring->k[t % kRing];
+        if (k < 0) break;
         Cursor cur;
         walk.decode(k, cur);
         if (cur.n == 0) continue;
@@ -225,6 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < C::kBoxes; ++b)
           tma_load_2d(sQ + qb * C::kTile + b * 16384, &tmQ, b * 64, qrow, &bars->q_full[qb]);
         ++q;
+        // the next item's slot (and the work counter's round trip) while
+        // this item's K tiles load
+        if (!(ok = publish(t + 2))) break;
         for (int j = 0; j < cur.n; ++j, ++g) {
           int n = a.col_idx[cur.first + j];
           if (n < 0 || n >= a.d.nb) {
@@ -273,139 +294,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = (vg > C::kVStages ? vg - C::kVStages : 0); i < vg; ++i)
         drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA --
-    // The whole warp walks the schedule (so the descriptor arithmetic stays
-    // warp-uniform); one elected lane issues the MMAs and commits.
-    // S of block g+1 is issued (as soon as the softmax has taken S of block
-    // g) before P.V of block g.
-    const uint32_t leader = elect_one();
-    const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
-    const uint32_t idPV = instr_desc(1, 0, 1, D, 128);
-    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-    auto issue_s = [&](const Cursor& c) -> bool {
-      const int i = c.g;
-      const int ks = i % C::kKStages;
-      const int qb = c.q & 1;
-      if (c.i == 0 && !warp_wait(&bars->q_full[qb], (c.q >> 1) & 1, bars, a.status)) return false;
-      if (!warp_wait(&bars->k_full[ks], (i / C::kKStages) & 1, bars, a.status)) return false;
-      if (!warp_wait(&bars->s_free, (i & 1) ^ 1, bars, a.status)) return false;
-      tc_fence_after();
-      const SDesc dQ(aQ + qb * C::kTile, 16, 1024), dK(aK + ks * C::kTile, 16, 1024);
+  } else if (warp == 1 || warp == kWarpPV) {
+    // ------------------------------------------------------------ MMAs --
+    // Lane 0 of warp 1 issues S = Q K^T of every block as soon as the
+    // softmax has taken the previous S out of TMEM; lane 0 of warp 11
+    // issues P.V of every block as soon as both halves' P are there.  Each
+    // walks the schedule on its own.
+    if (lane == 0) {
+      const bool s_role = warp == 1;
+      const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
+      const uint32_t idPV = instr_desc(1, 0, 1, D, 128);
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      int g = 0, q = 0;  // blocks / non-empty items walked so far
+      bool ok = true;
+      for (int t = 0; ok; ++t) {
+        int k = -1;
+        if (!(ok = ring_get(ring, t, &k, ab, a.status)) || k < 0) break;
+        Cursor cur;
+        walk.decode(k, cur);
+        const int qb = q & 1;
+        for (int j = 0; j < cur.n && ok; ++j, ++g) {
+          if (s_role) {
+            const int ks = g % C::kKStages;
+            if (j == 0 && !(ok = mbar_wait(&bars->q_full[qb], (q >> 1) & 1, ab, a.status))) break;
+            if (!(ok = mbar_wait(&bars->k_full[ks], (g / C::kKStages) & 1, ab, a.status))) break;
+            // both warpgroups have loaded S of the previous block
+            if (!(ok = mbar_wait(&bars->s_free, (g & 1) ^ 1, ab, a.status))) break;
+            tc_fence_after();
+            const SDesc dQ(aQ + qb * C::kTile, 16, 1024), dK(aK + ks * C::kTile, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_bf16_ss_by(leader, tmem, dQ.at(off), dK.at(off), idS, kk > 0);
-      }
-      mma_commit_by(leader, &bars->k_empty[ks]);
-      mma_commit_by(leader, &bars->s_full);
-      if (c.i == c.n - 1) mma_commit_by(leader, &bars->q_empty[qb]);
-      __syncwarp();
-      return true;
-    };
-    bool ok = true;
-    auto get = [&](int t, int* k) -> bool {
-      int kk = -1;
-      bool good = true;
-      if (lane == 0) good = ring_get(ring, t, &kk, ab, a.status);
-      good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
-      *k = __shfl_sync(0xffffffffu, kk, 0);
-      return good;
-    };
-    auto seek_a = [&](Cursor& c) {
-      while (true) {
-        int k;
-        if (!(ok = get(c.t, &k)) || k < 0) {
-          c.done = true;
-          return;
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              mma_bf16_ss(tmem, dQ.at(off), dK.at(off), idS, kk > 0);
+            }
+            mma_commit(&bars->k_empty[ks]);
+            mma_commit(&bars->s_full);
+            if (j == cur.n - 1) mma_commit(&bars->q_empty[qb]);
+          } else {
+            const int vs = g % C::kVStages;
+            const int b = g & 1;
+            if (!(ok = mbar_wait(&bars->v_full[vs], (g / C::kVStages) & 1, ab, a.status))) break;
+            // both halves' P (the first block of a row also overwrites both
+            // accumulators, which both warpgroups read while combining the
+            // previous row)
+            if (!(ok = mbar_wait(&bars->p_full[b], (g >> 1) & 1, ab, a.status))) break;
+            tc_fence_after();
+            const SDesc dV(aV + vs * C::kTile, 16384, 1024);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ts(tmem + kColO + h * D, tmem + kColP + b * 64 + h * 32 + kk * 8,
+                            dV.at((4 * h + kk) * 2048), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->v_empty[vs]);
+            mma_commit(&bars->pv_done[b]);
+          }
         }
-        walk.decode(k, c);
-        if (c.n > 0) {
-          c.i = 0;
-          return;
-        }
-        ++c.t;
-      }
-    };
-    auto seek_b = [&](Cursor& c) {
-      while (true) {
-        const int k = *(volatile int32_t*)&ring->k[c.t % kRing];
-        if (k < 0) {
-          c.done = true;
-          return;
-        }
-        walk.decode(k, c);
-        if (c.n > 0) {
-          c.i = 0;
-          return;
-        }
-        __syncwarp();
-        if (lane == 0) ring_release(ring, c.t);
-        ++c.t;
-      }
-    };
-    auto next_a = [&](Cursor& c) {
-      ++c.g;
-      if (++c.i == c.n) {
-        ++c.q;
-        ++c.t;
-        seek_a(c);
-      }
-    };
-    Cursor A{0, 0, 0, 0, 0, 0, 0, 0, 0, false};
-    seek_a(A);
-    Cursor B = A;
-    if (ok && !A.done) {
-      if ((ok = issue_s(A))) next_a(A);
-    }
-    while (ok && !B.done) {
-      // S of the next block goes first, unless that block starts another
-      // row: then this row's last P.V goes first, so that the row's
-      // epilogue does not wait behind the next row's S.
-      const bool a_later = !A.done && A.i == 0;
-      if (!A.done && !a_later) {
-        if (!(ok = issue_s(A))) break;
-        next_a(A);
         if (!ok) break;
+        if (cur.n > 0) ++q;
+        ring_release(ring, t);
       }
-      const int i = B.g;
-      const int vs = i % C::kVStages;
-      const int b = i & 1;
-      if (!(ok = warp_wait(&bars->v_full[vs], (i / C::kVStages) & 1, bars, a.status))) break;
-      // both halves' P (the first block of a row also overwrites both
-      // accumulators, which both warpgroups read while combining the
-      // previous row)
-      if (!(ok = warp_wait(&bars->p_full[b], (i >> 1) & 1, bars, a.status))) break;
-      tc_fence_after();
-      const SDesc dV(aV + vs * C::kTile, 16384, 1024);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts_by(leader, tmem + kColO + h * D, tmem + kColP + b * 64 + h * 32 + kk * 8,
-                         dV.at((4 * h + kk) * 2048), idPV, (B.i > 0 || kk > 0) ? 1u : 0u);
-        if (h == 1) {
-          mma_commit_by(leader, &bars->v_empty[vs]);
-          mma_commit_by(leader, &bars->pv_done[b]);
-        }
-      }
-      __syncwarp();
-      if (!ok) break;
-      if (a_later) {
-        if (!(ok = issue_s(A))) break;
-        next_a(A);
-        if (!ok) break;
-      }
-      ++B.g;
-      if (++B.i == B.n) {
-        if (lane == 0) ring_release(ring, B.t);
-        ++B.q;
-        ++B.t;
-        seek_b(B);
-      }
+      // every MMA this thread issued has completed before the CTA exits
+      uint64_t* fin = &bars->final_mma[s_role ? 0 : 1];
+      mma_commit(fin);
+      drain_wait(fin, 0);
     }
-    mma_commit_by(leader, &bars->final_mma);
-    if (leader) drain_wait(&bars->final_mma, 0);
     __syncwarp();
   } else if (warp < kWarpV) {
     // -------------------------------------------------------- softmax --
