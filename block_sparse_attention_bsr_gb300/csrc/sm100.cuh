@@ -473,18 +473,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return r;
 }
 
-// Per-thread register budget of the executing warpgroup (all four warps
-// execute it): .dec returns registers to the CTA's pool, .inc waits until
-// the pool holds enough; the split must add up to the launch allocation.
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // Named barrier over `count` threads (a multiple of 32) with id `id` (1..15).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
