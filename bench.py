@@ -48,12 +48,12 @@ def alg_flops(wl, nnzb, part="total"):
 # current sources still hash the same (otherwise the roofline's traffic is
 # null until the kernel is captured again).
 MEASURED_TRAFFIC = {
-    ("global_s8192", "dkdv_tc"): {"bytes": 206.4e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                  "sha256": "a212b964cb154ff9eafaa41f290f69bc79ff835db449a6a088f26e0b73914766"},
-    ("global_s8192", "dq_tc"): {"bytes": 176.2e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                "sha256": "a212b964cb154ff9eafaa41f290f69bc79ff835db449a6a088f26e0b73914766"},
-    ("global_s8192", "fwd_tc"): {"bytes": 136.0e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "ea57701435aa8cc5857ac26a86e50efd7d9950366276c733e95cbe5f31ce078c"},
+    ("global_s8192", "dkdv_tc"): {"bytes": 206.7e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                  "sha256": "bf9b07a77f77fe39b3b656d98f216f074474116c25211e72869787855afcfffb"},
+    ("global_s8192", "dq_tc"): {"bytes": 176.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                "sha256": "bf9b07a77f77fe39b3b656d98f216f074474116c25211e72869787855afcfffb"},
+    ("global_s8192", "fwd_tc"): {"bytes": 135.0e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+                                 "sha256": "f017955e90d57c8cb360166bf6d183700cadc222085636028810c93d62720935"},
 }
 
 

@@ -18,7 +18,7 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libbsrattn.so")
 
-BSR_F32, BSR_BF16 = 0, 1
+BSR_F32, BSR_BF16, BSR_F16 = 0, 1, 2
 STATUS_NAMES = {0: "BSR_OK", 1: "BSR_ERR_INVALID_ARG", 2: "BSR_ERR_UNSUPPORTED", 3: "BSR_ERR_CUDA",
                 4: "BSR_ERR_TIMEOUT", 5: "BSR_ERR_DEVICE_CHECK"}
 
@@ -87,8 +87,10 @@ def _desc(t) -> bsr_tensor:
         dt = BSR_F32
     elif t.dtype == torch.bfloat16:
         dt = BSR_BF16
+    elif t.dtype == torch.float16:
+        dt = BSR_F16
     else:
-        raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+        raise TypeError(f"unsupported dtype {t.dtype} (float32, bfloat16 or float16)")
     if t.dim() != 4 or not t.is_contiguous() or not t.is_cuda:
         raise ValueError("dense operands must be contiguous CUDA tensors [batch, heads, seq, head_dim]")
     b, h, s, d = t.shape

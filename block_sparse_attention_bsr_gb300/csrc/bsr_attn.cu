@@ -139,8 +139,8 @@ bsr_status check_tensor(const bsr_tensor* t, const char* name, const bsr_tensor*
   if (!t) return fail(BSR_ERR_INVALID_ARG, "%s: null descriptor", name);
   if (!t->data) return fail(BSR_ERR_INVALID_ARG, "%s: null data pointer", name);
   if ((uintptr_t)t->data & 15) return fail(BSR_ERR_INVALID_ARG, "%s: data pointer is not 16-byte aligned", name);
-  if (t->dtype != BSR_F32 && t->dtype != BSR_BF16)
-    return fail(BSR_ERR_UNSUPPORTED, "%s: dtype %d not supported (BSR_F32 or BSR_BF16)", name, t->dtype);
+  if (t->dtype != BSR_F32 && t->dtype != BSR_BF16 && t->dtype != BSR_F16)
+    return fail(BSR_ERR_UNSUPPORTED, "%s: dtype %d not supported (BSR_F32, BSR_BF16 or BSR_F16)", name, t->dtype);
   if (t->batch < 1 || t->heads < 1 || t->seq < 1)
     return fail(BSR_ERR_INVALID_ARG, "%s: non-positive shape [%d, %d, %d, %d]", name, t->batch, t->heads, t->seq,
                 t->head_dim);

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 #include <stddef.h>
 
@@ -22,11 +23,16 @@ struct Raw8<__nv_bfloat16> {
   uint4 v;
 };
 template <>
+struct Raw8<__half> {
+  uint4 v;
+};
+template <>
 struct Raw8<float> {
   float4 v0, v1;
 };
 
 __device__ __forceinline__ Raw8<__nv_bfloat16> ld8(const __nv_bfloat16* p) { return Raw8<__nv_bfloat16>{*(const uint4*)p}; }
+__device__ __forceinline__ Raw8<__half> ld8(const __half* p) { return Raw8<__half>{*(const uint4*)p}; }
 __device__ __forceinline__ Raw8<float> ld8(const float* p) {
   return Raw8<float>{*(const float4*)p, *(const float4*)(p + 4)};
 }
@@ -38,6 +44,18 @@ __device__ __forceinline__ float dot8(const Raw8<__nv_bfloat16>& a, const Raw8<_
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float2 u = __bfloat1622float2(xa[k]), v = __bfloat1622float2(ya[k]);
+    s = fmaf(u.x, v.x, s);
+    s = fmaf(u.y, v.y, s);
+  }
+  return s;
+}
+__device__ __forceinline__ float dot8(const Raw8<__half>& a, const Raw8<__half>& b) {
+  const __half2* xa = (const __half2*)&a.v;
+  const __half2* ya = (const __half2*)&b.v;
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 u = __half22float2(xa[k]), v = __half22float2(ya[k]);
     s = fmaf(u.x, v.x, s);
     s = fmaf(u.y, v.y, s);
   }

@@ -262,12 +262,14 @@ bsr_status launch_delta_plan(const BwdArgs& a, const PlanArgs& p, int lists, cud
   // fused only while the planner's shared memory and its O(n^2 / threads)
   // stable placement stay small
   const size_t smem = sizeof(int) * plan_smem_ints(p.n);
-  const bool fuse = p.n <= 512 && a.d.dtype == BSR_BF16 && (a.d.D == 64 || a.d.D == 128);
+  const bool fuse = p.n <= 512 && a.d.dtype != BSR_F32 && (a.d.D == 64 || a.d.D == 128);
   if (!fuse) {
     bsr_status st = launch_delta(a, s);
     if (st != BSR_OK) return st;
     return launch_plan(p, lists, s);
   }
+  if (a.d.dtype == BSR_F16)
+    return a.d.D == 64 ? launch_fused<__half, 64>(a, p, lists, smem, s) : launch_fused<__half, 128>(a, p, lists, smem, s);
   return a.d.D == 64 ? launch_fused<__nv_bfloat16, 64>(a, p, lists, smem, s)
                      : launch_fused<__nv_bfloat16, 128>(a, p, lists, smem, s);
 }

@@ -34,6 +34,8 @@ template <>
 __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <>
+__device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
 
 template <typename T>
 __device__ __forceinline__ T from_f(float x);
@@ -41,6 +43,8 @@ template <>
 __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <>
+__device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
 
 // Copies `rows` contiguous rows of D elements into fp32 shared memory with row stride `ld`.
 template <typename T, int D>
@@ -400,16 +404,22 @@ bsr_status delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   return launch(delta_kernel<T, D>, grid, 0, s, "delta", &a);
 }
 
-#define BSR_DISPATCH(FN, ARGS, STREAM)                                                  \
-  do {                                                                                 \
-    const bool bf = (ARGS).d.dtype == BSR_BF16;                                        \
-    switch ((ARGS).d.D) {                                                              \
-      case 64: return bf ? FN<__nv_bfloat16, 64>(ARGS, STREAM) : FN<float, 64>(ARGS, STREAM);     \
-      case 128: return bf ? FN<__nv_bfloat16, 128>(ARGS, STREAM) : FN<float, 128>(ARGS, STREAM);  \
-      case 256: return bf ? FN<__nv_bfloat16, 256>(ARGS, STREAM) : FN<float, 256>(ARGS, STREAM);  \
-      case 512: return bf ? FN<__nv_bfloat16, 512>(ARGS, STREAM) : FN<float, 512>(ARGS, STREAM);  \
-      default: return fail(BSR_ERR_UNSUPPORTED, "head_dim %d not supported", (ARGS).d.D);        \
-    }                                                                                  \
+#define BSR_DISPATCH_D(FN, T, ARGS, STREAM)                                      \
+  do {                                                                          \
+    switch ((ARGS).d.D) {                                                       \
+      case 64: return FN<T, 64>(ARGS, STREAM);                                  \
+      case 128: return FN<T, 128>(ARGS, STREAM);                                \
+      case 256: return FN<T, 256>(ARGS, STREAM);                                \
+      case 512: return FN<T, 512>(ARGS, STREAM);                                \
+      default: return fail(BSR_ERR_UNSUPPORTED, "head_dim %d not supported", (ARGS).d.D); \
+    }                                                                           \
+  } while (0)
+
+#define BSR_DISPATCH(FN, ARGS, STREAM)                                  \
+  do {                                                                 \
+    if ((ARGS).d.dtype == BSR_BF16) BSR_DISPATCH_D(FN, __nv_bfloat16, ARGS, STREAM); \
+    if ((ARGS).d.dtype == BSR_F16) BSR_DISPATCH_D(FN, __half, ARGS, STREAM);         \
+    BSR_DISPATCH_D(FN, float, ARGS, STREAM);                                         \
   } while (0)
 
 }  // namespace

@@ -9,6 +9,7 @@
 #include <stddef.h>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace bsr {
 namespace sm100 {
@@ -193,9 +194,9 @@ struct SDesc {
   __device__ __forceinline__ uint64_t at(uint32_t off) const { return ((uint64_t)hi << 32) | (lo + (off >> 4)); }
 };
 
-// Instruction descriptor for kind::f16 / kind::tf32: fp32 accumulator,
-// operand format code `ab_fmt` (1 = bf16, 0 = f16 under kind::f16; 2 = tf32
-// under kind::tf32), A / B major-ness (0 = K-major, 1 = MN-major), N and M.
+// Instruction descriptor for kind::f16: fp32 accumulator, operand format
+// code `ab_fmt` (1 = bf16, 0 = f16), A / B major-ness (0 = K-major,
+// 1 = MN-major), N and M.
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_fmt, uint32_t a_mn_major, uint32_t b_mn_major,
                                                   uint32_t N, uint32_t M) {
   return (1u << 4)                 // D format: f32
@@ -210,7 +211,7 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_fmt, uint32_t a_mn
 // ------------------------------------------------------------------ MMA --
 // D[tmem] (+)= A[smem] * B[smem]^T per the descriptors; `accumulate` = 0
 // overwrites D.  Issued by one thread.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -222,23 +223,13 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
 
 // Same with the A operand read from TMEM (M = 128 lanes; for 16-bit types
 // two consecutive K elements per 32-bit column, the lower one in the low half).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -255,7 +246,7 @@ __device__ __forceinline__ uint32_t elect_one() {
   return pred;
 }
 
-__device__ __forceinline__ void mma_bf16_ss_by(uint32_t leader, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+__device__ __forceinline__ void mma_ss_by(uint32_t leader, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, l;\n\t"
@@ -266,7 +257,7 @@ __device__ __forceinline__ void mma_bf16_ss_by(uint32_t leader, uint32_t d_tmem,
       : "memory");
 }
 
-__device__ __forceinline__ void mma_bf16_ts_by(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+__device__ __forceinline__ void mma_ts_by(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, l;\n\t"
@@ -343,8 +334,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
-// Stores 16 words (32 bf16) at p (16-byte aligned): two 256-bit stores when
+// The 16-bit operand types of the tensor-core kernels: the A / B format
+// code of a kind::f16 MMA (A and B always of the same type) and
+// round-to-nearest-even packing of two fp32 values, the first in the low
+// half.
+template <typename T>
+struct Half16;
+template <>
+struct Half16<__nv_bfloat16> {
+  static constexpr uint32_t kFmt = 1;
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+};
+template <>
+struct Half16<__half> {
+  static constexpr uint32_t kFmt = 0;
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
+};
+
+// Stores 16 words (32 16-bit values) at p (16-byte aligned): two 256-bit stores when
 // p is 32-byte aligned (each then fills whole 32-byte sectors), else four
 // 128-bit stores.
 __device__ __forceinline__ void st_global_64B(void* p, const uint32_t (&w)[16]) {
@@ -361,7 +374,7 @@ __device__ __forceinline__ void st_global_64B(void* p, const uint32_t (&w)[16]) 
   }
 }
 
-// Stores 64 bf16 (32 packed words w) of each of the warp's 32 consecutive
+// Stores 64 16-bit values (32 packed words w) of each of the warp's 32 consecutive
 // rows: lane l holds row l, which starts at `row` (its own pointer), rows
 // `ld` elements apart.  The four lanes of each group of four rows exchange
 // 32-byte chunks (a 4 x 4 block transpose in two shuffle steps: partner
@@ -370,7 +383,9 @@ __device__ __forceinline__ void st_global_64B(void* p, const uint32_t (&w)[16]) 
 // cache-line touches).  The whole warp calls it; `row` must be 32-byte
 // aligned and ld * 2 a multiple of 32 (otherwise rows are stored as they
 // are).  w is clobbered.
-__device__ __forceinline__ void st_rows64_bf16(uint32_t (&w)[32], __nv_bfloat16* row, size_t ld) {
+template <typename T>
+__device__ __forceinline__ void st_rows64(uint32_t (&w)[32], T* row, size_t ld) {
+  static_assert(sizeof(T) == 2, "16-bit elements");
   const int q = threadIdx.x & 3;
   const bool aligned = ((reinterpret_cast<uintptr_t>(row) & 31) == 0) && ((ld * 2) % 32 == 0);
   if (!__all_sync(0xffffffffu, aligned)) {
@@ -408,7 +423,7 @@ __device__ __forceinline__ void st_rows64_bf16(uint32_t (&w)[32], __nv_bfloat16*
   // lane q now holds, in words 8 k .. 8 k + 7, chunk q of row (l - q) + k
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    __nv_bfloat16* p = row + (ptrdiff_t)(k - q) * (ptrdiff_t)ld + 16 * q;
+    T* p = row + (ptrdiff_t)(k - q) * (ptrdiff_t)ld + 16 * q;
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[8 * k]),
                  "r"(w[8 * k + 1]), "r"(w[8 * k + 2]), "r"(w[8 * k + 3]), "r"(w[8 * k + 4]), "r"(w[8 * k + 5]),
                  "r"(w[8 * k + 6]), "r"(w[8 * k + 7])

@@ -1,4 +1,5 @@
-// Tensor-core backward pass for bf16 operands (head_dim 64 / 128) on sm_103a.
+// Tensor-core backward pass for 16-bit operands (bf16 or fp16, fp32
+// accumulation; head_dim 64 / 128) on sm_103a.
 //
 // Two kernels, each output tile with exactly one writer and no atomics
 // ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.5.1]):
@@ -63,13 +64,13 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Stores NC fp32 TMEM columns of this thread's lane (from taddr) as bf16
+// Stores NC fp32 TMEM columns of this thread's lane (from taddr) as T
 // times `mul` to global memory at grow (the warp's 32 lanes hold 32
 // consecutive rows, ld elements apart): 64 columns per round, both 32-column
 // loads in flight before the one wait, rows exchanged in groups of four so
-// the stores cover whole 128-byte lines (st_rows64_bf16).
-template <int NC>
-__device__ __forceinline__ void store_acc_cols(uint32_t taddr, __nv_bfloat16* grow, float mul, size_t ld) {
+// the stores cover whole 128-byte lines (st_rows64).
+template <int NC, typename T>
+__device__ __forceinline__ void store_acc_cols(uint32_t taddr, T* grow, float mul, size_t ld) {
   static_assert(NC % 32 == 0, "whole 32-column loads");
 #pragma unroll 1
   for (int c = 0; c < NC / 64; ++c) {
@@ -80,10 +81,10 @@ __device__ __forceinline__ void store_acc_cols(uint32_t taddr, __nv_bfloat16* gr
     uint32_t w[32];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
-      w[16 + j] = pack_bf16x2(__uint_as_float(u[2 * j]) * mul, __uint_as_float(u[2 * j + 1]) * mul);
+      w[j] = Half16<T>::pack(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
+      w[16 + j] = Half16<T>::pack(__uint_as_float(u[2 * j]) * mul, __uint_as_float(u[2 * j + 1]) * mul);
     }
-    st_rows64_bf16(w, grow + c * 64, ld);
+    st_rows64(w, grow + c * 64, ld);
   }
   if constexpr (NC % 64 != 0) {
     uint32_t v[32];
@@ -91,23 +92,25 @@ __device__ __forceinline__ void store_acc_cols(uint32_t taddr, __nv_bfloat16* gr
     tmem_wait_ld();
     uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
+    for (int j = 0; j < 16; ++j)
+      w[j] = Half16<T>::pack(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
     st_global_64B(grow + NC - 32, w);
   }
 }
 
-template <int NC>
-__device__ __forceinline__ void zero_cols(__nv_bfloat16* grow) {
+template <int NC, typename T>
+__device__ __forceinline__ void zero_cols(T* grow) {
   const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 1
   for (int c = 0; c < NC / 8; ++c) ((uint4*)grow)[c] = z;
 }
 
-// Packs 64 fp32 values to bf16 pairs and stores them in 32 TMEM columns.
-__device__ __forceinline__ void tmem_st_bf16x64(uint32_t taddr, const float (&x)[64]) {
+// Packs 64 fp32 values to pairs of T and stores them in 32 TMEM columns.
+template <typename T>
+__device__ __forceinline__ void tmem_st_pairs64(uint32_t taddr, const float (&x)[64]) {
   uint32_t v[32];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) v[k] = pack_bf16x2(x[2 * k], x[2 * k + 1]);
+  for (int k = 0; k < 32; ++k) v[k] = Half16<T>::pack(x[2 * k], x[2 * k + 1]);
   tmem_st32(taddr, v);
 }
 
@@ -125,10 +128,10 @@ __device__ __forceinline__ void store_acc_part(uint32_t taddr, float* tile, int 
 }
 
 // Sums NC columns of row r (from column group cg0) over `nc` partial tiles
-// spaced `stride` floats apart and stores them as bf16 times `mul` at dst.
-template <int NC>
-__device__ __forceinline__ void merge_tiles(const float* tile0, size_t stride, int nc, int cg0, int r,
-                                            __nv_bfloat16* dst, float mul) {
+// spaced `stride` floats apart and stores them as T times `mul` at dst.
+template <int NC, typename T>
+__device__ __forceinline__ void merge_tiles(const float* tile0, size_t stride, int nc, int cg0, int r, T* dst,
+                                            float mul) {
 #pragma unroll 1
   for (int c = 0; c < NC / 32; ++c) {
     float acc[32];
@@ -137,7 +140,7 @@ __device__ __forceinline__ void merge_tiles(const float* tile0, size_t stride, i
     for (int ch = 0; ch < nc; ++ch) part_accum32(tile0 + ch * stride, cg0 + c * 8, r, 1.f, acc);
     uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(acc[2 * j] * mul, acc[2 * j + 1] * mul);
+    for (int j = 0; j < 16; ++j) w[j] = Half16<T>::pack(acc[2 * j] * mul, acc[2 * j + 1] * mul);
     st_global_64B(dst + c * 32, w);
   }
 }
@@ -177,7 +180,7 @@ struct DqBars {
 };
 static_assert(sizeof(DqBars) <= 512, "barrier block overflows its shared-memory slot");
 
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, BwdArgs a) {
@@ -297,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (cursor B), so they run while the elementwise pass of block g
       // computes dS.  A draws items from the ring; B follows and releases
       // each item once it is past it.
-      const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
-      const uint32_t idDQ = instr_desc(1, 0, 1, D, 128);
+      const uint32_t idS = instr_desc(Half16<T>::kFmt, 0, 0, 128, 128);
+      const uint32_t idDQ = instr_desc(Half16<T>::kFmt, 0, 1, D, 128);
       const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO), aK = smem_u32(sK), aV = smem_u32(sV);
       bool ok = true;
       auto seek_a = [&](Cursor& c) {
@@ -350,12 +353,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColS, dQ.at(off), dK.at(off), idS, kk > 0);
+          mma_ss_by(leader, tmem + kColS, dQ.at(off), dK.at(off), idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColDP, dO.at(off), dV.at(off), idS, kk > 0);
+          mma_ss_by(leader, tmem + kColDP, dO.at(off), dV.at(off), idS, kk > 0);
         }
         mma_commit_by(leader, &bars->v_empty[vs]);
         mma_commit_by(leader, &bars->sdp_full);
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ds = tmem + kColDS + (B.g & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts_by(leader, tmem + kColDQ, ds + kk * 8, dK.at(kk * 2048), idDQ, (B.i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_by(leader, tmem + kColDQ, ds + kk * 8, dK.at(kk * 2048), idDQ, (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->k_empty[st]);
         mma_commit_by(leader, &bars->dq_done[B.g & 1]);
         __syncwarp();
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Cursor cur;
       walk.decode(k, cur);
       const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
-      __nv_bfloat16* dqrow = (__nv_bfloat16*)a.dQ + grow * D + hg * (D / 2);
+      T* dqrow = (T*)a.dQ + grow * D + hg * (D / 2);
       if (cur.n == 0) {
         zero_cols<D / 2>(dqrow);
       } else {
@@ -458,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (g > 1 && !(ok = warp_wait(&bars->dq_done[g & 1], ((g - 2) >> 1) & 1, ab, a.status))) break;
           tc_fence_after();
-          tmem_st_bf16x64(tmem + lane_base + kColDS + (g & 1) * 64 + hg * 32, s);
+          tmem_st_pairs64<T>(tmem + lane_base + kColDS + (g & 1) * 64 + hg * 32, s);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->ds_full[g & 1]);
@@ -542,7 +545,7 @@ struct DkvBars {
 };
 static_assert(sizeof(DkvBars) <= 512, "barrier block overflows its shared-memory slot");
 
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, BwdArgs a) {
@@ -692,8 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // block g+3 loads as soon as dK_g is done.  When block g+1 starts
       // another item, dK_g goes before S^T_{g+1}, so that this item's
       // epilogue does not wait behind the next item's MMAs.
-      const uint32_t idST = instr_desc(1, 0, 0, 128, 128);
-      const uint32_t idG = instr_desc(1, 0, 1, D, 128);
+      const uint32_t idST = instr_desc(Half16<T>::kFmt, 0, 0, 128, 128);
+      const uint32_t idG = instr_desc(Half16<T>::kFmt, 0, 1, D, 128);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
       bool ok = true;
       auto seek_a = [&](Cursor& c) {
@@ -750,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColST, dK.at(off), dQ.at(off), idST, kk > 0);
+          mma_ss_by(leader, tmem + kColST, dK.at(off), dQ.at(off), idST, kk > 0);
         }
         mma_commit_by(leader, &bars->st_full);
         if (c.i == c.n - 1) mma_commit_by(leader, &bars->k_empty);
@@ -765,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss_by(leader, tmem + kColDPT, dV.at(off), dO.at(off), idST, kk > 0);
+          mma_ss_by(leader, tmem + kColDPT, dV.at(off), dO.at(off), idST, kk > 0);
         }
         mma_commit_by(leader, &bars->dpt_full);
         if (c.i == c.n - 1) mma_commit_by(leader, &bars->v_empty);
@@ -784,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts_by(leader, tmem + kColDV, tmem + kColST + kk * 8 + (kk >= 4 ? 32 : 0), dOmn.at(kk * 2048), idG,
+          mma_ts_by(leader, tmem + kColDV, tmem + kColST + kk * 8 + (kk >= 4 ? 32 : 0), dOmn.at(kk * 2048), idG,
                          (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->do_empty[so]);
         mma_commit_by(leader, &bars->pt_free);
@@ -798,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts_by(leader, tmem + kColDK, tmem + kColDPT + kk * 8 + (kk >= 4 ? 32 : 0), dQmn.at(kk * 2048), idG,
+          mma_ts_by(leader, tmem + kColDK, tmem + kColDPT + kk * 8 + (kk >= 4 ? 32 : 0), dQmn.at(kk * 2048), idG,
                          (B.i > 0 || kk > 0) ? 1u : 0u);
         mma_commit_by(leader, &bars->q_empty[sq]);
         mma_commit_by(leader, &bars->dk_done);
@@ -841,8 +844,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       Cursor cur;
       walk.decode(k, cur);
       const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
-      __nv_bfloat16* dkrow = (__nv_bfloat16*)a.dK + grow * D + hg * (D / 2);
-      __nv_bfloat16* dvrow = (__nv_bfloat16*)a.dV + grow * D + hg * (D / 2);
+      T* dkrow = (T*)a.dK + grow * D + hg * (D / 2);
+      T* dvrow = (T*)a.dV + grow * D + hg * (D / 2);
       if (cur.n == 0) {
         zero_cols<D / 2>(dkrow);
         zero_cols<D / 2>(dvrow);
@@ -867,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // P^T over this warpgroup's own S^T columns (already read above;
           // dV of the previous block finished before S^T of this one began)
-          tmem_st_bf16x64(tmem + lane_base + kColST + hg * 64, s);
+          tmem_st_pairs64<T>(tmem + lane_base + kColST + hg * 64, s);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->pt_ready);
@@ -885,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->stat_empty[ss]);
           // dS^T over this warpgroup's own dP^T columns (read above; dK of
           // the previous block finished before dP^T of this one began)
-          tmem_st_bf16x64(tmem + lane_base + kColDPT + hg * 64, dp);
+          tmem_st_pairs64<T>(tmem + lane_base + kColDPT + hg * 64, dp);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->ds_ready);
@@ -940,10 +943,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // back into it.  Their CTAs never share an SM (each needs almost all of its
 // shared memory), so the second kernel's CTAs take the SMs the first one
 // leaves in its tail.
-template <int D>
+template <typename T, int D>
 bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, int grid, cudaStream_t s) {
-  auto dq = dq_tc_kernel<D>;
-  auto dkdv = dkdv_tc_kernel<D>;
+  auto dq = dq_tc_kernel<T, D>;
+  auto dkdv = dkdv_tc_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmem);
   if (e != cudaSuccess)
     return fail(BSR_ERR_CUDA, "dq_tc: cudaFuncSetAttribute(%d): %s", DqCfg<D>::kSmem, cudaGetErrorString(e));
@@ -981,7 +984,9 @@ bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap&
 
 }  // namespace
 
-bool tc_bwd_supported(const Dims& d) { return d.dtype == BSR_BF16 && (d.D == 64 || d.D == 128); }
+bool tc_bwd_supported(const Dims& d) {
+  return (d.dtype == BSR_BF16 || d.dtype == BSR_F16) && (d.D == 64 || d.D == 128);
+}
 
 int tc_grid(const Dims& d) {
   const int sms = sm_count();
@@ -1000,8 +1005,12 @@ bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap tmdO;
   if ((st = make_tensor_map(a.d, a.dO, &tmdO, "dO")) != BSR_OK) return st;
   switch (a.d.D) {
-    case 64: return launch_bwd<64>(a, tm, tmdO, grid, s);
-    case 128: return launch_bwd<128>(a, tm, tmdO, grid, s);
+    case 64:
+      return a.d.dtype == BSR_F16 ? launch_bwd<__half, 64>(a, tm, tmdO, grid, s)
+                                  : launch_bwd<__nv_bfloat16, 64>(a, tm, tmdO, grid, s);
+    case 128:
+      return a.d.dtype == BSR_F16 ? launch_bwd<__half, 128>(a, tm, tmdO, grid, s)
+                                  : launch_bwd<__nv_bfloat16, 128>(a, tm, tmdO, grid, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "bwd_tc: head_dim %d", a.d.D);
   }
 }

@@ -1,4 +1,4 @@
-// Tensor-core forward pass for bf16 operands (head_dim 64 / 128 / 256) on
+// Tensor-core forward pass for 16-bit operands (bf16 or fp16; head_dim 256) on
 // sm_103a: TMA block walker, tcgen05 MMAs with TMEM accumulators, online
 // softmax with the statistics kept on chip.
 //
@@ -9,9 +9,9 @@
 // launch, statistics on chip, no K/V gather, no host reduction, no per-block
 // score round trip through HBM).  head_dim 256 is K-tiled: the Q.K^T
 // contraction runs over 64-column chunks of head_dim accumulated into one fp32
-// score tile ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.6.0]).  bf16
-// operands, fp32 accumulation, fp32 scores and statistics ("trnsparse 0.7.0
-// -> 0.9.0" diff, CHANGELOG [0.9.0]).
+// score tile ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.6.0]).  bf16 or
+// fp16 operands, fp32 accumulation, fp32 scores and statistics ("trnsparse
+// 0.7.0 -> 0.9.0" diff, CHANGELOG [0.9.0]).
 //
 // Warp roles (256 threads):
 //   warp 0      TMA producer (one thread): Q once, then K / V tiles per block
@@ -78,7 +78,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && nblk > 0) {
       // ----------------------------------------------------------- MMA --
-      const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
-      const uint32_t idPV = instr_desc(1, 0, 1, D, 128);
+      const uint32_t idS = instr_desc(Half16<T>::kFmt, 0, 0, 128, 128);
+      const uint32_t idPV = instr_desc(Half16<T>::kFmt, 0, 1, D, 128);
       const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
       bool ok = mbar_wait(&bars->q_full, 0, &bars->abort_flag, a.status);
       auto issue_s = [&](int i) -> bool {
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + b * 128, smem_desc(aQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
+          mma_ss(tmem + b * 128, smem_desc(aQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, kk > 0);
         }
         mma_commit(&bars->k_empty[st]);
         mma_commit(&bars->s_full[b]);
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColO, smem_desc(aP + poff, 16, 1024), smem_desc(vb + kk * 2048, 16384, 1024), idPV,
+          mma_ss(tmem + kColO, smem_desc(aP + poff, 16, 1024), smem_desc(vb + kk * 2048, 16384, 1024), idPV,
                       (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars->v_empty[st]);
@@ -281,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           sum += p[e];
         }
         const uint32_t addr = prow + (c16 >> 3) * 16384 + (((c16 & 7) ^ (r & 7)) << 4);
-        st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-                     pack_bf16x2(p[6], p[7]));
+        st_shared_v4(addr, Half16<T>::pack(p[0], p[1]), Half16<T>::pack(p[2], p[3]), Half16<T>::pack(p[4], p[5]),
+                     Half16<T>::pack(p[6], p[7]));
       }
       l += sum;
       fence_proxy_async_smem();
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ------------------------------------------------------- epilogue --
     const size_t grow = (size_t)bh * S + (size_t)m * 128 + r;
-    __nv_bfloat16* orow = (__nv_bfloat16*)a.O + grow * D;
+    T* orow = (T*)a.O + grow * D;
     if (ok && nblk > 0) ok = warp_wait(&bars->pv_done, (nblk - 1) & 1, bars, a.status);
     if (ok && nblk > 0) {
       tc_fence_after();
@@ -305,10 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 o;
-          o.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
-          o.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
-          o.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
-          o.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
+          o.x = Half16<T>::pack(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
+          o.y = Half16<T>::pack(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
+          o.z = Half16<T>::pack(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
+          o.w = Half16<T>::pack(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
           dst[q] = o;
         }
       }
@@ -328,10 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D>
+template <typename T, int D>
 bsr_status launch_fwd(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
   using C = FwdCfg<D>;
-  auto kern = fwd_tc_kernel<D>;
+  auto kern = fwd_tc_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "fwd_tc: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
   dim3 grid(a.d.nb * a.d.BH);
@@ -342,7 +342,9 @@ bsr_status launch_fwd(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
 
 }  // namespace
 
-bool tc_fwd_supported(const Dims& d) { return d.dtype == BSR_BF16 && (d.D == 64 || d.D == 128 || d.D == 256); }
+bool tc_fwd_supported(const Dims& d) {
+  return (d.dtype == BSR_BF16 || d.dtype == BSR_F16) && (d.D == 64 || d.D == 128 || d.D == 256);
+}
 
 bsr_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   if (a.d.D <= 128) return launch_fwd_tc2(a, s);
@@ -350,9 +352,8 @@ bsr_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
   if (st != BSR_OK) return st;
   switch (a.d.D) {
-    case 64: return launch_fwd<64>(a, tm, s);
-    case 128: return launch_fwd<128>(a, tm, s);
-    case 256: return launch_fwd<256>(a, tm, s);
+    case 256:
+      return a.d.dtype == BSR_F16 ? launch_fwd<__half, 256>(a, tm, s) : launch_fwd<__nv_bfloat16, 256>(a, tm, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "fwd_tc: head_dim %d", a.d.D);
   }
 }

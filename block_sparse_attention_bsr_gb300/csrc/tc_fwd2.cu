@@ -1,5 +1,6 @@
-// Tensor-core forward pass for bf16 operands with head_dim 64 / 128 on
-// sm_103a, with P kept in tensor memory.
+// Tensor-core forward pass for 16-bit operands (bf16 or fp16, fp32
+// accumulation) with head_dim 64 / 128 on sm_103a, with P kept in tensor
+// memory in the operand type.
 //
 // Same walk as the head_dim-256 kernel in tc_fwd.cu (for each block row m
 // of one (batch, head) the row's stored blocks j in [row_ptr[m],
@@ -143,7 +144,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
@@ -302,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // walks the schedule on its own.
     if (lane == 0) {
       const bool s_role = warp == 1;
-      const uint32_t idS = instr_desc(1, 0, 0, 128, 128);
-      const uint32_t idPV = instr_desc(1, 0, 1, D, 128);
+      const uint32_t idS = instr_desc(Half16<T>::kFmt, 0, 0, 128, 128);
+      const uint32_t idPV = instr_desc(Half16<T>::kFmt, 0, 1, D, 128);
       const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
       int g = 0, q = 0;  // blocks / non-empty items walked so far
       bool ok = true;
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              mma_bf16_ss(tmem, dQ.at(off), dK.at(off), idS, kk > 0);
+              mma_ss(tmem, dQ.at(off), dK.at(off), idS, kk > 0);
             }
             mma_commit(&bars->k_empty[ks]);
             mma_commit(&bars->s_full);
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < 2; ++h) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ts(tmem + kColO + h * D, tmem + kColP + b * 64 + h * 32 + kk * 8,
+                mma_ts(tmem + kColO + h * D, tmem + kColP + b * 64 + h * 32 + kk * 8,
                             dV.at((4 * h + kk) * 2048), idPV, (j > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars->v_empty[vs]);
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       walk.decode(k, cur);
       const int nblk = cur.n;
       const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
-      __nv_bfloat16* orow = (__nv_bfloat16*)a.O + grow * D + hg * (D / 2);
+      T* orow = (T*)a.O + grow * D + hg * (D / 2);
       if (nblk == 0) {
         const uint4 z = make_uint4(0, 0, 0, 0);
         for (int c = 0; c < D / 16; ++c) ((uint4*)orow)[c] = z;
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x = fma2(make_float2(tt[2 * k], tt[2 * k + 1]), sc, nm);
           const float2 p = make_float2(ex2(x.x), ex2(x.y));
           sum4[k & 3] = add2(sum4[k & 3], p);
-          pk[k] = pack_bf16x2(p.x, p.y);
+          pk[k] = Half16<T>::pack(p.x, p.y);
         }
         l += (sum4[0].x + sum4[0].y + sum4[1].x + sum4[1].y) + (sum4[2].x + sum4[2].y + sum4[3].x + sum4[3].y);
         // P of this block goes to buffer b once P.V of block g - 2 (the
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = 1.f / L;
         const float2 w = make_float2(c0 * inv, c1 * inv);
         // this half's D / 2 output columns as bf16, stored 64 at a time with
-        // the rows exchanged in groups of four (st_rows64_bf16)
+        // the rows exchanged in groups of four (st_rows64)
         uint32_t o[D / 4];
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
@@ -511,11 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   make_float2(w.x, w.x),
                                   mul2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
                                        make_float2(w.y, w.y)));
-            o[16 * c + j] = pack_bf16x2(y.x, y.y);
+            o[16 * c + j] = Half16<T>::pack(y.x, y.y);
           }
         }
         if constexpr (D == 128) {
-          st_rows64_bf16(o, orow, (size_t)D);
+          st_rows64(o, orow, (size_t)D);
         } else {
           st_global_64B(orow, o);
         }
@@ -581,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint32_t o[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+            for (int j = 0; j < 16; ++j) o[j] = Half16<T>::pack(acc[2 * j], acc[2 * j + 1]);
             st_global_64B(orow + c * 32, o);
           }
           if (hg == 0) {
@@ -604,10 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D>
+template <typename T, int D>
 bsr_status launch(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
   using C = Fwd2Cfg<D>;
-  auto kern = fwd_tc2_kernel<D>;
+  auto kern = fwd_tc2_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess)
     return fail(BSR_ERR_CUDA, "fwd_tc: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
@@ -630,8 +631,8 @@ bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s) {
   bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
   if (st != BSR_OK) return st;
   switch (a.d.D) {
-    case 64: return launch<64>(a, tm, s);
-    case 128: return launch<128>(a, tm, s);
+    case 64: return a.d.dtype == BSR_F16 ? launch<__half, 64>(a, tm, s) : launch<__nv_bfloat16, 64>(a, tm, s);
+    case 128: return a.d.dtype == BSR_F16 ? launch<__half, 128>(a, tm, s) : launch<__nv_bfloat16, 128>(a, tm, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "fwd_tc2: head_dim %d", a.d.D);
   }
 }

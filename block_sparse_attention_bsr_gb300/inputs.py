@@ -75,15 +75,15 @@ def bsr_from_block_mask(bm: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return row_ptr, np.ascontiguousarray(col_idx)
 
 
-_TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+_TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 def make_qkvdo(batch: int, heads: int, seq: int, head_dim: int, dtype: str = "f32",
                std: float = 1.0, seed: int = 0):
-    """Q, K, V, dO as CPU tensors [B, H, S, D] of ``dtype`` (``"f32"`` or ``"bf16"``).
+    """Q, K, V, dO as CPU tensors [B, H, S, D] of ``dtype`` (``"f32"``, ``"bf16"`` or ``"f16"``).
 
     Values are iid N(0, std^2) drawn in the order Q, K, V, dO from one seeded
-    generator and rounded to ``dtype`` (round to nearest even for bf16).
+    generator and rounded to ``dtype`` (round to nearest even for bf16 and f16).
     """
     g = torch.Generator().manual_seed(seed)
     out = []

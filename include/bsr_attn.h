@@ -23,7 +23,11 @@
  *    aligned (inputs are read by TMA, outputs written with 16- and 32-byte
  *    vector stores; a misaligned pointer is BSR_ERR_INVALID_ARG).  All dense
  *    tensors of one call have the same shape and dtype.  Supported:
- *    head_dim in {64, 128, 256, 512}; dtype BSR_F32 or BSR_BF16;
+ *    head_dim in {64, 128, 256, 512}; dtype BSR_F32, BSR_BF16 or BSR_F16
+ *    (16-bit operands are multiplied on the tensor cores with fp32
+ *    accumulation, and outputs are rounded to the operand type; the
+ *    statistics are fp32 for every dtype, as the "trnsparse 0.7.0 -> 0.9.0"
+ *    diff, CHANGELOG [0.9.0], has them for fp16 and bf16 inputs);
  *    seq = n_brows * 128; batch, heads >= 1.
  *  - Statistics row_max / row_denom are fp32 DEVICE arrays [batch, heads, seq].
  *    row_max is the maximum of the scaled scores scale * q.k of the row over
@@ -49,7 +53,7 @@
 extern "C" {
 #endif
 
-typedef enum { BSR_F32 = 0, BSR_BF16 = 1 } bsr_dtype;
+typedef enum { BSR_F32 = 0, BSR_BF16 = 1, BSR_F16 = 2 } bsr_dtype;
 
 typedef enum {
   BSR_OK = 0,

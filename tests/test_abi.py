@@ -91,6 +91,7 @@ def _fwd(lib, Q=None, K=None, V=None, O=None, n_brows=2, block=128, scale=0.125,
     (dict(Q=_fake(d=32)), 2, "head_dim"),
     (dict(K=_fake(dtype=1)), 2, "dtype"),
     (dict(V=_fake(dtype=7)), 2, "dtype"),
+    (dict(Q=_fake(dtype=2), K=_fake(dtype=2), V=_fake(dtype=2)), 2, "dtype"),  # fp16 beside an fp32 O
     (dict(O=_fake(s=384)), 1, "shape"),
     (dict(Q=_fake(ptr=0)), 1, "null"),
     (dict(ptrs=(0, 0x20, 0x30, 0x40)), 1, "null"),

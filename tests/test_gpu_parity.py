@@ -36,6 +36,26 @@ def test_dilated_s2048_bf16_all_heads():
     _workload("dilated_s2048")
 
 
+def _workload_as(name, dtype, heads=None, seed=0):
+    # a workload's mask and shape with operands drawn in another dtype
+    wl = inputs.WORKLOADS[name]
+    bm = wl.block_mask()
+    Q, K, V, dO = inputs.make_qkvdo(wl.batch, wl.heads, wl.seq, wl.head_dim, dtype, 1.0, seed)
+    got = run_gpu(Q, K, V, dO, bm, wl.scale)
+    if heads is None:
+        heads = [(b, h) for b in range(wl.batch) for h in range(wl.heads)]
+    ref = oracle_heads(Q, K, V, dO, bm, wl.scale, heads)
+    return compare(got, ref, dtype, heads=heads, what=f"{name} {dtype}")
+
+
+def test_dilated_s2048_f16_all_heads():
+    _workload_as("dilated_s2048", "f16")
+
+
+def test_global_s8192_f16_sampled_heads():
+    _workload_as("global_s8192", "f16", heads=[(0, 0), (0, 15)])
+
+
 @pytest.mark.parametrize("name", ["global_s8192", "global_s8192_f32"])
 def test_global_s8192_sampled_heads(name):
     _workload(name, heads=[(0, 0), (0, 15)])
@@ -62,7 +82,7 @@ def _edge(bm, dtype, D=64, B=1, H=2, std=1.0, seed=3):
     return got, compare(got, ref, dtype, heads=[(b, h) for b in range(B) for h in range(H)])
 
 
-DTYPES = ["f32", "bf16"]
+DTYPES = ["f32", "bf16", "f16"]
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
