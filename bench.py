@@ -34,7 +34,7 @@ from block_sparse_attention_bsr_gb300 import inputs  # noqa: E402
 BLOCK = 128
 METRIC = "fwd+bwd ms & TFLOP/s over stored blocks at seq 8192; % of GB300 bf16 TC peak"
 # contraction FLOP per stored block and head, as each kernel executes them
-FLOP_PER_BLOCK = {"fwd": 4, "dq": 6, "dkdv": 8}  # x 128^2 * D
+FLOP_PER_BLOCK = {"fwd_": 4, "fwd2p_stats": 2, "fwd2p_out": 4, "dq": 6, "dkdv": 8}  # x 128^2 * D
 
 
 def alg_flops(wl, nnzb, part="total"):
@@ -52,8 +52,8 @@ MEASURED_TRAFFIC = {
                                   "sha256": "bf9b07a77f77fe39b3b656d98f216f074474116c25211e72869787855afcfffb"},
     ("global_s8192", "dq_tc"): {"bytes": 176.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
                                 "sha256": "bf9b07a77f77fe39b3b656d98f216f074474116c25211e72869787855afcfffb"},
-    ("global_s8192", "fwd_tc"): {"bytes": 135.0e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "f017955e90d57c8cb360166bf6d183700cadc222085636028810c93d62720935"},
+    ("global_s8192", "fwd_tc"): {"bytes": 137.0e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+                                 "sha256": "9146b0b1e30a5e5ea18f4af9e6204ee1884646fdd4d60aa8e4367aa77e96d0b2"},
 }
 
 
@@ -158,8 +158,10 @@ def run_ours(args, rank, world, dev):
     dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
     stream = torch.cuda.current_stream(dev)
 
+    two_pass = args.forward == "two-pass"
+
     def step(q, k, v, do, o, m, d, gq, gk, gv):
-        bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale, o, m, d, stream)
+        bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale, o, m, d, stream, two_pass)
         bsr.bsr_attn_bwd(q, k, v, o, do, m, d, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, wl.scale,
                          gq, gk, gv, stream)
 
@@ -209,7 +211,7 @@ def run_ours(args, rank, world, dev):
         return statistics.median(a.elapsed_time(b) for a, b in e)
 
     ms_fwd = time_part(lambda: bsr.bsr_attn_fwd(Q, K, V, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale,
-                                                 O, rm, rd, stream), max(args.steps, 5))
+                                                 O, rm, rd, stream, two_pass), max(args.steps, 5))
     ms_bwd = time_part(lambda: bsr.bsr_attn_bwd(Q, K, V, O, dO, rm, rd, st.row_ptr, st.col_idx, st.col_ptr,
                                                  st.row_idx, wl.scale, dQ, dK, dV, stream), max(args.steps, 5))
 
@@ -245,7 +247,8 @@ def run_ours(args, rank, world, dev):
         roofline = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
                     "unit": "TFLOP/s", "frac": (achieved / peaks["bf16"]) if achieved else None,
                     "traffic": measured_traffic(wl.name, name), "traffic_unit": "bytes per launch (ncu DRAM)",
-                    "peak_source": peaks["source"] + " bf16 burst",
+                    "peak_source": peaks["source"] + " bf16 burst"
+                    + (" (fp16 operands: the same dense rate as bf16 nominally)" if wl.dtype == "f16" else ""),
                     "flop_per_launch": kf, "ms_per_launch": avg_ms}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -254,7 +257,7 @@ def run_ours(args, rank, world, dev):
         "config": {"workload": wl.name, "batch": wl.batch, "heads": wl.heads, "seq": wl.seq,
                    "head_dim": wl.head_dim, "block": BLOCK, "mask": wl.mask, "radius": wl.radius,
                    "nnzb": nnzb, "density": round(nnzb / wl.nb ** 2, 4), "l2": "flushed before every step",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "forward": args.forward},
         "ms_fwd": round(ms_fwd, 4), "ms_bwd": round(ms_bwd, 4),
         "kernel_timing": {"pass": "second pass of the same K steps with CUDA events around every launch; "
                                   "dQ and dK/dV run one after the other there (the headline pass overlaps them "
@@ -345,6 +348,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="global_s8192", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--forward", default="online", choices=["online", "two-pass"],
+                    help="forward variant: the online-softmax pass, or the statistics-first two-pass variant")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

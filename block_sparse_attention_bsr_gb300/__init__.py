@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "BSR_OK", 1: "BSR_ERR_INVALID_ARG", 2: "BSR_ERR_UNSUPPORTED",
                 4: "BSR_ERR_TIMEOUT", 5: "BSR_ERR_DEVICE_CHECK"}
 
 # Every symbol include/bsr_attn.h declares.
-EXPORTS = ("bsr_attn_fwd", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
+EXPORTS = ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
            "bsr_last_error", "bsr_profile_enable", "bsr_profile_collect")
 
 
@@ -57,6 +57,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I32, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
     T = ctypes.POINTER(bsr_tensor)
     lib.bsr_attn_fwd.argtypes = [T, T, T, P, P, I32, I32, F32, T, P, P, P]
+    lib.bsr_attn_fwd_two_pass.argtypes = [T, T, T, P, P, I32, I32, F32, T, P, P, P]
     lib.bsr_attn_bwd.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_attn_bwd_noalloc.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_build_bsc.argtypes = [P, P, I32, I32, P, P]
@@ -68,7 +69,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsr_profile_enable.restype = None
     lib.bsr_profile_collect.argtypes = [ctypes.POINTER(bsr_kernel_time), I32]
     lib.bsr_profile_collect.restype = I32
-    for name in ("bsr_attn_fwd", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
+    for name in ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
         getattr(lib, name).restype = I32
     _lib_handle = lib
     return lib
@@ -114,11 +115,14 @@ def _stream(stream, like) -> int:
 
 
 def bsr_attn_fwd(Q, K, V, row_ptr, col_idx, n_brows: int, block: int, scale: float, O, row_max, row_denom,
-                 stream=None) -> None:
-    """Forward block-sparse attention: writes O, row_max, row_denom (see include/bsr_attn.h)."""
+                 stream=None, two_pass: bool = False) -> None:
+    """Forward block-sparse attention: writes O, row_max, row_denom (see include/bsr_attn.h).
+
+    ``two_pass`` selects the statistics-first variant (bsr_attn_fwd_two_pass)."""
     lib = load_library()
     q, k, v, o = (_desc(t) for t in (Q, K, V, O))
-    _check(lib.bsr_attn_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+    fn = lib.bsr_attn_fwd_two_pass if two_pass else lib.bsr_attn_fwd
+    _check(fn(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
                             _dev_ptr(row_ptr, "torch.int32"), _dev_ptr(col_idx, "torch.int32"),
                             int(n_brows), int(block), float(scale), ctypes.byref(o),
                             _dev_ptr(row_max, "torch.float32"), _dev_ptr(row_denom, "torch.float32"),

@@ -176,10 +176,14 @@ using namespace bsr;
 
 extern "C" const char* bsr_last_error(void) { return g_error.c_str(); }
 
-extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
-                                   const int32_t* row_ptr, const int32_t* col_idx, int32_t n_brows,
-                                   int32_t block, float scale,
-                                   bsr_tensor* O, float* row_max, float* row_denom, void* stream) {
+namespace bsr {
+namespace {
+
+// The forward entry points: the online-softmax pass, or (two_pass) the
+// statistics pass and then the output pass of the statistics-first variant.
+bsr_status fwd_impl(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V, const int32_t* row_ptr,
+                    const int32_t* col_idx, int32_t n_brows, int32_t block, float scale, bsr_tensor* O,
+                    float* row_max, float* row_denom, void* stream, bool two_pass) {
   bsr_status st;
   if (block != 128) return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd: block %d not supported (128)", block);
   if ((st = check_tensor(Q, "Q", nullptr)) || (st = check_tensor(K, "K", Q)) || (st = check_tensor(V, "V", Q)) ||
@@ -202,6 +206,8 @@ extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, con
   a.status = status_ptr();
   if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
   cudaStream_t s = (cudaStream_t)stream;
+  if (two_pass && !(tc_fwd_supported(a.d) && a.d.D <= 128))
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd_two_pass: bf16 / fp16 operands with head_dim 64 or 128 only");
   if (!tc_fwd_supported(a.d)) return launch_fwd_simt(a, s);
   const int G = tc_grid(a.d);
   if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cannot query the SM count");
@@ -222,10 +228,35 @@ extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, con
   p.allow_split = persistent ? 1 : 0;
   p.status = a.status;
   st = launch_plan(p, 1, s);
-  if (st == BSR_OK) st = launch_fwd_tc(a, s);
+  if (!two_pass) {
+    if (st == BSR_OK) st = launch_fwd_tc(a, s);
+  } else {
+    // the planner runs again before the output pass: it also clears the
+    // split lines' arrival counters the statistics pass used
+    if (st == BSR_OK) st = launch_fwd_tc2(a, s, 1);
+    if (st == BSR_OK) st = launch_plan(p, 1, s);
+    if (st == BSR_OK) st = launch_fwd_tc2(a, s, 2);
+  }
   e = cudaFreeAsync(scratch, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaFreeAsync: %s", cudaGetErrorString(e));
   return st;
+}
+
+}  // namespace
+}  // namespace bsr
+
+extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                                   const int32_t* row_ptr, const int32_t* col_idx, int32_t n_brows,
+                                   int32_t block, float scale,
+                                   bsr_tensor* O, float* row_max, float* row_denom, void* stream) {
+  return bsr::fwd_impl(Q, K, V, row_ptr, col_idx, n_brows, block, scale, O, row_max, row_denom, stream, false);
+}
+
+extern "C" bsr_status bsr_attn_fwd_two_pass(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                                            const int32_t* row_ptr, const int32_t* col_idx, int32_t n_brows,
+                                            int32_t block, float scale, bsr_tensor* O, float* row_max,
+                                            float* row_denom, void* stream) {
+  return bsr::fwd_impl(Q, K, V, row_ptr, col_idx, n_brows, block, scale, O, row_max, row_denom, stream, true);
 }
 
 namespace bsr {

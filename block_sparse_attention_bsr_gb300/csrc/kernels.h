@@ -233,7 +233,10 @@ bsr_status launch_dkdv_simt(const BwdArgs& a, cudaStream_t s);
 // 128) must hold the block-row plan built by launch_plan.
 bool tc_fwd_supported(const Dims& d);
 bsr_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
-bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s);  // head_dim 64 / 128, P in TMEM
+// head_dim 64 / 128, P in TMEM.  pass 0: the online-softmax forward; 1 and
+// 2: the statistics pass and then the output pass of the statistics-first
+// variant (the output pass reads the row_max / row_denom the first wrote).
+bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s, int pass = 0);
 bool tc_bwd_supported(const Dims& d);
 // Persistent grid of the tensor-core kernels: min(SMs, lines * BH); 0 on error.
 int tc_grid(const Dims& d);

@@ -63,6 +63,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: stale max may lag by 2^8
 
+// Forward variants: the single online-softmax pass, or the two launches of
+// the statistics-first variant ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG
+// [0.4.3]: the row statistics in a first pass over the row's blocks, the
+// output in a second one with P normalised by them).  The statistics pass
+// issues no P.V and loads no V; the output pass takes no maximum and never
+// rescales.
+constexpr int kOnline = 0, kStatsPass = 1, kOutPass = 2;
+
 template <int D>
 struct Fwd2Cfg {
   static constexpr int kBoxes = D / 64;
@@ -144,7 +152,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, int kPass>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, FwdArgs a) {
@@ -279,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ring_get(ring, t, &k, ab, a.status)) || k < 0) break;
         Cursor cur;
         walk.decode(k, cur);
-        for (int j = 0; j < cur.n; ++j, ++g) {
+        const int nv = kPass == kStatsPass ? 0 : cur.n;
+        for (int j = 0; j < nv; ++j, ++g) {
           int n = a.col_idx[cur.first + j];
           n = (n < 0 || n >= a.d.nb) ? 0 : n;
           const int krow = cur.bh * S + n * 128;
@@ -331,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&bars->k_empty[ks]);
             mma_commit(&bars->s_full);
             if (j == cur.n - 1) mma_commit(&bars->q_empty[qb]);
-          } else {
+          } else if constexpr (kPass != kStatsPass) {
             const int vs = g % C::kVStages;
             const int b = g & 1;
             if (!(ok = mbar_wait(&bars->v_full[vs], (g / C::kVStages) & 1, ab, a.status))) break;
@@ -386,9 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
       T* orow = (T*)a.O + grow * D + hg * (D / 2);
       if (nblk == 0) {
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int c = 0; c < D / 16; ++c) ((uint4*)orow)[c] = z;
-        if (hg == 0) {
+        if constexpr (kPass != kStatsPass) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < D / 16; ++c) ((uint4*)orow)[c] = z;
+        }
+        if (kPass != kOutPass && hg == 0) {
           a.row_max[grow] = -INFINITY;
           a.row_denom[grow] = 0.f;
         }
@@ -397,6 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+      if constexpr (kPass == kOutPass) {
+        // the row's base-2 log-sum-exp from the statistics pass: P comes
+        // out normalised, 2^(scale log2(e) s - lse2)
+        m_ref = a.row_max[grow] * kLog2e + log2f(a.row_denom[grow]);
+      }
       for (int i = 0; i < nblk; ++i, ++g) {
         const int b = g & 1;
         if (!(ok = warp_wait(&bars->s_full, g & 1, bars, a.status))) break;
@@ -415,23 +431,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tt[32 + k] = __uint_as_float(v1[k]);
           }
         }
-        // row maximum of this half in log2 units (the scale is applied to
-        // the extreme raw score, not to every score)
-        const float mx = (sl2 >= 0.f ? extreme64<true>(tt) : extreme64<false>(tt)) * sl2;
-        m_true = fmaxf(m_true, mx);
         float alpha = 1.f;
         bool rescale = false;
-        if (i > 0) {
-          const bool need = mx - m_ref > kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            const float m_new = fmaxf(m_ref, mx);
-            alpha = ex2(m_ref - m_new);
-            l *= alpha;
-            m_ref = m_new;
-            rescale = true;
+        if constexpr (kPass != kOutPass) {
+          // row maximum of this half in log2 units (the scale is applied to
+          // the extreme raw score, not to every score)
+          const float mx = (sl2 >= 0.f ? extreme64<true>(tt) : extreme64<false>(tt)) * sl2;
+          m_true = fmaxf(m_true, mx);
+          if (i > 0) {
+            const bool need = mx - m_ref > kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need)) {
+              const float m_new = fmaxf(m_ref, mx);
+              alpha = ex2(m_ref - m_new);
+              l *= alpha;
+              m_ref = m_new;
+              rescale = kPass == kOnline;  // the statistics pass keeps no O
+            }
+          } else {
+            m_ref = mx;
           }
-        } else {
-          m_ref = mx;
         }
         float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
@@ -446,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[k] = Half16<T>::pack(p.x, p.y);
         }
         l += (sum4[0].x + sum4[0].y + sum4[1].x + sum4[1].y) + (sum4[2].x + sum4[2].y + sum4[3].x + sum4[3].y);
+        if constexpr (kPass == kStatsPass) continue;  // no P, no P.V
         // P of this block goes to buffer b once P.V of block g - 2 (the
         // buffer's previous use) is done; the MMA thread's p_full wait for
         // block g - 2 came before that P.V, so this warpgroup's arrivals on
@@ -477,10 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ----------------------------------------------------- epilogue --
       // exchange (m_ref, l) of the two halves (and half 1's true max)
+      // (the output pass's halves are already normalised: O = O_0 + O_1,
+      // which the same combine gives with m = 0, l = 1/2 for both)
       if (x > 0 && !(ok = warp_wait(&bars->red_empty, (x - 1) & 1, bars, a.status))) break;
-      sRed[(2 * hg) * 128 + r] = m_ref;
-      sRed[(2 * hg + 1) * 128 + r] = l;
-      if (hg == 1) sRed[4 * 128 + r] = m_true;
+      sRed[(2 * hg) * 128 + r] = kPass == kOutPass ? 0.f : m_ref;
+      sRed[(2 * hg + 1) * 128 + r] = kPass == kOutPass ? 0.5f : l;
+      if (hg == 1) sRed[4 * 128 + r] = kPass == kOutPass ? 0.f : m_true;
       mbar_arrive(&bars->red_full);
       if (!(ok = warp_wait(&bars->red_full, x & 1, bars, a.status))) break;
       const float m0 = sRed[r], l0 = sRed[128 + r], m1 = sRed[256 + r], l1 = sRed[384 + r];
@@ -491,36 +512,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c0 = ex2(m0 - R), c1 = ex2(m1 - R);
       const float L = l0 * c0 + l1 * c1;
       // both halves' last P.V
-      if (!(ok = warp_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, bars, a.status))) break;
+      if (kPass != kStatsPass && !(ok = warp_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, bars, a.status)))
+        break;
       tc_fence_after();
       const uint32_t t0 = tmem + lane_base + kColO + hg * (D / 2);
       if (cur.slot < 0) {
-        const float inv = 1.f / L;
-        const float2 w = make_float2(c0 * inv, c1 * inv);
-        // this half's D / 2 output columns as bf16, stored 64 at a time with
-        // the rows exchanged in groups of four (st_rows64)
-        uint32_t o[D / 4];
+        if constexpr (kPass != kStatsPass) {
+          const float inv = 1.f / L;
+          const float2 w = make_float2(c0 * inv, c1 * inv);
+          // this half's D / 2 output columns as bf16, stored 64 at a time with
+          // the rows exchanged in groups of four (st_rows64)
+          uint32_t o[D / 4];
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t u[32], v[32];
-          tmem_ld32(t0 + c * 32, u);
-          tmem_ld32(t0 + D + c * 32, v);
-          tmem_wait_ld();
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t u[32], v[32];
+            tmem_ld32(t0 + c * 32, u);
+            tmem_ld32(t0 + D + c * 32, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 y = fma2(make_float2(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1])),
-                                  make_float2(w.x, w.x),
-                                  mul2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
-                                       make_float2(w.y, w.y)));
-            o[16 * c + j] = Half16<T>::pack(y.x, y.y);
+            for (int j = 0; j < 16; ++j) {
+              const float2 y = fma2(make_float2(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1])),
+                                    make_float2(w.x, w.x),
+                                    mul2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                                         make_float2(w.y, w.y)));
+              o[16 * c + j] = Half16<T>::pack(y.x, y.y);
+            }
+          }
+          if constexpr (D == 128) {
+            st_rows64(o, orow, (size_t)D);
+          } else {
+            st_global_64B(orow, o);
           }
         }
-        if constexpr (D == 128) {
-          st_rows64(o, orow, (size_t)D);
-        } else {
-          st_global_64B(orow, o);
-        }
-        if (hg == 0) {
+        if (kPass != kOutPass && hg == 0) {
           const float M = fmaxf(m_true, mt1);
           a.row_max[grow] = M * kLn2;
           a.row_denom[grow] = L * ex2(R - M);
@@ -536,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr size_t kPart = fwd_part_floats<D>();
         float* tile = a.part + ((size_t)cur.slot * a.d.BH + cur.bh) * kPart;
 #pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < (kPass == kStatsPass ? 0 : D / 64); ++c) {
           uint32_t u[32], v[32];
           tmem_ld32(t0 + c * 32, u);
           tmem_ld32(t0 + D + c * 32, v);
@@ -552,7 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           part_store32(tile, hg * (D / 8) + c * 8, r, u);
         }
         const float Z = hg == 0 ? fmaxf(m_true, mt1) : R;
-        *(float4*)(tile + 128 * D + (hg * 128 + r) * 4) = make_float4(R, L, Z, 0.f);
+        // the output pass's chunks are already normalised: equal weights
+        // 1 / (chunks) make the merge a plain sum
+        const float Lc = kPass == kOutPass ? 1.f / (float)lay.line_chunks[lay.slot_line[cur.slot]] : L;
+        *(float4*)(tile + 128 * D + (hg * 128 + r) * 4) = make_float4(R, Lc, Z, 0.f);
         bool last = false;
         if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
                                 sync_phase, ab, a.status, &last)))
@@ -571,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float inv = 1.f / lsum;
 #pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
+          for (int c = 0; c < (kPass == kStatsPass ? 0 : D / 64); ++c) {
             float acc[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[j] = 0.f;
@@ -585,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 16; ++j) o[j] = Half16<T>::pack(acc[2 * j], acc[2 * j + 1]);
             st_global_64B(orow + c * 32, o);
           }
-          if (hg == 0) {
+          if (kPass != kOutPass && hg == 0) {
             a.row_max[grow] = M * kLn2;
             a.row_denom[grow] = lsum;
           }
@@ -605,16 +632,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int D>
+template <typename T, int D, int kPass>
 bsr_status launch(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
   using C = Fwd2Cfg<D>;
-  auto kern = fwd_tc2_kernel<T, D>;
+  auto kern = fwd_tc2_kernel<T, D, kPass>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess)
     return fail(BSR_ERR_CUDA, "fwd_tc: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
   const int grid = tc_grid(a.d);
   if (grid <= 0) return fail(BSR_ERR_CUDA, "fwd_tc: cannot query the SM count");
-  LaunchTimer timer("fwd_tc", s);
+  LaunchTimer timer(kPass == kOnline ? "fwd_tc" : kPass == kStatsPass ? "fwd2p_stats_tc" : "fwd2p_out_tc", s);
   e = launch_dependent(kern, dim3(grid), dim3(kThreads), C::kSmem, s, tm.q, tm.k, tm.v, a);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "fwd_tc launch: %s", cudaGetErrorString(e));
   return check_launch("fwd_tc launch");
@@ -626,14 +653,26 @@ size_t fwd_part_bytes(int D) {
   return sizeof(float) * (D == 64 ? fwd_part_floats<64>() : fwd_part_floats<128>());
 }
 
-bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s) {
+template <int kPass>
+bsr_status launch_pass(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
+  switch (a.d.D) {
+    case 64:
+      return a.d.dtype == BSR_F16 ? launch<__half, 64, kPass>(a, tm, s) : launch<__nv_bfloat16, 64, kPass>(a, tm, s);
+    case 128:
+      return a.d.dtype == BSR_F16 ? launch<__half, 128, kPass>(a, tm, s) : launch<__nv_bfloat16, 128, kPass>(a, tm, s);
+    default: return fail(BSR_ERR_UNSUPPORTED, "fwd_tc2: head_dim %d", a.d.D);
+  }
+}
+
+bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s, int pass) {
   TensorMaps tm;
   bsr_status st = make_tensor_maps(a.d, a.Q, a.K, a.V, &tm);
   if (st != BSR_OK) return st;
-  switch (a.d.D) {
-    case 64: return a.d.dtype == BSR_F16 ? launch<__half, 64>(a, tm, s) : launch<__nv_bfloat16, 64>(a, tm, s);
-    case 128: return a.d.dtype == BSR_F16 ? launch<__half, 128>(a, tm, s) : launch<__nv_bfloat16, 128>(a, tm, s);
-    default: return fail(BSR_ERR_UNSUPPORTED, "fwd_tc2: head_dim %d", a.d.D);
+  switch (pass) {
+    case kOnline: return launch_pass<kOnline>(a, tm, s);
+    case kStatsPass: return launch_pass<kStatsPass>(a, tm, s);
+    case kOutPass: return launch_pass<kOutPass>(a, tm, s);
+    default: return fail(BSR_ERR_INVALID_ARG, "fwd_tc2: pass %d", pass);
   }
 }
 

@@ -133,6 +133,7 @@ WORKLOADS = {
     # 64x64 grid, band of radius 2 plus global block row 0 and column 0 (436 stored blocks)
     "global_s8192": Workload("global_s8192", 1, 16, 8192, 128, "global", radius=2, dtype="bf16"),
     "global_s8192_f32": Workload("global_s8192_f32", 1, 16, 8192, 128, "global", radius=2, dtype="f32"),
+    "global_s8192_f16": Workload("global_s8192_f16", 1, 16, 8192, 128, "global", radius=2, dtype="f16"),
     # head_dim 256 and 512 on a band of radius 3, inputs N(0, 0.5^2)
     "local_s8192_d256": Workload("local_s8192_d256", 1, 8, 8192, 256, "local", radius=3, dtype="bf16", std=0.5),
     "local_s8192_d512": Workload("local_s8192_d512", 1, 8, 8192, 512, "local", radius=3, dtype="bf16", std=0.5),

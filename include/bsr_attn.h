@@ -95,6 +95,21 @@ bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tens
                         bsr_tensor* O, float* row_max, float* row_denom, void* stream);
 
 /*
+ * The statistics-first variant of the forward pass ("trnsparse 0.4.1 ->
+ * 0.6.0" diff, CHANGELOG [0.4.3]: first the row statistics over the row's
+ * stored blocks, then the output with P = exp(scale * Q[i].K[j] - row_max[i])
+ * / row_denom[i]), for comparison with bsr_attn_fwd: same arguments, same
+ * results up to rounding, two tensor-core launches (the first reads Q and K
+ * only and writes row_max / row_denom, the second reads them back).
+ * Supported for BSR_BF16 / BSR_F16 operands with head_dim 64 or 128;
+ * otherwise BSR_ERR_UNSUPPORTED.  Other errors as bsr_attn_fwd.
+ */
+bsr_status bsr_attn_fwd_two_pass(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
+                                 const int32_t* row_ptr, const int32_t* col_idx, int32_t n_brows,
+                                 int32_t block, float scale,
+                                 bsr_tensor* O, float* row_max, float* row_denom, void* stream);
+
+/*
  * Backward pass ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.5.0] delta
  * identity D_i = dO_i . O_i; [0.5.1] _attn_bwd_dq_kernel row-first and
  * _attn_bwd_dkdv_kernel column-first over the host-built BSC view, no

@@ -22,8 +22,10 @@ TOL = {
 }
 
 
-def run_gpu(Q, K, V, dO, bm, scale, device="cuda", backward=True):
-    """Runs forward (+ backward) through the C ABI on `device`; returns CPU float64 numpy arrays."""
+def run_gpu(Q, K, V, dO, bm, scale, device="cuda", backward=True, two_pass=False):
+    """Runs forward (+ backward) through the C ABI on `device`; returns CPU float64 numpy arrays.
+
+    ``two_pass`` runs the statistics-first forward (bsr_attn_fwd_two_pass)."""
     dev = torch.device(device)
     rp, ci = _bsr(bm)
     st = bsr.Structure(rp, ci, bm.shape[1], dev)
@@ -31,7 +33,7 @@ def run_gpu(Q, K, V, dO, bm, scale, device="cuda", backward=True):
     O = torch.empty_like(q)
     rm = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
     rd = torch.empty_like(rm)
-    bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, 128, scale, O, rm, rd)
+    bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, 128, scale, O, rm, rd, two_pass=two_pass)
     out = dict(O=O, row_max=rm, row_denom=rd)
     if backward:
         dQ, dK, dV = (torch.empty_like(q) for _ in range(3))

@@ -229,3 +229,67 @@ def test_autograd_wrapper_matches_direct_calls():
     got = dict(O=O.detach(), row_max=rm, row_denom=rd, dQ=q.grad, dK=k.grad, dV=v.grad)
     for name, t in got.items():
         assert np.array_equal(t.double().cpu().numpy(), direct[name]), name
+
+
+# ------------------------------------------------ statistics-first forward --
+
+FWD = ("O", "row_max", "row_denom")
+
+
+def _two_pass(bm, dtype, D=128, B=1, H=2, seed=5, backward=False, heads=None):
+    nb = bm.shape[0]
+    Q, K, V, dO = inputs.make_qkvdo(B, H, nb * 128, D, dtype, 1.0, seed)
+    scale = 1.0 / np.sqrt(D)
+    got = run_gpu(Q, K, V, dO, bm, scale, backward=backward, two_pass=True)
+    heads = heads or [(b, h) for b in range(B) for h in range(H)]
+    ref = oracle_heads(Q, K, V, dO, bm, scale, heads, backward=backward)
+    names = FWD + (("dQ", "dK", "dV") if backward else ())
+    compare({k: got[k] for k in names}, {k: ref[k] for k in names}, dtype, heads=heads, what="two-pass")
+    return Q, K, V, dO, bm, scale, got
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_two_pass_forward_matches_oracle(dtype):
+    # a heavy row (split into chunks on the full-size grid below) beside
+    # single-block rows, and the statistics feeding the backward
+    bm = np.eye(9, dtype=bool)
+    bm[0, :] = True
+    bm[:, 3] = True
+    _two_pass(bm, dtype, H=3, backward=True)
+
+
+def test_two_pass_forward_global_s8192_sampled_heads():
+    # the full-size launch configuration: block row 0 (64 blocks) is split
+    # across CTAs in both passes
+    wl = inputs.WORKLOADS["global_s8192"]
+    bm = wl.block_mask()
+    Q, K, V, dO = wl.inputs(seed=0)
+    got = run_gpu(Q, K, V, dO, bm, wl.scale, backward=False, two_pass=True)
+    heads = [(0, 0), (0, 15)]
+    ref = oracle_heads(Q, K, V, dO, bm, wl.scale, heads, backward=False)
+    compare({k: got[k] for k in FWD}, {k: ref[k] for k in FWD}, "bf16", heads=heads, what="two-pass global_s8192")
+    # same statistics as the online forward up to rounding, same output
+    one = run_gpu(Q, K, V, dO, bm, wl.scale, backward=False)
+    for k in ("row_max", "row_denom"):
+        scale_ = np.abs(one[k][np.isfinite(one[k])]).max()
+        assert np.nanmax(np.abs(got[k] - one[k])) <= 1e-5 * scale_, k
+    assert np.abs(got["O"] - one["O"]).max() <= 2e-2 * np.abs(one["O"]).max()
+
+
+def test_two_pass_forward_empty_block_row():
+    bm = inputs.block_mask("local", 5, radius=1)
+    bm[2, :] = False
+    *_, got = _two_pass(bm, "bf16", D=64)
+    rows = slice(2 * 128, 3 * 128)
+    assert np.all(got["O"][:, :, rows] == 0)
+    assert np.all(got["row_max"][:, :, rows] == -np.inf) and np.all(got["row_denom"][:, :, rows] == 0)
+
+
+def test_two_pass_forward_refuses_fp32():
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    bm = np.ones((2, 2), bool)
+    Q, K, V, dO = inputs.make_qkvdo(1, 1, 256, 64, "f32", 1.0, 1)
+    with pytest.raises(bsr.BsrError) as e:
+        run_gpu(Q, K, V, dO, bm, 0.125, backward=False, two_pass=True)
+    assert e.value.status == 2
