@@ -203,11 +203,11 @@ bsr_status fwd_impl(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* 
   a.row_denom = row_denom;
   a.row_ptr = row_ptr;
   a.col_idx = col_idx;
+  if (two_pass && !(a.d.dtype != BSR_F32 && a.d.D <= 128))
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd_two_pass: bf16 / fp16 operands with head_dim 64 or 128 only");
   a.status = status_ptr();
   if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
   cudaStream_t s = (cudaStream_t)stream;
-  if (two_pass && !(tc_fwd_supported(a.d) && a.d.D <= 128))
-    return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd_two_pass: bf16 / fp16 operands with head_dim 64 or 128 only");
   if (!tc_fwd_supported(a.d)) return launch_fwd_simt(a, s);
   const int G = tc_grid(a.d);
   if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cannot query the SM count");

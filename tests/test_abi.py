@@ -108,6 +108,17 @@ def test_fwd_rejects_bad_arguments_on_host(lib, kw, status, msg):
     assert re.search(msg, lib.bsr_last_error().decode())
 
 
+@pytest.mark.parametrize("kw", [dict(), dict(d=256)])
+def test_two_pass_forward_refuses_unsupported_operands_on_host(lib, kw):
+    # fp32 operands, or bf16 with head_dim 256: refused before any CUDA call
+    dtype = 0 if not kw else 1
+    Q, K, V, O = (_fake(dtype=dtype, **kw) for _ in range(4))
+    P = ctypes.c_void_p
+    st = lib.bsr_attn_fwd_two_pass(ctypes.byref(Q), ctypes.byref(K), ctypes.byref(V), P(0x10), P(0x20), 2, 128,
+                                   0.125, ctypes.byref(O), P(0x30), P(0x40), None)
+    assert st == 2 and "two_pass" in lib.bsr_last_error().decode()
+
+
 def test_bwd_rejects_bad_arguments_on_host(lib):
     t = [_fake() for _ in range(8)]
     t[4] = _fake(dtype=1)  # dO in bf16 beside fp32 operands
