@@ -78,6 +78,23 @@ def bsr_from_block_mask(bm: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
 _TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
+def make_spmm(n_brows: int, n_bcols: int, n_cols: int, p: float, dtype: str = "bf16", seed: int = 0):
+    """Inputs of Y = A X for a random BSR matrix A: (block mask, blocks, X) as CPU tensors.
+
+    Block (m, k) is stored iid with probability ``p`` (one ``torch.rand`` draw
+    of the ``[n_brows, n_bcols]`` grid, so block rows may be empty); the
+    stored blocks ``[nnzb, 128, 128]`` in row-major BSR order and X
+    ``[n_bcols * 128, n_cols]`` are iid N(0, 1), drawn in that order from one
+    seeded generator and rounded to ``dtype``.
+    """
+    g = torch.Generator().manual_seed(seed)
+    bm = (torch.rand(n_brows, n_bcols, generator=g, dtype=torch.float64) < p).numpy()
+    nnzb = int(bm.sum())
+    blocks = torch.randn(nnzb, BLOCK, BLOCK, generator=g, dtype=torch.float32).to(_TORCH_DTYPES[dtype])
+    X = torch.randn(n_bcols * BLOCK, n_cols, generator=g, dtype=torch.float32).to(_TORCH_DTYPES[dtype])
+    return np.ascontiguousarray(bm), blocks.contiguous(), X.contiguous()
+
+
 def make_qkvdo(batch: int, heads: int, seq: int, head_dim: int, dtype: str = "f32",
                std: float = 1.0, seed: int = 0):
     """Q, K, V, dO as CPU tensors [B, H, S, D] of ``dtype`` (``"f32"``, ``"bf16"`` or ``"f16"``).

@@ -1,7 +1,8 @@
-"""CPU fp64 oracle for block-sparse attention (test infrastructure only).
+"""CPU fp64 oracles for block-sparse attention and BSR SpMM (test infrastructure only).
 
 Imported by ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
-baseline leg; never by the library.  See ``oracle/attention.py``.
+baseline leg; never by the library.  See ``oracle/attention.py`` and
+``oracle/spmm.py``.
 """
 
 from .attention import (  # noqa: F401
@@ -13,3 +14,4 @@ from .attention import (  # noqa: F401
     bsc_from_block_mask,
     element_mask,
 )
+from .spmm import bsr_to_dense, spmm  # noqa: F401
