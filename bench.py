@@ -342,6 +342,55 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+SPMM_DENSITIES = (0.01, 0.05, 0.13, 0.27, 0.5, 1.0)
+
+
+def run_spmm_sweep(args, dev):
+    """bsr_spmm on an 8192 x 8192 BSR matrix (64 x 64 blocks of 128) times 8192 x width, bf16, one JSON
+    line per block density, beside dense torch.matmul of the same operands on the same GPU."""
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    l2 = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush_l2(l2)
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            flush_l2(l2)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    for p in SPMM_DENSITIES:
+        bm, blocks, X = inputs.make_spmm(64, 64, args.width, p, "bf16", seed=0)
+        rp, ci = inputs.bsr_from_block_mask(bm)
+        nnzb = int(bm.sum())
+        blocks_d, X_d = blocks.to(dev), X.to(dev)
+        rp_d, ci_d = torch.from_numpy(rp).to(dev), torch.from_numpy(ci).to(dev)
+        Y = torch.empty(64 * BLOCK, args.width, dtype=torch.bfloat16, device=dev)
+        # the dense operand of the comparison: A with zeros outside the stored blocks
+        A = torch.zeros(64 * BLOCK, 64 * BLOCK, dtype=torch.bfloat16, device=dev)
+        rows = np.repeat(np.arange(64), np.diff(rp))
+        for j, (m, k) in enumerate(zip(rows, ci)):
+            A[m * BLOCK:(m + 1) * BLOCK, k * BLOCK:(k + 1) * BLOCK] = blocks_d[j]
+        ms = timed(lambda: bsr.bsr_spmm(blocks_d, rp_d, ci_d, 64, 64, X_d, Y, stream))
+        bsr.bsr_attn_check()
+        dense_ms = timed(lambda: torch.matmul(A, X_d))
+        flops = 2 * BLOCK * BLOCK * args.width * nnzb
+        print(json.dumps({"op": "bsr_spmm", "metric": "ms per Y = A X, 8192 x 8192 BSR (blocks of 128) x 8192 x width",
+                          "density": round(nnzb / 64 ** 2, 4), "nnzb": nnzb, "width": args.width, "dtype": "bf16",
+                          "ms": round(ms, 4), "dense_matmul_ms": round(dense_ms, 4),
+                          "speedup_vs_dense": round(dense_ms / ms, 3),
+                          "tflops_over_stored_blocks": round(flops / (ms * 1e-3) / 1e12, 2),
+                          "steps": args.steps, "warmup": args.warmup, "l2": "flushed before every call",
+                          "data": "synthetic"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -355,6 +404,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sdpa", action=argparse.BooleanOptionalAction, default=True,
                     help="also time dense masked / unmasked SDPA on the same GPU")
+    ap.add_argument("--spmm-sweep", action="store_true",
+                    help="instead of attention: bsr_spmm against dense matmul over block densities (one line each)")
+    ap.add_argument("--width", type=int, default=512, help="columns of X for --spmm-sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -362,6 +414,11 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     wl = inputs.WORKLOADS[args.workload]
+    if args.spmm_sweep:
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        run_spmm_sweep(args, dev)
+        return
 
     if args.impl == "reference":
         # the CPU oracle stands as the reference arm; rank 0 alone runs it.

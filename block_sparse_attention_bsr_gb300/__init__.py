@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "BSR_OK", 1: "BSR_ERR_INVALID_ARG", 2: "BSR_ERR_UNSUPPORTED",
                 4: "BSR_ERR_TIMEOUT", 5: "BSR_ERR_DEVICE_CHECK"}
 
 # Every symbol include/bsr_attn.h declares.
-EXPORTS = ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
+EXPORTS = ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
            "bsr_last_error", "bsr_profile_enable", "bsr_profile_collect")
 
 
@@ -58,6 +58,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     T = ctypes.POINTER(bsr_tensor)
     lib.bsr_attn_fwd.argtypes = [T, T, T, P, P, I32, I32, F32, T, P, P, P]
     lib.bsr_attn_fwd_two_pass.argtypes = [T, T, T, P, P, I32, I32, F32, T, P, P, P]
+    lib.bsr_spmm.argtypes = [P, I32, P, P, I32, I32, I32, I32, P, I32, P, P]
     lib.bsr_attn_bwd.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_attn_bwd_noalloc.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_build_bsc.argtypes = [P, P, I32, I32, P, P]
@@ -69,7 +70,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsr_profile_enable.restype = None
     lib.bsr_profile_collect.argtypes = [ctypes.POINTER(bsr_kernel_time), I32]
     lib.bsr_profile_collect.restype = I32
-    for name in ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
+    for name in ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
         getattr(lib, name).restype = I32
     _lib_handle = lib
     return lib
@@ -127,6 +128,31 @@ def bsr_attn_fwd(Q, K, V, row_ptr, col_idx, n_brows: int, block: int, scale: flo
                             int(n_brows), int(block), float(scale), ctypes.byref(o),
                             _dev_ptr(row_max, "torch.float32"), _dev_ptr(row_denom, "torch.float32"),
                             _stream(stream, Q)))
+
+
+def bsr_spmm(blocks, row_ptr, col_idx, n_brows: int, n_bcols: int, X, Y, stream=None) -> None:
+    """Y = A X for the BSR matrix A of 128 x 128 blocks and a dense X (see include/bsr_attn.h).
+
+    blocks: [nnzb, 128, 128] bf16 / fp16 CUDA tensor (the stored blocks in BSR
+    order); X: [n_bcols * 128, n_cols] and Y: [n_brows * 128, n_cols] of the
+    same dtype; row_ptr / col_idx int32 CUDA tensors.
+    """
+    import torch
+
+    codes = {torch.bfloat16: BSR_BF16, torch.float16: BSR_F16}
+    if blocks.dtype not in codes:
+        raise TypeError(f"unsupported dtype {blocks.dtype} (bfloat16 or float16)")
+    for name, t in (("blocks", blocks), ("X", X), ("Y", Y)):
+        if t.dtype != blocks.dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of dtype {blocks.dtype}")
+    if blocks.dim() != 3 or tuple(blocks.shape[1:]) != (128, 128) or X.dim() != 2 or Y.dim() != 2:
+        raise ValueError("blocks must be [nnzb, 128, 128], X and Y two-dimensional")
+    if X.shape[0] != n_bcols * 128 or Y.shape[0] != n_brows * 128 or X.shape[1] != Y.shape[1]:
+        raise ValueError("X must be [n_bcols * 128, n_cols] and Y [n_brows * 128, n_cols]")
+    lib = load_library()
+    _check(lib.bsr_spmm(blocks.data_ptr(), codes[blocks.dtype], _dev_ptr(row_ptr, "torch.int32"),
+                        _dev_ptr(col_idx, "torch.int32"), int(n_brows), int(n_bcols), int(blocks.shape[0]), 128,
+                        X.data_ptr(), int(X.shape[1]), Y.data_ptr(), _stream(stream, X)))
 
 
 def bsr_attn_bwd(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx, scale: float,

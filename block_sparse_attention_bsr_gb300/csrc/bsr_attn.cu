@@ -252,6 +252,32 @@ extern "C" bsr_status bsr_attn_fwd(const bsr_tensor* Q, const bsr_tensor* K, con
   return bsr::fwd_impl(Q, K, V, row_ptr, col_idx, n_brows, block, scale, O, row_max, row_denom, stream, false);
 }
 
+extern "C" bsr_status bsr_spmm(const void* blocks, int32_t dtype, const int32_t* row_ptr, const int32_t* col_idx,
+                               int32_t n_brows, int32_t n_bcols, int32_t nnzb, int32_t block, const void* X,
+                               int32_t n_cols, void* Y, void* stream) {
+  if (block != 128) return fail(BSR_ERR_UNSUPPORTED, "bsr_spmm: block %d not supported (128)", block);
+  if (dtype != BSR_BF16 && dtype != BSR_F16)
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_spmm: dtype %d not supported (BSR_BF16 or BSR_F16)", dtype);
+  if (n_brows < 1 || n_bcols < 1 || nnzb < 0 || n_cols < 1)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_spmm: sizes n_brows %d, n_bcols %d, nnzb %d, n_cols %d", n_brows, n_bcols,
+                nnzb, n_cols);
+  if (n_cols % 64 != 0) return fail(BSR_ERR_UNSUPPORTED, "bsr_spmm: n_cols %d is not a multiple of 64", n_cols);
+  if ((long long)n_bcols * 128 > INT32_MAX || (long long)nnzb * 128 > INT32_MAX || (long long)n_brows * 128 > INT32_MAX)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_spmm: too many rows");
+  if (!row_ptr || !col_idx || !X || !Y || (nnzb > 0 && !blocks))
+    return fail(BSR_ERR_INVALID_ARG, "bsr_spmm: null pointer");
+  if ((((uintptr_t)Y) | ((uintptr_t)X) | ((uintptr_t)blocks)) & 15)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_spmm: data pointer is not 16-byte aligned");
+  SpmmArgs a{blocks, X, Y, row_ptr, col_idx, n_brows, n_bcols, nnzb, n_cols, dtype, status_ptr()};
+  if (!a.status) return fail(BSR_ERR_CUDA, "bsr_spmm: no CUDA device");
+  cudaStream_t s = (cudaStream_t)stream;
+  if (nnzb == 0) {  // no stored block: Y = 0
+    const cudaError_t e = cudaMemsetAsync(Y, 0, (size_t)n_brows * 128 * (size_t)n_cols * 2, s);
+    return e == cudaSuccess ? BSR_OK : fail(BSR_ERR_CUDA, "bsr_spmm: cudaMemsetAsync: %s", cudaGetErrorString(e));
+  }
+  return launch_spmm_tc(a, s);
+}
+
 extern "C" bsr_status bsr_attn_fwd_two_pass(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
                                             const int32_t* row_ptr, const int32_t* col_idx, int32_t n_brows,
                                             int32_t block, float scale, bsr_tensor* O, float* row_max,

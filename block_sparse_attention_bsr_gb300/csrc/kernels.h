@@ -238,6 +238,19 @@ bsr_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
 // variant (the output pass reads the row_max / row_denom the first wrote).
 bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s, int pass = 0);
 bool tc_bwd_supported(const Dims& d);
+
+// Y = A X for a BSR matrix A of 128 x 128 blocks (tc_spmm.cu).
+struct SpmmArgs {
+  const void* A;            // stored blocks, [nnzb][128][128] row-major
+  const void* X;            // [n_bcols * 128][n_cols] row-major
+  void* Y;                  // [n_brows * 128][n_cols] row-major
+  const int32_t* row_ptr;   // [n_brows + 1]
+  const int32_t* col_idx;   // [nnzb]
+  int n_brows, n_bcols, nnzb, n_cols;
+  int dtype;                // BSR_BF16 or BSR_F16
+  int* status;
+};
+bsr_status launch_spmm_tc(const SpmmArgs& a, cudaStream_t s);
 // Persistent grid of the tensor-core kernels: min(SMs, lines * BH); 0 on error.
 int tc_grid(const Dims& d);
 // Bytes of one forward partial-result tile (split rows), head_dim 64 / 128.

@@ -110,6 +110,30 @@ bsr_status bsr_attn_fwd_two_pass(const bsr_tensor* Q, const bsr_tensor* K, const
                                  bsr_tensor* O, float* row_max, float* row_denom, void* stream);
 
 /*
+ * Block-sparse times dense ("trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG
+ * [0.8.0]: bsr_spmm_static walks exactly the stored blocks and addresses X
+ * by block column; [0.9.0]: bf16 operands with fp32 accumulation):
+ *
+ *   Y[m*128 + i, c] = sum over stored blocks j of block row m, k = col_idx[j],
+ *                     sum_t blocks[j][i][t] * X[k*128 + t, c]
+ *
+ * blocks: [nnzb][128][128] row-major (device), the stored blocks in BSR order;
+ * row_ptr: int32 [n_brows + 1], col_idx: int32 [nnzb] (device), columns in
+ * [0, n_bcols); X: [n_bcols * 128][n_cols], Y: [n_brows * 128][n_cols],
+ * row-major (device); blocks, X and Y have element type `dtype` (BSR_BF16 or
+ * BSR_F16; products accumulated in fp32, Y rounded to the element type).
+ * Pointers 16-byte aligned; block must be 128; n_cols a positive multiple
+ * of 64.  A block row with no stored block gets Y rows of zeros.
+ * Errors: BSR_ERR_INVALID_ARG (null / misaligned pointer, bad size),
+ * BSR_ERR_UNSUPPORTED (block, dtype, n_cols), BSR_ERR_CUDA; a col_idx
+ * outside [0, n_bcols) or a row_ptr outside [0, nnzb] is skipped on the
+ * device and reported by bsr_attn_check as BSR_ERR_DEVICE_CHECK.
+ */
+bsr_status bsr_spmm(const void* blocks, int32_t dtype, const int32_t* row_ptr, const int32_t* col_idx,
+                    int32_t n_brows, int32_t n_bcols, int32_t nnzb, int32_t block, const void* X,
+                    int32_t n_cols, void* Y, void* stream);
+
+/*
  * Backward pass ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.5.0] delta
  * identity D_i = dO_i . O_i; [0.5.1] _attn_bwd_dq_kernel row-first and
  * _attn_bwd_dkdv_kernel column-first over the host-built BSC view, no

@@ -119,6 +119,25 @@ def test_two_pass_forward_refuses_unsupported_operands_on_host(lib, kw):
     assert st == 2 and "two_pass" in lib.bsr_last_error().decode()
 
 
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(block=64), 2, "block"),
+    (dict(dtype=0), 2, "dtype"),
+    (dict(n_cols=96), 2, "multiple of 64"),
+    (dict(n_cols=0), 1, "sizes"),
+    (dict(X=0), 1, "null"),
+    (dict(Y=0x1008), 1, "aligned"),
+])
+def test_spmm_rejects_bad_arguments_on_host(lib, kw, status, msg):
+    a = dict(blocks=0x1000, dtype=1, row_ptr=0x10, col_idx=0x20, n_brows=2, n_bcols=2, nnzb=3, block=128,
+             X=0x2000, n_cols=128, Y=0x3000)
+    a.update(kw)
+    P = ctypes.c_void_p
+    st = lib.bsr_spmm(P(a["blocks"]), a["dtype"], P(a["row_ptr"]), P(a["col_idx"]), a["n_brows"], a["n_bcols"],
+                      a["nnzb"], a["block"], P(a["X"]), a["n_cols"], P(a["Y"]), None)
+    assert st == status
+    assert re.search(msg, lib.bsr_last_error().decode())
+
+
 def test_bwd_rejects_bad_arguments_on_host(lib):
     t = [_fake() for _ in range(8)]
     t[4] = _fake(dtype=1)  # dO in bf16 beside fp32 operands
