@@ -157,3 +157,19 @@ WORKLOADS = {
 }
 for _p in (0.01, 0.05, 0.13, 0.27, 0.5):
     WORKLOADS[f"random_p{_p}"] = Workload(f"random_p{_p}", 1, 16, 8192, 128, "random", p=_p, dtype="bf16")
+
+
+def make_screened(n: int, n_cols: int, dtype: str = "bf16", seed: int = 0):
+    """Inputs of the screened SpMM as CPU tensors: (A [n, n], diag [n] fp32, B [n, n_cols]).
+
+    A and B are iid N(0, 1) drawn in that order from one seeded generator and
+    rounded to ``dtype``; the bounds decay exponentially along the diagonal,
+    diag_i = exp(-i / (n / 8)) + 1e-12, so a threshold keeps a band (the
+    pages' screened-SpMM benchmark recipe).
+    """
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn(n, n, generator=g, dtype=torch.float32).to(_TORCH_DTYPES[dtype])
+    B = torch.randn(n, n_cols, generator=g, dtype=torch.float32).to(_TORCH_DTYPES[dtype])
+    pos = torch.arange(n, dtype=torch.float32)
+    diag = torch.exp(-pos / (n / 8)) + 1e-12
+    return A.contiguous(), diag.contiguous(), B.contiguous()

@@ -1,8 +1,8 @@
-"""CPU fp64 oracles for block-sparse attention and BSR SpMM (test infrastructure only).
+"""CPU fp64 oracles for block-sparse attention, BSR SpMM and screened SpMM (test infrastructure only).
 
 Imported by ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
-baseline leg; never by the library.  See ``oracle/attention.py`` and
-``oracle/spmm.py``.
+baseline leg; never by the library.  See ``oracle/attention.py``,
+``oracle/spmm.py`` and ``oracle/screened.py``.
 """
 
 from .attention import (  # noqa: F401
@@ -15,3 +15,4 @@ from .attention import (  # noqa: F401
     element_mask,
 )
 from .spmm import bsr_to_dense, spmm  # noqa: F401
+from .screened import schwarz_mask, screened_spmm  # noqa: F401
