@@ -391,6 +391,52 @@ def run_spmm_sweep(args, dev):
                           "data": "synthetic"}), flush=True)
 
 
+SCREEN_THRESHOLDS = (1e-6, 1e-4, 1e-2, 1e-1)
+
+
+def run_screen_sweep(args, dev):
+    """bsr_screened_spmm at n = 8192 (bounds decaying along the diagonal) times 8192 x width, bf16, one
+    JSON line per threshold, beside the unfused dense (A * mask) @ B and the plain A @ B on the same GPU."""
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    n = 8192
+    l2 = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush_l2(l2)
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            flush_l2(l2)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    hA, hdiag, hB = inputs.make_screened(n, args.width, "bf16", seed=0)
+    A, diag, B = hA.to(dev), hdiag.to(dev), hB.to(dev)
+    C = torch.empty(n, args.width, dtype=torch.bfloat16, device=dev)
+    q = diag.abs().sqrt()
+    for thr in SCREEN_THRESHOLDS:
+        mask = (q[:, None] * q[None, :]) > torch.tensor(thr, dtype=torch.float32, device=dev).sqrt()
+        kept = float(mask.float().mean())
+        maskb = mask.to(torch.bfloat16)
+        ms = timed(lambda: bsr.bsr_screened_spmm(A, diag, B, thr, C, stream))
+        bsr.bsr_attn_check()
+        unfused_ms = timed(lambda: torch.matmul(A * maskb, B))
+        dense_ms = timed(lambda: torch.matmul(A, B))
+        print(json.dumps({"op": "bsr_screened_spmm", "metric": "ms per C = (A o M) B, n = 8192, B 8192 x width",
+                          "threshold": thr, "kept_fraction": round(kept, 4), "width": args.width, "dtype": "bf16",
+                          "ms": round(ms, 4), "unfused_masked_matmul_ms": round(unfused_ms, 4),
+                          "dense_matmul_ms": round(dense_ms, 4),
+                          "speedup_vs_unfused": round(unfused_ms / ms, 3), "steps": args.steps,
+                          "warmup": args.warmup, "l2": "flushed before every call", "data": "synthetic"}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -406,7 +452,9 @@ def main():
                     help="also time dense masked / unmasked SDPA on the same GPU")
     ap.add_argument("--spmm-sweep", action="store_true",
                     help="instead of attention: bsr_spmm against dense matmul over block densities (one line each)")
-    ap.add_argument("--width", type=int, default=512, help="columns of X for --spmm-sweep")
+    ap.add_argument("--screen-sweep", action="store_true",
+                    help="instead of attention: bsr_screened_spmm against the unfused masked matmul over thresholds")
+    ap.add_argument("--width", type=int, default=512, help="columns of X / B for --spmm-sweep / --screen-sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -414,10 +462,10 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     wl = inputs.WORKLOADS[args.workload]
-    if args.spmm_sweep:
+    if args.spmm_sweep or args.screen_sweep:
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        run_spmm_sweep(args, dev)
+        (run_spmm_sweep if args.spmm_sweep else run_screen_sweep)(args, dev)
         return
 
     if args.impl == "reference":

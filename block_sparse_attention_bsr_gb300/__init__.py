@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "BSR_OK", 1: "BSR_ERR_INVALID_ARG", 2: "BSR_ERR_UNSUPPORTED",
                 4: "BSR_ERR_TIMEOUT", 5: "BSR_ERR_DEVICE_CHECK"}
 
 # Every symbol include/bsr_attn.h declares.
-EXPORTS = ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
+EXPORTS = ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_screened_spmm", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
            "bsr_last_error", "bsr_profile_enable", "bsr_profile_collect")
 
 
@@ -59,6 +59,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsr_attn_fwd.argtypes = [T, T, T, P, P, I32, I32, F32, T, P, P, P]
     lib.bsr_attn_fwd_two_pass.argtypes = [T, T, T, P, P, I32, I32, F32, T, P, P, P]
     lib.bsr_spmm.argtypes = [P, I32, P, P, I32, I32, I32, I32, P, I32, P, P]
+    lib.bsr_screened_spmm.argtypes = [P, P, P, I32, I32, I32, F32, P, P]
     lib.bsr_attn_bwd.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_attn_bwd_noalloc.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_build_bsc.argtypes = [P, P, I32, I32, P, P]
@@ -70,7 +71,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsr_profile_enable.restype = None
     lib.bsr_profile_collect.argtypes = [ctypes.POINTER(bsr_kernel_time), I32]
     lib.bsr_profile_collect.restype = I32
-    for name in ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
+    for name in ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_screened_spmm", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
         getattr(lib, name).restype = I32
     _lib_handle = lib
     return lib
@@ -153,6 +154,27 @@ def bsr_spmm(blocks, row_ptr, col_idx, n_brows: int, n_bcols: int, X, Y, stream=
     _check(lib.bsr_spmm(blocks.data_ptr(), codes[blocks.dtype], _dev_ptr(row_ptr, "torch.int32"),
                         _dev_ptr(col_idx, "torch.int32"), int(n_brows), int(n_bcols), int(blocks.shape[0]), 128,
                         X.data_ptr(), int(X.shape[1]), Y.data_ptr(), _stream(stream, X)))
+
+
+def bsr_screened_spmm(A, diag, B, threshold: float, C, stream=None) -> None:
+    """C = (A o M) B with M[i, j] = sqrt|diag_i| sqrt|diag_j| > sqrt(threshold) (see include/bsr_attn.h).
+
+    A: [n, n], B and C: [n, n_cols] bf16 / fp16 CUDA tensors; diag: fp32 CUDA tensor [n].
+    """
+    import torch
+
+    codes = {torch.bfloat16: BSR_BF16, torch.float16: BSR_F16}
+    if A.dtype not in codes:
+        raise TypeError(f"unsupported dtype {A.dtype} (bfloat16 or float16)")
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if t.dtype != A.dtype or not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous two-dimensional CUDA tensor of dtype {A.dtype}")
+    n = A.shape[0]
+    if A.shape[1] != n or B.shape[0] != n or tuple(C.shape) != tuple(B.shape) or tuple(diag.shape) != (n,):
+        raise ValueError("A must be [n, n], B and C [n, n_cols], diag [n]")
+    lib = load_library()
+    _check(lib.bsr_screened_spmm(A.data_ptr(), _dev_ptr(diag, "torch.float32"), B.data_ptr(), codes[A.dtype], int(n),
+                                 int(B.shape[1]), float(threshold), C.data_ptr(), _stream(stream, A)))
 
 
 def bsr_attn_bwd(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx, scale: float,

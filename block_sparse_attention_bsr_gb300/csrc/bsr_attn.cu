@@ -278,6 +278,25 @@ extern "C" bsr_status bsr_spmm(const void* blocks, int32_t dtype, const int32_t*
   return launch_spmm_tc(a, s);
 }
 
+extern "C" bsr_status bsr_screened_spmm(const void* A, const float* diag, const void* B, int32_t dtype, int32_t n,
+                                        int32_t n_cols, float threshold, void* C, void* stream) {
+  if (dtype != BSR_BF16 && dtype != BSR_F16)
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_screened_spmm: dtype %d not supported (BSR_BF16 or BSR_F16)", dtype);
+  if (n < 1 || n_cols < 1) return fail(BSR_ERR_INVALID_ARG, "bsr_screened_spmm: sizes n %d, n_cols %d", n, n_cols);
+  if (n % 128 != 0 || n > 65536)
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_screened_spmm: n %d is not a multiple of 128 up to 65536", n);
+  if (n_cols % 64 != 0)
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_screened_spmm: n_cols %d is not a multiple of 64", n_cols);
+  if (!(threshold >= 0.f) || isinf(threshold))
+    return fail(BSR_ERR_INVALID_ARG, "bsr_screened_spmm: threshold must be finite and >= 0");
+  if (!A || !diag || !B || !C) return fail(BSR_ERR_INVALID_ARG, "bsr_screened_spmm: null pointer");
+  if ((((uintptr_t)A) | ((uintptr_t)diag) | ((uintptr_t)B) | ((uintptr_t)C)) & 15)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_screened_spmm: data pointer is not 16-byte aligned");
+  ScreenedArgs a{A, diag, B, C, n, n_cols, threshold, dtype, status_ptr()};
+  if (!a.status) return fail(BSR_ERR_CUDA, "bsr_screened_spmm: no CUDA device");
+  return launch_screened_tc(a, (cudaStream_t)stream);
+}
+
 extern "C" bsr_status bsr_attn_fwd_two_pass(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
                                             const int32_t* row_ptr, const int32_t* col_idx, int32_t n_brows,
                                             int32_t block, float scale, bsr_tensor* O, float* row_max,

@@ -251,6 +251,19 @@ struct SpmmArgs {
   int* status;
 };
 bsr_status launch_spmm_tc(const SpmmArgs& a, cudaStream_t s);
+
+// C = (A o M) B with M[i, j] = (sqrt|diag_i| sqrt|diag_j| > sqrt(threshold)) (tc_screened.cu).
+struct ScreenedArgs {
+  const void* A;       // [n][n] row-major
+  const float* diag;   // [n]
+  const void* B;       // [n][n_cols] row-major
+  void* C;             // [n][n_cols] row-major
+  int n, n_cols;
+  float threshold;
+  int dtype;           // BSR_BF16 or BSR_F16
+  int* status;
+};
+bsr_status launch_screened_tc(const ScreenedArgs& a, cudaStream_t s);
 // Persistent grid of the tensor-core kernels: min(SMs, lines * BH); 0 on error.
 int tc_grid(const Dims& d);
 // Bytes of one forward partial-result tile (split rows), head_dim 64 / 128.

@@ -134,6 +134,25 @@ bsr_status bsr_spmm(const void* blocks, int32_t dtype, const int32_t* row_ptr, c
                     int32_t n_cols, void* Y, void* stream);
 
 /*
+ * Fused screened SpMM ("trnsparse 0.7.0 -> 0.9.0" diff, docs:
+ * screened_spmm(A, diag, B, threshold) fuses the Schwarz pair bound, the
+ * threshold mask and the matmul into one dispatch):
+ *
+ *   C = (A o M) B,  M[i, j] = sqrt(|diag[i]|) * sqrt(|diag[j]|) > sqrt(threshold)
+ *
+ * with the square roots, the product and the comparison in fp32.  A:
+ * [n][n], B and C: [n][n_cols], row-major, element type `dtype` (BSR_BF16
+ * or BSR_F16; fp32 accumulation, C rounded to the element type); diag: fp32
+ * [n]; all device pointers, 16-byte aligned.  n a multiple of 128 up to
+ * 65536, n_cols a positive multiple of 64, threshold finite and >= 0.
+ * 128 x 128 tiles of A whose pairs all fail the bound are never read.
+ * Errors: BSR_ERR_INVALID_ARG (null / misaligned pointer, bad size or
+ * threshold), BSR_ERR_UNSUPPORTED (dtype, n, n_cols), BSR_ERR_CUDA.
+ */
+bsr_status bsr_screened_spmm(const void* A, const float* diag, const void* B, int32_t dtype, int32_t n,
+                             int32_t n_cols, float threshold, void* C, void* stream);
+
+/*
  * Backward pass ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.5.0] delta
  * identity D_i = dO_i . O_i; [0.5.1] _attn_bwd_dq_kernel row-first and
  * _attn_bwd_dkdv_kernel column-first over the host-built BSC view, no

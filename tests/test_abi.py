@@ -138,6 +138,25 @@ def test_spmm_rejects_bad_arguments_on_host(lib, kw, status, msg):
     assert re.search(msg, lib.bsr_last_error().decode())
 
 
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(dtype=0), 2, "dtype"),
+    (dict(n=200), 2, "multiple of 128"),
+    (dict(n_cols=96), 2, "multiple of 64"),
+    (dict(threshold=-1.0), 1, "threshold"),
+    (dict(threshold=float("nan")), 1, "threshold"),
+    (dict(diag=0), 1, "null"),
+    (dict(C=0x1008), 1, "aligned"),
+])
+def test_screened_spmm_rejects_bad_arguments_on_host(lib, kw, status, msg):
+    a = dict(A=0x1000, diag=0x2000, B=0x3000, dtype=1, n=256, n_cols=128, threshold=1e-3, C=0x4000)
+    a.update(kw)
+    P = ctypes.c_void_p
+    st = lib.bsr_screened_spmm(P(a["A"]), P(a["diag"]), P(a["B"]), a["dtype"], a["n"], a["n_cols"],
+                               a["threshold"], P(a["C"]), None)
+    assert st == status
+    assert re.search(msg, lib.bsr_last_error().decode())
+
+
 def test_bwd_rejects_bad_arguments_on_host(lib):
     t = [_fake() for _ in range(8)]
     t[4] = _fake(dtype=1)  # dO in bf16 beside fp32 operands
