@@ -1,0 +1,47 @@
+"""The Python binding only marshals arguments: wrong shapes, dtypes or host
+tensors are refused before anything reaches the library (no GPU needed)."""
+
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import block_sparse_attention_bsr_gb300 as bsr  # noqa: E402
+
+
+def _spmm_args(**kw):
+    a = dict(blocks=torch.zeros(2, 128, 128, dtype=torch.bfloat16), row_ptr=torch.zeros(3, dtype=torch.int32),
+             col_idx=torch.zeros(2, dtype=torch.int32), n_brows=2, n_bcols=1,
+             X=torch.zeros(128, 64, dtype=torch.bfloat16), Y=torch.zeros(256, 64, dtype=torch.bfloat16))
+    a.update(kw)
+    return a
+
+
+def test_spmm_refuses_fp32_blocks():
+    with pytest.raises(TypeError):
+        bsr.bsr_spmm(**_spmm_args(blocks=torch.zeros(2, 128, 128)))
+
+
+def test_spmm_refuses_host_tensors():
+    with pytest.raises(ValueError):
+        bsr.bsr_spmm(**_spmm_args())
+
+
+def test_spmm_refuses_mixed_dtypes():
+    with pytest.raises(ValueError):
+        bsr.bsr_spmm(**_spmm_args(X=torch.zeros(128, 64, dtype=torch.float16)))
+
+
+def test_screened_refuses_fp32_and_host_tensors():
+    A = torch.zeros(256, 256)
+    with pytest.raises(TypeError):
+        bsr.bsr_screened_spmm(A, torch.ones(256), torch.zeros(256, 64), 1e-3, torch.zeros(256, 64))
+    A = A.bfloat16()
+    with pytest.raises(ValueError):
+        bsr.bsr_screened_spmm(A, torch.ones(256), torch.zeros(256, 64, dtype=torch.bfloat16), 1e-3,
+                              torch.zeros(256, 64, dtype=torch.bfloat16))
+
+
+def test_forward_refuses_unsupported_dtype():
+    q = torch.zeros(1, 1, 256, 64, dtype=torch.float64)
+    with pytest.raises(TypeError):
+        bsr.bsr_attn_fwd(q, q, q, None, None, 2, 128, 0.125, q, None, None)
