@@ -345,6 +345,21 @@ def max_over_ranks(x, world):
 SPMM_DENSITIES = (0.01, 0.05, 0.13, 0.27, 0.5, 1.0)
 
 
+def median_call_ms(fn, args, l2, stream, dev):
+    """Median ms of `fn` over args.steps calls after args.warmup, L2 flushed before each, CUDA events on `stream`."""
+    for _ in range(args.warmup):
+        flush_l2(l2)
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        flush_l2(l2)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
 def run_spmm_sweep(args, dev):
     """bsr_spmm on an 8192 x 8192 BSR matrix (64 x 64 blocks of 128) times 8192 x width, bf16, one JSON
     line per block density, beside dense torch.matmul of the same operands on the same GPU."""
@@ -354,17 +369,7 @@ def run_spmm_sweep(args, dev):
     stream = torch.cuda.current_stream(dev)
 
     def timed(fn):
-        for _ in range(args.warmup):
-            flush_l2(l2)
-            fn()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for a, b in ev:
-            flush_l2(l2)
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        return statistics.median(a.elapsed_time(b) for a, b in ev)
+        return median_call_ms(fn, args, l2, stream, dev)
 
     for p in SPMM_DENSITIES:
         bm, blocks, X = inputs.make_spmm(64, 64, args.width, p, "bf16", seed=0)
@@ -404,17 +409,7 @@ def run_screen_sweep(args, dev):
     stream = torch.cuda.current_stream(dev)
 
     def timed(fn):
-        for _ in range(args.warmup):
-            flush_l2(l2)
-            fn()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for a, b in ev:
-            flush_l2(l2)
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        return statistics.median(a.elapsed_time(b) for a, b in ev)
+        return median_call_ms(fn, args, l2, stream, dev)
 
     hA, hdiag, hB = inputs.make_screened(n, args.width, "bf16", seed=0)
     A, diag, B = hA.to(dev), hdiag.to(dev), hB.to(dev)
