@@ -53,7 +53,7 @@ MEASURED_TRAFFIC = {
     ("global_s8192", "dq_tc"): {"bytes": 176.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
                                 "sha256": "bf9b07a77f77fe39b3b656d98f216f074474116c25211e72869787855afcfffb"},
     ("global_s8192", "fwd_tc"): {"bytes": 137.0e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "9146b0b1e30a5e5ea18f4af9e6204ee1884646fdd4d60aa8e4367aa77e96d0b2"},
+                                 "sha256": "6e8e58578ca2f5b374da342a87214713aa4822fdca435d2f6cced9569dadae69"},
 }
 
 

@@ -18,8 +18,8 @@
 //     row; once per row the two partial results are combined exactly like
 //     two chunks of a split row:  R = max(m_0, m_1),
 //     O = (2^(m_0 - R) O_0 + 2^(m_1 - R) O_1) / (2^(m_0 - R) l_0 + 2^(m_1 - R) l_1);
-//   * P goes back to tensor memory as bf16 (two buffers) and the P.V MMA
-//     reads its A operand from there;
+//   * P goes back to tensor memory in the operand type (two buffers) and
+//     the P.V MMA reads its A operand from there;
 //   * S has one TMEM buffer, released as soon as both warpgroups have
 //     loaded their halves into registers, so S_{j+1} = Q K_{j+1}^T runs
 //     while the softmax of block j is computed;
@@ -29,15 +29,18 @@
 //     barriers that the other one does not need);
 //   * the producer keeps the work ring one item ahead of the item it loads,
 //     so the global work counter's round trip is off the item boundary.
+// The same kernel also runs the two launches of the statistics-first
+// variant (kStatsPass, kOutPass below).
 //
 // Warp roles (384 threads): warp 0 TMA producer of Q and K, warp 10 TMA
 // producer of V, warp 1 TMEM owner and issuer of the S MMAs, warp 11 issuer
-// of the P.V MMAs, warps 2..9 two softmax warpgroups; thread (warp w, lane l) owns query row 32 (w % 4) + l (its
-// TMEM lane), warpgroup h = (w - 2) / 4 owns keys [64 h, 64 h + 64) of each
-// block and, in the final combine, output columns [h D / 2, h D / 2 + D / 2).
-// TMEM columns: S at 0 (half h at +64 h), bf16 P of block j at
-// 128 + 64 (j % 2) (half h at +32 h), O_0 at 256, O_1 at 256 + D.  All waits
-// are bounded (see sm100.cuh).
+// of the P.V MMAs, warps 2..9 two softmax warpgroups; thread (warp w, lane
+// l) owns query row 32 (w % 4) + l (its TMEM lane), warpgroup
+// h = (w - 2) / 4 owns keys [64 h, 64 h + 64) of each block and, in the
+// final combine, output columns [h D / 2, h D / 2 + D / 2).
+// TMEM columns: S at 0 (half h at +64 h), P of block j at 128 + 64 (j % 2)
+// (half h at +32 h), O_0 at 256, O_1 at 256 + D.  All waits are bounded
+// (see sm100.cuh).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
