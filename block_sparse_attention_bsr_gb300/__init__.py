@@ -328,8 +328,8 @@ def _autograd_fn():
 def block_sparse_attention(Q, K, V, structure: "Structure", scale=None, return_stats: bool = False):
     """softmax(scale * Q K^T over the stored 128 x 128 blocks) V, differentiable in Q, K and V.
 
-    Q, K, V: contiguous CUDA tensors [batch, heads, seq, head_dim] (bf16 or fp32,
-    16-byte aligned); `structure`: a Structure of the block mask on the same
+    Q, K, V: contiguous CUDA tensors [batch, heads, seq, head_dim] (bf16, fp16 or
+    fp32, 16-byte aligned); `structure`: a Structure of the block mask on the same
     device; scale defaults to 1 / sqrt(head_dim).  The forward and backward
     passes are bsr_attn_fwd and bsr_attn_bwd on the current stream.  With
     return_stats the fp32 row_max / row_denom statistics come back as well

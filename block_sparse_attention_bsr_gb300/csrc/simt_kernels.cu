@@ -1,7 +1,8 @@
 // Portable SIMT kernels for block-sparse attention (fp32 arithmetic).
 //
-// They serve every supported head_dim (64/128/256/512) and both operand types
-// (fp32, bf16 -> fp32), with the same walk as the tensor-core kernels:
+// They serve every supported head_dim (64/128/256/512) and every operand type
+// (fp32; bf16 and fp16 widened to fp32), with the same walk as the
+// tensor-core kernels:
 //   * forward: one CTA per 16 query rows of a block row m, walking the row's
 //     stored blocks j in [row_ptr[m], row_ptr[m+1]) and the 128 keys of block
 //     col_idx[j] in chunks, with an online softmax ("trnsparse 0.7.0 -> 0.9.0"
