@@ -208,28 +208,35 @@ bsr_status fwd_impl(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* 
   a.status = status_ptr();
   if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
   cudaStream_t s = (cudaStream_t)stream;
-  if (!tc_fwd_supported(a.d)) return launch_fwd_simt(a, s);
+  // bf16 / fp16 with head_dim 64 / 128: the key-halves kernel (tc_fwd2.cu),
+  // which splits long rows; everything else: the wide kernel (tc_wide.cu)
+  const bool tc2 = tc_fwd_supported(a.d);
+  if (!tc2 && !wide_supported(a.d))
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd: dtype %d with head_dim %d", a.d.dtype, a.d.D);
   const int G = tc_grid(a.d);
   if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cannot query the SM count");
-  const bool persistent = a.d.D <= 128;  // the head_dim-256 kernel keeps one CTA per row
   const size_t plan_bytes = sizeof(int32_t) * plan_words(a.d.nb, G, a.d.BH);
-  const size_t part_bytes = persistent ? fwd_part_bytes(a.d.D) * plan_tiles(a.d.nb, G, a.d.BH) : 0;
+  const size_t part_bytes = tc2 ? fwd_part_bytes(a.d.D) * plan_tiles(a.d.nb, G, a.d.BH) : 0;
+  const size_t piece_bytes = tc2 ? 0 : wide_piece_bytes(a.d, 3);
   void* scratch = nullptr;
-  cudaError_t e = cudaMallocAsync(&scratch, plan_bytes + part_bytes, s);
+  cudaError_t e = cudaMallocAsync(&scratch, plan_bytes + part_bytes + piece_bytes, s);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaMallocAsync: %s", cudaGetErrorString(e));
   a.plan = (int32_t*)scratch;
   a.G = G;
-  a.part = persistent ? (float*)((char*)scratch + plan_bytes) : nullptr;
+  a.part = tc2 ? (float*)((char*)scratch + plan_bytes) : nullptr;
+  a.pieces = piece_bytes ? (char*)scratch + plan_bytes + part_bytes : nullptr;
   PlanArgs p{};
   p.list[0] = PlanList{row_ptr, a.plan};
   p.n = a.d.nb;
   p.G = G;
   p.BH = a.d.BH;
-  p.allow_split = persistent ? 1 : 0;
+  p.allow_split = tc2 ? 1 : 0;
   p.status = a.status;
   st = launch_plan(p, 1, s);
-  if (!two_pass) {
-    if (st == BSR_OK) st = launch_fwd_tc(a, s);
+  if (!tc2) {
+    if (st == BSR_OK) st = launch_fwd_wide(a, s);
+  } else if (!two_pass) {
+    if (st == BSR_OK) st = launch_fwd_tc2(a, s, 0);
   } else {
     // the planner runs again before the output pass: it also clears the
     // split lines' arrival counters the statistics pass used
@@ -343,41 +350,52 @@ bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
 size_t bwd_scratch_bytes(const Dims& d, int G, bool split) {
   const size_t rows = (size_t)d.BH * d.S;
   size_t bytes = 2 * sizeof(float) * rows;
-  bytes += 2 * sizeof(int32_t) * plan_words(d.nb, G, d.BH);
-  if (split) bytes += 3 * sizeof(float) * (size_t)128 * d.D * plan_tiles(d.nb, G, d.BH);
+  bytes += 3 * sizeof(int32_t) * plan_words(d.nb, G, d.BH);
+  if (split && tc_bwd_supported(d)) bytes += 3 * sizeof(float) * (size_t)128 * d.D * plan_tiles(d.nb, G, d.BH);
+  if (!tc_bwd_supported(d)) bytes += wide_piece_bytes(d, 4);
   return bytes;
 }
 
 void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split) {
   const size_t rows = (size_t)a->d.BH * a->d.S;
+  const size_t pw = plan_words(a->d.nb, G, a->d.BH);
   a->delta = (float*)base;
   a->lse2 = a->delta + rows;
   a->row_plan = (int32_t*)(a->lse2 + rows);
-  a->col_plan = a->row_plan + plan_words(a->d.nb, G, a->d.BH);
-  float* part = (float*)(a->col_plan + plan_words(a->d.nb, G, a->d.BH));
+  a->col_plan = a->row_plan + pw;
+  a->col_plan2 = a->col_plan + pw;
+  char* next = (char*)(a->col_plan2 + pw);
+  const bool tc = tc_bwd_supported(a->d);
   const size_t tiles = plan_tiles(a->d.nb, G, a->d.BH);
-  a->part_q = split ? part : nullptr;
-  a->part_kv = split ? part + (size_t)128 * a->d.D * tiles : nullptr;
+  float* part = (float*)next;
+  a->part_q = split && tc ? part : nullptr;
+  a->part_kv = split && tc ? part + (size_t)128 * a->d.D * tiles : nullptr;
+  if (split && tc) next += 3 * sizeof(float) * (size_t)128 * a->d.D * tiles;
+  a->pieces = tc ? nullptr : (void*)next;
 }
 
 bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split) {
   bsr_status st;
+  PlanArgs p{};
+  p.list[0] = PlanList{a.row_ptr, a.row_plan};
+  p.list[1] = PlanList{a.col_ptr, a.col_plan};
+  p.list[2] = PlanList{a.col_ptr, a.col_plan2};
+  p.n = a.d.nb;
+  p.G = tc_grid(a.d);
+  p.BH = a.d.BH;
+  p.status = a.status;
   if (tc_bwd_supported(a.d)) {
-    PlanArgs p{};
-    p.list[0] = PlanList{a.row_ptr, a.row_plan};
-    p.list[1] = PlanList{a.col_ptr, a.col_plan};
-    p.n = a.d.nb;
-    p.G = tc_grid(a.d);
-    p.BH = a.d.BH;
     p.allow_split = split ? 1 : 0;
-    p.status = a.status;
     if ((st = launch_delta_plan(a, p, 2, s)) != BSR_OK) return st;
     return launch_bwd_tc(a, s);
   }
-  if ((st = launch_delta(a, s)) != BSR_OK) return st;
-  st = launch_dq_simt(a, s);
-  if (st == BSR_OK) st = launch_dkdv_simt(a, s);
-  return st;
+  if (!wide_supported(a.d))
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_bwd: dtype %d with head_dim %d", a.d.dtype, a.d.D);
+  // the wide kernels walk whole lines (no split partials): dQ, dV and dK
+  // each on a plan of its own
+  p.allow_split = 0;
+  if ((st = launch_delta_plan(a, p, 3, s)) != BSR_OK) return st;
+  return launch_bwd_wide(a, s);
 }
 
 }  // namespace bsr

@@ -1,0 +1,61 @@
+// The delta pass of the backward: D_i = dO_i . O_i and the base-2
+// log-sum-exp lse2_i = row_max_i log2(e) + log2(row_denom_i), one fp32 value
+// each per query row ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.5.0]:
+// the delta identity).  An HBM-bound elementwise pass over O and dO (no
+// contraction), for every operand type and head_dim; the 16-bit head_dim
+// 64 / 128 backward runs the same rows fused with its planner (plan.cu).
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "delta.cuh"
+#include "kernels.h"
+
+namespace bsr {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) delta_kernel(BwdArgs a) {
+  delta_pass<T, D, kThreads>(a, blockIdx.x, gridDim.x);
+}
+
+template <typename T, int D>
+bsr_status delta_dispatch(const BwdArgs& a, cudaStream_t s) {
+  const size_t rows = (size_t)a.d.BH * a.d.S;
+  constexpr size_t per = delta_rows_per_cta<T, D, kThreads>();
+  const size_t groups = (rows + per - 1) / per;
+  // as many CTAs as the SMs hold at once; they loop over the row groups
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, delta_kernel<T, D>, kThreads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const size_t sms = (size_t)sm_count();
+  const size_t resident = sms > 0 ? sms * per_sm : groups;
+  const dim3 grid((unsigned)(groups < resident ? groups : resident));
+  LaunchTimer timer("delta", s);
+  delta_kernel<T, D><<<grid, kThreads, 0, s>>>(a);
+  return check_launch("delta launch");
+}
+
+template <typename T>
+bsr_status delta_dim(const BwdArgs& a, cudaStream_t s) {
+  switch (a.d.D) {
+    case 64: return delta_dispatch<T, 64>(a, s);
+    case 128: return delta_dispatch<T, 128>(a, s);
+    case 256: return delta_dispatch<T, 256>(a, s);
+    case 512: return delta_dispatch<T, 512>(a, s);
+    default: return fail(BSR_ERR_UNSUPPORTED, "delta: head_dim %d not supported", a.d.D);
+  }
+}
+
+}  // namespace
+
+bsr_status launch_delta(const BwdArgs& a, cudaStream_t s) {
+  if (a.d.dtype == BSR_BF16) return delta_dim<__nv_bfloat16>(a, s);
+  if (a.d.dtype == BSR_F16) return delta_dim<__half>(a, s);
+  return delta_dim<float>(a, s);
+}
+
+}  // namespace bsr

@@ -36,6 +36,7 @@ struct FwdArgs {
   int32_t* plan;          // block-row plan (plan.cu)
   int G;                  // persistent CTAs the plan was built for
   float* part;            // partial results of split rows: O (128 x D) and 3 x 128 stats per tile
+  void* pieces;           // fp32 operands: the three bf16 pieces of Q, K, V (wide_piece_bytes(d, 3))
   int* status;
 };
 
@@ -58,7 +59,9 @@ struct BwdArgs {
   float* delta;  // [BH * S] scratch: D_i = dO_i . O_i
   float* lse2;   // [BH * S] scratch: row_max * log2(e) + log2(row_denom)
   int32_t* row_plan;   // block-row plan (dQ walk)
-  int32_t* col_plan;   // block-column plan (dK/dV walk)
+  int32_t* col_plan;   // block-column plan (dK/dV walk; the dV walk of the wide kernels)
+  int32_t* col_plan2;  // block-column plan of the wide kernels' dK walk
+  void* pieces;        // fp32 operands: the three bf16 pieces of Q, K, V, dO (wide_piece_bytes(d, 4))
   float* part_q;       // partial dQ of split rows (128 x D per tile)
   float* part_kv;      // partial dK, dV of split columns (2 x 128 x D per tile)
   int* status;
@@ -140,7 +143,7 @@ struct PlanList {
 };
 
 struct PlanArgs {
-  PlanList list[2];
+  PlanList list[3];
   int n;            // lines per list (block rows = block columns)
   int G;            // persistent CTAs of the kernels that read the plan
   int BH;
@@ -148,7 +151,7 @@ struct PlanArgs {
   int* status;
 };
 
-// Builds `lists` (1 or 2) plans.
+// Builds `lists` (1 to 3) plans.
 bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s);
 // Delta / lse2 and the plans of `p` in one launch where the plans are small
 // (else launch_delta then launch_plan).
@@ -223,21 +226,28 @@ int sm_count();
 // Returns a status for the last launch on this thread (cudaGetLastError).
 bsr_status check_launch(const char* what);
 
-// Portable SIMT kernels (every head_dim and dtype).
-bsr_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
+// Delta D_i = dO_i . O_i and lse2_i of the backward pass (every dtype and head_dim).
 bsr_status launch_delta(const BwdArgs& a, cudaStream_t s);
-bsr_status launch_dq_simt(const BwdArgs& a, cudaStream_t s);
-bsr_status launch_dkdv_simt(const BwdArgs& a, cudaStream_t s);
 
-// Tensor-core (tcgen05 / TMA) kernels; a.plan (and a.part for head_dim <=
-// 128) must hold the block-row plan built by launch_plan.
+// Tensor-core (tcgen05 / TMA) kernels for bf16 / fp16 operands with head_dim
+// 64 / 128; a.plan and a.part must hold the block-row plan built by
+// launch_plan and its partial-result tiles.
 bool tc_fwd_supported(const Dims& d);
-bsr_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
 // head_dim 64 / 128, P in TMEM.  pass 0: the online-softmax forward; 1 and
 // 2: the statistics pass and then the output pass of the statistics-first
 // variant (the output pass reads the row_max / row_denom the first wrote).
 bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s, int pass = 0);
 bool tc_bwd_supported(const Dims& d);
+
+// Tensor-core kernels for the other cases (tc_wide.cu): bf16 / fp16 with
+// head_dim 256 / 512 and fp32 with any head_dim, on unsplit plans
+// (allow_split = 0).  fp32 operands need wide_piece_bytes(d, tensors) of
+// scratch in a.pieces for their bf16 pieces.
+bool wide_supported(const Dims& d);
+size_t wide_piece_bytes(const Dims& d, int tensors);
+bsr_status launch_fwd_wide(const FwdArgs& a, cudaStream_t s);
+// dQ on the row plan, dV on col_plan, dK on col_plan2, after launch_delta.
+bsr_status launch_bwd_wide(const BwdArgs& a, cudaStream_t s);
 
 // Y = A X for a BSR matrix A of 128 x 128 blocks (tc_spmm.cu).
 struct SpmmArgs {

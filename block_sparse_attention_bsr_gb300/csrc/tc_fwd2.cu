@@ -2,12 +2,12 @@
 // accumulation) with head_dim 64 / 128 on sm_103a, with P kept in tensor
 // memory in the operand type.
 //
-// Same walk as the head_dim-256 kernel in tc_fwd.cu (for each block row m
-// of one (batch, head) the row's stored blocks j in [row_ptr[m],
-// row_ptr[m+1]) are visited in order and the K / V tiles of block column
-// col_idx[j] come straight from HBM by TMA; "trnsparse 0.7.0 -> 0.9.0" diff,
-// CHANGELOG [0.8.0], attn_fwd_static), with these changes that keep the
-// tensor pipe fed:
+// For each block row m of one (batch, head) the row's stored blocks j in
+// [row_ptr[m], row_ptr[m+1]) are visited in order and the K / V tiles of
+// block column col_idx[j] come straight from HBM by TMA ("trnsparse 0.7.0 ->
+// 0.9.0" diff, CHANGELOG [0.8.0], attn_fwd_static: one launch, statistics on
+// chip, no K/V gather, no per-block score round trip through HBM), with
+// these choices that keep the tensor pipe fed:
 //   * persistent CTAs, one per SM, take (row, head) work items longest row
 //     first from a queue (sched.cuh) and prefetch the next item's Q (two Q
 //     buffers) and K / V tiles while the current one finishes;
@@ -651,6 +651,10 @@ bsr_status launch(const FwdArgs& a, const TensorMaps& tm, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool tc_fwd_supported(const Dims& d) {
+  return (d.dtype == BSR_BF16 || d.dtype == BSR_F16) && (d.D == 64 || d.D == 128);
+}
 
 size_t fwd_part_bytes(int D) {
   return sizeof(float) * (D == 64 ? fwd_part_floats<64>() : fwd_part_floats<128>());
