@@ -159,8 +159,22 @@ def run_ours(args, rank, world, dev):
     stream = torch.cuda.current_stream(dev)
 
     two_pass = args.forward == "two-pass"
+    # The step runs on a reusable plan of the mask (bsr_plan_create, built once
+    # here, outside the timed region: the work lists and scratch of a static
+    # structure); --api per-call times the entry points that plan on every call.
+    planned = args.api == "plan" and not two_pass
+    plan = st.plan(Q) if planned else None
 
     def step(q, k, v, do, o, m, d, gq, gk, gv):
+        if planned:
+            bsr.bsr_attn_fwd_plan(plan, q, k, v, wl.scale, o, m, d, stream)
+            bsr.bsr_attn_bwd_plan(plan, q, k, v, o, do, m, d, wl.scale, gq, gk, gv, stream)
+            return
+        bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale, o, m, d, stream, two_pass)
+        bsr.bsr_attn_bwd(q, k, v, o, do, m, d, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, wl.scale,
+                         gq, gk, gv, stream)
+
+    def step_per_call(q, k, v, do, o, m, d, gq, gk, gv):
         bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale, o, m, d, stream, two_pass)
         bsr.bsr_attn_bwd(q, k, v, o, do, m, d, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, wl.scale,
                          gq, gk, gv, stream)
@@ -173,13 +187,13 @@ def run_ours(args, rank, world, dev):
     bsr.bsr_attn_check()
 
     # device-resident timed region: per-step CUDA events, L2 flushed before each step
-    def timed_steps(per_kernel):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    def timed_steps(per_kernel, nsteps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nsteps)]
         bsr.profile_collect()
         bsr.profile_enable(per_kernel)
         barrier(world)
         torch.cuda.synchronize(dev)
-        for i in range(args.steps):
+        for i in range(nsteps):
             flush_l2(l2)
             evs[i][0].record(stream)
             step(*args_dev)
@@ -189,15 +203,19 @@ def run_ours(args, rank, world, dev):
         bsr.profile_enable(False)
         prof = bsr.profile_collect()
         bsr.bsr_attn_check()
-        return max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world) / args.steps, prof
+        ts = [a.elapsed_time(b) for a, b in evs]
+        return (max_over_ranks(statistics.median(ts), world), max_over_ranks(sum(ts) / nsteps, world), prof)
 
     # The headline pass records no events between the kernels of a step (each
     # such record adds a few microseconds of idle GPU time); a second pass of
     # the same K steps brackets every launch with events for the per-kernel
-    # durations the roofline uses.
+    # durations the roofline uses.  The headline statistic is the median of
+    # the K per-step times; a longer pass of 100 steps is reported beside it.
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        ms_per_step, _ = timed_steps(False)
-        ms_per_step_instr, prof = timed_steps(True)
+        ms_per_step, ms_mean, _ = timed_steps(False, args.steps)
+        ms_per_step_instr, _, prof = timed_steps(True, args.steps)
+    long_steps = max(100, args.steps)
+    ms_long, ms_long_mean, _ = timed_steps(False, long_steps)
 
     # forward alone and backward alone (same protocol, untimed for the headline)
     def time_part(fn, reps):
@@ -210,10 +228,18 @@ def run_ours(args, rank, world, dev):
         torch.cuda.synchronize(dev)
         return statistics.median(a.elapsed_time(b) for a, b in e)
 
-    ms_fwd = time_part(lambda: bsr.bsr_attn_fwd(Q, K, V, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale,
-                                                 O, rm, rd, stream, two_pass), max(args.steps, 5))
-    ms_bwd = time_part(lambda: bsr.bsr_attn_bwd(Q, K, V, O, dO, rm, rd, st.row_ptr, st.col_idx, st.col_ptr,
-                                                 st.row_idx, wl.scale, dQ, dK, dV, stream), max(args.steps, 5))
+    if planned:
+        ms_fwd = time_part(lambda: bsr.bsr_attn_fwd_plan(plan, Q, K, V, wl.scale, O, rm, rd, stream),
+                           max(args.steps, 5))
+        ms_bwd = time_part(lambda: bsr.bsr_attn_bwd_plan(plan, Q, K, V, O, dO, rm, rd, wl.scale, dQ, dK, dV,
+                                                         stream), max(args.steps, 5))
+    else:
+        ms_fwd = time_part(lambda: bsr.bsr_attn_fwd(Q, K, V, st.row_ptr, st.col_idx, st.n_brows, BLOCK, wl.scale,
+                                                     O, rm, rd, stream, two_pass), max(args.steps, 5))
+        ms_bwd = time_part(lambda: bsr.bsr_attn_bwd(Q, K, V, O, dO, rm, rd, st.row_ptr, st.col_idx, st.col_ptr,
+                                                     st.row_idx, wl.scale, dQ, dK, dV, stream), max(args.steps, 5))
+    # the entry points that build the work lists on every call, same protocol
+    ms_per_call = time_part(lambda: step_per_call(*args_dev), max(args.steps, 5))
 
     # end to end through the C ABI from pinned host buffers
     pin = [t.pin_memory() for t in (hQ, hK, hV, hdO)]
@@ -252,18 +278,22 @@ def run_ours(args, rank, world, dev):
                     "flop_per_launch": kf, "ms_per_launch": avg_ms}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "statistic": "median of the per-step times",
+        "ms_per_step_mean": round(ms_mean, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.batch, "heads": wl.heads, "seq": wl.seq,
-                   "head_dim": wl.head_dim, "block": BLOCK, "mask": wl.mask, "radius": wl.radius,
-                   "nnzb": nnzb, "density": round(nnzb / wl.nb ** 2, 4), "l2": "flushed before every step",
-                   "parallelism": f"replicas x{world}", "forward": args.forward},
+        "config": workload_config(wl, nnzb, world, args.forward),
         "ms_fwd": round(ms_fwd, 4), "ms_bwd": round(ms_bwd, 4),
+        "api": "bsr_attn_fwd_plan + bsr_attn_bwd_plan on one plan built before timing" if planned
+               else "bsr_attn_fwd + bsr_attn_bwd (work lists built on every call)",
+        "per_call_api_ms_per_step": round(ms_per_call, 4),
         "kernel_timing": {"pass": "second pass of the same K steps with CUDA events around every launch; "
                                   "dQ and dK/dV run one after the other there (the headline pass overlaps them "
                                   "on two streams)",
                           "ms_per_step": round(ms_per_step_instr, 4)},
         "pct_of_bf16_peak": round(100 * value / world / peaks["bf16"], 2),
+        "long_run": {"steps": long_steps, "ms_per_step_median": round(ms_long, 4),
+                     "ms_per_step_mean": round(ms_long_mean, 4),
+                     "tflops_median": round(world * flops / (ms_long * 1e-3) / 1e12, 3)},
         "alg_gflop_per_step": flops / 1e9,
         "kernels": kern,
         "gpu_launches": sum(n for n, _ in prof.values()),
@@ -274,15 +304,79 @@ def run_ours(args, rank, world, dev):
     }
     if args.sdpa:
         line["sdpa"] = sdpa_comparators(Q, K, V, dO, bm, l2, stream, dev, args)
+    if args.other_workloads and world == 1:
+        del Q, K, V, dO, O, rm, rd, dQ, dK, dV, args_dev
+        line["other_workloads"] = other_workloads(wl.name, dev, args, l2, stream, peaks)
     return line
 
 
-def sdpa_comparators(Q, K, V, dO, bm, l2, stream, dev, args):
+OTHER_WORKLOADS = ("tiny", "dilated_s2048", "global_s8192_f32", "local_s8192_d256", "local_s8192_d512",
+                   "random_p0.01", "random_p0.05", "random_p0.13", "random_p0.27", "random_p0.5")
+
+
+def other_workloads(headline, dev, args, l2, stream, peaks):
+    """fwd+bwd of every other configuration the metric names, same protocol (L2 flushed before every step,
+    CUDA events on the stream, median of `args.steps` steps after `args.warmup`): ms, TFLOP/s over stored
+    blocks and fraction of the bf16 peak; the density sweep also times dense masked SDPA on the same inputs."""
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    out = {}
+    for name in OTHER_WORKLOADS:
+        if name == headline:
+            continue
+        wl = inputs.WORKLOADS[name]
+        bm = wl.block_mask()
+        rp, ci = inputs.bsr_from_block_mask(bm)
+        st = bsr.Structure(rp, ci, wl.nb, dev)
+        Q, K, V, dO = (t.to(dev) for t in wl.inputs(seed=0))
+        O = torch.empty_like(Q)
+        rm = torch.empty(Q.shape[:3], device=dev, dtype=torch.float32)
+        rd = torch.empty_like(rm)
+        dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
+
+        plan = st.plan(Q)
+
+        def step():
+            bsr.bsr_attn_fwd_plan(plan, Q, K, V, wl.scale, O, rm, rd, stream)
+            bsr.bsr_attn_bwd_plan(plan, Q, K, V, O, dO, rm, rd, wl.scale, dQ, dK, dV, stream)
+
+        ms = median_call_ms(step, args, l2, stream, dev)
+        bsr.profile_collect()
+        bsr.profile_enable(True)
+        step()
+        torch.cuda.synchronize(dev)
+        bsr.profile_enable(False)
+        kern = {k: round(t * 1e3 / n, 2) for k, (n, t) in bsr.profile_collect().items()}
+        bsr.bsr_attn_check()
+        flops = alg_flops(wl, st.nnzb)
+        tf = flops / (ms * 1e-3) / 1e12
+        e = {"ms": round(ms, 4), "tflops": round(tf, 3), "frac_of_bf16_peak": round(tf / peaks["bf16"], 4),
+             "dtype": wl.dtype, "shape": [wl.batch, wl.heads, wl.seq, wl.head_dim], "mask": wl.mask,
+             "nnzb": st.nnzb, "density": round(st.nnzb / wl.nb ** 2, 4), "kernel_us_one_step": kern}
+        if name.startswith("random_p") and args.sdpa:
+            e["sdpa_masked_fwd_bwd_ms"] = sdpa_comparators(Q, K, V, dO, bm, l2, stream, dev, args,
+                                                           kinds=("masked",))["sdpa_masked_fwd_bwd_ms"]
+        out[name] = e
+        del Q, K, V, dO, O, rm, rd, dQ, dK, dV, plan, st
+        torch.cuda.empty_cache()
+    return out
+
+
+def workload_config(wl, nnzb, world, forward):
+    return {"workload": wl.name, "batch": wl.batch, "heads": wl.heads, "seq": wl.seq, "head_dim": wl.head_dim,
+            "block": BLOCK, "mask": wl.mask, "radius": wl.radius, "nnzb": nnzb,
+            "density": round(nnzb / wl.nb ** 2, 4), "l2": "flushed before every step",
+            "parallelism": f"replicas x{world}", "forward": forward}
+
+
+def sdpa_comparators(Q, K, V, dO, bm, l2, stream, dev, args, kinds=("masked", "dense")):
     """Dense masked SDPA (boolean element mask) and unmasked dense SDPA on the same GPU, fwd+bwd ms."""
     F = torch.nn.functional
     em = torch.from_numpy(np.repeat(np.repeat(bm, BLOCK, 0), BLOCK, 1)).to(dev)
     res = {}
     for name, mask in (("masked", em), ("dense", None)):
+        if name not in kinds:
+            continue
         def fb():
             q, k, v = (t.detach().requires_grad_() for t in (Q, K, V))
             o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask)
@@ -441,10 +535,14 @@ def main():
     ap.add_argument("--forward", default="online", choices=["online", "two-pass"],
                     help="forward variant: the online-softmax pass, or the statistics-first two-pass variant")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--api", default="plan", choices=["plan", "per-call"],
+                    help="entry points of the step: a reusable plan built once, or the per-call ones")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sdpa", action=argparse.BooleanOptionalAction, default=True,
                     help="also time dense masked / unmasked SDPA on the same GPU")
+    ap.add_argument("--other-workloads", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time every other configuration (tiny, dilated, fp32, head_dim 256 / 512, densities)")
     ap.add_argument("--spmm-sweep", action="store_true",
                     help="instead of attention: bsr_spmm against dense matmul over block densities (one line each)")
     ap.add_argument("--screen-sweep", action="store_true",
@@ -464,8 +562,11 @@ def main():
         return
 
     if args.impl == "reference":
-        # the CPU oracle stands as the reference arm; rank 0 alone runs it.
-        # One step = the oracle's fwd+bwd on one (batch, head) slice of the workload.
+        # The CPU oracle stands as the reference arm; rank 0 alone runs it.  A
+        # whole step (all B * H slices of seq 8192, ~1.5 s of fp64 each) would
+        # not fit a few minutes, so one reference step is ONE (batch, head)
+        # slice of the workload, fwd+bwd, and value / ms_per_step are for that
+        # slice; the full-step time is reported separately, extrapolated.
         if rank != 0:
             return
         import oracle
@@ -484,13 +585,14 @@ def main():
         flops_head = 14 * BLOCK * BLOCK * wl.head_dim * nnzb
         v = flops_head / sec / 1e12
         cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-        sample = f"one (batch, head) slice of {wl.name} per step, fwd+bwd, dense fp64 numpy, median {sec:.2f} s"
+        sample = (f"one (batch, head) slice of {wl.name} per step ({wl.batch * wl.heads} slices make a full step), "
+                  f"fwd+bwd, dense fp64 numpy, median {sec:.2f} s")
         line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1,
-                "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": round(sec * 1e3 * wl.batch * wl.heads, 3), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": wl.name, "batch": wl.batch, "heads": wl.heads, "seq": wl.seq,
-                           "head_dim": wl.head_dim, "block": BLOCK, "mask": wl.mask, "nnzb": nnzb},
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+                "step": "one (batch, head) slice of the workload",
+                "ms_per_full_step_extrapolated": round(sec * 1e3 * wl.batch * wl.heads, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload_config(wl, nnzb, 1, args.forward),
                 "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                  "sample": sample},
                 "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

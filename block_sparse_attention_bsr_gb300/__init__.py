@@ -23,8 +23,10 @@ STATUS_NAMES = {0: "BSR_OK", 1: "BSR_ERR_INVALID_ARG", 2: "BSR_ERR_UNSUPPORTED",
                 4: "BSR_ERR_TIMEOUT", 5: "BSR_ERR_DEVICE_CHECK"}
 
 # Every symbol include/bsr_attn.h declares.
-EXPORTS = ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_screened_spmm", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check",
-           "bsr_last_error", "bsr_profile_enable", "bsr_profile_collect")
+EXPORTS = ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_screened_spmm", "bsr_attn_bwd",
+           "bsr_attn_bwd_noalloc", "bsr_plan_create", "bsr_plan_destroy", "bsr_attn_fwd_plan", "bsr_attn_bwd_plan",
+           "bsr_build_bsc", "bsr_validate", "bsr_attn_check", "bsr_set_wait_limit", "bsr_last_error",
+           "bsr_profile_enable", "bsr_profile_collect")
 
 
 class BsrError(RuntimeError):
@@ -62,16 +64,23 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsr_screened_spmm.argtypes = [P, P, P, I32, I32, I32, F32, P, P]
     lib.bsr_attn_bwd.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_attn_bwd_noalloc.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
+    lib.bsr_plan_create.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, P, ctypes.POINTER(ctypes.c_void_p)]
+    lib.bsr_plan_destroy.argtypes = [P]
+    lib.bsr_attn_fwd_plan.argtypes = [P, T, T, T, F32, T, P, P, P]
+    lib.bsr_attn_bwd_plan.argtypes = [P, T, T, T, T, T, P, P, F32, T, T, T, P]
     lib.bsr_build_bsc.argtypes = [P, P, I32, I32, P, P]
     lib.bsr_validate.argtypes = [P, P, I32, I32]
     lib.bsr_attn_check.argtypes = [P]
+    lib.bsr_set_wait_limit.argtypes = [ctypes.c_uint64]
     lib.bsr_last_error.argtypes = []
     lib.bsr_last_error.restype = ctypes.c_char_p
     lib.bsr_profile_enable.argtypes = [I32]
     lib.bsr_profile_enable.restype = None
     lib.bsr_profile_collect.argtypes = [ctypes.POINTER(bsr_kernel_time), I32]
     lib.bsr_profile_collect.restype = I32
-    for name in ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_screened_spmm", "bsr_attn_bwd", "bsr_attn_bwd_noalloc", "bsr_build_bsc", "bsr_validate", "bsr_attn_check"):
+    for name in ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_screened_spmm", "bsr_attn_bwd",
+                 "bsr_attn_bwd_noalloc", "bsr_plan_create", "bsr_plan_destroy", "bsr_attn_fwd_plan",
+                 "bsr_attn_bwd_plan", "bsr_build_bsc", "bsr_validate", "bsr_attn_check", "bsr_set_wait_limit"):
         getattr(lib, name).restype = I32
     _lib_handle = lib
     return lib
@@ -210,6 +219,60 @@ def bsr_attn_bwd_noalloc(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, c
                                     _stream(stream, Q)))
 
 
+class Plan:
+    """A reusable plan (bsr_plan_create): the work lists and scratch of one block mask for operands of
+    shape [batch, heads, n_brows * 128, head_dim] and one dtype.  Freed with bsr_plan_destroy when
+    the object is collected (or by close())."""
+
+    _CODES = None
+
+    def __init__(self, structure: "Structure", batch: int, heads: int, head_dim: int, dtype, stream=None):
+        import torch
+
+        codes = {torch.float32: BSR_F32, torch.bfloat16: BSR_BF16, torch.float16: BSR_F16}
+        if dtype not in codes:
+            raise TypeError(f"unsupported dtype {dtype} (float32, bfloat16 or float16)")
+        lib = load_library()
+        h = ctypes.c_void_p()
+        s = torch.cuda.current_stream(structure.row_ptr.device).cuda_stream if stream is None else _stream(stream, None)
+        _check(lib.bsr_plan_create(structure.row_ptr.data_ptr(), structure.col_idx.data_ptr(),
+                                   structure.col_ptr.data_ptr(), structure.row_idx.data_ptr(), structure.n_brows,
+                                   int(batch), int(heads), int(head_dim), codes[dtype], s, ctypes.byref(h)))
+        self.handle = h.value
+        self.key = (int(batch), int(heads), int(head_dim), dtype)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            load_library().bsr_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown
+            pass
+
+
+def bsr_attn_fwd_plan(plan: Plan, Q, K, V, scale: float, O, row_max, row_denom, stream=None) -> None:
+    """Forward pass on a reusable plan (bsr_attn_fwd_plan in include/bsr_attn.h)."""
+    lib = load_library()
+    q, k, v, o = (_desc(t) for t in (Q, K, V, O))
+    _check(lib.bsr_attn_fwd_plan(plan.handle, ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), float(scale),
+                                 ctypes.byref(o), _dev_ptr(row_max, "torch.float32"),
+                                 _dev_ptr(row_denom, "torch.float32"), _stream(stream, Q)))
+
+
+def bsr_attn_bwd_plan(plan: Plan, Q, K, V, O, dO, row_max, row_denom, scale: float, dQ, dK, dV,
+                      stream=None) -> None:
+    """Backward pass on a reusable plan (bsr_attn_bwd_plan in include/bsr_attn.h)."""
+    lib = load_library()
+    q, k, v, o, do, dq, dk, dv = (_desc(t) for t in (Q, K, V, O, dO, dQ, dK, dV))
+    _check(lib.bsr_attn_bwd_plan(plan.handle, ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(o),
+                                 ctypes.byref(do), _dev_ptr(row_max, "torch.float32"),
+                                 _dev_ptr(row_denom, "torch.float32"), float(scale), ctypes.byref(dq),
+                                 ctypes.byref(dk), ctypes.byref(dv), _stream(stream, Q)))
+
+
 def _host_i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
@@ -243,6 +306,11 @@ def bsr_attn_check(stream=None) -> None:
     _check(load_library().bsr_attn_check(s))
 
 
+def set_wait_limit(ns: int = 0) -> None:
+    """Limit of the kernels' bounded device-side waits in ns (0: the default 2 s); see include/bsr_attn.h."""
+    _check(load_library().bsr_set_wait_limit(int(ns)))
+
+
 def profile_enable(on: bool = True) -> None:
     load_library().bsr_profile_enable(1 if on else 0)
 
@@ -270,6 +338,17 @@ class Structure:
         self.dev = {k: torch.from_numpy(v if v.size else np.zeros(1, np.int32)).to(device)
                     for k, v in self.host.items()}
         self.nnzb = int(rp[-1])
+        self._plans = {}
+
+    def plan(self, Q) -> "Plan":
+        """The reusable plan of this mask for operands shaped and typed like Q (built on first use)."""
+        b, h, s, d = Q.shape
+        if s != self.n_brows * 128:
+            raise ValueError(f"seq {s} does not match the mask's {self.n_brows} block rows")
+        key = (b, h, d, Q.dtype)
+        if key not in self._plans:
+            self._plans[key] = Plan(self, b, h, d, Q.dtype)
+        return self._plans[key]
 
     @property
     def row_ptr(self):
@@ -288,41 +367,72 @@ class Structure:
         return self.dev["row_idx"]
 
 
-_AUTOGRAD_FN = None
+_OPS = None
 
 
-def _autograd_fn():
-    """The torch.autograd.Function pairing bsr_attn_fwd with bsr_attn_bwd (built on first use)."""
-    global _AUTOGRAD_FN
-    if _AUTOGRAD_FN is not None:
-        return _AUTOGRAD_FN
+def register_ops():
+    """Registers the custom-op pair torch.ops.bsr.bsr_attn / torch.ops.bsr.bsr_attn_bwd (once) and returns
+    the torch.ops.bsr namespace.
+
+    bsr_attn(Q, K, V, row_ptr, col_idx, col_ptr, row_idx, scale) -> (O, row_max, row_denom) runs
+    bsr_attn_fwd; bsr_attn_bwd(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx,
+    scale) -> (dQ, dK, dV) runs bsr_attn_bwd.  The forward carries the BSC lists (col_ptr, row_idx) only so
+    that its registered autograd formula can hand them to the backward op.  Both have fake (meta)
+    implementations, so graph tracing (torch.compile, torch.export) sees each as one opaque op; the pages
+    register their kernels the same way, as a custom-op pair with register_autograd ("trnsparse 0.7.0 ->
+    0.9.0" diff, CHANGELOG [0.8.0]).
+    """
+    global _OPS
+    if _OPS is not None:
+        return _OPS
     import torch
 
-    class BlockSparseAttention(torch.autograd.Function):
-        @staticmethod
-        def forward(ctx, Q, K, V, structure, scale):
-            O = torch.empty_like(Q)
-            rm = torch.empty(Q.shape[:3], device=Q.device, dtype=torch.float32)
-            rd = torch.empty_like(rm)
-            bsr_attn_fwd(Q, K, V, structure.row_ptr, structure.col_idx, structure.n_brows, 128, scale, O, rm, rd)
-            ctx.save_for_backward(Q, K, V, O, rm, rd)
-            ctx.structure = structure
-            ctx.scale = scale
-            ctx.mark_non_differentiable(rm, rd)
-            return O, rm, rd
+    # explicit schemas: this module's annotations are strings (postponed evaluation)
+    @torch.library.custom_op("bsr::bsr_attn", mutates_args=(),
+                             schema="(Tensor Q, Tensor K, Tensor V, Tensor row_ptr, Tensor col_idx, Tensor col_ptr, "
+                                    "Tensor row_idx, float scale) -> (Tensor, Tensor, Tensor)")
+    def _fwd(Q, K, V, row_ptr, col_idx, col_ptr, row_idx, scale):
+        O = torch.empty_like(Q)
+        rm = torch.empty(Q.shape[:3], device=Q.device, dtype=torch.float32)
+        rd = torch.empty_like(rm)
+        bsr_attn_fwd(Q, K, V, row_ptr, col_idx, Q.shape[2] // 128, 128, scale, O, rm, rd)
+        return O, rm, rd
 
-        @staticmethod
-        def backward(ctx, dO, _drm, _drd):
-            Q, K, V, O, rm, rd = ctx.saved_tensors
-            st = ctx.structure
-            dO = dO.contiguous()
-            dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
-            bsr_attn_bwd(Q, K, V, O, dO, rm, rd, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, ctx.scale,
-                         dQ, dK, dV)
-            return dQ, dK, dV, None, None
+    @_fwd.register_fake
+    def _fwd_fake(Q, K, V, row_ptr, col_idx, col_ptr, row_idx, scale):
+        rm = Q.new_empty(Q.shape[:3], dtype=torch.float32)
+        return torch.empty_like(Q), rm, torch.empty_like(rm)
 
-    _AUTOGRAD_FN = BlockSparseAttention
-    return _AUTOGRAD_FN
+    @torch.library.custom_op("bsr::bsr_attn_bwd", mutates_args=(),
+                             schema="(Tensor Q, Tensor K, Tensor V, Tensor O, Tensor dO, Tensor row_max, "
+                                    "Tensor row_denom, Tensor row_ptr, Tensor col_idx, Tensor col_ptr, "
+                                    "Tensor row_idx, float scale) -> (Tensor, Tensor, Tensor)")
+    def _bwd(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx, scale):
+        dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
+        bsr_attn_bwd(Q, K, V, O, dO.contiguous(), row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx, scale,
+                     dQ, dK, dV)
+        return dQ, dK, dV
+
+    @_bwd.register_fake
+    def _bwd_fake(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, col_ptr, row_idx, scale):
+        return torch.empty_like(Q), torch.empty_like(Q), torch.empty_like(Q)
+
+    def _setup_context(ctx, inputs, output):
+        Q, K, V, row_ptr, col_idx, col_ptr, row_idx, scale = inputs
+        O, rm, rd = output
+        ctx.save_for_backward(Q, K, V, O, rm, rd, row_ptr, col_idx, col_ptr, row_idx)
+        ctx.scale = scale
+        ctx.mark_non_differentiable(rm, rd)
+
+    def _backward(ctx, dO, _drm, _drd):
+        Q, K, V, O, rm, rd, row_ptr, col_idx, col_ptr, row_idx = ctx.saved_tensors
+        dQ, dK, dV = torch.ops.bsr.bsr_attn_bwd(Q, K, V, O, dO.contiguous(), rm, rd, row_ptr, col_idx, col_ptr,
+                                                row_idx, ctx.scale)
+        return dQ, dK, dV, None, None, None, None, None
+
+    _fwd.register_autograd(_backward, setup_context=_setup_context)
+    _OPS = torch.ops.bsr
+    return _OPS
 
 
 def block_sparse_attention(Q, K, V, structure: "Structure", scale=None, return_stats: bool = False):
@@ -330,12 +440,15 @@ def block_sparse_attention(Q, K, V, structure: "Structure", scale=None, return_s
 
     Q, K, V: contiguous CUDA tensors [batch, heads, seq, head_dim] (bf16, fp16 or
     fp32, 16-byte aligned); `structure`: a Structure of the block mask on the same
-    device; scale defaults to 1 / sqrt(head_dim).  The forward and backward
-    passes are bsr_attn_fwd and bsr_attn_bwd on the current stream.  With
+    device; scale defaults to 1 / sqrt(head_dim).  Runs the custom op
+    torch.ops.bsr.bsr_attn (bsr_attn_fwd on the current stream) with its
+    registered backward torch.ops.bsr.bsr_attn_bwd (bsr_attn_bwd).  With
     return_stats the fp32 row_max / row_denom statistics come back as well
     (they carry no gradient).
     """
     if scale is None:
         scale = 1.0 / float(Q.shape[-1]) ** 0.5
-    O, rm, rd = _autograd_fn().apply(Q, K, V, structure, float(scale))
+    ops = register_ops()
+    O, rm, rd = ops.bsr_attn(Q, K, V, structure.row_ptr, structure.col_idx, structure.col_ptr, structure.row_idx,
+                             float(scale))
     return (O, rm, rd) if return_stats else O

@@ -18,9 +18,14 @@ namespace bsr {
 namespace {
 thread_local std::string g_error;
 
-// Device status word: set by kernels whose bounded waits give up or whose
-// index checks fail; read and cleared by bsr_attn_check.
-__device__ int g_status;
+// Device status block (see wait_limit_ns in sm100.cuh): word 0 is the
+// status word, set by kernels whose bounded waits give up or whose index
+// checks fail and read and cleared by bsr_attn_check; words 2..3 hold the
+// bounded waits' limit in nanoseconds (2 s; bsr_set_wait_limit changes it).
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+__device__ __align__(16) int g_status[4] = {0, 0, (int)kDefaultWaitLimitNs, 0};
+
+}  // namespace
 
 int* status_ptr() {
   int dev = 0;
@@ -36,6 +41,8 @@ int* status_ptr() {
   }
   return cache[dev];
 }
+
+namespace {
 
 // ------------------------------------------------------------ profiling --
 struct TimedLaunch {
@@ -177,13 +184,10 @@ using namespace bsr;
 extern "C" const char* bsr_last_error(void) { return g_error.c_str(); }
 
 namespace bsr {
-namespace {
 
-// The forward entry points: the online-softmax pass, or (two_pass) the
-// statistics pass and then the output pass of the statistics-first variant.
-bsr_status fwd_impl(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V, const int32_t* row_ptr,
-                    const int32_t* col_idx, int32_t n_brows, int32_t block, float scale, bsr_tensor* O,
-                    float* row_max, float* row_denom, void* stream, bool two_pass) {
+bsr_status build_fwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V, const int32_t* row_ptr,
+                          const int32_t* col_idx, int32_t n_brows, int32_t block, float scale, bsr_tensor* O,
+                          float* row_max, float* row_denom, bool two_pass, FwdArgs* out) {
   bsr_status st;
   if (block != 128) return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd: block %d not supported (128)", block);
   if ((st = check_tensor(Q, "Q", nullptr)) || (st = check_tensor(K, "K", Q)) || (st = check_tensor(V, "V", Q)) ||
@@ -203,47 +207,75 @@ bsr_status fwd_impl(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* 
   a.row_denom = row_denom;
   a.row_ptr = row_ptr;
   a.col_idx = col_idx;
-  if (two_pass && !(a.d.dtype != BSR_F32 && a.d.D <= 128))
+  if (two_pass && !tc_fwd_supported(a.d))
     return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd_two_pass: bf16 / fp16 operands with head_dim 64 or 128 only");
-  a.status = status_ptr();
-  if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
-  cudaStream_t s = (cudaStream_t)stream;
   // bf16 / fp16 with head_dim 64 / 128: the key-halves kernel (tc_fwd2.cu),
   // which splits long rows; everything else: the wide kernel (tc_wide.cu)
-  const bool tc2 = tc_fwd_supported(a.d);
-  if (!tc2 && !wide_supported(a.d))
+  if (!tc_fwd_supported(a.d) && !wide_supported(a.d))
     return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_fwd: dtype %d with head_dim %d", a.d.dtype, a.d.D);
-  const int G = tc_grid(a.d);
-  if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cannot query the SM count");
-  const size_t plan_bytes = sizeof(int32_t) * plan_words(a.d.nb, G, a.d.BH);
-  const size_t part_bytes = tc2 ? fwd_part_bytes(a.d.D) * plan_tiles(a.d.nb, G, a.d.BH) : 0;
-  const size_t piece_bytes = tc2 ? 0 : wide_piece_bytes(a.d, 3);
-  void* scratch = nullptr;
-  cudaError_t e = cudaMallocAsync(&scratch, plan_bytes + part_bytes + piece_bytes, s);
-  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaMallocAsync: %s", cudaGetErrorString(e));
-  a.plan = (int32_t*)scratch;
-  a.G = G;
-  a.part = tc2 ? (float*)((char*)scratch + plan_bytes) : nullptr;
-  a.pieces = piece_bytes ? (char*)scratch + plan_bytes + part_bytes : nullptr;
-  PlanArgs p{};
-  p.list[0] = PlanList{row_ptr, a.plan};
-  p.n = a.d.nb;
-  p.G = G;
-  p.BH = a.d.BH;
-  p.allow_split = tc2 ? 1 : 0;
-  p.status = a.status;
-  st = launch_plan(p, 1, s);
-  if (!tc2) {
-    if (st == BSR_OK) st = launch_fwd_wide(a, s);
-  } else if (!two_pass) {
-    if (st == BSR_OK) st = launch_fwd_tc2(a, s, 0);
-  } else {
-    // the planner runs again before the output pass: it also clears the
-    // split lines' arrival counters the statistics pass used
-    if (st == BSR_OK) st = launch_fwd_tc2(a, s, 1);
-    if (st == BSR_OK) st = launch_plan(p, 1, s);
-    if (st == BSR_OK) st = launch_fwd_tc2(a, s, 2);
+  a.status = status_ptr();
+  if (!a.status) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: no CUDA device");
+  a.G = tc_grid(a.d);
+  if (a.G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cannot query the SM count");
+  *out = a;
+  return BSR_OK;
+}
+
+size_t fwd_scratch_bytes(const Dims& d, int G) {
+  const bool tc2 = tc_fwd_supported(d);
+  size_t bytes = sizeof(int32_t) * plan_words(d.nb, G, d.BH);
+  if (tc2) bytes += fwd_part_bytes(d.D) * plan_tiles(d.nb, G, d.BH);
+  else bytes += wide_piece_bytes(d, 3);
+  return bytes;
+}
+
+void fwd_scratch_carve(FwdArgs* a, void* base) {
+  const bool tc2 = tc_fwd_supported(a->d);
+  char* p = (char*)base;
+  a->plan = (int32_t*)p;
+  p += sizeof(int32_t) * plan_words(a->d.nb, a->G, a->d.BH);
+  a->part = tc2 ? (float*)p : nullptr;
+  a->pieces = tc2 ? nullptr : (void*)p;
+}
+
+// The forward pass on carved scratch: the planner first unless the plan in
+// a.plan is already built (a bsr_plan), then the online-softmax pass, or
+// (two_pass) the statistics pass and then the output pass of the
+// statistics-first variant.  The kernels leave the plan's counters at 0, so
+// both passes run on one plan.
+bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned) {
+  bsr_status st = BSR_OK;
+  const bool tc2 = tc_fwd_supported(a.d);
+  if (!planned) {
+    PlanArgs p{};
+    p.list[0] = PlanList{a.row_ptr, a.plan};
+    p.n = a.d.nb;
+    p.G = a.G;
+    p.BH = a.d.BH;
+    p.allow_split = tc2 ? 1 : 0;
+    p.status = a.status;
+    if ((st = launch_plan(p, 1, s)) != BSR_OK) return st;
   }
+  if (!tc2) return launch_fwd_wide(a, s);
+  if (!two_pass) return launch_fwd_tc2(a, s, 0);
+  if ((st = launch_fwd_tc2(a, s, 1)) != BSR_OK) return st;
+  return launch_fwd_tc2(a, s, 2);
+}
+
+namespace {
+
+bsr_status fwd_impl(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V, const int32_t* row_ptr,
+                    const int32_t* col_idx, int32_t n_brows, int32_t block, float scale, bsr_tensor* O,
+                    float* row_max, float* row_denom, void* stream, bool two_pass) {
+  FwdArgs a{};
+  bsr_status st = build_fwd_args(Q, K, V, row_ptr, col_idx, n_brows, block, scale, O, row_max, row_denom, two_pass, &a);
+  if (st != BSR_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, fwd_scratch_bytes(a.d, a.G), s);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaMallocAsync: %s", cudaGetErrorString(e));
+  fwd_scratch_carve(&a, scratch);
+  st = run_fwd(a, s, two_pass, false);
   e = cudaFreeAsync(scratch, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaFreeAsync: %s", cudaGetErrorString(e));
   return st;
@@ -374,8 +406,14 @@ void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split) {
   a->pieces = tc ? nullptr : (void*)next;
 }
 
-bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split) {
+bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned) {
   bsr_status st;
+  if (planned) {  // the work lists are built already (a bsr_plan): delta, then the walks
+    if (!tc_bwd_supported(a.d) && !wide_supported(a.d))
+      return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_bwd: dtype %d with head_dim %d", a.d.dtype, a.d.D);
+    if ((st = launch_delta(a, s)) != BSR_OK) return st;
+    return tc_bwd_supported(a.d) ? launch_bwd_tc(a, s) : launch_bwd_wide(a, s);
+  }
   PlanArgs p{};
   p.list[0] = PlanList{a.row_ptr, a.row_plan};
   p.list[1] = PlanList{a.col_ptr, a.col_plan};
@@ -420,7 +458,7 @@ extern "C" bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, con
   if (e != cudaSuccess)
     return fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaMallocAsync(%zu): %s", scratch_bytes, cudaGetErrorString(e));
   bwd_scratch_carve(&a, scratch, G, true);
-  st = run_bwd(a, s, true);
+  st = run_bwd(a, s, true, false);
   e = cudaFreeAsync(scratch, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaFreeAsync: %s", cudaGetErrorString(e));
   return st;
@@ -438,6 +476,17 @@ extern "C" bsr_status bsr_attn_check(void* stream) {
   if (v == kStatusTimeout) return fail(BSR_ERR_TIMEOUT, "a bounded device-side wait gave up");
   if (v == kStatusDeviceCheck) return fail(BSR_ERR_DEVICE_CHECK, "a device-side index check failed (block index out of range)");
   if (v != 0) return fail(BSR_ERR_CUDA, "unknown device status %d", v);
+  return BSR_OK;
+}
+
+extern "C" bsr_status bsr_set_wait_limit(uint64_t ns) {
+  int* p = status_ptr();
+  if (!p) return fail(BSR_ERR_CUDA, "bsr_set_wait_limit: no CUDA device");
+  const unsigned long long v = ns ? (unsigned long long)ns : kDefaultWaitLimitNs;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(p + 2, &v, sizeof(v), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_set_wait_limit: %s", cudaGetErrorString(e));
   return BSR_OK;
 }
 

@@ -13,10 +13,13 @@
 //
 // Limits and rules:
 //  * The array holds 2 * kNoAllocMaxRows floats plus kNoAllocPlanWords ints
-//    for the two work lists (9 MiB in all), so batch * heads * seq must not
-//    exceed 1,048,576 (e.g. 128 heads at seq 8192); larger calls are
-//    rejected with BSR_ERR_INVALID_ARG.  Every GPU that loads the library
-//    keeps the array reserved until the process exits.
+//    for the work lists (9 MiB in all), so batch * heads * seq must not
+//    exceed 1,048,576 (e.g. 128 heads at seq 8192).  fp32 operands also keep
+//    their bf16 pieces there (3 pieces of Q, K, V and dO: 24 bytes per
+//    element of Q), which caps fp32 calls near batch * heads * seq *
+//    head_dim = 390,000.  Larger calls are rejected with
+//    BSR_ERR_INVALID_ARG.  Every GPU that loads the library keeps the array
+//    reserved until the process exits.
 //  * Long block rows / columns are not split into chunks here (that needs
 //    partial-result buffers); the work is still spread longest first.
 //  * All calls share the one array.  The delta kernel overwrites every entry
@@ -25,7 +28,9 @@
 //    threads on the same device) race on the array: order them.
 //  * The device address of the array is looked up once per device, on the
 //    first call made with that device current; make that first call before
-//    any stream capture.
+//    any stream capture.  The address is kept for the life of the process:
+//    do not call this entry point after cudaDeviceReset, which destroys the
+//    primary context that the address belongs to.
 
 #include <cuda_runtime.h>
 
@@ -90,9 +95,12 @@ extern "C" bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor
   const int G = tc_grid(a.d);
   if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_attn_bwd_noalloc: cannot query the SM count");
   if (bwd_scratch_bytes(a.d, G, false) > sizeof(g_noalloc_delta))
-    return fail(BSR_ERR_INVALID_ARG, "bsr_attn_bwd_noalloc: the work lists need more than the static scratch");
+    return fail(BSR_ERR_INVALID_ARG,
+                "bsr_attn_bwd_noalloc: the work lists (and, for fp32 operands, their bf16 pieces) need more than "
+                "the static scratch of %zu bytes; use bsr_attn_bwd",
+                sizeof(g_noalloc_delta));
   float* base = nullptr;
   if ((st = noalloc_scratch(&base)) != BSR_OK) return st;
   bwd_scratch_carve(&a, base, G, false);
-  return run_bwd(a, (cudaStream_t)stream, false);
+  return run_bwd(a, (cudaStream_t)stream, false, false);
 }

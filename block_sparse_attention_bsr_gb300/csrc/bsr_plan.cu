@@ -1,0 +1,226 @@
+// Reusable plans: the work lists of one block mask built once and kept, with
+// every scratch array the forward and backward passes need, so that a call
+// on a plan launches only the attention kernels (and the backward's delta
+// pass): no planner, no allocation.  The pages build their kernels once per
+// static structure and reuse them call after call ("trnsparse 0.7.0 ->
+// 0.9.0" diff, CHANGELOG [0.8.0], static structure); here the structure is
+// data, so what is built once is the work lists over it.
+//
+// A plan owns one cudaMalloc block:
+//   copies of row_ptr, col_idx, col_ptr, row_idx (16-byte aligned each)
+//   the block-row plan (forward and dQ), two block-column plans (dK / dV;
+//     the wide kernels' dV and dK walks)
+//   the forward's split-row partial tiles and the backward's (16-bit
+//     operands, head_dim 64 / 128), or the bf16 pieces of fp32 operands
+//   delta and lse2 (one fp32 value each per query row)
+// The kernels put the plans' work-queue and arrival counters back to 0 when
+// they finish, so the lists are built once, at creation.
+
+#include <cuda_runtime.h>
+
+#include <new>
+
+#include "kernels.h"
+
+struct bsr_plan_s {
+  int device;
+  int batch, heads, seq, head_dim, dtype;
+  int nb, nnzb, G;
+  void* mem;
+  int32_t *row_ptr, *col_idx, *col_ptr, *row_idx;
+  int32_t *row_plan, *col_plan, *col_plan2;
+  float *fwd_part, *part_q, *part_kv, *delta, *lse2;
+  void* pieces;
+};
+
+namespace bsr {
+namespace {
+
+size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+bsr_status plan_matches(const bsr_plan* plan, const bsr_tensor* Q, const char* who) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(BSR_ERR_CUDA, "%s: cudaGetDevice failed", who);
+  if (dev != plan->device)
+    return fail(BSR_ERR_INVALID_ARG, "%s: the plan was built on device %d, the current device is %d", who,
+                plan->device, dev);
+  if (Q->batch != plan->batch || Q->heads != plan->heads || Q->seq != plan->seq || Q->head_dim != plan->head_dim ||
+      Q->dtype != plan->dtype)
+    return fail(BSR_ERR_INVALID_ARG,
+                "%s: operands [%d, %d, %d, %d] dtype %d differ from the plan's [%d, %d, %d, %d] dtype %d", who,
+                Q->batch, Q->heads, Q->seq, Q->head_dim, Q->dtype, plan->batch, plan->heads, plan->seq,
+                plan->head_dim, plan->dtype);
+  return BSR_OK;
+}
+
+}  // namespace
+}  // namespace bsr
+
+using namespace bsr;
+
+extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col_idx, const int32_t* col_ptr,
+                                      const int32_t* row_idx, int32_t n_brows, int32_t batch, int32_t heads,
+                                      int32_t head_dim, int32_t dtype, void* stream, bsr_plan** out) {
+  if (!out) return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: null output handle");
+  *out = nullptr;
+  if (!row_ptr || !col_idx || !col_ptr || !row_idx)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: null structure array");
+  if (n_brows < 1 || batch < 1 || heads < 1 || (long long)n_brows * 128 > (1LL << 30) ||
+      (long long)batch * heads > (1LL << 30))
+    return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: sizes n_brows %d, batch %d, heads %d", n_brows, batch, heads);
+  if (dtype != BSR_F32 && dtype != BSR_BF16 && dtype != BSR_F16)
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_plan_create: dtype %d not supported", dtype);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256 && head_dim != 512)
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_plan_create: head_dim %d not supported (64, 128, 256 or 512)", head_dim);
+  Dims d{};
+  d.BH = batch * heads;
+  d.S = n_brows * 128;
+  d.D = head_dim;
+  d.nb = n_brows;
+  d.dtype = dtype;
+  d.scale = 1.f;
+  if (!tc_bwd_supported(d) && !wide_supported(d))
+    return fail(BSR_ERR_UNSUPPORTED, "bsr_plan_create: dtype %d with head_dim %d", dtype, head_dim);
+  int* status = status_ptr();
+  if (!status) return fail(BSR_ERR_CUDA, "bsr_plan_create: no CUDA device");
+  const int G = tc_grid(d);
+  if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_plan_create: cannot query the SM count");
+  cudaStream_t s = (cudaStream_t)stream;
+  // the number of stored blocks, from both pointer arrays
+  int32_t ends[2] = {-1, -1};
+  cudaError_t e = cudaMemcpyAsync(&ends[0], row_ptr + n_brows, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&ends[1], col_ptr + n_brows, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_plan_create: reading nnzb: %s", cudaGetErrorString(e));
+  const int nnzb = ends[0];
+  if (nnzb < 0 || (long long)nnzb > (long long)n_brows * n_brows || ends[1] != nnzb)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: row_ptr[n_brows] = %d and col_ptr[n_brows] = %d", ends[0],
+                ends[1]);
+
+  const bool tc = tc_bwd_supported(d);  // 16-bit operands, head_dim 64 / 128: split lines, partial tiles
+  const size_t pw = plan_words(d.nb, G, d.BH);
+  const size_t tiles = plan_tiles(d.nb, G, d.BH);
+  const size_t rows = (size_t)d.BH * d.S;
+  const size_t ptr_b = align16(sizeof(int32_t) * (n_brows + 1));
+  const size_t idx_b = align16(sizeof(int32_t) * (nnzb > 0 ? nnzb : 1));
+  const size_t plans_b = 3 * sizeof(int32_t) * pw;  // a multiple of 16 (plan_words is a multiple of 4)
+  const size_t fpart_b = tc ? align16(fwd_part_bytes(d.D) * tiles) : 0;
+  const size_t bpart_b = tc ? 3 * sizeof(float) * (size_t)128 * d.D * tiles : 0;
+  const size_t stat_b = 2 * align16(sizeof(float) * rows);
+  const size_t piece_b = wide_piece_bytes(d, 4);
+  const size_t total = 2 * ptr_b + 2 * idx_b + plans_b + fpart_b + bpart_b + stat_b + piece_b;
+
+  bsr_plan* p = new (std::nothrow) bsr_plan();
+  if (!p) return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: out of host memory");
+  if ((e = cudaGetDevice(&p->device)) != cudaSuccess || (e = cudaMalloc(&p->mem, total)) != cudaSuccess) {
+    delete p;
+    return fail(BSR_ERR_CUDA, "bsr_plan_create: cudaMalloc(%zu): %s", total, cudaGetErrorString(e));
+  }
+  p->batch = batch;
+  p->heads = heads;
+  p->seq = d.S;
+  p->head_dim = head_dim;
+  p->dtype = dtype;
+  p->nb = n_brows;
+  p->nnzb = nnzb;
+  p->G = G;
+  char* c = (char*)p->mem;
+  p->row_ptr = (int32_t*)c;
+  c += ptr_b;
+  p->col_ptr = (int32_t*)c;
+  c += ptr_b;
+  p->col_idx = (int32_t*)c;
+  c += idx_b;
+  p->row_idx = (int32_t*)c;
+  c += idx_b;
+  p->row_plan = (int32_t*)c;
+  p->col_plan = p->row_plan + pw;
+  p->col_plan2 = p->col_plan + pw;
+  c += plans_b;
+  p->fwd_part = tc ? (float*)c : nullptr;
+  c += fpart_b;
+  p->part_q = tc ? (float*)c : nullptr;
+  p->part_kv = tc ? (float*)c + (size_t)128 * d.D * tiles : nullptr;
+  c += bpart_b;
+  p->delta = (float*)c;
+  p->lse2 = (float*)(c + align16(sizeof(float) * rows));
+  c += stat_b;
+  p->pieces = piece_b ? (void*)c : nullptr;
+
+  e = cudaMemcpyAsync(p->row_ptr, row_ptr, sizeof(int32_t) * (n_brows + 1), cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(p->col_ptr, col_ptr, sizeof(int32_t) * (n_brows + 1), cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && nnzb > 0)
+    e = cudaMemcpyAsync(p->col_idx, col_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && nnzb > 0)
+    e = cudaMemcpyAsync(p->row_idx, row_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) {
+    cudaFree(p->mem);
+    delete p;
+    return fail(BSR_ERR_CUDA, "bsr_plan_create: copying the structure: %s", cudaGetErrorString(e));
+  }
+  PlanArgs pa{};
+  pa.list[0] = PlanList{p->row_ptr, p->row_plan};
+  pa.list[1] = PlanList{p->col_ptr, p->col_plan};
+  pa.list[2] = PlanList{p->col_ptr, p->col_plan2};
+  pa.n = d.nb;
+  pa.G = G;
+  pa.BH = d.BH;
+  pa.allow_split = tc ? 1 : 0;
+  pa.status = status;
+  bsr_status st = launch_plan(pa, 3, s);
+  if (st != BSR_OK) {
+    cudaStreamSynchronize(s);
+    cudaFree(p->mem);
+    delete p;
+    return st;
+  }
+  *out = p;
+  return BSR_OK;
+}
+
+extern "C" bsr_status bsr_plan_destroy(bsr_plan* plan) {
+  if (!plan) return BSR_OK;
+  const cudaError_t e = cudaFree(plan->mem);
+  delete plan;
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_plan_destroy: cudaFree: %s", cudaGetErrorString(e));
+  return BSR_OK;
+}
+
+extern "C" bsr_status bsr_attn_fwd_plan(const bsr_plan* plan, const bsr_tensor* Q, const bsr_tensor* K,
+                                        const bsr_tensor* V, float scale, bsr_tensor* O, float* row_max,
+                                        float* row_denom, void* stream) {
+  if (!plan) return fail(BSR_ERR_INVALID_ARG, "bsr_attn_fwd_plan: null plan");
+  FwdArgs a{};
+  bsr_status st = build_fwd_args(Q, K, V, plan->row_ptr, plan->col_idx, plan->nb, 128, scale, O, row_max, row_denom,
+                                 false, &a);
+  if (st != BSR_OK) return st;
+  if ((st = plan_matches(plan, Q, "bsr_attn_fwd_plan")) != BSR_OK) return st;
+  if (a.G != plan->G) return fail(BSR_ERR_INVALID_ARG, "bsr_attn_fwd_plan: the plan was built for another grid");
+  a.plan = plan->row_plan;
+  a.part = plan->fwd_part;
+  a.pieces = plan->pieces;
+  return run_fwd(a, (cudaStream_t)stream, false, true);
+}
+
+extern "C" bsr_status bsr_attn_bwd_plan(const bsr_plan* plan, const bsr_tensor* Q, const bsr_tensor* K,
+                                        const bsr_tensor* V, const bsr_tensor* O, const bsr_tensor* dO,
+                                        const float* row_max, const float* row_denom, float scale, bsr_tensor* dQ,
+                                        bsr_tensor* dK, bsr_tensor* dV, void* stream) {
+  if (!plan) return fail(BSR_ERR_INVALID_ARG, "bsr_attn_bwd_plan: null plan");
+  BwdArgs a{};
+  bsr_status st = build_bwd_args(Q, K, V, O, dO, row_max, row_denom, plan->row_ptr, plan->col_idx, plan->col_ptr,
+                                 plan->row_idx, scale, dQ, dK, dV, &a);
+  if (st != BSR_OK) return st;
+  if ((st = plan_matches(plan, Q, "bsr_attn_bwd_plan")) != BSR_OK) return st;
+  if (tc_grid(a.d) != plan->G) return fail(BSR_ERR_INVALID_ARG, "bsr_attn_bwd_plan: the plan was built for another grid");
+  a.delta = plan->delta;
+  a.lse2 = plan->lse2;
+  a.row_plan = plan->row_plan;
+  a.col_plan = plan->col_plan;
+  a.col_plan2 = plan->col_plan2;
+  a.part_q = plan->part_q;
+  a.part_kv = plan->part_kv;
+  a.pieces = plan->pieces;
+  return run_bwd(a, (cudaStream_t)stream, true, true);
+}

@@ -10,6 +10,7 @@
 
 #include "delta.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace bsr {
 namespace {
@@ -18,6 +19,8 @@ constexpr int kThreads = 256;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) delta_kernel(BwdArgs a) {
+  sm100::griddep_wait();  // may run as a programmatic dependent of the forward
+  sm100::griddep_launch_dependents();
   delta_pass<T, D, kThreads>(a, blockIdx.x, gridDim.x);
 }
 
@@ -35,7 +38,8 @@ bsr_status delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   const size_t resident = sms > 0 ? sms * per_sm : groups;
   const dim3 grid((unsigned)(groups < resident ? groups : resident));
   LaunchTimer timer("delta", s);
-  delta_kernel<T, D><<<grid, kThreads, 0, s>>>(a);
+  const cudaError_t e = launch_dependent(delta_kernel<T, D>, grid, dim3(kThreads), 0, s, a);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "delta launch: %s", cudaGetErrorString(e));
   return check_launch("delta launch");
 }
 

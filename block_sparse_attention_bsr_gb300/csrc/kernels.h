@@ -76,7 +76,12 @@ struct PlanItem {
 };
 
 // Layout of one plan in device scratch (int32 units, 16-byte aligned base):
-//   header[4]                  items, work-queue counter, split lines, buckets
+//   header[8]                  items, work-queue counter, split lines, buckets,
+//                              CTAs that finished the current launch, pad
+//                              (the kernels leave the work-queue counter, the
+//                              exit count and every arrival counter at 0 when
+//                              they finish, so a plan can be reused launch
+//                              after launch without running the planner again)
 //   items[cap_items]           PlanItem, longest first
 //   buckets[cap_buckets]       PlanBucket, one per item length, longest first
 //   slot_line[cap_slots]       split line of each partial slot
@@ -112,7 +117,7 @@ __host__ __device__ inline void plan_caps(int n, int G, int BH, int* items, int*
 __host__ __device__ inline size_t plan_words(int n, int G, int BH) {
   int ci, cs, cl;
   plan_caps(n, G, BH, &ci, &cs, &cl);
-  size_t w = 4 + 4 * (size_t)ci + 4 * (size_t)(n + 1) + cs + 2 * (size_t)cl + 2 * (size_t)cl * BH;
+  size_t w = 8 + 4 * (size_t)ci + 4 * (size_t)(n + 1) + cs + 2 * (size_t)cl + 2 * (size_t)cl * BH;
   return (w + 3) & ~(size_t)3;
 }
 
@@ -121,8 +126,8 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t* base, int n, int G, i
   plan_caps(n, G, BH, &l.cap_items, &l.cap_slots, &l.cap_lines);
   l.cap_buckets = n + 1;
   l.header = base;
-  l.items = (PlanItem*)(base + 4);
-  l.buckets = (PlanBucket*)(base + 4 + 4 * (size_t)l.cap_items);
+  l.items = (PlanItem*)(base + 8);
+  l.buckets = (PlanBucket*)(base + 8 + 4 * (size_t)l.cap_items);
   l.slot_line = (int32_t*)(l.buckets + l.cap_buckets);
   l.line_base = l.slot_line + l.cap_slots;
   l.line_chunks = l.line_base + l.cap_lines;
@@ -208,8 +213,21 @@ bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
 size_t bwd_scratch_bytes(const Dims& d, int G, bool split);
 // Carves a scratch block of bwd_scratch_bytes at `base` into a's arrays.
 void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split);
-// Launches delta, plan, dQ and dK/dV on `s` (scratch carved already).
-bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split);
+// Launches delta, plan (unless `planned`: the plans in a are built), dQ and
+// dK/dV on `s` (scratch carved already).
+bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned);
+
+// The forward's argument checks, scratch (its plan, the split rows' partial
+// results or the fp32 pieces) and launches (the planner unless `planned`).
+bsr_status build_fwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V, const int32_t* row_ptr,
+                          const int32_t* col_idx, int32_t n_brows, int32_t block, float scale, bsr_tensor* O,
+                          float* row_max, float* row_denom, bool two_pass, FwdArgs* out);
+size_t fwd_scratch_bytes(const Dims& d, int G);
+void fwd_scratch_carve(FwdArgs* a, void* base);
+bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned);
+
+// The device status block of the current device (see sm100.cuh wait_limit_ns).
+int* status_ptr();
 
 // A second stream of the current device with a fork / join event pair.
 // The fork and join must happen while *hold is held (calls from several host

@@ -189,6 +189,8 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
     lay.header[0] = items;
     lay.header[1] = 0;  // work-queue counter
     lay.header[2] = nsl;
+    lay.header[4] = 0;  // CTAs finished
+    lay.header[5] = lay.header[6] = lay.header[7] = 0;
   }
 }
 

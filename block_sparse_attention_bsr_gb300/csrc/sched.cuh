@@ -121,13 +121,31 @@ __device__ __forceinline__ bool merge_arrive(const PlanLayout& lay, int slot, in
   if (!group_sync(bar, phase, abort_flag, status)) return false;
   if (r == 0) {
     const int sl = lay.slot_line[slot];
-    const int old = atomicAdd(&lay.counters[(sl * BH + bh) * 2 + hg], 1);
-    *flag = (old == lay.line_chunks[sl] - 1) ? 1 : 0;
+    int* ctr = &lay.counters[(sl * BH + bh) * 2 + hg];
+    const int old = atomicAdd(ctr, 1);
+    const bool is_last = old == lay.line_chunks[sl] - 1;
+    // the last arrival leaves the counter at 0 for the plan's next launch
+    if (is_last) atomicExch(ctr, 0);
+    *flag = is_last ? 1 : 0;
   }
   if (!group_sync(bar, phase, abort_flag, status)) return false;
   *last = *flag != 0;
   if (*last) __threadfence();
   return true;
+}
+
+// Called by one thread of every CTA after the CTA's last use of the plan
+// (after its final __syncthreads): the last CTA of the launch to finish
+// puts the work-queue counter and the exit count back to 0, so the next
+// launch on the same plan starts from a clean queue (every CTA has drawn its
+// last work index before it counts itself out).
+__device__ __forceinline__ void plan_exit(const PlanLayout& lay) {
+  __threadfence();
+  if (atomicAdd(&lay.header[4], 1) == (int)gridDim.x - 1) {
+    atomicExch(&lay.header[1], 0);
+    atomicExch(&lay.header[4], 0);
+    __threadfence();
+  }
 }
 
 // Reads 4 floats of another CTA's partial result (L2, bypassing L1).

@@ -68,18 +68,28 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The device status block every kernel receives as `status`: word 0 is the
+// status word (kStatusTimeout / kStatusDeviceCheck, read and cleared by the
+// host), words 2..3 the limit of the bounded waits in nanoseconds (64-bit,
+// default 2 s; the host lowers it only to test the give-up path).
+__device__ __forceinline__ uint64_t wait_limit_ns(const int* status) {
+  return *(const volatile unsigned long long*)(status + 2);
+}
+
 // Waits until the phase of `bar` with the given parity has completed.  Gives
-// up after `timeout_ns` of wall time; on give-up it records kStatusTimeout in
-// *status, raises the CTA's abort flag and returns false.  Once the abort flag
-// is up every later wait returns false immediately.
+// up after `timeout_ns` of wall time (0: the status block's limit); on
+// give-up it records kStatusTimeout in *status, raises the CTA's abort flag
+// and returns false.  Once the abort flag is up every later wait returns
+// false immediately.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                          uint64_t timeout_ns = 2000000000ull) {
+                                          uint64_t timeout_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = timeout_ns ? timeout_ns : wait_limit_ns(status);
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > timeout_ns) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort_flag = 1;
       atomicExch(status, 4 /* BSR_ERR_TIMEOUT */);
       return false;

@@ -497,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0) plan_exit(lay);
 }
 
 // ================================================================ dK/dV ====
@@ -936,6 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0) plan_exit(lay);
 }
 
 // dQ and dK / dV read the same inputs and write different outputs, so they

@@ -633,6 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0) plan_exit(lay);
 }
 
 template <typename T, int D, int kPass>

@@ -823,6 +823,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0) plan_exit(lay);
 }
 
 // fp32 -> three bf16 pieces, x = x0 + x1 + x2 (see the file comment), for

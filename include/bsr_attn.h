@@ -192,11 +192,15 @@ bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tens
  * memory (9 MiB per GPU that loads the library, held until the process
  * exits) instead of cudaMallocAsync.  Long block rows / columns are not
  * split into chunks on this path (that would need partial-result buffers).
- * Limits: batch * heads * seq <= 1,048,576, else BSR_ERR_INVALID_ARG.
+ * Limits: batch * heads * seq <= 1,048,576; for fp32 operands, whose bf16
+ * pieces (24 bytes per element of Q) share the array, also batch * heads *
+ * seq * head_dim up to about 390,000; beyond that BSR_ERR_INVALID_ARG.
  * All calls share the array: calls whose kernels overlap on the GPU race, so
  * order them on one stream.  The first call on a device (with that device
  * current) looks up the array's device address; make it before any stream
- * capture.
+ * capture.  That address is kept for the rest of the process, so this entry
+ * point must not be called after cudaDeviceReset has destroyed the device's
+ * primary context (the array would move, the kept address would not).
  */
 bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* V,
                                 const bsr_tensor* O, const bsr_tensor* dO,
@@ -205,6 +209,54 @@ bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor* K, const 
                                 const int32_t* col_ptr, const int32_t* row_idx,
                                 float scale,
                                 bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream);
+
+/*
+ * Reusable plans.  A plan holds, for one block mask and one operand shape,
+ * the work lists of the forward / dQ walk and of the dK / dV walk, built
+ * once, plus every scratch array the passes need (split-row partial
+ * results, the fp32 operands' bf16 pieces, delta and lse2): a call on a plan
+ * launches only the attention kernels and the backward's delta pass, with
+ * no planner and no allocation.  This follows the pages' static-structure
+ * design ("trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.8.0]: kernels built
+ * once per structure and reused) with the structure kept as data.
+ *
+ * bsr_plan_create: row_ptr [n_brows+1], col_idx [nnzb], col_ptr [n_brows+1]
+ *   and row_idx [nnzb] are int32 DEVICE arrays (the BSR lists and their BSC
+ *   transpose from bsr_build_bsc; the grid is square, n_bcols = n_brows);
+ *   the plan copies them, so the caller may free or change them afterwards.
+ *   batch, heads, head_dim and dtype fix the operand shape [batch, heads,
+ *   n_brows * 128, head_dim] the plan serves.  The call reads nnzb from the
+ *   device (it synchronises `stream`), allocates the plan's device memory
+ *   with cudaMalloc on the current device and builds the lists on `stream`;
+ *   use the plan on that stream (or synchronise first).  *out receives the
+ *   handle (NULL on failure).  Errors: BSR_ERR_INVALID_ARG for null
+ *   pointers, bad sizes or row_ptr / col_ptr whose last entries disagree;
+ *   BSR_ERR_UNSUPPORTED for a head_dim / dtype outside the supported set;
+ *   BSR_ERR_CUDA when an allocation or copy fails.
+ * bsr_plan_destroy: frees the plan (cudaFree: synchronises the device).
+ *   NULL is accepted.
+ * bsr_attn_fwd_plan / bsr_attn_bwd_plan: the same computations and the same
+ *   argument meaning as bsr_attn_fwd / bsr_attn_bwd, with the structure taken
+ *   from the plan.  The operands must have the plan's shape and dtype and the
+ *   current device must be the plan's (BSR_ERR_INVALID_ARG otherwise).
+ *   Calls on one plan share its scratch: order them on one stream (calls on
+ *   different plans are independent).  After BSR_ERR_TIMEOUT from
+ *   bsr_attn_check the plan's work counters may be left mid-launch: destroy
+ *   the plan and build it again.
+ */
+typedef struct bsr_plan_s bsr_plan;
+
+bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col_idx, const int32_t* col_ptr,
+                           const int32_t* row_idx, int32_t n_brows, int32_t batch, int32_t heads,
+                           int32_t head_dim, int32_t dtype, void* stream, bsr_plan** out);
+bsr_status bsr_plan_destroy(bsr_plan* plan);
+bsr_status bsr_attn_fwd_plan(const bsr_plan* plan, const bsr_tensor* Q, const bsr_tensor* K,
+                             const bsr_tensor* V, float scale, bsr_tensor* O, float* row_max,
+                             float* row_denom, void* stream);
+bsr_status bsr_attn_bwd_plan(const bsr_plan* plan, const bsr_tensor* Q, const bsr_tensor* K,
+                             const bsr_tensor* V, const bsr_tensor* O, const bsr_tensor* dO,
+                             const float* row_max, const float* row_denom, float scale,
+                             bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream);
 
 /*
  * Host helper: BSC transpose of a BSR block structure ("trnsparse 0.4.1 ->
@@ -233,6 +285,20 @@ bsr_status bsr_validate(const int32_t* row_ptr_h, const int32_t* col_idx_h,
  * bounds check fails (BSR_ERR_DEVICE_CHECK).  BSR_OK when neither happened.
  */
 bsr_status bsr_attn_check(void* stream);
+
+/*
+ * Limit of the kernels' bounded device-side waits on the current device, in
+ * nanoseconds (0 restores the default of 2 s).  No passage of the pages
+ * defines it: every wait inside the kernels (pipeline barriers between the
+ * copy, MMA and elementwise roles) gives up after this much wall time, the
+ * kernel then drains its copies and MMAs, frees its tensor memory, returns,
+ * and bsr_attn_check reports BSR_ERR_TIMEOUT.  Lowering the limit to a few
+ * hundred nanoseconds makes those waits expire on purpose, which is how the
+ * give-up path is tested; results of calls made under such a limit are
+ * undefined.  The call synchronises the device before and after it changes
+ * the limit; make it while no call of this library is in flight.
+ */
+bsr_status bsr_set_wait_limit(uint64_t ns);
 
 /* Message for the last non-OK status returned on the calling thread. */
 const char* bsr_last_error(void);

@@ -45,3 +45,22 @@ def test_forward_refuses_unsupported_dtype():
     q = torch.zeros(1, 1, 256, 64, dtype=torch.float64)
     with pytest.raises(TypeError):
         bsr.bsr_attn_fwd(q, q, q, None, None, 2, 128, 0.125, q, None, None)
+
+
+def test_custom_op_pair_is_registered_with_fake_implementations():
+    # torch.ops.bsr.bsr_attn / bsr_attn_bwd exist with their schemas, and
+    # their fake implementations give the output shapes and dtypes graph
+    # tracing needs (no kernel runs under FakeTensorMode).
+    from torch._subclasses.fake_tensor import FakeTensorMode
+
+    ops = bsr.register_ops()
+    assert "float scale" in str(ops.bsr_attn.default._schema)
+    assert "Tensor dO" in str(ops.bsr_attn_bwd.default._schema)
+    with FakeTensorMode():
+        q = torch.empty(2, 3, 256, 64, dtype=torch.bfloat16)
+        i = torch.empty(3, dtype=torch.int32)
+        O, rm, rd = ops.bsr_attn(q, q, q, i, i, i, i, 0.125)
+        assert O.shape == q.shape and O.dtype == q.dtype
+        assert rm.shape == (2, 3, 256) and rm.dtype == torch.float32 and rd.shape == rm.shape
+        dq, dk, dv = ops.bsr_attn_bwd(q, q, q, O, O, rm, rd, i, i, i, i, 0.125)
+        assert dq.shape == dk.shape == dv.shape == q.shape and dq.dtype == q.dtype
