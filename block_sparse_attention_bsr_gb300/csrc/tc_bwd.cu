@@ -198,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dS (bf16) of block g at column 384 + 64 (g % 2): two buffers, so the
   // elementwise pass of block g waits only for dQ of block g - 2
   constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
+  static_assert(kColDQ + D <= kColDS && kColDS + 2 * 64 <= kTmemCols, "TMEM columns over the allocation");
+  static_assert(C::kSmem <= 232448, "shared memory over the per-CTA limit");
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
@@ -571,6 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // columns each warpgroup has read: queries [0, 64) at column +0, queries
   // [64, 128) at column +64.
   constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
+  static_assert(kColDK + D <= kTmemCols, "TMEM columns over the allocation");
+  static_assert(C::kSmem <= 232448, "shared memory over the per-CTA limit");
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;

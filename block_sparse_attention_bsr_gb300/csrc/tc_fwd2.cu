@@ -90,6 +90,9 @@ struct Fwd2Cfg {
   // time); with head_dim 128 the tiles take almost all of the 227 KB, so no
   // alignment slack is kept.
   static constexpr int kSmem = kBarOff + 512;
+  static_assert(kSmem <= 232448, "shared memory over the per-CTA limit");
+  // TMEM: S (128 columns), two P buffers of 64, O_0 and O_1 (D each)
+  static_assert(kColP + 2 * 64 <= kColO && kColO + 2 * D <= kTmemCols, "TMEM columns over the allocation");
 };
 
 struct Bars {

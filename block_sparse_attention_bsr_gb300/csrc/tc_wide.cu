@@ -81,12 +81,13 @@ constexpr int kMaxRing = 12;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: the stale max may lag by 2^8
+constexpr int kMinRing = 4;  // ring slots a layout must leave to be preferred
 
 // Which operands stay resident for a whole item: 2 = the row operand R1 (and
 // R2 when the mode has a second score contraction), 1 = R1 only, 0 = none;
 // the first choice whose leftover ring holds two chunk groups (one group =
-// the streamed pieces of one 64-column chunk of a contraction), else the
-// first that holds one.
+// the streamed pieces of one 64-column chunk of a contraction) and at least
+// kMinRing slots, else the first that holds one group.
 constexpr int wide_residency(int NP, int KC, int WC, bool x2) {
   const int C = NP * WC * kChunk, R = NP * KC * kChunk;
   for (int strict = 1; strict >= 0; --strict) {
@@ -99,7 +100,7 @@ constexpr int wide_residency(int NP, int KC, int WC, bool x2) {
       const int g1 = (opt >= 1 ? 0 : NP) + NP;
       const int g2 = x2 ? ((opt == 2 ? 0 : NP) + NP) : 0;
       const int g = g1 > g2 ? g1 : g2;
-      if (ring >= (strict ? 2 * g : g)) return opt;
+      if (ring >= (strict ? (2 * g > kMinRing ? 2 * g : kMinRing) : g)) return opt;
     }
   }
   return -1;
