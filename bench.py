@@ -454,6 +454,18 @@ def median_call_ms(fn, args, l2, stream, dev):
     return statistics.median(a.elapsed_time(b) for a, b in ev)
 
 
+def one_call_kernels(fn, dev):
+    """{kernel: us} of one call with per-launch timing on."""
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    bsr.profile_collect()
+    bsr.profile_enable(True)
+    fn()
+    torch.cuda.synchronize(dev)
+    bsr.profile_enable(False)
+    return {k: round(t * 1e3 / n, 2) for k, (n, t) in bsr.profile_collect().items()}
+
+
 def run_spmm_sweep(args, dev):
     """bsr_spmm on an 8192 x 8192 BSR matrix (64 x 64 blocks of 128) times 8192 x width, bf16, one JSON
     line per block density, beside dense torch.matmul of the same operands on the same GPU."""
@@ -465,8 +477,13 @@ def run_spmm_sweep(args, dev):
     def timed(fn):
         return median_call_ms(fn, args, l2, stream, dev)
 
-    for p in SPMM_DENSITIES:
+    cases = [(p, None) for p in SPMM_DENSITIES] + [(0.05, "rows 0-3 full")]
+    for p, skew in cases:
         bm, blocks, X = inputs.make_spmm(64, 64, args.width, p, "bf16", seed=0)
+        if skew:  # a few dense block rows among sparse ones: the longest row bounds a one-CTA-per-row walk
+            g = torch.Generator().manual_seed(7)
+            bm[:4, :] = True
+            blocks = torch.randn(int(bm.sum()), BLOCK, BLOCK, generator=g).to(torch.bfloat16)
         rp, ci = inputs.bsr_from_block_mask(bm)
         nnzb = int(bm.sum())
         blocks_d, X_d = blocks.to(dev), X.to(dev)
@@ -479,13 +496,15 @@ def run_spmm_sweep(args, dev):
             A[m * BLOCK:(m + 1) * BLOCK, k * BLOCK:(k + 1) * BLOCK] = blocks_d[j]
         ms = timed(lambda: bsr.bsr_spmm(blocks_d, rp_d, ci_d, 64, 64, X_d, Y, stream))
         bsr.bsr_attn_check()
+        kern = one_call_kernels(lambda: bsr.bsr_spmm(blocks_d, rp_d, ci_d, 64, 64, X_d, Y, stream), dev)
         dense_ms = timed(lambda: torch.matmul(A, X_d))
         flops = 2 * BLOCK * BLOCK * args.width * nnzb
         print(json.dumps({"op": "bsr_spmm", "metric": "ms per Y = A X, 8192 x 8192 BSR (blocks of 128) x 8192 x width",
-                          "density": round(nnzb / 64 ** 2, 4), "nnzb": nnzb, "width": args.width, "dtype": "bf16",
+                          "density": round(nnzb / 64 ** 2, 4), "nnzb": nnzb, "structure": skew or "iid blocks", "width": args.width, "dtype": "bf16",
                           "ms": round(ms, 4), "dense_matmul_ms": round(dense_ms, 4),
                           "speedup_vs_dense": round(dense_ms / ms, 3),
                           "tflops_over_stored_blocks": round(flops / (ms * 1e-3) / 1e12, 2),
+                          "kernel_us_one_call": kern,
                           "steps": args.steps, "warmup": args.warmup, "l2": "flushed before every call",
                           "data": "synthetic"}), flush=True)
 
@@ -515,13 +534,15 @@ def run_screen_sweep(args, dev):
         maskb = mask.to(torch.bfloat16)
         ms = timed(lambda: bsr.bsr_screened_spmm(A, diag, B, thr, C, stream))
         bsr.bsr_attn_check()
+        kern = one_call_kernels(lambda: bsr.bsr_screened_spmm(A, diag, B, thr, C, stream), dev)
         unfused_ms = timed(lambda: torch.matmul(A * maskb, B))
         dense_ms = timed(lambda: torch.matmul(A, B))
         print(json.dumps({"op": "bsr_screened_spmm", "metric": "ms per C = (A o M) B, n = 8192, B 8192 x width",
                           "threshold": thr, "kept_fraction": round(kept, 4), "width": args.width, "dtype": "bf16",
                           "ms": round(ms, 4), "unfused_masked_matmul_ms": round(unfused_ms, 4),
                           "dense_matmul_ms": round(dense_ms, 4),
-                          "speedup_vs_unfused": round(unfused_ms / ms, 3), "steps": args.steps,
+                          "speedup_vs_unfused": round(unfused_ms / ms, 3), "kernel_us_one_call": kern,
+                          "steps": args.steps,
                           "warmup": args.warmup, "l2": "flushed before every call", "data": "synthetic"}),
               flush=True)
 

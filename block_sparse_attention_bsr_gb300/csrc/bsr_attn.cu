@@ -307,7 +307,18 @@ extern "C" bsr_status bsr_spmm(const void* blocks, int32_t dtype, const int32_t*
     return fail(BSR_ERR_INVALID_ARG, "bsr_spmm: null pointer");
   if ((((uintptr_t)Y) | ((uintptr_t)X) | ((uintptr_t)blocks)) & 15)
     return fail(BSR_ERR_INVALID_ARG, "bsr_spmm: data pointer is not 16-byte aligned");
-  SpmmArgs a{blocks, X, Y, row_ptr, col_idx, n_brows, n_bcols, nnzb, n_cols, dtype, status_ptr()};
+  SpmmArgs a{};
+  a.A = blocks;
+  a.X = X;
+  a.Y = Y;
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.n_brows = n_brows;
+  a.n_bcols = n_bcols;
+  a.nnzb = nnzb;
+  a.n_cols = n_cols;
+  a.dtype = dtype;
+  a.status = status_ptr();
   if (!a.status) return fail(BSR_ERR_CUDA, "bsr_spmm: no CUDA device");
   cudaStream_t s = (cudaStream_t)stream;
   if (nnzb == 0) {  // no stored block: Y = 0

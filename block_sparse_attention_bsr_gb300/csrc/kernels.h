@@ -107,24 +107,30 @@ struct PlanLayout {
   int cap_items, cap_slots, cap_lines, cap_buckets;
 };
 
-__host__ __device__ inline void plan_caps(int n, int G, int BH, int* items, int* slots, int* lines) {
-  *items = n + 2 * G + 2;
-  *slots = 2 * G / BH + 2;
-  *lines = G / BH + 2;
+// max_len: the longest possible line (0: n, the square grids of attention,
+// where no line is ever longer than the n blocks a chunk may hold).  With
+// longer lines (an SpMM with more block columns than rows) chunks are capped
+// at n blocks, which may need up to max_len + n slots and n split lines.
+__host__ __device__ inline void plan_caps(int n, int G, int BH, int* items, int* slots, int* lines, int max_len = 0) {
+  const bool wide = max_len > n;
+  *items = n + 2 * G + 2 + (wide ? max_len + n : 0);
+  *slots = 2 * G / BH + 2 + (wide ? max_len + n : 0);
+  *lines = G / BH + 2 + (wide ? n : 0);
 }
 
 // int32 words one plan occupies (a multiple of 4).
-__host__ __device__ inline size_t plan_words(int n, int G, int BH) {
+__host__ __device__ inline size_t plan_words(int n, int G, int BH, int max_len = 0) {
   int ci, cs, cl;
-  plan_caps(n, G, BH, &ci, &cs, &cl);
-  size_t w = 8 + 4 * (size_t)ci + 4 * (size_t)(n + 1) + cs + 2 * (size_t)cl + 2 * (size_t)cl * BH;
+  plan_caps(n, G, BH, &ci, &cs, &cl, max_len);
+  const int nl = max_len > n ? max_len : n;  // distinct chunk lengths
+  size_t w = 8 + 4 * (size_t)ci + 4 * (size_t)(nl + 1) + cs + 2 * (size_t)cl + 2 * (size_t)cl * BH;
   return (w + 3) & ~(size_t)3;
 }
 
-__host__ __device__ inline PlanLayout plan_layout(int32_t* base, int n, int G, int BH) {
+__host__ __device__ inline PlanLayout plan_layout(int32_t* base, int n, int G, int BH, int max_len = 0) {
   PlanLayout l;
-  plan_caps(n, G, BH, &l.cap_items, &l.cap_slots, &l.cap_lines);
-  l.cap_buckets = n + 1;
+  plan_caps(n, G, BH, &l.cap_items, &l.cap_slots, &l.cap_lines, max_len);
+  l.cap_buckets = (max_len > n ? max_len : n) + 1;
   l.header = base;
   l.items = (PlanItem*)(base + 8);
   l.buckets = (PlanBucket*)(base + 8 + 4 * (size_t)l.cap_items);
@@ -136,9 +142,9 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t* base, int n, int G, i
 }
 
 // Partial-result tiles a split plan may need: cap_slots * BH.
-__host__ __device__ inline size_t plan_tiles(int n, int G, int BH) {
+__host__ __device__ inline size_t plan_tiles(int n, int G, int BH, int max_len = 0) {
   int ci, cs, cl;
-  plan_caps(n, G, BH, &ci, &cs, &cl);
+  plan_caps(n, G, BH, &ci, &cs, &cl, max_len);
   return (size_t)cs * BH;
 }
 
@@ -150,6 +156,7 @@ struct PlanList {
 struct PlanArgs {
   PlanList list[3];
   int n;            // lines per list (block rows = block columns)
+  int max_len;      // longest possible line (blocks per line; 0: n, the square grids of attention)
   int G;            // persistent CTAs of the kernels that read the plan
   int BH;
   int allow_split;  // 0: every line is one item (no partial results)
@@ -267,9 +274,10 @@ bsr_status launch_fwd_wide(const FwdArgs& a, cudaStream_t s);
 // dQ on the row plan, dV on col_plan, dK on col_plan2, after launch_delta.
 bsr_status launch_bwd_wide(const BwdArgs& a, cudaStream_t s);
 
-// Y = A X for a BSR matrix A of 128 x 128 blocks (tc_spmm.cu).
+// Y = A X for a BSR matrix A of 128 x 128 blocks, and the walk of the
+// screened product over its kept tiles (tc_spmm.cu).
 struct SpmmArgs {
-  const void* A;            // stored blocks, [nnzb][128][128] row-major
+  const void* A;            // stored blocks, [nnzb][128][128] row-major (screened: the dense [n][n] A)
   const void* X;            // [n_bcols * 128][n_cols] row-major
   void* Y;                  // [n_brows * 128][n_cols] row-major
   const int32_t* row_ptr;   // [n_brows + 1]
@@ -277,8 +285,29 @@ struct SpmmArgs {
   int n_brows, n_bcols, nnzb, n_cols;
   int dtype;                // BSR_BF16 or BSR_F16
   int* status;
+  int32_t* plan;            // set by the launcher: the rows' work list (column tiles as heads)
+  float* part;              // set by the launcher: partial products of split rows
+  const int32_t* cls;       // screened: per listed tile, 1 = kept whole, 2 = masked element by element
+  const float* diag;        // screened: the bounds' diagonal
+  float t;                  // screened: sqrt(threshold)
 };
 bsr_status launch_spmm_tc(const SpmmArgs& a, cudaStream_t s);
+
+// The screened product's tile list (plan.cu): every 128 x 128 tile (m, k) of
+// A classified by the least and largest bound q = sqrt(|diag|) of its rows
+// and columns (skipped, kept whole, masked element by element), the kept
+// tiles of each block row listed in BSR form with their class.
+enum : int { kTileSkip = 0, kTileFull = 1, kTilePartial = 2, kScreenMaxBlocks = 512 };
+struct ScreenListArgs {
+  const float* diag;
+  int nb;            // n / 128 <= kScreenMaxBlocks
+  float t;           // sqrt(threshold)
+  int32_t* row_ptr;  // [nb + 1]
+  int32_t* col_idx;  // [nb * nb]
+  int32_t* cls;      // [nb * nb]
+};
+// Builds the tile list and then plan p (one list, over l.row_ptr) in one launch.
+bsr_status launch_screen_plan(const ScreenListArgs& l, const PlanArgs& p, cudaStream_t s);
 
 // C = (A o M) B with M[i, j] = (sqrt|diag_i| sqrt|diag_j| > sqrt(threshold)) (tc_screened.cu).
 struct ScreenedArgs {

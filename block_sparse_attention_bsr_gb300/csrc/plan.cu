@@ -98,7 +98,7 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   int* cb = sm_plan + 4 * (n + 1);
   int* crn = cb + n;
   int* offs = crn + n;
-  PlanLayout lay = plan_layout(L.plan, n, p.G, p.BH);
+  PlanLayout lay = plan_layout(L.plan, n, p.G, p.BH, p.max_len);
 
   // all offsets in one round trip to memory
   for (int v = threadIdx.x; v <= n; v += blockDim.x) {
@@ -111,11 +111,15 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   const long long nnzb = ptr[n] > 0 ? ptr[n] : 0;
   long long lim = (nnzb * p.BH + p.G - 1) / p.G;
   if (lim < 8) lim = 8;
+  // chunks never exceed n blocks (the histograms are indexed by length
+  // 0..n; a square grid has no longer line, so without allow_split nothing
+  // is cut)
   const int Lmax = p.allow_split ? (int)(lim < n ? lim : n) : n;
+  const int max_len = p.max_len > 0 ? p.max_len : n;
 
   // pass 1: chunking of every line and histogram of chunk lengths
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int len = line_len(ptr, i, n);
+    const int len = line_len(ptr, i, max_len);
     offs[i] = ptr[i];
     int rn;
     const int bl = chunking(len, Lmax, &rn);
@@ -240,6 +244,83 @@ bsr_status launch_fused(const BwdArgs& a, const PlanArgs& p, int lists, size_t s
 
 }  // namespace
 
+// The screened SpMM's tile list, then its plan, in one CTA.
+__device__ __forceinline__ int tile_class(float2 row, float2 col, float t) {
+  if (!(row.y * col.y > t)) return kTileSkip;
+  return row.x * col.x > t ? kTileFull : kTilePartial;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) screen_plan_kernel(ScreenListArgs s, PlanArgs p) {
+  sm100::griddep_wait();  // may run as a programmatic dependent
+  sm100::griddep_launch_dependents();
+  __shared__ float2 bnd[kScreenMaxBlocks];
+  __shared__ int cnt[kScreenMaxBlocks + 1];
+  extern __shared__ int sm_plan[];
+  const int lane = threadIdx.x % 32, wp = threadIdx.x / 32, nw = blockDim.x / 32;
+  // bounds of every 128-block: one warp per block, 4 values per lane
+  for (int k = wp; k < s.nb; k += nw) {
+    const float4 x = ((const float4*)(s.diag + (size_t)k * 128))[lane];
+    const float q0 = sqrtf(fabsf(x.x)), q1 = sqrtf(fabsf(x.y)), q2 = sqrtf(fabsf(x.z)), q3 = sqrtf(fabsf(x.w));
+    float lo = fminf(fminf(q0, q1), fminf(q2, q3)), hi = fmaxf(fmaxf(q0, q1), fmaxf(q2, q3));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) bnd[k] = make_float2(lo, hi);
+  }
+  __syncthreads();
+  // kept tiles per block row (one warp per row)
+  for (int m = wp; m < s.nb; m += nw) {
+    int c = 0;
+    for (int k0 = 0; k0 < s.nb; k0 += 32) {
+      const int k = k0 + lane;
+      const bool kept = k < s.nb && tile_class(bnd[m], bnd[k], s.t) != kTileSkip;
+      c += __popc(__ballot_sync(0xffffffffu, kept));
+    }
+    if (lane == 0) cnt[m] = c;
+  }
+  __syncthreads();
+  if (wp == 0) {  // exclusive prefix sum of the counts by one warp
+    int run = 0;
+    for (int m0 = 0; m0 < s.nb; m0 += 32) {
+      const int m = m0 + lane;
+      const int c = m < s.nb ? cnt[m] : 0;
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (m < s.nb) {
+        cnt[m] = run + x - c;
+        s.row_ptr[m] = run + x - c;
+      }
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) s.row_ptr[s.nb] = run;
+  }
+  __syncthreads();
+  for (int m = wp; m < s.nb; m += nw) {
+    int off = cnt[m];
+    for (int k0 = 0; k0 < s.nb; k0 += 32) {
+      const int k = k0 + lane;
+      const int cl = k < s.nb ? tile_class(bnd[m], bnd[k], s.t) : kTileSkip;
+      const unsigned kept = __ballot_sync(0xffffffffu, cl != kTileSkip);
+      if (cl != kTileSkip) {
+        const int pos = off + __popc(kept & ((1u << lane) - 1u));
+        s.col_idx[pos] = k;
+        s.cls[pos] = cl;
+      }
+      off += __popc(kept);
+    }
+  }
+  // the list is in global memory, written by this CTA: the plan reads it back
+  __threadfence_block();
+  __syncthreads();
+  plan_body(p, 0, sm_plan);
+}
+
 // Planner threads: enough for one line each (the loops stride past that),
 // a whole number of warps, at most the kernel's bound.
 static int plan_threads(int n) {
@@ -258,6 +339,20 @@ bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
   const cudaError_t e = launch_dependent(plan_kernel, dim3(lists), dim3(plan_threads(p.n)), smem, s, p);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "plan launch: %s", cudaGetErrorString(e));
   return check_launch("plan launch");
+}
+
+bsr_status launch_screen_plan(const ScreenListArgs& l, const PlanArgs& p, cudaStream_t s) {
+  if (l.nb < 1 || l.nb > kScreenMaxBlocks || p.n != l.nb)
+    return fail(BSR_ERR_UNSUPPORTED, "screened list: %d block rows (1 .. %d)", l.nb, (int)kScreenMaxBlocks);
+  const size_t smem = sizeof(int) * plan_smem_ints(p.n);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(screen_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "screen_plan: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  }
+  LaunchTimer timer("screen_plan", s);
+  const cudaError_t e = launch_dependent(screen_plan_kernel, dim3(1), dim3(kPlanThreads), smem, s, l, p);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "screen_plan launch: %s", cudaGetErrorString(e));
+  return check_launch("screen_plan launch");
 }
 
 bsr_status launch_delta_plan(const BwdArgs& a, const PlanArgs& p, int lists, cudaStream_t s) {

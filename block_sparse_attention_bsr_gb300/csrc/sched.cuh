@@ -179,4 +179,35 @@ __device__ __forceinline__ void part_accum32(const float* tile, int cg0, int r, 
   }
 }
 
+// Writes NC fp32 TMEM columns of this lane (row r) into a partial tile,
+// starting at column group cg0 (see part_group).
+template <int NC>
+__device__ __forceinline__ void store_acc_part(uint32_t taddr, float* tile, int cg0, int r) {
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    uint32_t v[32];
+    sm100::tmem_ld32(taddr + c * 32, v);
+    sm100::tmem_wait_ld();
+    part_store32(tile, cg0 + c * 8, r, v);
+  }
+}
+
+// Sums NC columns of row r (from column group cg0) over `nc` partial tiles
+// spaced `stride` floats apart and stores them as T times `mul` at dst.
+template <int NC, typename T>
+__device__ __forceinline__ void merge_tiles(const float* tile0, size_t stride, int nc, int cg0, int r, T* dst,
+                                            float mul) {
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    float acc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    for (int ch = 0; ch < nc; ++ch) part_accum32(tile0 + ch * stride, cg0 + c * 8, r, 1.f, acc);
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = sm100::Half16<T>::pack(acc[2 * j] * mul, acc[2 * j + 1] * mul);
+    sm100::st_global_64B(dst + c * 32, w);
+  }
+}
+
 }  // namespace bsr

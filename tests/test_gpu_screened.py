@@ -30,7 +30,8 @@ def _run(n, w, thr, dtype, seed=0):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-@pytest.mark.parametrize("n,w,thr", [(1024, 128, 1e-2), (768, 64, 1e-1), (1024, 384, 1e-3), (512, 128, 0.5)])
+@pytest.mark.parametrize("n,w,thr", [(1024, 128, 1e-2), (768, 64, 1e-1), (1024, 384, 1e-3), (512, 128, 0.5),
+                                     (4096, 128, 1e-2), (4096, 256, 1e-3)])
 def test_screened_matches_oracle(n, w, thr, dtype):
     got, ref = _run(n, w, thr, dtype)
     scale = max(np.abs(ref).max(), 1e-30)

@@ -72,3 +72,28 @@ def test_spmm_no_stored_block_gives_zeros():
     bsr.bsr_spmm(blocks, rp, ci, 2, 1, X, Y)
     torch.cuda.synchronize()
     assert bool((Y == 0).all())
+
+
+@pytest.mark.parametrize("n_cols", [128, 256])
+def test_spmm_heavy_row_split_across_ctas(n_cols):
+    # block row 0 stores all 40 blocks, the others one to three: with the
+    # persistent walk's per-CTA share of 8 blocks, row 0 is cut into chunks
+    # whose partial products the last chunk sums; compared whole against the
+    # oracle.
+    nb = 40
+    g = torch.Generator().manual_seed(5)
+    bm = (torch.rand(nb, nb, generator=g) < 0.05).numpy()
+    bm[np.arange(nb), np.arange(nb)] = True
+    bm[0, :] = True
+    nnzb = int(bm.sum())
+    blocks = torch.randn(nnzb, 128, 128, generator=g).bfloat16()
+    X = torch.randn(nb * 128, n_cols, generator=g).bfloat16()
+    rp, ci = inputs.bsr_from_block_mask(bm)
+    dev = torch.device("cuda")
+    Y = torch.empty(nb * 128, n_cols, dtype=torch.bfloat16, device=dev)
+    bsr.bsr_spmm(blocks.to(dev), torch.from_numpy(rp).to(dev), torch.from_numpy(ci).to(dev), nb, nb, X.to(dev), Y)
+    bsr.bsr_attn_check()
+    got = Y.double().cpu().numpy()
+    ref = oracle.spmm(blocks.double().numpy(), rp, ci, nb, nb, X.double().numpy())
+    err = np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
+    assert err <= TOL["bf16"], err
