@@ -34,7 +34,12 @@ from block_sparse_attention_bsr_gb300 import inputs  # noqa: E402
 BLOCK = 128
 METRIC = "fwd+bwd ms & TFLOP/s over stored blocks at seq 8192; % of GB300 bf16 TC peak"
 # contraction FLOP per stored block and head, as each kernel executes them
-FLOP_PER_BLOCK = {"fwd_": 4, "fwd2p_stats": 2, "fwd2p_out": 4, "dq": 6, "dkdv": 8}  # x 128^2 * D
+# (x 128^2 * D).  The head_dim-64/128 kernels recompute S and dP once in each
+# backward walk; the wide kernels recompute the scores once per output slice
+# of W columns (W = 256 for 16-bit operands, 128 for fp32) and run fp32 as six
+# bf16 piece products, all counted here as the bf16 MMAs they issue.
+FLOP_PER_BLOCK = {"fwd_tc": 4, "fwd2p_stats": 2, "fwd2p_out": 4, "dq_tc": 6, "dkdv_tc": 8}
+WIDE_SCORE_MMAS = {"fwd_wide": 1, "dq_wide": 2, "dv_wide": 1, "dk_wide": 2}  # score contractions per slice
 
 
 def alg_flops(wl, nnzb, part="total"):
@@ -48,12 +53,18 @@ def alg_flops(wl, nnzb, part="total"):
 # current sources still hash the same (otherwise the roofline's traffic is
 # null until the kernel is captured again).
 MEASURED_TRAFFIC = {
-    ("global_s8192", "dkdv_tc"): {"bytes": 206.7e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                  "sha256": "bf9b07a77f77fe39b3b656d98f216f074474116c25211e72869787855afcfffb"},
-    ("global_s8192", "dq_tc"): {"bytes": 176.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                "sha256": "bf9b07a77f77fe39b3b656d98f216f074474116c25211e72869787855afcfffb"},
-    ("global_s8192", "fwd_tc"): {"bytes": 137.0e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "6e8e58578ca2f5b374da342a87214713aa4822fdca435d2f6cced9569dadae69"},
+    ("global_s8192", "dkdv_tc"): {"bytes": 204.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                  "sha256": "196cb3aa924dd962d7c178a36b667211fd66a94edb9e978cce19222f11d94a19"},
+    ("global_s8192", "dq_tc"): {"bytes": 176.7e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                "sha256": "196cb3aa924dd962d7c178a36b667211fd66a94edb9e978cce19222f11d94a19"},
+    ("global_s8192", "fwd_tc"): {"bytes": 136.2e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+                                 "sha256": "5fdb58c0f65d778ca1e74196134fdb114c4236ec5e0dbbd52a0451a9446c8b0e"},
+    ("local_s8192_d256", "dq_wide"): {"bytes": 152.7e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "b90df6cd9dad795887f006e70992369bdb894af55b1a963ea2ec513efc4feadc"},
+    ("local_s8192_d512", "dq_wide"): {"bytes": 338.5e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "b90df6cd9dad795887f006e70992369bdb894af55b1a963ea2ec513efc4feadc"},
+    ("global_s8192_f32", "dk_wide"): {"bytes": 675.1e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "b90df6cd9dad795887f006e70992369bdb894af55b1a963ea2ec513efc4feadc"},
 }
 
 
@@ -72,9 +83,15 @@ def measured_traffic(workload, kernel):
 
 
 def kernel_flops(name, wl, nnzb):
+    per_head = BLOCK * BLOCK * wl.head_dim * nnzb * wl.batch * wl.heads
     for key, mult in FLOP_PER_BLOCK.items():
         if name.startswith(key):
-            return mult * BLOCK * BLOCK * wl.head_dim * nnzb * wl.batch * wl.heads
+            return mult * per_head
+    if name in WIDE_SCORE_MMAS:
+        w = 128 if wl.dtype == "f32" else 256
+        nsl = max(1, wl.head_dim // w)
+        terms = 6 if wl.dtype == "f32" else 1
+        return terms * (2 * WIDE_SCORE_MMAS[name] * nsl + 2) * per_head
     return None
 
 

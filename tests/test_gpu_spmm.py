@@ -75,11 +75,9 @@ def test_spmm_no_stored_block_gives_zeros():
 
 
 @pytest.mark.parametrize("n_cols", [128, 256])
-def test_spmm_heavy_row_split_across_ctas(n_cols):
-    # block row 0 stores all 40 blocks, the others one to three: with the
-    # persistent walk's per-CTA share of 8 blocks, row 0 is cut into chunks
-    # whose partial products the last chunk sums; compared whole against the
-    # oracle.
+def test_spmm_heavy_row_beside_sparse_rows(n_cols):
+    # block row 0 stores all 40 blocks, the others one to three; compared
+    # whole against the oracle.
     nb = 40
     g = torch.Generator().manual_seed(5)
     bm = (torch.rand(nb, nb, generator=g) < 0.05).numpy()
