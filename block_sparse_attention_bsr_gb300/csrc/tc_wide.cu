@@ -612,18 +612,24 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
       if ((ok = issue_x2(A) && issue_x1(A))) next_a(A);
     }
     while (ok && !B.done) {
+      // When the next block starts another item, this item's last
+      // accumulate MMA goes first: the next item's score MMAs wait for its
+      // resident operands to load, and the epilogue must not wait behind them.
+      const bool a_later = !A.done && A.i == 0;
       if constexpr (C::kZOwn) {
         // the next block's scores run while this block's P is computed
+        if (a_later && !(ok = issue_acc(B))) break;
         if (!A.done) {
           if (!(ok = issue_x1(A))) break;
           next_a(A);
           if (!ok) break;
         }
-        if (!(ok = issue_acc(B))) break;
+        if (!a_later && !(ok = issue_acc(B))) break;
       } else if constexpr (NP == 1) {
         // dP of the next block while this block's dS is computed
+        if (a_later && !(ok = issue_acc(B))) break;
         if (!A.done && !(ok = issue_x2(A))) break;
-        if (!(ok = issue_acc(B))) break;
+        if (!a_later && !(ok = issue_acc(B))) break;
         if (!A.done) {
           if (!(ok = issue_x1(A))) break;
           next_a(A);
