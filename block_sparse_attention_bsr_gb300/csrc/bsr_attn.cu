@@ -222,20 +222,21 @@ bsr_status build_fwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
 }
 
 size_t fwd_scratch_bytes(const Dims& d, int G) {
-  const bool tc2 = tc_fwd_supported(d);
-  size_t bytes = sizeof(int32_t) * plan_words(d.nb, G, d.BH);
-  if (tc2) bytes += fwd_part_bytes(d.D) * plan_tiles(d.nb, G, d.BH);
-  else bytes += wide_piece_bytes(d, 3);
+  const int heads = plan_heads(d);
+  size_t bytes = sizeof(int32_t) * plan_words(d.nb, G, heads);
+  bytes += part_tile_bytes(d, true) * plan_tiles(d.nb, G, heads);
+  if (!tc_fwd_supported(d)) bytes += wide_piece_bytes(d, 3);
   return bytes;
 }
 
 void fwd_scratch_carve(FwdArgs* a, void* base) {
-  const bool tc2 = tc_fwd_supported(a->d);
+  const int heads = plan_heads(a->d);
   char* p = (char*)base;
   a->plan = (int32_t*)p;
-  p += sizeof(int32_t) * plan_words(a->d.nb, a->G, a->d.BH);
-  a->part = tc2 ? (float*)p : nullptr;
-  a->pieces = tc2 ? nullptr : (void*)p;
+  p += sizeof(int32_t) * plan_words(a->d.nb, a->G, heads);
+  a->part = (float*)p;
+  p += part_tile_bytes(a->d, true) * plan_tiles(a->d.nb, a->G, heads);  // a multiple of 16 bytes
+  a->pieces = tc_fwd_supported(a->d) ? nullptr : (void*)p;
 }
 
 // The forward pass on carved scratch: the planner first unless the plan in
@@ -251,8 +252,8 @@ bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned
     p.list[0] = PlanList{a.row_ptr, a.plan};
     p.n = a.d.nb;
     p.G = a.G;
-    p.BH = a.d.BH;
-    p.allow_split = tc2 ? 1 : 0;
+    p.BH = plan_heads(a.d);
+    p.allow_split = 1;
     p.status = a.status;
     if ((st = launch_plan(p, 1, s)) != BSR_OK) return st;
   }
@@ -392,29 +393,30 @@ bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
 
 size_t bwd_scratch_bytes(const Dims& d, int G, bool split) {
   const size_t rows = (size_t)d.BH * d.S;
+  const int heads = plan_heads(d);
   size_t bytes = 2 * sizeof(float) * rows;
-  bytes += 3 * sizeof(int32_t) * plan_words(d.nb, G, d.BH);
-  if (split && tc_bwd_supported(d)) bytes += 3 * sizeof(float) * (size_t)128 * d.D * plan_tiles(d.nb, G, d.BH);
+  bytes += 3 * sizeof(int32_t) * plan_words(d.nb, G, heads);
+  if (split) bytes += 3 * part_tile_bytes(d, false) * plan_tiles(d.nb, G, heads);
   if (!tc_bwd_supported(d)) bytes += wide_piece_bytes(d, 4);
   return bytes;
 }
 
 void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split) {
   const size_t rows = (size_t)a->d.BH * a->d.S;
-  const size_t pw = plan_words(a->d.nb, G, a->d.BH);
+  const int heads = plan_heads(a->d);
+  const size_t pw = plan_words(a->d.nb, G, heads);
   a->delta = (float*)base;
   a->lse2 = a->delta + rows;
   a->row_plan = (int32_t*)(a->lse2 + rows);
   a->col_plan = a->row_plan + pw;
   a->col_plan2 = a->col_plan + pw;
   char* next = (char*)(a->col_plan2 + pw);
-  const bool tc = tc_bwd_supported(a->d);
-  const size_t tiles = plan_tiles(a->d.nb, G, a->d.BH);
-  float* part = (float*)next;
-  a->part_q = split && tc ? part : nullptr;
-  a->part_kv = split && tc ? part + (size_t)128 * a->d.D * tiles : nullptr;
-  if (split && tc) next += 3 * sizeof(float) * (size_t)128 * a->d.D * tiles;
-  a->pieces = tc ? nullptr : (void*)next;
+  // partial tiles: one set for dQ, then two for dK / dV
+  const size_t set = part_tile_bytes(a->d, false) * plan_tiles(a->d.nb, G, heads);
+  a->part_q = split ? (float*)next : nullptr;
+  a->part_kv = split ? (float*)(next + set) : nullptr;
+  if (split) next += 3 * set;
+  a->pieces = tc_bwd_supported(a->d) ? nullptr : (void*)next;
 }
 
 bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned) {
@@ -431,18 +433,16 @@ bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned) {
   p.list[2] = PlanList{a.col_ptr, a.col_plan2};
   p.n = a.d.nb;
   p.G = tc_grid(a.d);
-  p.BH = a.d.BH;
+  p.BH = plan_heads(a.d);
+  p.allow_split = split ? 1 : 0;
   p.status = a.status;
   if (tc_bwd_supported(a.d)) {
-    p.allow_split = split ? 1 : 0;
     if ((st = launch_delta_plan(a, p, 2, s)) != BSR_OK) return st;
     return launch_bwd_tc(a, s);
   }
   if (!wide_supported(a.d))
     return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_bwd: dtype %d with head_dim %d", a.d.dtype, a.d.D);
-  // the wide kernels walk whole lines (no split partials): dQ, dV and dK
-  // each on a plan of its own
-  p.allow_split = 0;
+  // dQ, dV and dK each on a plan of its own
   if ((st = launch_delta_plan(a, p, 3, s)) != BSR_OK) return st;
   return launch_bwd_wide(a, s);
 }

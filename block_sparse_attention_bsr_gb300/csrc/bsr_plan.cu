@@ -10,8 +10,8 @@
 //   copies of row_ptr, col_idx, col_ptr, row_idx (16-byte aligned each)
 //   the block-row plan (forward and dQ), two block-column plans (dK / dV;
 //     the wide kernels' dV and dK walks)
-//   the forward's split-row partial tiles and the backward's (16-bit
-//     operands, head_dim 64 / 128), or the bf16 pieces of fp32 operands
+//   the forward's split-line partial tiles and the backward's
+//   the bf16 pieces of fp32 operands (wide kernels)
 //   delta and lse2 (one fp32 value each per query row)
 // The kernels put the plans' work-queue and arrival counters back to 0 when
 // they finish, so the lists are built once, at creation.
@@ -97,15 +97,16 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
     return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: row_ptr[n_brows] = %d and col_ptr[n_brows] = %d", ends[0],
                 ends[1]);
 
-  const bool tc = tc_bwd_supported(d);  // 16-bit operands, head_dim 64 / 128: split lines, partial tiles
-  const size_t pw = plan_words(d.nb, G, d.BH);
-  const size_t tiles = plan_tiles(d.nb, G, d.BH);
+  const int pheads = plan_heads(d);
+  const size_t pw = plan_words(d.nb, G, pheads);
+  const size_t tiles = plan_tiles(d.nb, G, pheads);
   const size_t rows = (size_t)d.BH * d.S;
   const size_t ptr_b = align16(sizeof(int32_t) * (n_brows + 1));
   const size_t idx_b = align16(sizeof(int32_t) * (nnzb > 0 ? nnzb : 1));
   const size_t plans_b = 3 * sizeof(int32_t) * pw;  // a multiple of 16 (plan_words is a multiple of 4)
-  const size_t fpart_b = tc ? align16(fwd_part_bytes(d.D) * tiles) : 0;
-  const size_t bpart_b = tc ? 3 * sizeof(float) * (size_t)128 * d.D * tiles : 0;
+  const size_t fpart_b = align16(part_tile_bytes(d, true) * tiles);
+  const size_t bset_b = part_tile_bytes(d, false) * tiles;  // one set: dQ, dV or dK (a multiple of 16)
+  const size_t bpart_b = 3 * bset_b;
   const size_t stat_b = 2 * align16(sizeof(float) * rows);
   const size_t piece_b = wide_piece_bytes(d, 4);
   const size_t total = 2 * ptr_b + 2 * idx_b + plans_b + fpart_b + bpart_b + stat_b + piece_b;
@@ -137,10 +138,10 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   p->col_plan = p->row_plan + pw;
   p->col_plan2 = p->col_plan + pw;
   c += plans_b;
-  p->fwd_part = tc ? (float*)c : nullptr;
+  p->fwd_part = (float*)c;
   c += fpart_b;
-  p->part_q = tc ? (float*)c : nullptr;
-  p->part_kv = tc ? (float*)c + (size_t)128 * d.D * tiles : nullptr;
+  p->part_q = (float*)c;
+  p->part_kv = (float*)(c + bset_b);
   c += bpart_b;
   p->delta = (float*)c;
   p->lse2 = (float*)(c + align16(sizeof(float) * rows));
@@ -165,8 +166,8 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   pa.list[2] = PlanList{p->col_ptr, p->col_plan2};
   pa.n = d.nb;
   pa.G = G;
-  pa.BH = d.BH;
-  pa.allow_split = tc ? 1 : 0;
+  pa.BH = pheads;
+  pa.allow_split = 1;
   pa.status = status;
   bsr_status st = launch_plan(pa, 3, s);
   if (st != BSR_OK) {

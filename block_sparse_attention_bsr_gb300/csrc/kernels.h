@@ -265,11 +265,21 @@ bsr_status launch_fwd_tc2(const FwdArgs& a, cudaStream_t s, int pass = 0);
 bool tc_bwd_supported(const Dims& d);
 
 // Tensor-core kernels for the other cases (tc_wide.cu): bf16 / fp16 with
-// head_dim 256 / 512 and fp32 with any head_dim, on unsplit plans
-// (allow_split = 0).  fp32 operands need wide_piece_bytes(d, tensors) of
-// scratch in a.pieces for their bf16 pieces.
+// head_dim 256 / 512 and fp32 with any head_dim, on plans built with
+// plan_heads(d) heads (split plans need part_tile_bytes per partial tile:
+// the forward's a.part, the backward's part_q and, for dV then dK, two sets
+// at part_kv).  fp32 operands need wide_piece_bytes(d, tensors) of scratch
+// in a.pieces for their bf16 pieces.
 bool wide_supported(const Dims& d);
 size_t wide_piece_bytes(const Dims& d, int tensors);
+// Heads the planner is given for d's kernels: BH for the head_dim 64 / 128
+// tensor-core kernels; for the wide kernels BH times the output slices of
+// head_dim each work item covers (each slice is planned as a head of its
+// own, so its chunks of a split line merge on their own counter).
+int plan_heads(const Dims& d);
+// Bytes of one partial-result tile of a split line, forward or backward
+// (the forward's carries the chunk's row statistics).
+size_t part_tile_bytes(const Dims& d, bool fwd);
 bsr_status launch_fwd_wide(const FwdArgs& a, cudaStream_t s);
 // dQ on the row plan, dV on col_plan, dK on col_plan2, after launch_delta.
 bsr_status launch_bwd_wide(const BwdArgs& a, cudaStream_t s);

@@ -36,6 +36,18 @@
 // P and dS are split the same way by the elementwise warps before they go to
 // TMEM.
 //
+// The tensor cores' fp32 accumulation is not round-to-nearest: every MMA
+// into an accumulator of magnitude |s| costs up to about an ulp of |s|, so
+// with 6 D / 16 MMAs per score the error grows with head_dim.  The fp32
+// kernels therefore keep the scores (S, or S^T in the column walks) in two
+// accumulators: the leading products a0 b0 (D / 16 MMAs at full magnitude)
+// and the five smaller ones (magnitude 2^-8 |s|), added in registers; the
+// forward and the backward compute the scores the same way, so the P the
+// backward rebuilds from the forward's statistics stays normalised.  To free
+// the TMEM columns this takes, FWD and DV pass P to their accumulate MMAs as
+// two pieces, P = p0 + p1 up to 2^-18 |P|, with the five products p_i c_j,
+// i + j <= 2.
+//
 // Operands move in 64-column chunks (128 rows x 128 bytes, 128-byte swizzle,
 // 16 KB): the row operand(s) of the item stay resident in shared memory when
 // they fit, the other operands of the score contractions stream through a
@@ -106,6 +118,19 @@ constexpr int wide_residency(int NP, int KC, int WC, bool x2) {
   return -1;
 }
 
+// Output columns one work item computes: 128 for fp32 operands (three
+// pieces each), 256 for 16-bit ones, or head_dim if smaller.
+__host__ __device__ constexpr int wide_width(bool f32, int D) {
+  return f32 ? (D < 128 ? D : 128) : (D < 256 ? D : 256);
+}
+
+// fp32 values of one partial-result tile of a split line: 128 rows x W
+// columns, and for the forward the chunk's statistics (reference max, row
+// sum, true max, pad) per half and row.
+__host__ __device__ constexpr size_t wide_part_floats(int W, bool fwd) {
+  return (size_t)128 * W + (fwd ? 2 * 128 * 4 : 0);
+}
+
 template <typename T>
 struct OpType {
   using type = T;
@@ -122,7 +147,7 @@ struct WCfg {
   static constexpr bool kX2 = MODE == kDq || MODE == kDk;
   static constexpr bool kZOwn = MODE == kFwd || MODE == kDv;  // Z in its own TMEM columns
   static constexpr int KC = D / 64;
-  static constexpr int W = NP == 3 ? (D < 128 ? D : 128) : (D < 256 ? D : 256);
+  static constexpr int W = wide_width(NP == 3, D);
   static constexpr int NSL = D / W;
   static constexpr int WC = W / 64;
   static constexpr int kCBytes = NP * WC * kChunk;
@@ -152,6 +177,14 @@ struct WCfg {
   static constexpr uint32_t kColX1 = 0, kColX2 = 128;
   static constexpr uint32_t kColAcc = (kZOwn && NP == 3) ? 384 : 256;
   static constexpr int kZBufs = (kZOwn && NP == 1) ? 2 : 1;
+  // fp32: the X1 scores' smaller piece products in a second accumulator
+  // (FWD / DV: columns 256..383, with Z = P in two pieces at 128..255;
+  // DQ / DK: columns 384..511, after the accumulator)
+  static constexpr bool kSplitS = NP == 3;
+  static constexpr uint32_t kColXs = kZOwn ? 256 : 384;
+  static constexpr int kZP = (kZOwn && NP == 3) ? 2 : NP;  // pieces of Z
+  static_assert(!kSplitS || kColXs + 128 <= kColAcc || kColXs >= kColAcc + W, "score accumulators overlap");
+  static_assert(!kSplitS || kColXs + 128 <= kTmemCols, "score accumulator overflows TMEM");
   static_assert(kColAcc + W <= kTmemCols, "accumulator overflows TMEM");
 };
 
@@ -178,6 +211,7 @@ struct WideArgs {
   float* row_denom;     // FWD
   const float* lse2;    // backward: per query row
   const float* delta;   // backward: per query row
+  float* part;          // partial results of split lines (wide_part_floats per tile)
   int* status;
 };
 
@@ -190,7 +224,9 @@ struct WBars {
   uint64_t stat_full[2], stat_empty[2];
   uint64_t final_mma;
   uint64_t ring_full[kMaxRing], ring_empty[kMaxRing];
+  uint64_t wg_sync[2];  // each warpgroup's sync around a split line's merge
   RingSmem work;
+  int merge_flag[2];
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -216,14 +252,25 @@ __device__ __forceinline__ void split3(float x, float& x0, float& x1, float& x2)
 }
 
 // Writes this warpgroup's 64 values of Z (one per key, fp32) into TMEM as
-// NP pieces of the operand type (pairs of keys per column).
-template <typename Op, int MODE, int NP>
+// ZP pieces of the operand type (pairs of keys per column).
+template <typename Op, int MODE, int NP, int ZP>
 __device__ __forceinline__ void store_z(uint32_t tbase, int h, int zb, const float (&z)[64]) {
   if constexpr (NP == 1) {
     uint32_t v[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) v[k] = Half16<Op>::pack(z[2 * k], z[2 * k + 1]);
     tmem_st32(tbase + zcol<MODE, NP>(0, h, zb), v);
+  } else if constexpr (ZP == 2) {
+    uint32_t v0[32], v1[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float a0 = __bfloat162float(__float2bfloat16_rn(z[2 * k]));
+      const float b0 = __bfloat162float(__float2bfloat16_rn(z[2 * k + 1]));
+      v0[k] = pack_bf16x2(a0, b0);
+      v1[k] = pack_bf16x2(z[2 * k] - a0, z[2 * k + 1] - b0);
+    }
+    tmem_st32(tbase + zcol<MODE, NP>(0, h, zb), v0);
+    tmem_st32(tbase + zcol<MODE, NP>(1, h, zb), v1);
   } else {
     uint32_t v0[32], v1[32], v2[32];
 #pragma unroll
@@ -292,6 +339,85 @@ __device__ __forceinline__ void zero_out(T* p) {
   for (int c = 0; c < NC * (int)sizeof(T) / 16; ++c) ((uint4*)p)[c] = z;
 }
 
+// Sums NC columns of row r (from column group cg0) over the nc partial tiles
+// of a split line, chunk ch weighted by wgt(ch), times mul, and stores them
+// as T at dst.
+template <int NC, typename T, typename Wf>
+__device__ __forceinline__ void merge_out(const float* tile0, size_t stride, int nc, int cg0, int r, T* dst, float mul,
+                                          Wf wgt) {
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    float acc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    for (int ch = 0; ch < nc; ++ch) part_accum32(tile0 + ch * stride, cg0 + c * 8, r, wgt(ch), acc);
+    if constexpr (std::is_same<T, float>::value) {
+      float4* q = (float4*)(dst + c * 32);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        q[j] = make_float4(acc[4 * j] * mul, acc[4 * j + 1] * mul, acc[4 * j + 2] * mul, acc[4 * j + 3] * mul);
+    } else {
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = Half16<T>::pack(acc[2 * j] * mul, acc[2 * j + 1] * mul);
+      // 128-bit stores: inside the out-of-line split epilogue, the 256-bit
+      // form (st_global_64B) was measured to land only the first word of
+      // each 32 bytes on the head_dim-256 kernels
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        ((uint4*)(dst + c * 32))[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+  }
+}
+
+// Epilogue of one chunk of a split line, for warpgroup half hg, row r:
+// publishes the half's fp32 partial (the forward's relative to the chunk's
+// reference max m_ref, with the chunk's row statistics m_ref, L and m_true);
+// the last chunk to arrive (for this head, slice and half) sums them all in
+// chunk order into the output:
+//   forward:  M = max_c m_true_c, w_c = 2^(m_ref_c - M), l = sum_c L_c w_c,
+//             O = sum_c w_c O_c / l, row_max = M ln 2, row_denom = l;
+//   backward: the plain sum times mul.
+// Cold next to the block loop, so kept out of line: the loop's registers do
+// not carry the merge's.  False if a wait gave up.
+template <typename T, int MODE, int W>
+__device__ __noinline__ bool split_epilogue(const PlanLayout lay, float* part, int slot, int bhp, int BHp, int hg,
+                                            int r, uint32_t tacc, T* orow, float mul, float m_ref, float L,
+                                            float m_true, float* row_max, float* row_denom, int* merge_flag,
+                                            uint64_t* wg_sync, int* merge_phase, volatile int* ab, int* status) {
+  constexpr size_t kTileF = wide_part_floats(W, MODE == kFwd);
+  float* tile = part + ((size_t)slot * BHp + bhp) * kTileF;
+  store_acc_part<W / 2>(tacc, tile, hg * (W / 8), r);
+  if constexpr (MODE == kFwd) *(float4*)(tile + 128 * W + (hg * 128 + r) * 4) = make_float4(m_ref, L, m_true, 0.f);
+  bool last = false;
+  if (!merge_arrive(lay, slot, bhp, BHp, hg, r, merge_flag, wg_sync, *merge_phase, ab, status, &last)) return false;
+  if (!last) return true;
+  const int sln = lay.slot_line[slot];
+  const int nc = lay.line_chunks[sln];
+  const float* p0 = part + ((size_t)lay.line_base[sln] * BHp + bhp) * kTileF;
+  const size_t stride = (size_t)BHp * kTileF;
+  if constexpr (MODE == kFwd) {
+    const size_t so = 128 * W + (hg * 128 + r) * 4;
+    float M = -INFINITY;
+    for (int ch = 0; ch < nc; ++ch) M = fmaxf(M, ld_partial(p0 + ch * stride + so).z);
+    float lsum = 0.f;
+    for (int ch = 0; ch < nc; ++ch) {
+      const float4 st4 = ld_partial(p0 + ch * stride + so);
+      lsum += st4.y * ex2(st4.x - M);
+    }
+    const float inv = 1.f / lsum;
+    merge_out<W / 2, T>(p0, stride, nc, hg * (W / 8), r, orow, 1.f,
+                        [&](int ch) { return ex2(ld_partial(p0 + ch * stride + so).x - M) * inv; });
+    if (row_max) {
+      *row_max = M * kLn2;
+      *row_denom = lsum;
+    }
+  } else {
+    merge_out<W / 2, T>(p0, stride, nc, hg * (W / 8), r, orow, mul, [](int) { return 1.f; });
+  }
+  return true;
+}
+
 template <typename T, int D, int MODE>
 __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constant__ WideMaps tm, WideArgs a) {
   // may run as a programmatic dependent: the prologue touches only shared
@@ -312,9 +438,15 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
-  const PlanLayout lay = plan_layout(a.plan, a.d.nb, (int)gridDim.x, a.d.BH);
+  // The planner sees each output slice of a head as a head of its own
+  // (BHp = heads * NSL, slice fastest), so split lines get a merge counter
+  // and partial tiles per slice.
+  const int BHp = a.d.BH * NSL;
+  const PlanLayout lay = plan_layout(a.plan, a.d.nb, (int)gridDim.x, BHp);
 
   if (threadIdx.x == 0) {
+    mbar_init(&bars->wg_sync[0], 128);
+    mbar_init(&bars->wg_sync[1], 128);
     mbar_init(&bars->r_full, 1);
     mbar_init(&bars->r_empty, 1);
     mbar_init(&bars->c_full, 1);
@@ -350,8 +482,14 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   griddep_wait();
-  const Walk walk = make_walk(lay, a.d.BH);
-  const int total = walk.total * NSL;  // work index w = (item, head) * NSL + slice
+  const Walk walk = make_walk(lay, BHp);
+  const int total = walk.total;
+  // work index -> item, head and output slice
+  auto decode = [&](int w, Cursor& c, int& slice) {
+    walk.decode(w, c);
+    slice = c.bh % NSL;
+    c.bh /= NSL;
+  };
   const uint32_t tmem = bars->tmem_slot;
   volatile int* ab = &bars->abort_flag;
   RingSmem* ring = &bars->work;
@@ -374,7 +512,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
         int w;
         if (!(ok = ring_put(ring, t, lay.header + 1, total, &w, ab, a.status)) || w < 0) break;
         Cursor cur;
-        walk.decode(w / NSL, cur);
+        int slice;
+        decode(w, cur, slice);
         if (cur.n == 0) continue;
         const int lrow = cur.bh * S + cur.line * 128;
         if constexpr (C::kR1Res) {
@@ -430,8 +569,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
         int w;
         if (!(ok = ring_get(ring, t, &w, ab, a.status)) || w < 0) break;
         Cursor cur;
-        walk.decode(w / NSL, cur);
-        const int sl = w % NSL;
+        int sl;
+        decode(w, cur, sl);
         for (int i = 0; i < cur.n; ++i, ++g) {
           int pl = a.idx[cur.first + i];
           pl = (pl < 0 || pl >= a.d.nb) ? 0 : pl;
@@ -481,7 +620,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
           c.done = true;
           return;
         }
-        walk.decode(w / NSL, c);
+        int slice;
+        decode(w, c, slice);
         if (c.n > 0) {
           c.i = 0;
           return;
@@ -496,7 +636,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
           c.done = true;
           return;
         }
-        walk.decode(w / NSL, c);
+        int slice;
+        decode(w, c, slice);
         if (c.n > 0) {
           c.i = 0;
           return;
@@ -515,8 +656,9 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
       }
     };
     // One 64-column chunk of a score contraction into TMEM column colD: the
-    // piece products A_i B_j (i + j < NP) over the chunk's 64 columns.
-    auto x_chunk = [&](uint32_t colD, uint32_t resA, bool streamA, int c, bool first) -> bool {
+    // piece products A_i B_j (i + j < NP) over the chunk's 64 columns (with
+    // `split` the products other than A_0 B_0 into column kColXs).
+    auto x_chunk = [&](uint32_t colD, uint32_t resA, bool streamA, int c, bool first, bool split) -> bool {
       uint32_t aa[NP], bb[NP];
       const uint32_t s0 = slot;
 #pragma unroll
@@ -544,10 +686,12 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
 #pragma unroll
         for (int j = 0; j + i < NP; ++j, ++term) {
           const SDesc da(aa[i], 16, 1024), db(bb[j], 16, 1024);
+          const bool small = split && term > 0;
+          const int first_term = small ? 1 : 0;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss_by(leader, tmem + colD, da.at(kk * 32), db.at(kk * 32), idX,
-                      (first && term == 0 && kk == 0) ? 0u : 1u);
+            mma_ss_by(leader, tmem + (small ? C::kColXs : colD), da.at(kk * 32), db.at(kk * 32), idX,
+                      (first && term == first_term && kk == 0) ? 0u : 1u);
         }
       }
       for (uint32_t x = s0; x < slot; ++x) mma_commit_by(leader, &bars->ring_empty[x % C::kRing]);
@@ -564,7 +708,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
             return false;
         }
         for (int cc = 0; cc < KC; ++cc)
-          if (!x_chunk(C::kColX2, base + C::kOffR2, !C::kR2Res, cc, cc == 0)) return false;
+          if (!x_chunk(C::kColX2, base + C::kOffR2, !C::kR2Res, cc, cc == 0, false)) return false;
         mma_commit_by(leader, &bars->x2_full);
       }
       return true;
@@ -579,7 +723,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
           return false;
       }
       for (int cc = 0; cc < KC; ++cc)
-        if (!x_chunk(C::kColX1, base + C::kOffR1, !C::kR1Res, cc, cc == 0)) return false;
+        if (!x_chunk(C::kColX1, base + C::kOffR1, !C::kR1Res, cc, cc == 0, C::kSplitS)) return false;
       mma_commit_by(leader, &bars->x1_full);
       if (C::kR1Res && c.i == c.n - 1) mma_commit_by(leader, &bars->r_empty);
       return true;
@@ -591,7 +735,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
       const int zb = C::kZBufs == 2 ? (c.g & 1) : 0;
       int term = 0;
 #pragma unroll
-      for (int i = 0; i < NP; ++i) {
+      for (int i = 0; i < C::kZP; ++i) {
 #pragma unroll
         for (int j = 0; j + i < NP; ++j, ++term) {
           const SDesc dc(base + C::kOffC + j * WC * kChunk, 16384, 1024);
@@ -663,7 +807,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
     const int r = wl * 32 + lane;   // row of the item's tile
     const uint32_t lb = (uint32_t)(wl * 32) << 16;
     const float sl2 = a.d.scale * kLog2e;
-    int g = 0, ps = 0;
+    int g = 0, ps = 0, merge_phase = 0;
     bool ok = true;
     for (int t = 0; ok; ++t) {
       int w = -1;
@@ -672,8 +816,9 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!ok || w < 0) break;
       Cursor cur;
-      walk.decode(w / NSL, cur);
-      const int sl = w % NSL;
+      int sl;
+      decode(w, cur, sl);
+      const int bhp = cur.bh * NSL + sl;  // the planner's head of this item
       const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
       T* orow = (T*)a.out + grow * D + sl * W + hg * (W / 2);
       if (cur.n == 0) {
@@ -700,6 +845,16 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
         tc_fence_after();
         float z[64];
         tmem_ld64(tmem + lb + C::kColX1 + hg * 64, z);
+        if constexpr (C::kSplitS) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lb + C::kColXs + hg * 64 + h * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) z[h * 32 + k] += __uint_as_float(v[k]);
+          }
+        }
         if constexpr (C::kZOwn) {
           tc_fence_before();
           mbar_arrive(&bars->x1_free);
@@ -792,7 +947,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
             tc_fence_after();
           }
         }
-        store_z<Op, MODE, NP>(tmem + lb, hg, C::kZBufs == 2 ? (g & 1) : 0, z);
+        store_z<Op, MODE, NP, C::kZP>(tmem + lb, hg, C::kZBufs == 2 ? (g & 1) : 0, z);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->z_full[g & 1]);
@@ -802,21 +957,34 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
       if (!(ok = warp_wait(&bars->acc_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ab, a.status))) break;
       tc_fence_after();
       const uint32_t tacc = tmem + lb + C::kColAcc + hg * (W / 2);
+      float L = 0.f;
       if constexpr (MODE == kFwd) {
         // row sum of both halves (same reference max); the exchange buffer
         // is the one the next block's maximum will use, so a second sync
         // keeps the write of that maximum behind this read
         aux[(g & 1) * 256 + hg * 128 + r] = l;
         if (!(ok = group_sync(&bars->pair_sync, ps, ab, a.status))) break;
-        const float L = l + aux[(g & 1) * 256 + (hg ^ 1) * 128 + r];
+        L = l + aux[(g & 1) * 256 + (hg ^ 1) * 128 + r];
         if (!(ok = group_sync(&bars->pair_sync, ps, ab, a.status))) break;
-        store_out<W / 2, T>(tacc, orow, 1.f / L, (size_t)D);
-        if (sl == 0 && hg == 0) {
-          a.row_max[grow] = m_true * kLn2;
-          a.row_denom[grow] = L * ex2(m_ref - m_true);
+      }
+      if (cur.slot < 0) {
+        if constexpr (MODE == kFwd) {
+          store_out<W / 2, T>(tacc, orow, 1.f / L, (size_t)D);
+          if (sl == 0 && hg == 0) {
+            a.row_max[grow] = m_true * kLn2;
+            a.row_denom[grow] = L * ex2(m_ref - m_true);
+          }
+        } else {
+          store_out<W / 2, T>(tacc, orow, (MODE == kDv) ? 1.f : a.d.scale, (size_t)D);
         }
       } else {
-        store_out<W / 2, T>(tacc, orow, (MODE == kDv) ? 1.f : a.d.scale, (size_t)D);
+        const bool stats = MODE == kFwd && sl == 0 && hg == 0;
+        if (!(ok = split_epilogue<T, MODE, W>(lay, a.part, cur.slot, bhp, BHp, hg, r, tacc, orow,
+                                               MODE == kFwd ? 1.f : ((MODE == kDv) ? 1.f : a.d.scale), m_ref, L,
+                                               m_true, stats ? a.row_max + grow : nullptr,
+                                               stats ? a.row_denom + grow : nullptr, &bars->merge_flag[hg],
+                                               &bars->wg_sync[hg], &merge_phase, ab, a.status)))
+          break;
       }
       // this warp's reads of the accumulator are complete before its next
       // Z arrival lets the MMA overwrite it
@@ -943,6 +1111,16 @@ bool wide_supported(const Dims& d) {
   return (d.dtype == BSR_BF16 || d.dtype == BSR_F16) && (d.D == 256 || d.D == 512);
 }
 
+int plan_heads(const Dims& d) {
+  if (tc_bwd_supported(d) || !wide_supported(d)) return d.BH;
+  return d.BH * (d.D / wide_width(d.dtype == BSR_F32, d.D));
+}
+
+size_t part_tile_bytes(const Dims& d, bool fwd) {
+  if (tc_bwd_supported(d)) return fwd ? fwd_part_bytes(d.D) : sizeof(float) * 128 * (size_t)d.D;
+  return sizeof(float) * wide_part_floats(wide_width(d.dtype == BSR_F32, d.D), fwd);
+}
+
 size_t wide_piece_bytes(const Dims& d, int tensors) {
   return d.dtype == BSR_F32 ? (size_t)tensors * 3 * (size_t)d.BH * d.S * d.D * sizeof(__nv_bfloat16) : 0;
 }
@@ -955,7 +1133,7 @@ bsr_status launch_fwd_wide(const FwdArgs& a, cudaStream_t s) {
   if (a.d.dtype == BSR_F32 && (st = launch_split(a.d, ops, 3, a.pieces, s)) != BSR_OK) return st;
   WideMaps tm{};
   if ((st = wide_maps(a.d, ops, 3, a.pieces, &tm)) != BSR_OK) return st;
-  WideArgs w{a.d, a.col_idx, a.plan, a.O, a.row_max, a.row_denom, nullptr, nullptr, a.status};
+  WideArgs w{a.d, a.col_idx, a.plan, a.O, a.row_max, a.row_denom, nullptr, nullptr, a.part, a.status};
   return dispatch_mode<kFwd>(tm, w, grid, s, "fwd_wide");
 }
 
@@ -967,9 +1145,13 @@ bsr_status launch_bwd_wide(const BwdArgs& a, cudaStream_t s) {
   if (a.d.dtype == BSR_F32 && (st = launch_split(a.d, ops, 4, a.pieces, s)) != BSR_OK) return st;
   WideMaps tm{};
   if ((st = wide_maps(a.d, ops, 4, a.pieces, &tm)) != BSR_OK) return st;
-  const WideArgs q{a.d, a.col_idx, a.row_plan, a.dQ, nullptr, nullptr, a.lse2, a.delta, a.status};
-  const WideArgs v{a.d, a.row_idx, a.col_plan, a.dV, nullptr, nullptr, a.lse2, a.delta, a.status};
-  const WideArgs k{a.d, a.row_idx, a.col_plan2, a.dK, nullptr, nullptr, a.lse2, a.delta, a.status};
+  // partial tiles (split plans only): dQ's at part_q, dV's at part_kv and
+  // dK's after them
+  const size_t set = a.part_kv ? plan_tiles(a.d.nb, grid, plan_heads(a.d)) * (part_tile_bytes(a.d, false) / 4) : 0;
+  const WideArgs q{a.d, a.col_idx, a.row_plan, a.dQ, nullptr, nullptr, a.lse2, a.delta, a.part_q, a.status};
+  const WideArgs v{a.d, a.row_idx, a.col_plan, a.dV, nullptr, nullptr, a.lse2, a.delta, a.part_kv, a.status};
+  const WideArgs k{a.d, a.row_idx, a.col_plan2, a.dK, nullptr, nullptr, a.lse2, a.delta,
+                   a.part_kv ? a.part_kv + set : nullptr, a.status};
   // dQ, dV and dK read the same inputs and write different outputs; each is
   // a persistent grid of its own work list
   if ((st = dispatch_mode<kDq>(tm, q, grid, s, "dq_wide")) != BSR_OK) return st;
