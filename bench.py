@@ -59,12 +59,12 @@ MEASURED_TRAFFIC = {
                                 "sha256": "196cb3aa924dd962d7c178a36b667211fd66a94edb9e978cce19222f11d94a19"},
     ("global_s8192", "fwd_tc"): {"bytes": 136.2e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
                                  "sha256": "5fdb58c0f65d778ca1e74196134fdb114c4236ec5e0dbbd52a0451a9446c8b0e"},
-    ("local_s8192_d256", "dq_wide"): {"bytes": 152.7e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "b90df6cd9dad795887f006e70992369bdb894af55b1a963ea2ec513efc4feadc"},
-    ("local_s8192_d512", "dq_wide"): {"bytes": 338.5e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "b90df6cd9dad795887f006e70992369bdb894af55b1a963ea2ec513efc4feadc"},
-    ("global_s8192_f32", "dk_wide"): {"bytes": 675.1e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "b90df6cd9dad795887f006e70992369bdb894af55b1a963ea2ec513efc4feadc"},
+    ("local_s8192_d256", "dq_wide"): {"bytes": 152.9e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "c99c8ab1b76f6d8c5870c53e3f01aa0474a7c083229dbce279bb6ea5c98a372e"},
+    ("local_s8192_d512", "dq_wide"): {"bytes": 374.2e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "c99c8ab1b76f6d8c5870c53e3f01aa0474a7c083229dbce279bb6ea5c98a372e"},
+    ("global_s8192_f32", "dk_wide"): {"bytes": 654.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "c99c8ab1b76f6d8c5870c53e3f01aa0474a7c083229dbce279bb6ea5c98a372e"},
 }
 
 
@@ -88,10 +88,14 @@ def kernel_flops(name, wl, nnzb):
         if name.startswith(key):
             return mult * per_head
     if name in WIDE_SCORE_MMAS:
-        w = 128 if wl.dtype == "f32" else 256
+        w = min(wl.head_dim, 128 if wl.dtype == "f32" else 256)
         nsl = max(1, wl.head_dim // w)
-        terms = 6 if wl.dtype == "f32" else 1
-        return terms * (2 * WIDE_SCORE_MMAS[name] * nsl + 2) * per_head
+        f32 = wl.dtype == "f32"
+        # fp32: six bf16 piece products per score product; the accumulate
+        # products take six too, but five where P goes in two pieces (forward, dV)
+        score_terms = 6 if f32 else 1
+        acc_terms = (5 if name in ("fwd_wide", "dv_wide") else 6) if f32 else 1
+        return (score_terms * 2 * WIDE_SCORE_MMAS[name] * nsl + acc_terms * 2) * per_head
     return None
 
 
