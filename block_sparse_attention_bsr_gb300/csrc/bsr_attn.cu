@@ -243,10 +243,22 @@ void fwd_scratch_carve(FwdArgs* a, void* base) {
 // a.plan is already built (a bsr_plan), then the online-softmax pass, or
 // (two_pass) the statistics pass and then the output pass of the
 // statistics-first variant.  The kernels leave the plan's counters at 0, so
-// both passes run on one plan.
-bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned) {
+// both passes run on one plan.  The work lists leave out empty block rows;
+// with `zero` their outputs (zero rows, row_max -inf, row_denom 0) come from
+// the zero-lines pass.
+bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned, bool zero) {
   bsr_status st = BSR_OK;
   const bool tc2 = tc_fwd_supported(a.d);
+  if (zero) {
+    ZeroArgs z{};
+    z.t[0] = ZeroTarget{a.row_ptr, {a.O, nullptr}, a.row_max, a.row_denom};
+    z.targets = 1;
+    z.nb = a.d.nb;
+    z.BH = a.d.BH;
+    z.S = a.d.S;
+    z.row_bytes = a.d.D * (a.d.dtype == BSR_F32 ? 4 : 2);
+    if ((st = launch_zero_lines(z, s)) != BSR_OK) return st;
+  }
   if (!planned) {
     PlanArgs p{};
     p.list[0] = PlanList{a.row_ptr, a.plan};
@@ -254,6 +266,7 @@ bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned
     p.G = a.G;
     p.BH = plan_heads(a.d);
     p.allow_split = 1;
+    p.skip_empty = 1;
     p.status = a.status;
     if ((st = launch_plan(p, 1, s)) != BSR_OK) return st;
   }
@@ -276,7 +289,7 @@ bsr_status fwd_impl(const bsr_tensor* Q, const bsr_tensor* K, const bsr_tensor* 
   cudaError_t e = cudaMallocAsync(&scratch, fwd_scratch_bytes(a.d, a.G), s);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaMallocAsync: %s", cudaGetErrorString(e));
   fwd_scratch_carve(&a, scratch);
-  st = run_fwd(a, s, two_pass, false);
+  st = run_fwd(a, s, two_pass, false, true);
   e = cudaFreeAsync(scratch, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_fwd: cudaFreeAsync: %s", cudaGetErrorString(e));
   return st;
@@ -419,8 +432,19 @@ void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split) {
   a->pieces = tc_bwd_supported(a->d) ? nullptr : (void*)next;
 }
 
-bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned) {
+bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned, bool zero) {
   bsr_status st;
+  if (zero) {  // dQ of empty block rows, dK / dV of empty block columns
+    ZeroArgs z{};
+    z.t[0] = ZeroTarget{a.row_ptr, {a.dQ, nullptr}, nullptr, nullptr};
+    z.t[1] = ZeroTarget{a.col_ptr, {a.dK, a.dV}, nullptr, nullptr};
+    z.targets = 2;
+    z.nb = a.d.nb;
+    z.BH = a.d.BH;
+    z.S = a.d.S;
+    z.row_bytes = a.d.D * (a.d.dtype == BSR_F32 ? 4 : 2);
+    if ((st = launch_zero_lines(z, s)) != BSR_OK) return st;
+  }
   if (planned) {  // the work lists are built already (a bsr_plan): delta, then the walks
     if (!tc_bwd_supported(a.d) && !wide_supported(a.d))
       return fail(BSR_ERR_UNSUPPORTED, "bsr_attn_bwd: dtype %d with head_dim %d", a.d.dtype, a.d.D);
@@ -435,6 +459,7 @@ bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned) {
   p.G = tc_grid(a.d);
   p.BH = plan_heads(a.d);
   p.allow_split = split ? 1 : 0;
+  p.skip_empty = 1;
   p.status = a.status;
   if (tc_bwd_supported(a.d)) {
     if ((st = launch_delta_plan(a, p, 2, s)) != BSR_OK) return st;
@@ -469,7 +494,7 @@ extern "C" bsr_status bsr_attn_bwd(const bsr_tensor* Q, const bsr_tensor* K, con
   if (e != cudaSuccess)
     return fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaMallocAsync(%zu): %s", scratch_bytes, cudaGetErrorString(e));
   bwd_scratch_carve(&a, scratch, G, true);
-  st = run_bwd(a, s, true, false);
+  st = run_bwd(a, s, true, false, true);
   e = cudaFreeAsync(scratch, s);
   if (st == BSR_OK && e != cudaSuccess) st = fail(BSR_ERR_CUDA, "bsr_attn_bwd: cudaFreeAsync: %s", cudaGetErrorString(e));
   return st;

@@ -102,5 +102,5 @@ extern "C" bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor
   float* base = nullptr;
   if ((st = noalloc_scratch(&base)) != BSR_OK) return st;
   bwd_scratch_carve(&a, base, G, false);
-  return run_bwd(a, (cudaStream_t)stream, false, false);
+  return run_bwd(a, (cudaStream_t)stream, false, false, true);
 }

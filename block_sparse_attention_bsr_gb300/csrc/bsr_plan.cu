@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <new>
+#include <vector>
 
 #include "kernels.h"
 
@@ -26,6 +27,7 @@ struct bsr_plan_s {
   int device;
   int batch, heads, seq, head_dim, dtype;
   int nb, nnzb, G;
+  int empty_rows, empty_cols;  // block rows / columns with no stored block
   void* mem;
   int32_t *row_ptr, *col_idx, *col_ptr, *row_idx;
   int32_t *row_plan, *col_plan, *col_plan2;
@@ -86,16 +88,23 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   const int G = tc_grid(d);
   if (G <= 0) return fail(BSR_ERR_CUDA, "bsr_plan_create: cannot query the SM count");
   cudaStream_t s = (cudaStream_t)stream;
-  // the number of stored blocks, from both pointer arrays
-  int32_t ends[2] = {-1, -1};
-  cudaError_t e = cudaMemcpyAsync(&ends[0], row_ptr + n_brows, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(&ends[1], col_ptr + n_brows, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  // the number of stored blocks, from both pointer arrays, and the empty
+  // lines (no stored block), whose outputs the zero-lines pass writes
+  std::vector<int32_t> rp(n_brows + 1), cp(n_brows + 1);
+  cudaError_t e = cudaMemcpyAsync(rp.data(), row_ptr, sizeof(int32_t) * (n_brows + 1), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(cp.data(), col_ptr, sizeof(int32_t) * (n_brows + 1), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_plan_create: reading nnzb: %s", cudaGetErrorString(e));
-  const int nnzb = ends[0];
-  if (nnzb < 0 || (long long)nnzb > (long long)n_brows * n_brows || ends[1] != nnzb)
-    return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: row_ptr[n_brows] = %d and col_ptr[n_brows] = %d", ends[0],
-                ends[1]);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_plan_create: reading the offsets: %s", cudaGetErrorString(e));
+  const int nnzb = rp[n_brows];
+  if (nnzb < 0 || (long long)nnzb > (long long)n_brows * n_brows || cp[n_brows] != nnzb)
+    return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: row_ptr[n_brows] = %d and col_ptr[n_brows] = %d",
+                rp[n_brows], cp[n_brows]);
+  int empty_rows = 0, empty_cols = 0;
+  for (int i = 0; i < n_brows; ++i) {
+    empty_rows += rp[i + 1] == rp[i] ? 1 : 0;
+    empty_cols += cp[i + 1] == cp[i] ? 1 : 0;
+  }
 
   const int pheads = plan_heads(d);
   const size_t pw = plan_words(d.nb, G, pheads);
@@ -124,6 +133,8 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   p->dtype = dtype;
   p->nb = n_brows;
   p->nnzb = nnzb;
+  p->empty_rows = empty_rows;
+  p->empty_cols = empty_cols;
   p->G = G;
   char* c = (char*)p->mem;
   p->row_ptr = (int32_t*)c;
@@ -168,6 +179,7 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   pa.G = G;
   pa.BH = pheads;
   pa.allow_split = 1;
+  pa.skip_empty = 1;
   pa.status = status;
   bsr_status st = launch_plan(pa, 3, s);
   if (st != BSR_OK) {
@@ -201,7 +213,7 @@ extern "C" bsr_status bsr_attn_fwd_plan(const bsr_plan* plan, const bsr_tensor* 
   a.plan = plan->row_plan;
   a.part = plan->fwd_part;
   a.pieces = plan->pieces;
-  return run_fwd(a, (cudaStream_t)stream, false, true);
+  return run_fwd(a, (cudaStream_t)stream, false, true, plan->empty_rows > 0);
 }
 
 extern "C" bsr_status bsr_attn_bwd_plan(const bsr_plan* plan, const bsr_tensor* Q, const bsr_tensor* K,
@@ -223,5 +235,5 @@ extern "C" bsr_status bsr_attn_bwd_plan(const bsr_plan* plan, const bsr_tensor* 
   a.part_q = plan->part_q;
   a.part_kv = plan->part_kv;
   a.pieces = plan->pieces;
-  return run_bwd(a, (cudaStream_t)stream, true, true);
+  return run_bwd(a, (cudaStream_t)stream, true, true, plan->empty_rows + plan->empty_cols > 0);
 }

@@ -7,6 +7,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <math.h>
 
 #include "delta.cuh"
 #include "kernels.h"
@@ -54,7 +55,48 @@ bsr_status delta_dim(const BwdArgs& a, cudaStream_t s) {
   }
 }
 
+// Outputs of empty lines (no stored block): the work lists leave those
+// lines out (PlanArgs::skip_empty), so no attention kernel visits them; this
+// pass writes what the method gives them instead: zero output rows, and for
+// the forward row_max = -inf, row_denom = 0 (no key is attended).  One CTA per
+// (target, line, head) in turn; a line is empty when its two offsets agree.
+__global__ void __launch_bounds__(kThreads) zero_lines_kernel(ZeroArgs z) {
+  sm100::griddep_wait();  // may run as a programmatic dependent
+  sm100::griddep_launch_dependents();
+  const long long per = (long long)z.nb * z.BH;
+  for (long long w = blockIdx.x; w < per * z.targets; w += gridDim.x) {
+    const ZeroTarget t = w >= per ? z.t[1] : z.t[0];
+    const int line = (int)(w % per % z.nb), bh = (int)(w % per / z.nb);
+    if (t.ptr[line + 1] != t.ptr[line]) continue;
+    const size_t row0 = (size_t)bh * z.S + (size_t)line * 128;
+    const size_t n16 = (size_t)128 * z.row_bytes / 16;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < 2; ++k) {
+      if (!t.out[k]) continue;
+      uint4* o = (uint4*)((char*)t.out[k] + row0 * z.row_bytes);
+      for (size_t i = threadIdx.x; i < n16; i += blockDim.x) o[i] = zero;
+    }
+    if (t.row_max && threadIdx.x < 128) {
+      t.row_max[row0 + threadIdx.x] = -INFINITY;
+      t.row_denom[row0 + threadIdx.x] = 0.f;
+    }
+  }
+}
+
 }  // namespace
+
+bsr_status launch_zero_lines(const ZeroArgs& z, cudaStream_t s) {
+  if (z.targets < 1 || z.targets > 2 || z.row_bytes % 16 != 0)
+    return fail(BSR_ERR_INVALID_ARG, "zero_lines: %d targets, %d-byte rows", z.targets, z.row_bytes);
+  const long long pairs = (long long)z.nb * z.BH * z.targets;
+  const int sms = sm_count();
+  const long long cap = sms > 0 ? 4LL * sms : 1;
+  const dim3 grid((unsigned)(pairs < cap ? (pairs > 0 ? pairs : 1) : cap));
+  LaunchTimer timer("zero_lines", s);
+  const cudaError_t e = launch_dependent(zero_lines_kernel, grid, dim3(kThreads), 0, s, z);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "zero_lines launch: %s", cudaGetErrorString(e));
+  return check_launch("zero_lines launch");
+}
 
 bsr_status launch_delta(const BwdArgs& a, cudaStream_t s) {
   if (a.d.dtype == BSR_BF16) return delta_dim<__nv_bfloat16>(a, s);

@@ -160,6 +160,8 @@ struct PlanArgs {
   int G;            // persistent CTAs of the kernels that read the plan
   int BH;
   int allow_split;  // 0: every line is one item (no partial results)
+  int skip_empty;   // 1: lines with no stored block get no item (their
+                    // outputs come from launch_zero_lines)
   int* status;
 };
 
@@ -220,9 +222,11 @@ bsr_status build_bwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
 size_t bwd_scratch_bytes(const Dims& d, int G, bool split);
 // Carves a scratch block of bwd_scratch_bytes at `base` into a's arrays.
 void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split);
-// Launches delta, plan (unless `planned`: the plans in a are built), dQ and
-// dK/dV on `s` (scratch carved already).
-bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned);
+// Launches the zero-lines pass (with `zero`: dQ rows of empty block rows,
+// dK / dV rows of empty block columns), delta, plan (unless `planned`: the
+// plans in a are built, without empty lines), dQ and dK/dV on `s` (scratch
+// carved already).
+bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned, bool zero);
 
 // The forward's argument checks, scratch (its plan, the split rows' partial
 // results or the fp32 pieces) and launches (the planner unless `planned`).
@@ -231,7 +235,9 @@ bsr_status build_fwd_args(const bsr_tensor* Q, const bsr_tensor* K, const bsr_te
                           float* row_max, float* row_denom, bool two_pass, FwdArgs* out);
 size_t fwd_scratch_bytes(const Dims& d, int G);
 void fwd_scratch_carve(FwdArgs* a, void* base);
-bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned);
+// `zero`: first the zero-lines pass over the empty block rows (the work
+// lists leave them out).
+bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned, bool zero);
 
 // The device status block of the current device (see sm100.cuh wait_limit_ns).
 int* status_ptr();
@@ -253,6 +259,23 @@ bsr_status check_launch(const char* what);
 
 // Delta D_i = dO_i . O_i and lse2_i of the backward pass (every dtype and head_dim).
 bsr_status launch_delta(const BwdArgs& a, cudaStream_t s);
+
+// The outputs of empty lines (delta.cu): for every line with no stored block
+// (ptr[i + 1] == ptr[i]) and every head, the 128 rows of each non-null
+// output are zeroed and, when given, row_max = -inf and row_denom = 0.
+struct ZeroTarget {
+  const int32_t* ptr;  // [nb + 1] line offsets (row_ptr or col_ptr)
+  void* out[2];        // [BH * S, D] outputs (null: none)
+  float* row_max;      // [BH * S] or null
+  float* row_denom;    // [BH * S] or null
+};
+struct ZeroArgs {
+  ZeroTarget t[2];
+  int targets;    // 1 or 2
+  int nb, BH, S;
+  int row_bytes;  // D * element size, a multiple of 16
+};
+bsr_status launch_zero_lines(const ZeroArgs& z, cudaStream_t s);
 
 // Tensor-core (tcgen05 / TMA) kernels for bf16 / fp16 operands with head_dim
 // 64 / 128; a.plan and a.part must hold the block-row plan built by

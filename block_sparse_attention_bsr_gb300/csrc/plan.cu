@@ -11,6 +11,9 @@
 //     result), and records one bucket per length; the kernels read work
 //     index k of a bucket as head k / count, item k % count of the bucket
 //     (see sched.cuh);
+//   * leaves out lines with no stored block when asked (skip_empty; their
+//     outputs are written by a separate pass), so that no persistent CTA
+//     draws a run of empty items;
 //   * gives each chunk of a split line a partial-result slot, and zeroes the
 //     per-(line, head, column half) arrival counters used by the last-arriver
 //     merge, and the work-queue counter.
@@ -121,6 +124,11 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int len = line_len(ptr, i, max_len);
     offs[i] = ptr[i];
+    if (len == 0 && p.skip_empty) {  // no item: no chunk of any length
+      cb[i] = 0;
+      crn[i] = 0;
+      continue;
+    }
     int rn;
     const int bl = chunking(len, Lmax, &rn);
     cb[i] = bl;

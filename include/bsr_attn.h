@@ -283,13 +283,6 @@ bsr_status bsr_validate(const int32_t* row_ptr_h, const int32_t* col_idx_h,
  * Synchronises `stream`, then reads and clears the device status word that
  * the kernels set when a bounded wait gives up (BSR_ERR_TIMEOUT) or a device
  * bounds check fails (BSR_ERR_DEVICE_CHECK).  BSR_OK when neither happened.
- *
- * Known limitation: masks with many empty block rows (forward, dQ) or empty
- * block columns (dK / dV) can make the backward kernels, and every kernel of
- * the fp32 and head_dim-256 / 512 paths, report BSR_ERR_TIMEOUT.  This
- * happens when one persistent CTA draws two or more empty lines at the end
- * of its work.  The results of that call are then undefined; the context
- * stays usable.
  */
 bsr_status bsr_attn_check(void* stream);
 

@@ -21,9 +21,10 @@ the kernel.  It holds the protocol's arguments to account: the work lists
 come longest first (the planner's order), and for those the protocol is
 safe, except when a CTA draws two or more empty items (lines with no stored
 block) at the end of its sequence: the lookahead cursor skips them and waits
-on a ring slot that only the lagging cursor frees.
-The bounded device waits turn that case into BSR_ERR_TIMEOUT; the xfail
-below records it.
+on a ring slot that only the lagging cursor frees (on the GPU a bounded wait,
+BSR_ERR_TIMEOUT).  The xfail below records that limit of the protocol; the
+attention entry points never reach it, since their work lists leave empty
+lines out (PlanArgs::skip_empty) and a separate pass writes those outputs.
 """
 
 import heapq
@@ -359,8 +360,8 @@ def test_model_catches_an_aliasing_wait():
 
 @pytest.mark.xfail(strict=True, raises=Hazard,
                    reason="two or more empty items at the end of a CTA's sequence: the lookahead cursor skips them "
-                          "and waits on a ring slot that only the lagging cursor frees (a bounded device wait, "
-                          "BSR_ERR_TIMEOUT on the GPU)")
+                          "and waits on a ring slot that only the lagging cursor frees (the attention work lists "
+                          "leave empty lines out, so they never hold such a sequence)")
 def test_runs_of_empty_items():
     for seed in range(60):
         rng = random.Random(seed)

@@ -118,6 +118,28 @@ def test_empty_block_row_and_column(dtype):
     assert np.all(got["dK"][:, :, cols] == 0) and np.all(got["dV"][:, :, cols] == 0)
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 64), ("bf16", 256), ("f32", 128)])
+def test_mostly_empty_lines(dtype, D):
+    # Only block rows 0-1 and block columns 0-3 hold blocks: 30 of 32 block
+    # rows and 28 of 32 block columns are empty, in each of 16 heads.  The
+    # work lists leave empty lines out (most persistent CTAs get no item at
+    # all) and a separate pass writes their outputs.  Four heads are compared
+    # with the oracle; every head's empty lines must come out as exact zeros
+    # (-inf / 0 statistics).
+    nb, B, H = 32, 2, 8
+    bm = np.zeros((nb, nb), bool)
+    bm[0:2, 0:4] = True
+    Q, K, V, dO = inputs.make_qkvdo(B, H, nb * 128, D, dtype, 1.0, 5)
+    scale = 1.0 / np.sqrt(D)
+    got = run_gpu(Q, K, V, dO, bm, scale)
+    heads = [(0, 0), (0, 5), (1, 2), (1, 7)]
+    compare(got, oracle_heads(Q, K, V, dO, bm, scale, heads), dtype, heads=heads, what="mostly empty")
+    rows, cols = slice(2 * 128, None), slice(4 * 128, None)
+    assert np.all(got["O"][:, :, rows] == 0) and np.all(got["dQ"][:, :, rows] == 0)
+    assert np.all(got["row_max"][:, :, rows] == -np.inf) and np.all(got["row_denom"][:, :, rows] == 0)
+    assert np.all(got["dK"][:, :, cols] == 0) and np.all(got["dV"][:, :, cols] == 0)
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_single_stored_block(dtype):
     bm = np.zeros((3, 3), bool)
