@@ -444,6 +444,38 @@ def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
             assert np.array_equal(t.double().cpu().numpy(), ref[name]), name
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
+def test_plan_with_empty_lines(dtype, D):
+    # A plan over a mask with empty block rows and columns: the planned calls
+    # write the empty lines' outputs (they are not in the plan's work lists)
+    # into NaN-filled outputs and match the per-call entry points bit for bit.
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    dev = torch.device("cuda")
+    nb, H = 12, 3
+    bm = np.zeros((nb, nb), bool)
+    bm[0:3, 0:5] = True
+    bm[7, 7] = True
+    Q, K, V, dO = inputs.make_qkvdo(1, H, nb * 128, D, dtype, 1.0, 23)
+    scale = 1.0 / np.sqrt(D)
+    ref = run_gpu(Q, K, V, dO, bm, scale)
+    rp, ci = inputs.bsr_from_block_mask(bm)
+    st = bsr.Structure(rp, ci, nb, dev)
+    q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+    plan = st.plan(q)
+    for _ in range(2):
+        O = torch.full_like(q, float("nan"))
+        rm = torch.full(q.shape[:3], float("nan"), device=dev, dtype=torch.float32)
+        rd = torch.full_like(rm, float("nan"))
+        dQ, dK, dV = (torch.full_like(q, float("nan")) for _ in range(3))
+        bsr.bsr_attn_fwd_plan(plan, q, k, v, scale, O, rm, rd)
+        bsr.bsr_attn_bwd_plan(plan, q, k, v, O, do, rm, rd, scale, dQ, dK, dV)
+        bsr.bsr_attn_check()
+        got = dict(O=O, row_max=rm, row_denom=rd, dQ=dQ, dK=dK, dV=dV)
+        for name, t in got.items():
+            assert np.array_equal(t.double().cpu().numpy(), ref[name]), name
+
+
 def test_plan_refuses_other_shapes():
     import block_sparse_attention_bsr_gb300 as bsr
 
