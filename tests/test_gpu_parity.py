@@ -211,6 +211,56 @@ def test_repeated_calls_identical():
         assert np.array_equal(a[k], b[k]), k
 
 
+def _fwd_bwd_on_device(case):
+    # one per-call forward + backward; the outputs stay on the device
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    st, q, k, v, do, scale = case
+    O = torch.empty_like(q)
+    rm = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
+    rd = torch.empty_like(rm)
+    bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, 128, scale, O, rm, rd)
+    dQ, dK, dV = (torch.empty_like(q) for _ in range(3))
+    bsr.bsr_attn_bwd(q, k, v, O, do, rm, rd, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, scale, dQ, dK, dV)
+    return [O, rm, rd, dQ, dK, dV]
+
+
+def test_kernel_sequence_soak():
+    # The persistent kernels restart their work queues, rings and barriers on
+    # every launch.  This runs the fp32 wide path (tiny), the bf16 and fp16
+    # head_dim-128 kernels (dilated_s2048), the head_dim-256 wide kernels
+    # and the global mask's split lines back to back, twelve times over.
+    # Every repeat must reproduce the first results bit for bit: each output
+    # tile has one writer, split lines merge in chunk order and nothing
+    # accumulates by atomics, so the results do not depend on the schedule.
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    dev = torch.device("cuda")
+    cases = []
+    for name, dtype in (("tiny", None), ("dilated_s2048", None), ("dilated_s2048", "f16")):
+        wl = inputs.WORKLOADS[name]
+        bm = wl.block_mask()
+        if dtype is None:
+            host = wl.inputs(seed=1)
+        else:
+            host = inputs.make_qkvdo(wl.batch, wl.heads, wl.seq, wl.head_dim, dtype, 1.0, 1)
+        rp, ci = inputs.bsr_from_block_mask(bm)
+        cases.append((bsr.Structure(rp, ci, bm.shape[0], dev), *(t.to(dev) for t in host), wl.scale))
+    for kind, nb, D, heads in (("local", 6, 256, 2), ("global", 20, 128, 4)):
+        bm = inputs.block_mask(kind, nb, radius=1)
+        host = inputs.make_qkvdo(1, heads, nb * 128, D, "bf16", 1.0, 2)
+        rp, ci = inputs.bsr_from_block_mask(bm)
+        cases.append((bsr.Structure(rp, ci, nb, dev), *(t.to(dev) for t in host), 1.0 / np.sqrt(D)))
+    first = [_fwd_bwd_on_device(c) for c in cases]
+    bsr.bsr_attn_check()
+    for _ in range(11):
+        for c, ref in zip(cases, first):
+            got = _fwd_bwd_on_device(c)
+            bsr.bsr_attn_check()
+            for name, a, b in zip(("O", "row_max", "row_denom", "dQ", "dK", "dV"), got, ref):
+                assert torch.equal(a, b), name
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_device_index_check_reports_error(dtype):
     # A column index outside the grid is skipped by the kernels' own bounds
