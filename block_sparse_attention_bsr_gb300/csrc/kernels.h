@@ -78,10 +78,11 @@ struct PlanItem {
 // Layout of one plan in device scratch (int32 units, 16-byte aligned base):
 //   header[8]                  items, work-queue counter, split lines, buckets,
 //                              CTAs that finished the current launch, pad
-//                              (the kernels leave the work-queue counter, the
-//                              exit count and every arrival counter at 0 when
-//                              they finish, so a plan can be reused launch
-//                              after launch without running the planner again)
+//                              (the kernels leave the work-queue counter at G
+//                              and the exit count and every arrival counter
+//                              at 0 when they finish, so a plan can be reused
+//                              launch after launch without running the
+//                              planner again)
 //   items[cap_items]           PlanItem, longest first
 //   buckets[cap_buckets]       PlanBucket, one per item length, longest first
 //   slot_line[cap_slots]       split line of each partial slot

@@ -16,7 +16,8 @@
 //     draws a run of empty items;
 //   * gives each chunk of a split line a partial-result slot, and zeroes the
 //     per-(line, head, column half) arrival counters used by the last-arriver
-//     merge, and the work-queue counter.
+//     merge, and sets the work-queue counter to the grid size (CTA b takes
+//     work index b first without it, see sched.cuh).
 // Balancing the work by stored blocks with one writer per output tile
 // follows "trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.9.0].
 // Plan layout (int32): see PlanLayout in kernels.h.
@@ -199,7 +200,7 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
     const int items = counts[0] <= lay.cap_items ? counts[0] : 0;
     if (counts[0] > lay.cap_items) atomicExch(p.status, kStatusDeviceCheck);
     lay.header[0] = items;
-    lay.header[1] = 0;  // work-queue counter
+    lay.header[1] = p.G;  // work-queue counter: indices below G go to CTAs by block index
     lay.header[2] = nsl;
     lay.header[4] = 0;  // CTAs finished
     lay.header[5] = lay.header[6] = lay.header[7] = 0;

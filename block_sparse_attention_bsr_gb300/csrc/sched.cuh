@@ -3,11 +3,13 @@
 // The grid holds one CTA per SM.  The planner (plan.cu) lists the work items
 // of one kernel -- a block row (forward, dQ) or block column (dK/dV), or a
 // chunk of one when the line is long -- sorted longest first, and every item
-// is done once per (batch, head): work index k stands for item k / BH of head
-// k % BH.  CTAs take work indices from a global counter, so an SM that drew a
-// long item takes fewer short ones after it (longest-processing-time-first
-// list scheduling; the pages balance their two cores "by stored blocks",
-// "trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.9.0]).
+// is done once per (batch, head): a work index k stands for one (item, head)
+// pair through the plan's bucket table (Walk::decode).  CTA b takes work
+// index b first, then further indices from a global counter that starts at
+// the grid size, so an SM that drew a long item takes fewer short ones after
+// it (longest-processing-time-first list scheduling; the pages balance their
+// two cores "by stored blocks", "trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG
+// [0.9.0]) and no CTA's first item waits on the counter.
 //
 // Inside a CTA the producer thread draws the indices and hands them to the
 // MMA thread and the elementwise warps through a small ring in shared memory
@@ -75,13 +77,25 @@ __device__ __forceinline__ Walk make_walk(const PlanLayout& lay, int BH) {
   return Walk{lay.items, lay.buckets, lay.header[3], BH, lay.header[0] * BH};
 }
 
+// Warms L2 with the plan (`words` int32 from its header) before the grid
+// wait, so the header, bucket table and item reads of the first draws do not
+// go to HBM: lane l of the calling warp touches 128-byte line
+// blockIdx.x + l * gridDim.x.  A prefetch returns no data and L2 is the point
+// of coherence, so the planner may still be writing these lines; the reads
+// after the grid wait see what it wrote.
+__device__ __forceinline__ void plan_prefetch_l2(const int32_t* plan, size_t words) {
+  const size_t line = (size_t)blockIdx.x + (size_t)(threadIdx.x % 32) * gridDim.x;
+  if (line * 32 < words) asm volatile("prefetch.global.L2 [%0];" ::"l"(plan + line * 32));
+}
+
 // Producer side: draws the next work index into ring slot t % kRing once all
-// consumers released it; -1 marks the end.  Returns false on a timeout.
+// consumers released it (the CTA's first draw is its block index, the later
+// ones come from the counter); -1 marks the end.  Returns false on a timeout.
 __device__ __forceinline__ bool ring_put(RingSmem* ring, int t, int* queue, int total, int* k_out,
                                          volatile int* abort_flag, int* status) {
   const int s = t % kRing;
   if (!sm100::mbar_wait(&ring->empty[s], ((t / kRing) & 1) ^ 1, abort_flag, status)) return false;
-  int k = atomicAdd(queue, 1);
+  int k = t == 0 ? (int)blockIdx.x : atomicAdd(queue, 1);
   if (k >= total) k = -1;
   ring->k[s] = k;
   sm100::mbar_arrive(&ring->full[s]);
@@ -136,13 +150,13 @@ __device__ __forceinline__ bool merge_arrive(const PlanLayout& lay, int slot, in
 
 // Called by one thread of every CTA after the CTA's last use of the plan
 // (after its final __syncthreads): the last CTA of the launch to finish
-// puts the work-queue counter and the exit count back to 0, so the next
-// launch on the same plan starts from a clean queue (every CTA has drawn its
-// last work index before it counts itself out).
+// puts the work-queue counter back to the grid size and the exit count back
+// to 0, so the next launch on the same plan starts from a clean queue (every
+// CTA has drawn its last work index before it counts itself out).
 __device__ __forceinline__ void plan_exit(const PlanLayout& lay) {
   __threadfence();
   if (atomicAdd(&lay.header[4], 1) == (int)gridDim.x - 1) {
-    atomicExch(&lay.header[1], 0);
+    atomicExch(&lay.header[1], (int)gridDim.x);
     atomicExch(&lay.header[4], 0);
     __threadfence();
   }

@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
   const PlanLayout lay = plan_layout(a.row_plan, a.d.nb, (int)gridDim.x, a.d.BH);
+  if (warp == 0) plan_prefetch_l2(a.row_plan, plan_words(a.d.nb, (int)gridDim.x, a.d.BH));
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->qd_full, 1);
@@ -548,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
   const PlanLayout lay = plan_layout(a.col_plan, a.d.nb, (int)gridDim.x, a.d.BH);
+  if (warp == 0) plan_prefetch_l2(a.col_plan, plan_words(a.d.nb, (int)gridDim.x, a.d.BH));
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->k_full, 1);

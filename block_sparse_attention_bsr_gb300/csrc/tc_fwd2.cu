@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
   const PlanLayout lay = plan_layout(a.plan, a.d.nb, (int)gridDim.x, a.d.BH);
+  if (warp == 0) plan_prefetch_l2(a.plan, plan_words(a.d.nb, (int)gridDim.x, a.d.BH));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {

@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int BH = a.n_cols / NT;  // column tiles: the planner's "heads"
   const PlanLayout lay = plan_layout(a.plan, a.n_brows, (int)gridDim.x, BH, a.n_bcols);
+  if (warp == 0) plan_prefetch_l2(a.plan, plan_words(a.n_brows, (int)gridDim.x, BH, a.n_bcols));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {

@@ -443,6 +443,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
   // and partial tiles per slice.
   const int BHp = a.d.BH * NSL;
   const PlanLayout lay = plan_layout(a.plan, a.d.nb, (int)gridDim.x, BHp);
+  if (warp == 0) plan_prefetch_l2(a.plan, plan_words(a.d.nb, (int)gridDim.x, BHp));
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->wg_sync[0], 128);
