@@ -53,18 +53,18 @@ def alg_flops(wl, nnzb, part="total"):
 # current sources still hash the same (otherwise the roofline's traffic is
 # null until the kernel is captured again).
 MEASURED_TRAFFIC = {
-    ("global_s8192", "dkdv_tc"): {"bytes": 204.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                  "sha256": "196cb3aa924dd962d7c178a36b667211fd66a94edb9e978cce19222f11d94a19"},
-    ("global_s8192", "dq_tc"): {"bytes": 176.7e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                "sha256": "196cb3aa924dd962d7c178a36b667211fd66a94edb9e978cce19222f11d94a19"},
-    ("global_s8192", "fwd_tc"): {"bytes": 136.2e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "5fdb58c0f65d778ca1e74196134fdb114c4236ec5e0dbbd52a0451a9446c8b0e"},
-    ("local_s8192_d256", "dq_wide"): {"bytes": 152.9e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "c99c8ab1b76f6d8c5870c53e3f01aa0474a7c083229dbce279bb6ea5c98a372e"},
-    ("local_s8192_d512", "dq_wide"): {"bytes": 374.2e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "c99c8ab1b76f6d8c5870c53e3f01aa0474a7c083229dbce279bb6ea5c98a372e"},
-    ("global_s8192_f32", "dk_wide"): {"bytes": 654.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "c99c8ab1b76f6d8c5870c53e3f01aa0474a7c083229dbce279bb6ea5c98a372e"},
+    ("global_s8192", "dkdv_tc"): {"bytes": 206.3e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                  "sha256": "9761c5b3cc87127db2389aa6e6bab95628f2aa330ac2bca7ef5e747d9097ce4a"},
+    ("global_s8192", "dq_tc"): {"bytes": 177.2e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                "sha256": "9761c5b3cc87127db2389aa6e6bab95628f2aa330ac2bca7ef5e747d9097ce4a"},
+    ("global_s8192", "fwd_tc"): {"bytes": 137.4e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+                                 "sha256": "261d2f76a27e33d87f9d2deca512671bee41b617e2db1e231ce0ad328df6e67c"},
+    ("local_s8192_d256", "dq_wide"): {"bytes": 153.5e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "5700acdd3d099cdc1a594f2d41e514c4a109edeb4ce5ced4b88582200b2f8ee2"},
+    ("local_s8192_d512", "dq_wide"): {"bytes": 375.2e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "5700acdd3d099cdc1a594f2d41e514c4a109edeb4ce5ced4b88582200b2f8ee2"},
+    ("global_s8192_f32", "dk_wide"): {"bytes": 667.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "5700acdd3d099cdc1a594f2d41e514c4a109edeb4ce5ced4b88582200b2f8ee2"},
 }
 
 
