@@ -96,6 +96,7 @@ struct PlanBucket {
   int32_t count;  // items in the bucket (all of one length)
   int32_t len;
 };
+static_assert(sizeof(PlanBucket) == 16, "a bucket is read as one 16-byte vector");
 
 struct PlanLayout {
   int32_t* header;

@@ -71,6 +71,33 @@ struct Walk {
     c.n = it.n;
     c.slot = it.slot;
   }
+
+  // The same decode by a whole warp, every lane with the same k: lane i
+  // reads bucket i, so a table of up to 32 buckets costs one load instead of
+  // the binary search's chain of dependent loads (larger tables take
+  // decode()).  The buckets ascend in their first work index and bucket 0
+  // starts at 0, so the lanes whose bucket starts at or below k are 0 .. lo.
+  __device__ __forceinline__ void decode_warp(int k, Cursor& c) const {
+    if (nbuckets > 32) {
+      decode(k, c);
+      return;
+    }
+    const int lane = threadIdx.x % 32;
+    int4 b = make_int4(0x7fffffff, 0, 1, 0);
+    if (lane < nbuckets) b = *reinterpret_cast<const int4*>(buckets + lane);
+    const unsigned below = __ballot_sync(0xffffffffu, b.x <= k);
+    const int lo = below ? 31 - __clz(below) : 0;
+    const int work = __shfl_sync(0xffffffffu, b.x, lo);
+    const int start = __shfl_sync(0xffffffffu, b.y, lo);
+    const int count = __shfl_sync(0xffffffffu, b.z, lo);
+    const int kp = k - work;
+    const PlanItem it = items[start + kp % count];
+    c.bh = kp / count;
+    c.line = it.line;
+    c.first = it.first;
+    c.n = it.n;
+    c.slot = it.slot;
+  }
 };
 
 __device__ __forceinline__ Walk make_walk(const PlanLayout& lay, int BH) {

@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       k = __shfl_sync(0xffffffffu, k, 0);
       if (!ok || k < 0) break;
       Cursor cur;
-      walk.decode(k, cur);
+      walk.decode_warp(k, cur);
       const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
       T* dqrow = (T*)a.dQ + grow * D + hg * (D / 2);
       if (cur.n == 0) {
@@ -818,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       k = __shfl_sync(0xffffffffu, k, 0);
       if (!ok || k < 0) break;
       Cursor cur;
-      walk.decode(k, cur);
+      walk.decode_warp(k, cur);
       const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
       T* dkrow = (T*)a.dK + grow * D + hg * (D / 2);
       T* dvrow = (T*)a.dV + grow * D + hg * (D / 2);

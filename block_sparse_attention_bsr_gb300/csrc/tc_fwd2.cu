@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       k = __shfl_sync(0xffffffffu, k, 0);
       if (!ok || k < 0) break;
       Cursor cur;
-      walk.decode(k, cur);
+      walk.decode_warp(k, cur);
       const int nblk = cur.n;
       const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
       T* orow = (T*)a.O + grow * D + hg * (D / 2);
