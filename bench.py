@@ -53,18 +53,18 @@ def alg_flops(wl, nnzb, part="total"):
 # current sources still hash the same (otherwise the roofline's traffic is
 # null until the kernel is captured again).
 MEASURED_TRAFFIC = {
-    ("global_s8192", "dkdv_tc"): {"bytes": 206.3e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                  "sha256": "9761c5b3cc87127db2389aa6e6bab95628f2aa330ac2bca7ef5e747d9097ce4a"},
-    ("global_s8192", "dq_tc"): {"bytes": 177.2e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                "sha256": "9761c5b3cc87127db2389aa6e6bab95628f2aa330ac2bca7ef5e747d9097ce4a"},
-    ("global_s8192", "fwd_tc"): {"bytes": 137.4e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "261d2f76a27e33d87f9d2deca512671bee41b617e2db1e231ce0ad328df6e67c"},
-    ("local_s8192_d256", "dq_wide"): {"bytes": 153.5e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "5700acdd3d099cdc1a594f2d41e514c4a109edeb4ce5ced4b88582200b2f8ee2"},
-    ("local_s8192_d512", "dq_wide"): {"bytes": 375.2e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "5700acdd3d099cdc1a594f2d41e514c4a109edeb4ce5ced4b88582200b2f8ee2"},
-    ("global_s8192_f32", "dk_wide"): {"bytes": 667.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "5700acdd3d099cdc1a594f2d41e514c4a109edeb4ce5ced4b88582200b2f8ee2"},
+    ("global_s8192", "dkdv_tc"): {"bytes": 206.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                  "sha256": "1227773f105e7cdb580449cf8ed477a3a5eabebe8f1f970e4a1133b78f593621"},
+    ("global_s8192", "dq_tc"): {"bytes": 176.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                "sha256": "1227773f105e7cdb580449cf8ed477a3a5eabebe8f1f970e4a1133b78f593621"},
+    ("global_s8192", "fwd_tc"): {"bytes": 134.1e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+                                 "sha256": "454008d95f56c5d076ba97f9adb416c76aa7403a69379d7ec700507e6fa0dcf0"},
+    ("local_s8192_d256", "dq_wide"): {"bytes": 153.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "e08bc9dde37c17da6c7c35888f93e6b2df101e3d1c53299cfd63f5d5385224db"},
+    ("local_s8192_d512", "dq_wide"): {"bytes": 402.1e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "e08bc9dde37c17da6c7c35888f93e6b2df101e3d1c53299cfd63f5d5385224db"},
+    ("global_s8192_f32", "dk_wide"): {"bytes": 670.3e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "e08bc9dde37c17da6c7c35888f93e6b2df101e3d1c53299cfd63f5d5385224db"},
 }
 
 
