@@ -466,10 +466,11 @@ def test_two_pass_forward_refuses_fp32():
 @pytest.mark.parametrize("dtype,D,nb,H", [("bf16", 128, 20, 3), ("f16", 64, 9, 2), ("f32", 64, 6, 2),
                                           ("f32", 128, 20, 2), ("bf16", 256, 20, 2), ("bf16", 512, 4, 1)])
 def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
-    # Forward and backward on one plan, three times in a row (the kernels put
-    # the plan's counters back to 0 after each launch), give the per-call
-    # planned entry points' results bit for bit; nb = 20 has block row 0 and
-    # column 0 long enough to be split into chunks.
+    # Forward and backward on one plan, three times in a row (after each
+    # launch the kernels put the plan's work-queue counter back to the grid
+    # size and its other counters back to 0), give the per-call entry points'
+    # results bit for bit; nb = 20 has block row 0 and column 0 long enough
+    # to be split into chunks.
     import block_sparse_attention_bsr_gb300 as bsr
 
     dev = torch.device("cuda")
