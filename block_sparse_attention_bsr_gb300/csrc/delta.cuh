@@ -100,6 +100,14 @@ __device__ __forceinline__ void delta_rows(const BwdArgs& a, int cta) {
   using Sh = DeltaShape<T, D>;
   constexpr int G = Sh::G, NCH = Sh::NCH, RPW = Sh::RPW, U = Sh::U;
   static_assert(Sh::CH % G == 0, "whole chunks per lane");
+  constexpr int kPer = delta_rows_per_cta<T, D, kThreads>();
+  static_assert(128 % kPer == 0, "a group of rows lies inside one block row");
+  // The rows of a block row with no stored block are in no work item, and
+  // no kernel reads their statistics: the group skips them.
+  {
+    const int m = (int)(((size_t)cta * kPer % (size_t)a.d.S) / 128);
+    if (a.row_ptr[m + 1] == a.row_ptr[m]) return;
+  }
   const int lane = threadIdx.x % 32;
   const size_t rows = (size_t)a.d.BH * a.d.S;
   const size_t row0 = ((size_t)cta * (kThreads / 32) + threadIdx.x / 32) * RPW * U + lane / G;
