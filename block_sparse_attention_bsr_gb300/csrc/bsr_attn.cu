@@ -239,6 +239,16 @@ void fwd_scratch_carve(FwdArgs* a, void* base) {
   a->pieces = tc_fwd_supported(a->d) ? nullptr : (void*)p;
 }
 
+// CTAs for the zero pass when it rides in a planner launch: one per
+// (target, line, head) triple up to one per SM (most lines are not empty,
+// and a CTA checks a line with two loads).
+static int zero_ctas(const ZeroArgs& z) {
+  const long long triples = (long long)z.targets * z.nb * z.BH;
+  const int sms = sm_count();
+  const long long cap = sms > 0 ? sms : 1;
+  return (int)(triples < cap ? (triples > 0 ? triples : 1) : cap);
+}
+
 // The forward pass on carved scratch: the planner first unless the plan in
 // a.plan is already built (a bsr_plan), then the online-softmax pass, or
 // (two_pass) the statistics pass and then the output pass of the
@@ -249,15 +259,17 @@ void fwd_scratch_carve(FwdArgs* a, void* base) {
 bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned, bool zero) {
   bsr_status st = BSR_OK;
   const bool tc2 = tc_fwd_supported(a.d);
+  ZeroArgs z{};
   if (zero) {
-    ZeroArgs z{};
     z.t[0] = ZeroTarget{a.row_ptr, {a.O, nullptr}, a.row_max, a.row_denom};
     z.targets = 1;
     z.nb = a.d.nb;
     z.BH = a.d.BH;
     z.S = a.d.S;
     z.row_bytes = a.d.D * (a.d.dtype == BSR_F32 ? 4 : 2);
-    if ((st = launch_zero_lines(z, s)) != BSR_OK) return st;
+    // on a plan the zero pass has a launch of its own; otherwise it rides in
+    // the planner's launch
+    if (planned && (st = launch_zero_lines(z, s)) != BSR_OK) return st;
   }
   if (!planned) {
     PlanArgs p{};
@@ -268,6 +280,10 @@ bsr_status run_fwd(const FwdArgs& a, cudaStream_t s, bool two_pass, bool planned
     p.allow_split = 1;
     p.skip_empty = 1;
     p.status = a.status;
+    if (zero) {
+      p.zero = z;
+      p.zero_ctas = zero_ctas(z);
+    }
     if ((st = launch_plan(p, 1, s)) != BSR_OK) return st;
   }
   if (!tc2) return launch_fwd_wide(a, s);
@@ -434,8 +450,8 @@ void bwd_scratch_carve(BwdArgs* a, void* base, int G, bool split) {
 
 bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned, bool zero) {
   bsr_status st;
+  ZeroArgs z{};
   if (zero) {  // dQ of empty block rows, dK / dV of empty block columns
-    ZeroArgs z{};
     z.t[0] = ZeroTarget{a.row_ptr, {a.dQ, nullptr}, nullptr, nullptr};
     z.t[1] = ZeroTarget{a.col_ptr, {a.dK, a.dV}, nullptr, nullptr};
     z.targets = 2;
@@ -443,7 +459,9 @@ bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned, b
     z.BH = a.d.BH;
     z.S = a.d.S;
     z.row_bytes = a.d.D * (a.d.dtype == BSR_F32 ? 4 : 2);
-    if ((st = launch_zero_lines(z, s)) != BSR_OK) return st;
+    // on a plan the zero pass has a launch of its own; otherwise it rides in
+    // the planner's launch
+    if (planned && (st = launch_zero_lines(z, s)) != BSR_OK) return st;
   }
   if (planned) {  // the work lists are built already (a bsr_plan): delta, then the walks
     if (!tc_bwd_supported(a.d) && !wide_supported(a.d))
@@ -461,6 +479,10 @@ bsr_status run_bwd(const BwdArgs& a, cudaStream_t s, bool split, bool planned, b
   p.allow_split = split ? 1 : 0;
   p.skip_empty = 1;
   p.status = a.status;
+  if (zero) {
+    p.zero = z;
+    p.zero_ctas = zero_ctas(z);
+  }
   if (tc_bwd_supported(a.d)) {
     if ((st = launch_delta_plan(a, p, 2, s)) != BSR_OK) return st;
     return launch_bwd_tc(a, s);

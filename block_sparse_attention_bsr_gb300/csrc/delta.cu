@@ -55,32 +55,13 @@ bsr_status delta_dim(const BwdArgs& a, cudaStream_t s) {
   }
 }
 
-// Outputs of empty lines (no stored block): the work lists leave those
-// lines out (PlanArgs::skip_empty), so no attention kernel visits them; this
-// pass writes what the method gives them instead: zero output rows, and for
-// the forward row_max = -inf, row_denom = 0 (no key is attended).  One CTA per
-// (target, line, head) in turn; a line is empty when its two offsets agree.
+// Outputs of empty lines on their own launch (zero_lines_body, delta.cuh);
+// the per-call entry points run the same body in extra CTAs of their
+// planner launch instead.
 __global__ void __launch_bounds__(kThreads) zero_lines_kernel(ZeroArgs z) {
   sm100::griddep_wait();  // may run as a programmatic dependent
   sm100::griddep_launch_dependents();
-  const long long per = (long long)z.nb * z.BH;
-  for (long long w = blockIdx.x; w < per * z.targets; w += gridDim.x) {
-    const ZeroTarget t = w >= per ? z.t[1] : z.t[0];
-    const int line = (int)(w % per % z.nb), bh = (int)(w % per / z.nb);
-    if (t.ptr[line + 1] != t.ptr[line]) continue;
-    const size_t row0 = (size_t)bh * z.S + (size_t)line * 128;
-    const size_t n16 = (size_t)128 * z.row_bytes / 16;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int k = 0; k < 2; ++k) {
-      if (!t.out[k]) continue;
-      uint4* o = (uint4*)((char*)t.out[k] + row0 * z.row_bytes);
-      for (size_t i = threadIdx.x; i < n16; i += blockDim.x) o[i] = zero;
-    }
-    if (t.row_max && threadIdx.x < 128) {
-      t.row_max[row0 + threadIdx.x] = -INFINITY;
-      t.row_denom[row0 + threadIdx.x] = 0.f;
-    }
-  }
+  zero_lines_body(z, blockIdx.x, gridDim.x);
 }
 
 }  // namespace

@@ -155,4 +155,31 @@ __device__ __forceinline__ void delta_pass(const BwdArgs& a, int first, int stri
   for (int c = first; c < groups; c += stride) delta_rows<T, D, kThreads>(a, c);
 }
 
+// Outputs of empty lines (no stored block): the work lists leave those
+// lines out (PlanArgs::skip_empty), so no attention kernel visits them; this
+// writes what the method gives them instead: zero output rows, and for the
+// forward row_max = -inf, row_denom = 0 (no key is attended).  CTA `cta` of
+// `ncta` takes the (target, line, head) triples cta, cta + ncta, ...; a line
+// is empty when its two offsets agree.  Needs blockDim.x >= 128.
+__device__ __forceinline__ void zero_lines_body(const ZeroArgs& z, int cta, int ncta) {
+  const long long per = (long long)z.nb * z.BH;
+  for (long long w = cta; w < per * z.targets; w += ncta) {
+    const ZeroTarget& t = w >= per ? z.t[1] : z.t[0];
+    const int line = (int)(w % per % z.nb), bh = (int)(w % per / z.nb);
+    if (t.ptr[line + 1] != t.ptr[line]) continue;
+    const size_t row0 = (size_t)bh * z.S + (size_t)line * 128;
+    const size_t n16 = (size_t)128 * z.row_bytes / 16;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < 2; ++k) {
+      if (!t.out[k]) continue;
+      uint4* o = (uint4*)((char*)t.out[k] + row0 * z.row_bytes);
+      for (size_t i = threadIdx.x; i < n16; i += blockDim.x) o[i] = zero;
+    }
+    if (t.row_max && threadIdx.x < 128) {
+      t.row_max[row0 + threadIdx.x] = -INFINITY;
+      t.row_denom[row0 + threadIdx.x] = 0.f;
+    }
+  }
+}
+
 }  // namespace bsr

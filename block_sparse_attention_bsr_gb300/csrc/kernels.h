@@ -155,6 +155,21 @@ struct PlanList {
   int32_t* plan;       // plan_words(n, G, BH) int32 of scratch
 };
 
+// The outputs of empty lines (delta.cu): for every line with no stored block
+// (ptr[i + 1] == ptr[i]) and every head, the 128 rows of each non-null
+// output are zeroed and, when given, row_max = -inf and row_denom = 0.
+struct ZeroTarget {
+  const int32_t* ptr;  // [nb + 1] line offsets (row_ptr or col_ptr)
+  void* out[2];        // [BH * S, D] outputs (null: none)
+  float* row_max;      // [BH * S] or null
+  float* row_denom;    // [BH * S] or null
+};
+struct ZeroArgs {
+  ZeroTarget t[2];
+  int targets;    // 1 or 2
+  int nb, BH, S;
+  int row_bytes;  // D * element size, a multiple of 16
+};
 struct PlanArgs {
   PlanList list[3];
   int n;            // lines per list (block rows = block columns)
@@ -163,8 +178,13 @@ struct PlanArgs {
   int BH;
   int allow_split;  // 0: every line is one item (no partial results)
   int skip_empty;   // 1: lines with no stored block get no item (their
-                    // outputs come from launch_zero_lines)
+                    // outputs come from launch_zero_lines, or from the
+                    // zero_ctas CTAs below)
   int* status;
+  // zero_ctas > 0: the planner launch also writes the outputs of the empty
+  // lines of `zero` with that many CTAs (what launch_zero_lines does)
+  ZeroArgs zero;
+  int zero_ctas;
 };
 
 // Builds `lists` (1 to 3) plans.
@@ -262,21 +282,6 @@ bsr_status check_launch(const char* what);
 // Delta D_i = dO_i . O_i and lse2_i of the backward pass (every dtype and head_dim).
 bsr_status launch_delta(const BwdArgs& a, cudaStream_t s);
 
-// The outputs of empty lines (delta.cu): for every line with no stored block
-// (ptr[i + 1] == ptr[i]) and every head, the 128 rows of each non-null
-// output are zeroed and, when given, row_max = -inf and row_denom = 0.
-struct ZeroTarget {
-  const int32_t* ptr;  // [nb + 1] line offsets (row_ptr or col_ptr)
-  void* out[2];        // [BH * S, D] outputs (null: none)
-  float* row_max;      // [BH * S] or null
-  float* row_denom;    // [BH * S] or null
-};
-struct ZeroArgs {
-  ZeroTarget t[2];
-  int targets;    // 1 or 2
-  int nb, BH, S;
-  int row_bytes;  // D * element size, a multiple of 16
-};
 bsr_status launch_zero_lines(const ZeroArgs& z, cudaStream_t s);
 
 // Tensor-core (tcgen05 / TMA) kernels for bf16 / fp16 operands with head_dim

@@ -207,17 +207,22 @@ __device__ void plan_body(const PlanArgs& p, int li, int* sm_plan) {
   }
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
+// CTAs [0, lists) build one plan each; the p.zero_ctas CTAs after them
+// write the outputs of the empty lines (zero_lines_body).
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p, int lists) {
   sm100::griddep_wait();  // may run as a programmatic dependent
   sm100::griddep_launch_dependents();
   extern __shared__ int sm_plan[];
-  plan_body(p, blockIdx.x, sm_plan);
+  if ((int)blockIdx.x < lists)
+    plan_body(p, blockIdx.x, sm_plan);
+  else
+    zero_lines_body(p.zero, (int)blockIdx.x - lists, (int)gridDim.x - lists);
 }
 
 // Delta / lse2 of the backward pass and its work lists in one launch: the
-// first `lists` CTAs build the plans while the others compute the per-row
-// statistics (the two are independent; both must be done before dQ and
-// dK / dV start).
+// first `lists` CTAs build the plans, the next p.zero_ctas write the outputs
+// of the empty lines, and the others compute the per-row statistics (the
+// three are independent; all must be done before dQ and dK / dV start).
 constexpr int kFusedThreads = 256;
 
 template <typename T, int D>
@@ -225,10 +230,13 @@ __global__ void __launch_bounds__(kFusedThreads) delta_plan_kernel(BwdArgs a, Pl
   sm100::griddep_wait();  // may run as a programmatic dependent
   sm100::griddep_launch_dependents();
   extern __shared__ int sm_plan[];
-  if ((int)blockIdx.x < lists)
-    plan_body(p, blockIdx.x, sm_plan);
+  const int b = (int)blockIdx.x, zc = p.zero_ctas;
+  if (b < lists)
+    plan_body(p, b, sm_plan);
+  else if (b < lists + zc)
+    zero_lines_body(p.zero, b - lists, zc);
   else
-    delta_pass<T, D, kFusedThreads>(a, (int)blockIdx.x - lists, (int)gridDim.x - lists);
+    delta_pass<T, D, kFusedThreads>(a, b - lists - zc, (int)gridDim.x - lists - zc);
 }
 
 template <typename T, int D>
@@ -244,7 +252,7 @@ bsr_status launch_fused(const BwdArgs& a, const PlanArgs& p, int lists, size_t s
     per_sm = 1;
   const size_t sms = (size_t)sm_count();
   const size_t resident = sms > 0 ? sms * per_sm : groups;
-  const unsigned grid = (unsigned)(lists + (groups < resident ? groups : resident));
+  const unsigned grid = (unsigned)(lists + p.zero_ctas + (groups < resident ? groups : resident));
   LaunchTimer timer("delta_plan", s);
   const cudaError_t e = launch_dependent(delta_plan_kernel<T, D>, dim3(grid), dim3(kFusedThreads), smem, s, a, p, lists);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "delta_plan launch: %s", cudaGetErrorString(e));
@@ -345,7 +353,8 @@ bsr_status launch_plan(const PlanArgs& p, int lists, cudaStream_t s) {
     if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "plan: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   }
   LaunchTimer timer("plan", s);
-  const cudaError_t e = launch_dependent(plan_kernel, dim3(lists), dim3(plan_threads(p.n)), smem, s, p);
+  const cudaError_t e =
+      launch_dependent(plan_kernel, dim3(lists + p.zero_ctas), dim3(plan_threads(p.n)), smem, s, p, lists);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "plan launch: %s", cudaGetErrorString(e));
   return check_launch("plan launch");
 }
