@@ -1,6 +1,7 @@
 """The oracle's pins catch plausible mistakes in the oracle (no GPU).
 
-Each case plants one mistake in a copy of ``oracle/attention.py`` -- a
+Each case plants one mistake in a copy of ``oracle/attention.py`` (and, at
+the end, of ``oracle/spmm.py`` and ``oracle/screened.py``) -- a
 dropped term, a wrong sign, a swapped axis or index, a transposed operand, a
 mask left out -- loads the copy as a module of its own, and runs the pins
 below on it: torch's fp64 scaled_dot_product_attention and its autograd with
@@ -21,8 +22,8 @@ import torch
 
 from block_sparse_attention_bsr_gb300 import inputs
 
-SRC_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "attention.py")
-SRC = open(SRC_PATH).read()
+ORACLE_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
+SRC = open(os.path.join(ORACLE_DIR, "attention.py")).read()
 
 
 def _load(src: str) -> types.ModuleType:
@@ -176,3 +177,128 @@ def test_each_planted_mistake_fails_a_pin(what, old, new):
     assert SRC.count(old) == 1, f"the mutation site for '{what}' must occur exactly once"
     failed = _failing_pins(_load(SRC.replace(old, new)))
     assert failed, f"no pin caught: {what}"
+
+
+# ---------------------------------------------------------------- SpMM --
+SPMM_SRC = open(os.path.join(ORACLE_DIR, "spmm.py")).read()
+BLK = 128
+
+
+def pin_spmm_defining_sum(mod):
+    bm = np.array([[True, False, True], [False, True, True]])
+    rp = np.concatenate([[0], np.cumsum(bm.sum(1))])
+    ci = np.nonzero(bm)[1]
+    rng = np.random.default_rng(50)
+    blocks = rng.standard_normal((len(ci), BLK, BLK))
+    X = rng.standard_normal((3 * BLK, 8))
+    Y = mod.spmm(blocks, rp, ci, 2, 3, X)
+    for row, c in ((5, 1), (130, 7), (255, 0), (77, 4)):
+        m, i = divmod(row, BLK)
+        want = sum(blocks[j][i][t] * X[ci[j] * BLK + t, c] for j in range(rp[m], rp[m + 1]) for t in range(BLK))
+        assert abs(Y[row, c] - want) <= 1e-10 * max(1.0, abs(want))
+
+
+def pin_spmm_placement(mod):
+    bm = np.zeros((2, 3), bool)
+    bm[1, 2] = True
+    blk = np.random.default_rng(51).standard_normal((1, BLK, BLK))
+    X = np.random.default_rng(52).standard_normal((3 * BLK, 4))
+    Y = mod.spmm(blk, np.array([0, 0, 1]), np.array([2]), 2, 3, X)
+    assert np.all(Y[:BLK] == 0)
+    assert np.allclose(Y[BLK:], blk[0] @ X[2 * BLK:], rtol=0, atol=1e-12)
+
+
+SPMM_MUTANTS = [
+    ("block placed at (column, row)", "A[m * B:(m + 1) * B, k * B:(k + 1) * B] = blocks[j]",
+     "A[k * B:(k + 1) * B, m * B:(m + 1) * B] = blocks[j]"),
+    ("block stored transposed", "A[m * B:(m + 1) * B, k * B:(k + 1) * B] = blocks[j]",
+     "A[m * B:(m + 1) * B, k * B:(k + 1) * B] = blocks[j].T"),
+    ("blocks taken from the wrong list entry", "] = blocks[j]", "] = blocks[j - 1]"),
+    ("X transposed in the product", "@ np.asarray(X, dtype=np.float64)", "@ np.asarray(X, dtype=np.float64)[::-1]"),
+]
+
+
+def _spmm_failing(src):
+    mod = types.ModuleType("oracle_spmm_variant")
+    exec(compile(src, "oracle_spmm_variant", "exec"), mod.__dict__)
+    failed = []
+    for pin in (pin_spmm_defining_sum, pin_spmm_placement):
+        try:
+            pin(mod)
+        except Exception:
+            failed.append(pin.__name__)
+    return failed
+
+
+def test_unmodified_spmm_oracle_passes_its_pins():
+    assert _spmm_failing(SPMM_SRC) == []
+
+
+@pytest.mark.parametrize("what,old,new", SPMM_MUTANTS, ids=[m[0] for m in SPMM_MUTANTS])
+def test_each_planted_spmm_mistake_fails_a_pin(what, old, new):
+    assert SPMM_SRC.count(old) == 1, f"the mutation site for '{what}' must occur exactly once"
+    assert _spmm_failing(SPMM_SRC.replace(old, new)), f"no pin caught: {what}"
+
+
+# ------------------------------------------------------ screened SpMM --
+SCREEN_SRC = open(os.path.join(ORACLE_DIR, "screened.py")).read()
+
+
+def pin_screen_pairs(mod):
+    diag = np.random.default_rng(60).standard_normal(96).astype(np.float32) * 0.3
+    thr = 1e-2
+    M = mod.schwarz_mask(diag, thr)
+    t = np.float32(math.sqrt(np.float32(thr)))
+    for i in range(0, 96, 7):
+        for j in range(0, 96, 5):
+            qi = np.float32(math.sqrt(abs(float(diag[i]))))
+            qj = np.float32(math.sqrt(abs(float(diag[j]))))
+            assert bool(M[i, j]) == bool(np.float32(qi * qj) > t)
+
+
+def pin_screen_defining_sum(mod):
+    rng = np.random.default_rng(61)
+    A, Bm = rng.standard_normal((48, 48)), rng.standard_normal((48, 6))
+    diag = rng.standard_normal(48).astype(np.float32)
+    thr = 0.05
+    C = mod.screened_spmm(A, diag, Bm, thr)
+    q = [math.sqrt(abs(float(x))) for x in diag]
+    for i in range(0, 48, 5):
+        for c in range(6):
+            want = sum(A[i, j] * Bm[j, c] for j in range(48) if np.float32(q[i]) * np.float32(q[j]) > np.float32(
+                math.sqrt(np.float32(thr))))
+            assert abs(C[i, c] - want) <= 1e-10 * max(1.0, abs(want))
+
+
+SCREEN_MUTANTS = [
+    ("absolute value left out", "q = np.sqrt(np.abs(np.asarray(diag, dtype=np.float32)))",
+     "q = np.sqrt(np.asarray(diag, dtype=np.float32))"),
+    ("threshold not square-rooted", "t = np.sqrt(np.float32(threshold))", "t = np.float32(threshold)"),
+    ("one-sided bound", "(q[:, None] * q[None, :]) > t", "(q[:, None] * q[:, None]) > t"),
+    ("mask inverted", "(q[:, None] * q[None, :]) > t", "(q[:, None] * q[None, :]) <= t"),
+    ("mask applied to B instead of A", "(np.asarray(A, dtype=np.float64) * M) @ np.asarray(B, dtype=np.float64)",
+     "np.asarray(A, dtype=np.float64) @ (M[:, :B.shape[1]] * np.asarray(B, dtype=np.float64))"),
+]
+
+
+def _screen_failing(src):
+    mod = types.ModuleType("oracle_screened_variant")
+    exec(compile(src, "oracle_screened_variant", "exec"), mod.__dict__)
+    failed = []
+    for pin in (pin_screen_pairs, pin_screen_defining_sum):
+        try:
+            pin(mod)
+        except Exception:
+            failed.append(pin.__name__)
+    return failed
+
+
+def test_unmodified_screened_oracle_passes_its_pins():
+    assert _screen_failing(SCREEN_SRC) == []
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")  # the square root of a negative bound
+@pytest.mark.parametrize("what,old,new", SCREEN_MUTANTS, ids=[m[0] for m in SCREEN_MUTANTS])
+def test_each_planted_screened_mistake_fails_a_pin(what, old, new):
+    assert SCREEN_SRC.count(old) == 1, f"the mutation site for '{what}' must occur exactly once"
+    assert _screen_failing(SCREEN_SRC.replace(old, new)), f"no pin caught: {what}"
