@@ -176,6 +176,32 @@ def test_single_block_sequence(dtype):
     _edge(np.ones((1, 1), bool), dtype, D=128, B=2, H=2)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_long_sequence_over_2048_block_rows(dtype):
+    # 2100 block rows (seq 268800): the planner takes its paths for long line
+    # lists (the backward's lists are built in a launch of their own above
+    # 512 lines, and placed with atomics instead of the stable order above
+    # 2048).  With the band |m - n| <= 1 the rows of block row m see only
+    # key blocks m-1..m+1 and the keys of block column n only query blocks
+    # n-1..n+1, so windows of five blocks around sampled n give the oracle's
+    # exact values for O, the statistics and dQ of block row n and dK, dV of
+    # block column n (the window's edge rows are complete for those).
+    nb, D = 2100, 64
+    bm = inputs.block_mask("local", nb, radius=1)
+    Q, K, V, dO = inputs.make_qkvdo(1, 1, nb * 128, D, dtype, 1.0, 41)
+    scale = 1.0 / np.sqrt(D)
+    got = run_gpu(Q, K, V, dO, bm, scale)
+    for n in (0, 1, 700, 1049, 2098, 2099):
+        lo, hi = max(n - 2, 0), min(n + 3, nb)
+        sl = slice(lo * 128, hi * 128)
+        sub = [t[:, :, sl] for t in (Q, K, V, dO)]
+        ref = oracle_heads(*sub, bm[lo:hi, lo:hi], scale, [(0, 0)])
+        rows = slice((n - lo) * 128, (n - lo + 1) * 128)
+        piece = {k: got[k][:, :, n * 128:(n + 1) * 128] for k in ref}
+        want = {k: r[:, rows] for k, r in ref.items()}
+        compare(piece, want, dtype, heads=[(0, 0)], what=f"long sequence, block {n}")
+
+
 def test_large_scores_stable():
     # Inputs with std 4: scores scale * q.k have std 16 and reach about +-70,
     # so the online rescaling runs often and the softmax is sharply peaked.
