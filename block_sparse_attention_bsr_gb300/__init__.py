@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "BSR_OK", 1: "BSR_ERR_INVALID_ARG", 2: "BSR_ERR_UNSUPPORTED",
 
 # Every symbol include/bsr_attn.h declares.
 EXPORTS = ("bsr_attn_fwd", "bsr_attn_fwd_two_pass", "bsr_spmm", "bsr_screened_spmm", "bsr_attn_bwd",
-           "bsr_attn_bwd_noalloc", "bsr_plan_create", "bsr_plan_destroy", "bsr_attn_fwd_plan", "bsr_attn_bwd_plan",
+           "bsr_attn_bwd_noalloc", "bsr_plan_create", "bsr_plan_destroy", "bsr_plan_work_list", "bsr_attn_fwd_plan",
+           "bsr_attn_bwd_plan",
            "bsr_build_bsc", "bsr_validate", "bsr_attn_check", "bsr_set_wait_limit", "bsr_last_error",
            "bsr_profile_enable", "bsr_profile_collect")
 
@@ -66,6 +67,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsr_attn_bwd_noalloc.argtypes = [T, T, T, T, T, P, P, P, P, P, P, F32, T, T, T, P]
     lib.bsr_plan_create.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, P, ctypes.POINTER(ctypes.c_void_p)]
     lib.bsr_plan_destroy.argtypes = [P]
+    lib.bsr_plan_work_list.argtypes = [P, I32, P, I32, P, P]
     lib.bsr_attn_fwd_plan.argtypes = [P, T, T, T, F32, T, P, P, P]
     lib.bsr_attn_bwd_plan.argtypes = [P, T, T, T, T, T, P, P, F32, T, T, T, P]
     lib.bsr_build_bsc.argtypes = [P, P, I32, I32, P, P]
@@ -240,6 +242,22 @@ class Plan:
                                    int(batch), int(heads), int(head_dim), codes[dtype], s, ctypes.byref(h)))
         self.handle = h.value
         self.key = (int(batch), int(heads), int(head_dim), dtype)
+
+    def work_list(self, which: int = 0, stream=None):
+        """One of the plan's work lists (bsr_plan_work_list): an int32 array [items, 4] of
+        (line, first, n, slot) in the order the kernels draw them, and a dict with the item count, the
+        persistent CTAs G, the heads the planner counts and the number of distinct item lengths."""
+        import numpy as np
+        import torch
+
+        lib = load_library()
+        info = np.zeros(4, dtype=np.int32)
+        cap = 1 << 16
+        items = np.zeros((cap, 4), dtype=np.int32)
+        s = torch.cuda.current_stream().cuda_stream if stream is None else _stream(stream, None)
+        _check(lib.bsr_plan_work_list(self.handle, int(which), items.ctypes.data, cap, info.ctypes.data, s))
+        n = int(info[0])
+        return items[:n].copy(), {"items": n, "G": int(info[1]), "heads": int(info[2]), "buckets": int(info[3])}
 
     def close(self) -> None:
         if getattr(self, "handle", None):

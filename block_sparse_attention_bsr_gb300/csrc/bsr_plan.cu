@@ -13,8 +13,9 @@
 //   the forward's split-line partial tiles and the backward's
 //   the bf16 pieces of fp32 operands (wide kernels)
 //   delta and lse2 (one fp32 value each per query row)
-// The kernels put the plans' work-queue and arrival counters back to 0 when
-// they finish, so the lists are built once, at creation.
+// The kernels put the plans' work-queue counters back to the grid size and
+// their arrival counters back to 0 when they finish, so the lists are built
+// once, at creation.
 
 #include <cuda_runtime.h>
 
@@ -236,4 +237,38 @@ extern "C" bsr_status bsr_attn_bwd_plan(const bsr_plan* plan, const bsr_tensor* 
   a.part_kv = plan->part_kv;
   a.pieces = plan->pieces;
   return run_bwd(a, (cudaStream_t)stream, true, true, plan->empty_rows + plan->empty_cols > 0);
+}
+
+extern "C" bsr_status bsr_plan_work_list(const bsr_plan* plan, int32_t list, int32_t* items, int32_t cap,
+                                         int32_t* info, void* stream) {
+  if (!plan || !items || !info) return fail(BSR_ERR_INVALID_ARG, "bsr_plan_work_list: null argument");
+  if (list < 0 || list > 2) return fail(BSR_ERR_INVALID_ARG, "bsr_plan_work_list: list %d (0, 1 or 2)", list);
+  Dims d{};
+  d.BH = plan->batch * plan->heads;
+  d.S = plan->seq;
+  d.D = plan->head_dim;
+  d.nb = plan->nb;
+  d.dtype = plan->dtype;
+  const int heads = plan_heads(d);
+  int32_t* base = list == 0 ? plan->row_plan : (list == 1 ? plan->col_plan : plan->col_plan2);
+  const PlanLayout lay = plan_layout(base, plan->nb, plan->G, heads);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t header[8];
+  cudaError_t e = cudaMemcpyAsync(header, lay.header, sizeof(header), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_plan_work_list: %s", cudaGetErrorString(e));
+  const int n = header[0];
+  if (n < 0 || n > lay.cap_items) return fail(BSR_ERR_DEVICE_CHECK, "bsr_plan_work_list: %d items in the plan", n);
+  if (n > cap) return fail(BSR_ERR_INVALID_ARG, "bsr_plan_work_list: %d items do not fit %d", n, cap);
+  static_assert(sizeof(PlanItem) == 4 * sizeof(int32_t), "an item is four int32");
+  if (n > 0) {
+    e = cudaMemcpyAsync(items, lay.items, sizeof(PlanItem) * (size_t)n, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_plan_work_list: %s", cudaGetErrorString(e));
+  }
+  info[0] = n;
+  info[1] = plan->G;
+  info[2] = heads;
+  info[3] = header[3];  // buckets (distinct item lengths)
+  return BSR_OK;
 }

@@ -259,6 +259,32 @@ bsr_status bsr_attn_bwd_plan(const bsr_plan* plan, const bsr_tensor* Q, const bs
                              bsr_tensor* dQ, bsr_tensor* dK, bsr_tensor* dV, void* stream);
 
 /*
+ * bsr_plan_work_list: copies one of a plan's work lists to the host
+ * (synchronises `stream`), for inspecting the schedule the persistent kernels
+ * follow.  list 0: block rows (forward, dQ); 1: block columns (dK / dV);
+ * 2: the second block-column list (the dK walk of the head_dim-256 / 512 and
+ * fp32 kernels).  The items come in the order the kernels draw them: by
+ * block count, longest first, and inside one count by line, ascending.  A
+ * line longer than the per-CTA share Lmax = max(8, ceil(nnzb * H' / G)) is
+ * cut into ceil(len / Lmax) chunks whose lengths differ by at most one,
+ * longer chunks first ("trnsparse 0.7.0 -> 0.9.0" diff, CHANGELOG [0.9.0]:
+ * work balanced by stored blocks, one writer per output tile); lines with
+ * no stored block get no item.  Item i goes to items[4 i .. 4 i + 3] as
+ * (line, first, n, slot): the block row / column, the offset of its first
+ * block in col_idx / row_idx, its block count, and -1 for a whole line or
+ * the partial-result slot of a chunk (the chunks of one line have
+ * consecutive slots).  items holds `cap` items (host memory, owned by the
+ * caller).  info (host, 4 int32) receives the item count, G (the persistent
+ * CTAs the plan serves), H' (the heads the planner counts: batch * heads,
+ * times the output slices of the head_dim-256 / 512 and fp32 kernels) and
+ * the number of distinct item lengths.  Errors: BSR_ERR_INVALID_ARG for a
+ * null argument, a list outside 0..2 or too small a `cap`; BSR_ERR_CUDA
+ * when a copy fails.
+ */
+bsr_status bsr_plan_work_list(const bsr_plan* plan, int32_t list, int32_t* items, int32_t cap, int32_t* info,
+                              void* stream);
+
+/*
  * Host helper: BSC transpose of a BSR block structure ("trnsparse 0.4.1 ->
  * 0.6.0" diff, CHANGELOG [0.5.1], _attn_bwd_gather, host-side BSC
  * construction).  All pointers are HOST arrays owned by the caller:
