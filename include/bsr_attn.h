@@ -40,6 +40,10 @@
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
  *    asynchronous on it.  The caller owns every buffer; the library allocates
  *    only stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *    The attention calls can be recorded by stream capture into a CUDA graph
+ *    and replayed (their second stream joins the capture through events);
+ *    make the first call of a process outside capture, since it sets kernel
+ *    attributes and creates that stream.
  *  - Every function returns a bsr_status; nothing throws across the ABI and
  *    there is no fallback path.  bsr_last_error() gives a message for the
  *    last failure on the calling thread.

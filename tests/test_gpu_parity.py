@@ -568,3 +568,56 @@ def test_plan_refuses_other_shapes():
         bsr.bsr_attn_fwd_plan(plan, q, q, q, 0.125, O, rm, rm.clone())
     assert e.value.status == 1 and "plan" in str(e.value)
     plan.close()
+
+
+@pytest.mark.parametrize("api", ["plan", "per-call"])
+def test_step_captured_in_a_cuda_graph(api):
+    # One forward + backward captured in a CUDA graph (stream capture through
+    # torch.cuda.graph) and replayed on new inputs copied into the captured
+    # buffers gives the eager calls' results bit for bit: the calls launch on
+    # the caller's stream, fork and join their second stream with events,
+    # and (per call) allocate their scratch stream-ordered, all of which
+    # capture records.
+    import block_sparse_attention_bsr_gb300 as bsr
+
+    dev = torch.device("cuda")
+    nb, H, D = 20, 3, 128
+    bm = inputs.block_mask("global", nb, radius=1)
+    rp, ci = inputs.bsr_from_block_mask(bm)
+    st = bsr.Structure(rp, ci, nb, dev)
+    scale = 1.0 / np.sqrt(D)
+    bufs = [t.to(dev) for t in inputs.make_qkvdo(1, H, nb * 128, D, "bf16", 1.0, 70)]
+    q, k, v, do = bufs
+    O = torch.empty_like(q)
+    rm = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
+    rd = torch.empty_like(rm)
+    dQ, dK, dV = (torch.empty_like(q) for _ in range(3))
+    plan = st.plan(q) if api == "plan" else None
+
+    def step():
+        if plan is not None:
+            bsr.bsr_attn_fwd_plan(plan, q, k, v, scale, O, rm, rd)
+            bsr.bsr_attn_bwd_plan(plan, q, k, v, O, do, rm, rd, scale, dQ, dK, dV)
+        else:
+            bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, 128, scale, O, rm, rd)
+            bsr.bsr_attn_bwd(q, k, v, O, do, rm, rd, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, scale,
+                             dQ, dK, dV)
+
+    step()  # first calls outside capture (kernel attributes, the second stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for seed in (71, 72):
+        new = [t.to(dev) for t in inputs.make_qkvdo(1, H, nb * 128, D, "bf16", 1.0, seed)]
+        for dst, src in zip(bufs, new):
+            dst.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        bsr.bsr_attn_check()
+        replayed = [t.clone() for t in (O, rm, rd, dQ, dK, dV)]
+        step()
+        torch.cuda.synchronize()
+        bsr.bsr_attn_check()
+        for name, a, b in zip(("O", "row_max", "row_denom", "dQ", "dK", "dV"), replayed, (O, rm, rd, dQ, dK, dV)):
+            assert torch.equal(a, b), (api, seed, name)
