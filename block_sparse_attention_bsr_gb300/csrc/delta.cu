@@ -30,14 +30,7 @@ bsr_status delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   const size_t rows = (size_t)a.d.BH * a.d.S;
   constexpr size_t per = delta_rows_per_cta<T, D, kThreads>();
   const size_t groups = (rows + per - 1) / per;
-  // as many CTAs as the SMs hold at once; they loop over the row groups
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, delta_kernel<T, D>, kThreads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const size_t sms = (size_t)sm_count();
-  const size_t resident = sms > 0 ? sms * per_sm : groups;
-  const dim3 grid((unsigned)(groups < resident ? groups : resident));
+  const dim3 grid((unsigned)groups);  // one CTA per row group (DeltaShape)
   LaunchTimer timer("delta", s);
   const cudaError_t e = launch_dependent(delta_kernel<T, D>, grid, dim3(kThreads), 0, s, a);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "delta launch: %s", cudaGetErrorString(e));

@@ -244,15 +244,8 @@ bsr_status launch_fused(const BwdArgs& a, const PlanArgs& p, int lists, size_t s
   const size_t rows = (size_t)a.d.BH * a.d.S;
   constexpr size_t per = delta_rows_per_cta<T, D, kFusedThreads>();
   const size_t groups = (rows + per - 1) / per;
-  // delta CTAs: as many as the SMs hold at once (they loop over the groups)
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, delta_plan_kernel<T, D>, kFusedThreads, smem) !=
-          cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const size_t sms = (size_t)sm_count();
-  const size_t resident = sms > 0 ? sms * per_sm : groups;
-  const unsigned grid = (unsigned)(lists + p.zero_ctas + (groups < resident ? groups : resident));
+  // one delta CTA per row group (DeltaShape, delta.cuh)
+  const unsigned grid = (unsigned)(lists + p.zero_ctas + groups);
   LaunchTimer timer("delta_plan", s);
   const cudaError_t e = launch_dependent(delta_plan_kernel<T, D>, dim3(grid), dim3(kFusedThreads), smem, s, a, p, lists);
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "delta_plan launch: %s", cudaGetErrorString(e));
