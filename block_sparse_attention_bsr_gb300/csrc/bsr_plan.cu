@@ -13,12 +13,17 @@
 //   the forward's split-line partial tiles and the backward's
 //   the bf16 pieces of fp32 operands (wide kernels)
 //   delta and lse2 (one fp32 value each per query row)
+//   (bf16 / fp16, head_dim 64 / 128) the BSR position of each BSC entry
+// and, in a second cudaMalloc block for those operands, the dS tiles the
+// dK/dV walk stores for the dQ walk (batch * heads * nnzb tiles of 32 KB;
+// without that memory the plan's dQ walk recomputes the scores instead).
 // The kernels put the plans' work-queue counters back to the grid size and
 // their arrival counters back to 0 when they finish, so the lists are built
 // once, at creation.
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -34,6 +39,8 @@ struct bsr_plan_s {
   int32_t *row_plan, *col_plan, *col_plan2;
   float *fwd_part, *part_q, *part_kv, *delta, *lse2;
   void* pieces;
+  int32_t* bsr_of_bsc;  // null unless dS is set
+  void* dS;             // own cudaMalloc block, or null
 };
 
 namespace bsr {
@@ -106,6 +113,38 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
     empty_rows += rp[i + 1] == rp[i] ? 1 : 0;
     empty_cols += cp[i + 1] == cp[i] ? 1 : 0;
   }
+  // 16-bit operands with head_dim 64 / 128: the dK/dV walk hands its dS
+  // tiles to the dQ walk, stored by BSR position; map each BSC entry to it
+  std::vector<int32_t> bsr_of_bsc;
+  const bool want_ds = tc_bwd_supported(d) && nnzb > 0 &&
+                       (size_t)d.BH * (size_t)nnzb <= ((size_t)1 << 62) / (128 * 128 * 2);
+  if (want_ds) {
+    std::vector<int32_t> ci(nnzb), ri(nnzb);
+    e = cudaMemcpyAsync(ci.data(), col_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ri.data(), row_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_plan_create: reading the indices: %s", cudaGetErrorString(e));
+    std::vector<int64_t> key(nnzb);
+    std::vector<int32_t> ord(nnzb);
+    for (int m = 0; m < n_brows; ++m)
+      for (int j = rp[m]; j < rp[m + 1]; ++j) key[j] = (int64_t)m * n_brows + ci[j];
+    for (int j = 0; j < nnzb; ++j) ord[j] = j;
+    std::sort(ord.begin(), ord.end(), [&](int32_t x, int32_t y) { return key[x] < key[y]; });
+    bsr_of_bsc.resize(nnzb);
+    for (int n = 0; n < n_brows; ++n) {
+      for (int q = cp[n]; q < cp[n + 1]; ++q) {
+        const int m = ri[q];
+        const int64_t want = (int64_t)m * n_brows + n;
+        auto it = std::lower_bound(ord.begin(), ord.end(), want,
+                                   [&](int32_t x, int64_t v) { return key[x] < v; });
+        if (m < 0 || m >= n_brows || it == ord.end() || key[*it] != want)
+          return fail(BSR_ERR_INVALID_ARG,
+                      "bsr_plan_create: BSC entry %d (block row %d, column %d) is not a stored block of the BSR arrays",
+                      q, m, n);
+        bsr_of_bsc[q] = *it;
+      }
+    }
+  }
 
   const int pheads = plan_heads(d);
   const size_t pw = plan_words(d.nb, G, pheads);
@@ -119,7 +158,8 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   const size_t bpart_b = 3 * bset_b;
   const size_t stat_b = 2 * align16(sizeof(float) * rows);
   const size_t piece_b = wide_piece_bytes(d, 4);
-  const size_t total = 2 * ptr_b + 2 * idx_b + plans_b + fpart_b + bpart_b + stat_b + piece_b;
+  const size_t map_b = want_ds ? idx_b : 0;
+  const size_t total = 2 * ptr_b + 2 * idx_b + plans_b + fpart_b + bpart_b + stat_b + piece_b + map_b;
 
   bsr_plan* p = new (std::nothrow) bsr_plan();
   if (!p) return fail(BSR_ERR_INVALID_ARG, "bsr_plan_create: out of host memory");
@@ -159,6 +199,18 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   p->lse2 = (float*)(c + align16(sizeof(float) * rows));
   c += stat_b;
   p->pieces = piece_b ? (void*)c : nullptr;
+  c += piece_b;
+  p->bsr_of_bsc = nullptr;
+  p->dS = nullptr;
+  if (want_ds) {
+    void* ds = nullptr;
+    if (cudaMalloc(&ds, (size_t)d.BH * nnzb * (128 * 128 * 2)) == cudaSuccess) {
+      p->dS = ds;
+      p->bsr_of_bsc = (int32_t*)c;
+    } else {
+      cudaGetLastError();  // out of memory: the dQ walk recomputes the scores
+    }
+  }
 
   e = cudaMemcpyAsync(p->row_ptr, row_ptr, sizeof(int32_t) * (n_brows + 1), cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess)
@@ -167,7 +219,12 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
     e = cudaMemcpyAsync(p->col_idx, col_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && nnzb > 0)
     e = cudaMemcpyAsync(p->row_idx, row_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && p->dS) {
+    e = cudaMemcpyAsync(p->bsr_of_bsc, bsr_of_bsc.data(), sizeof(int32_t) * nnzb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // the host vector goes out of scope
+  }
   if (e != cudaSuccess) {
+    if (p->dS) cudaFree(p->dS);
     cudaFree(p->mem);
     delete p;
     return fail(BSR_ERR_CUDA, "bsr_plan_create: copying the structure: %s", cudaGetErrorString(e));
@@ -185,6 +242,7 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   bsr_status st = launch_plan(pa, 3, s);
   if (st != BSR_OK) {
     cudaStreamSynchronize(s);
+    if (p->dS) cudaFree(p->dS);
     cudaFree(p->mem);
     delete p;
     return st;
@@ -195,7 +253,9 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
 
 extern "C" bsr_status bsr_plan_destroy(bsr_plan* plan) {
   if (!plan) return BSR_OK;
-  const cudaError_t e = cudaFree(plan->mem);
+  cudaError_t e = plan->dS ? cudaFree(plan->dS) : cudaSuccess;
+  const cudaError_t e2 = cudaFree(plan->mem);
+  if (e == cudaSuccess) e = e2;
   delete plan;
   if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "bsr_plan_destroy: cudaFree: %s", cudaGetErrorString(e));
   return BSR_OK;
@@ -236,6 +296,9 @@ extern "C" bsr_status bsr_attn_bwd_plan(const bsr_plan* plan, const bsr_tensor* 
   a.part_q = plan->part_q;
   a.part_kv = plan->part_kv;
   a.pieces = plan->pieces;
+  a.dS = plan->dS;
+  a.bsr_of_bsc = plan->bsr_of_bsc;
+  a.nnzb = plan->nnzb;
   return run_bwd(a, (cudaStream_t)stream, true, true, plan->empty_rows + plan->empty_cols > 0);
 }
 

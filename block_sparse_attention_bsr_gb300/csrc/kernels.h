@@ -64,6 +64,13 @@ struct BwdArgs {
   void* pieces;        // fp32 operands: the three bf16 pieces of Q, K, V, dO (wide_piece_bytes(d, 4))
   float* part_q;       // partial dQ of split rows (128 x D per tile)
   float* part_kv;      // partial dK, dV of split columns (2 x 128 x D per tile)
+  // head_dim 64 / 128 on a plan: the dK/dV walk stores every dS tile here
+  // ([BH][nnzb] tiles of 128 x 128 16-bit values, in BSR order, layout in
+  // tc_bwd.cu) and the dQ walk sums dS K over them instead of recomputing
+  // the scores; null: the dQ walk recomputes them.
+  void* dS;
+  const int32_t* bsr_of_bsc;  // [nnzb] BSR position of each BSC entry (with dS)
+  int nnzb;                   // stored blocks (with dS)
   int* status;
 };
 

@@ -828,6 +828,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         for (int i = 0; i < cur.n; ++i, ++g) {
           const int ss = g % C::kStatStages;
+          int jb = -1;  // BSR position of the block, where its dS tile goes
+          if (a.dS) {
+            jb = a.bsr_of_bsc[cur.first + i];
+            if (jb < 0 || jb >= a.nnzb) {
+              atomicExch(a.status, kStatusDeviceCheck);
+              jb = -1;
+            }
+          }
           if (!(ok = warp_wait(&bars->st_full, g & 1, ab, a.status))) break;
           if (!(ok = warp_wait(&bars->stat_full[ss], (g / C::kStatStages) & 1, ab, a.status))) break;
           tc_fence_after();
@@ -864,10 +872,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->stat_empty[ss]);
           // dS^T over this warpgroup's own dP^T columns (read above; dK of
           // the previous block finished before dP^T of this one began)
-          tmem_st_pairs64<T>(tmem + lane_base + kColDPT + hg * 64, dp);
+          uint32_t w[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) w[k] = Half16<T>::pack(dp[2 * k], dp[2 * k + 1]);
+          tmem_st32(tmem + lane_base + kColDPT + hg * 64, w);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->ds_ready);
+          if (jb >= 0) {
+            // the dS tile of (block row m, this column) for the dQ walk, in
+            // 16-byte groups of 8 queries: group c / 8 of key r at
+            // ((c / 8) * 128 + r) * 16 bytes, so the warp's 32 keys fill
+            // 512 contiguous bytes per store
+            uint4* dst = (uint4*)((T*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (128 * 128)) + hg * 8 * 128 + r;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j * 128] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
         }
         if (!ok) break;
         if (cur.slot < 0) {
@@ -913,6 +933,270 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0) plan_exit(lay);
+}
+
+// ========================================================== dQ from dS ====
+// On a plan the dK/dV walk stores each dS tile it computes (a.dS), and the
+// dQ walk becomes dQ_m = scale * sum_n dS_mn K_n over them: one MMA group
+// per stored block, no recomputed scores, no statistics.  It still walks
+// block rows with one writer per dQ tile ("trnsparse 0.4.1 -> 0.6.0" diff,
+// CHANGELOG [0.5.1]); what it saves is the S and dP products (two of the
+// three MMA groups of the recomputing walk) for 32 KB of dS written and read
+// back per block, which HBM has room for beside the MMA-bound dK/dV walk.
+//
+// A dS tile (128 queries x 128 keys, 16-bit) sits in memory as the dK/dV
+// walk writes it: 16-byte groups of 8 consecutive queries, key-fastest
+// (group c / 8 of key r at ((c / 8) * 128 + r) * 16 bytes).  As the A
+// operand of dQ += dS K (M = queries, K = keys) that is the MN-major layout
+// without swizzle: 8 x 8 core matrices of 128 contiguous bytes, the next 8
+// keys 128 bytes on (leading byte offset) and the next 8 queries 2048 bytes
+// on (stride byte offset), so a plain bulk copy stages it for the MMA.
+//
+// Warp roles (320 threads): warp 0 the producer (the tile pair of each block
+// through a ring of stages), warp 1 TMEM owner and MMA issuer, warps 2..9
+// the epilogue (thread (w, l) owns dQ row 32 (w % 4) + l and half of its
+// columns), which stores an item's dQ from one of two TMEM accumulators
+// while the MMAs of the next item fill the other.
+template <int D>
+struct DsCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kKTile = 128 * D * 2;
+  static constexpr int kDsTile = 128 * 128 * 2;
+  static constexpr int kStageBytes = kDsTile + kKTile;  // a multiple of 1024 (the K boxes are swizzled)
+  static constexpr int kStages = D == 64 ? 4 : 3;
+  static constexpr int kBarOff = kStageBytes * kStages;
+  static constexpr int kSmem = kBarOff + 512 + 1024;
+  static constexpr uint32_t kCols = D == 64 ? 128 : 256;  // two accumulators of D columns
+};
+
+struct DsBars {
+  uint64_t full[4];
+  uint64_t empty[4];
+  uint64_t acc_full[2];   // the item's last MMA into accumulator b is done
+  uint64_t acc_empty[2];  // the epilogue has read accumulator b
+  uint64_t final_mma;
+  uint64_t wg_sync[2];
+  RingSmem ring;
+  int merge_flag[2];
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+static_assert(sizeof(DsBars) <= 512, "barrier block overflows its shared-memory slot");
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constant__ CUtensorMap tmK, BwdArgs a) {
+  // runs as a programmatic dependent of the dK/dV walk: the prologue below
+  // touches only shared memory and TMEM; global memory waits for that grid
+  griddep_launch_dependents();
+  using C = DsCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  DsBars* bars = (DsBars*)(sm + C::kBarOff);
+  static_assert(C::kSmem <= 232448, "shared memory over the per-CTA limit");
+  static_assert(C::kStageBytes % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled boxes");
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int S = a.d.S;
+  const PlanLayout lay = plan_layout(a.row_plan, a.d.nb, (int)gridDim.x, a.d.BH);
+  if (warp == 0) plan_prefetch_l2(a.row_plan, plan_words(a.d.nb, (int)gridDim.x, a.d.BH));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->acc_full[i], 1);
+      mbar_init(&bars->acc_empty[i], kEw);
+      mbar_init(&bars->wg_sync[i], 128);
+    }
+    mbar_init(&bars->final_mma, 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bars->ring.full[i], 1);
+      mbar_init(&bars->ring.empty[i], 1 + kEw / 32);  // MMA warp + epilogue warps
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_slot, C::kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_wait();
+  const Walk walk = make_walk(lay, a.d.BH);
+  const uint32_t tmem = bars->tmem_slot;
+  volatile int* ab = &bars->abort_flag;
+  RingSmem* ring = &bars->ring;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ producer --
+      int g = 0;  // blocks whose copies were issued
+      bool ok = true;
+      for (int t = 0; ok; ++t) {
+        int k;
+        if (!(ok = ring_put(ring, t, lay.header + 1, walk.total, &k, ab, a.status)) || k < 0) break;
+        Cursor cur;
+        walk.decode(k, cur);
+        // the row's dS tiles are consecutive (BSR order)
+        const uint8_t* ds = (const uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + cur.first) * C::kDsTile;
+        for (int i = 0; i < cur.n; ++i, ++g) {
+          int n = a.col_idx[cur.first + i];
+          if (n < 0 || n >= a.d.nb) {
+            atomicExch(a.status, kStatusDeviceCheck);
+            n = 0;
+          }
+          const int st = g % C::kStages;
+          if (!(ok = mbar_wait(&bars->empty[st], ((g / C::kStages) & 1) ^ 1, ab, a.status))) break;
+          uint8_t* dst = sm + st * C::kStageBytes;
+          mbar_arrive_expect_tx(&bars->full[st], C::kStageBytes);
+          bulk_load(dst, ds + (size_t)i * C::kDsTile, C::kDsTile / 2, &bars->full[st]);
+          bulk_load(dst + C::kDsTile / 2, ds + (size_t)i * C::kDsTile + C::kDsTile / 2, C::kDsTile / 2,
+                    &bars->full[st]);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(dst + C::kDsTile + b * 16384, &tmK, b * 64, cur.bh * S + n * 128, &bars->full[st]);
+        }
+      }
+      // drain: every copy issued must land before the CTA exits
+      for (int i = (g > C::kStages ? g - C::kStages : 0); i < g; ++i)
+        drain_wait(&bars->full[i % C::kStages], (i / C::kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA --
+    const uint32_t leader = elect_one();
+    const uint32_t idDQ = instr_desc(Half16<T>::kFmt, 1, 1, D, 128);
+    const uint32_t base = smem_u32(sm);
+    int g = 0, q = 0;  // blocks, non-empty items
+    bool ok = true;
+    for (int t = 0; ok; ++t) {
+      int k0 = -1;
+      bool good = true;
+      if (lane == 0) good = ring_get(ring, t, &k0, ab, a.status);
+      ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+      const int k = __shfl_sync(0xffffffffu, k0, 0);
+      if (!ok || k < 0) break;
+      Cursor cur;
+      walk.decode(k, cur);
+      if (cur.n > 0) {
+        const int buf = q & 1;
+        if (!(ok = warp_wait(&bars->acc_empty[buf], ((q >> 1) & 1) ^ 1, ab, a.status))) break;
+        tc_fence_after();
+        for (int i = 0; i < cur.n; ++i, ++g) {
+          const int st = g % C::kStages;
+          if (!(ok = warp_wait(&bars->full[st], (g / C::kStages) & 1, ab, a.status))) break;
+          tc_fence_after();
+          const uint32_t sds = base + st * C::kStageBytes;
+          const uint64_t dA = smem_desc(sds, 128, 2048, 0);  // dS: MN-major, no swizzle
+          const SDesc dK(sds + C::kDsTile, 16384, 1024);     // K: MN-major, 128-byte swizzle
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: two core matrices of dS, 16 rows of K
+            mma_ss_by(leader, tmem + buf * D, dA + (uint64_t)(kk * 16), dK.at(kk * 2048), idDQ,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_by(leader, &bars->empty[st]);
+        }
+        if (!ok) break;
+        mma_commit_by(leader, &bars->acc_full[buf]);
+        ++q;
+      }
+      __syncwarp();
+      if (lane == 0) ring_release(ring, t);
+    }
+    mma_commit_by(leader, &bars->final_mma);
+    if (leader) drain_wait(&bars->final_mma, 0);
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------- epilogue --
+    const int hg = (warp - 2) / 4;  // column half
+    const int wl = warp % 4;
+    const int r = wl * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wl * 32) << 16;
+    int q = 0, sync_phase = 0;
+    bool ok = true;
+    for (int t = 0; ok; ++t) {
+      int k = -1;
+      if (lane == 0) ok = ring_get(ring, t, &k, ab, a.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      k = __shfl_sync(0xffffffffu, k, 0);
+      if (!ok || k < 0) break;
+      Cursor cur;
+      walk.decode_warp(k, cur);
+      const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
+      T* dqrow = (T*)a.dQ + grow * D + hg * (D / 2);
+      if (cur.n == 0) {
+        zero_cols<D / 2>(dqrow);
+      } else {
+        const int buf = q & 1;
+        if (!(ok = warp_wait(&bars->acc_full[buf], (q >> 1) & 1, ab, a.status))) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + lane_base + buf * D + hg * (D / 2);
+        ++q;
+        if (cur.slot < 0) {
+          store_acc_cols<D / 2>(acc, dqrow, a.d.scale, (size_t)D);
+          tc_fence_before();
+          mbar_arrive(&bars->acc_empty[buf]);
+        } else {
+          // chunk of a split row: publish the fp32 partial, the last chunk merges
+          const size_t kTileF = (size_t)128 * D;
+          store_acc_part<D / 2>(acc, a.part_q + (size_t)(cur.slot * a.d.BH + cur.bh) * kTileF, hg * (D / 8), r);
+          tc_fence_before();
+          mbar_arrive(&bars->acc_empty[buf]);
+          bool last = false;
+          if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
+                                  sync_phase, ab, a.status, &last)))
+            break;
+          if (last) {
+            const int sl = lay.slot_line[cur.slot];
+            const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
+            merge_tiles<D / 2>(a.part_q + (size_t)(base * a.d.BH + cur.bh) * kTileF, (size_t)a.d.BH * kTileF, nc,
+                               hg * (D / 8), r, dqrow, a.d.scale);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ring_release(ring, t);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kCols);
+  if (threadIdx.x == 0) plan_exit(lay);
+}
+
+// On a plan (a.dS set): the dK/dV walk, which stores the dS tiles, then the
+// dQ walk over them, both in `s` as programmatic dependents.
+template <typename T, int D>
+bsr_status launch_bwd_ds(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, int grid, cudaStream_t s) {
+  auto dkdv = dkdv_tc_kernel<T, D>;
+  auto dq = dq_ds_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<D>::kSmem);
+  if (e != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "dkdv_tc: cudaFuncSetAttribute(%d): %s", DkvCfg<D>::kSmem, cudaGetErrorString(e));
+  e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, DsCfg<D>::kSmem);
+  if (e != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "dq_ds: cudaFuncSetAttribute(%d): %s", DsCfg<D>::kSmem, cudaGetErrorString(e));
+  if (profiling_launches()) {
+    {
+      LaunchTimer timer("dkdv_tc", s);
+      dkdv<<<grid, kThreads, DkvCfg<D>::kSmem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
+      bsr_status st = check_launch("dkdv_tc launch");
+      if (st != BSR_OK) return st;
+    }
+    LaunchTimer timer("dq_ds", s);
+    dq<<<grid, kThreads, DsCfg<D>::kSmem, s>>>(tm.k, a);
+    return check_launch("dq_ds launch");
+  }
+  e = launch_dependent(dkdv, dim3(grid), dim3(kThreads), DkvCfg<D>::kSmem, s, tm.q, tm.k, tm.v, tmdO, a);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dkdv_tc launch: %s", cudaGetErrorString(e));
+  bsr_status st = check_launch("dkdv_tc launch");
+  if (st != BSR_OK) return st;
+  e = launch_dependent(dq, dim3(grid), dim3(kThreads), DsCfg<D>::kSmem, s, tm.k, a);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_ds launch: %s", cudaGetErrorString(e));
+  return check_launch("dq_ds launch");
 }
 
 // dQ and dK / dV read the same inputs and write different outputs, so they
@@ -981,11 +1265,20 @@ bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   if (st != BSR_OK) return st;
   CUtensorMap tmdO;
   if ((st = make_tensor_map(a.d, a.dO, &tmdO, "dO")) != BSR_OK) return st;
+  if (a.dS && (((uintptr_t)a.dS) & 15 || !a.bsr_of_bsc))
+    return fail(BSR_ERR_INVALID_ARG, "bwd_tc: the dS tiles need 16-byte alignment and the BSC-to-BSR map");
+  const bool ds = a.dS != nullptr;
   switch (a.d.D) {
     case 64:
+      if (ds)
+        return a.d.dtype == BSR_F16 ? launch_bwd_ds<__half, 64>(a, tm, tmdO, grid, s)
+                                    : launch_bwd_ds<__nv_bfloat16, 64>(a, tm, tmdO, grid, s);
       return a.d.dtype == BSR_F16 ? launch_bwd<__half, 64>(a, tm, tmdO, grid, s)
                                   : launch_bwd<__nv_bfloat16, 64>(a, tm, tmdO, grid, s);
     case 128:
+      if (ds)
+        return a.d.dtype == BSR_F16 ? launch_bwd_ds<__half, 128>(a, tm, tmdO, grid, s)
+                                    : launch_bwd_ds<__nv_bfloat16, 128>(a, tm, tmdO, grid, s);
       return a.d.dtype == BSR_F16 ? launch_bwd<__half, 128>(a, tm, tmdO, grid, s)
                                   : launch_bwd<__nv_bfloat16, 128>(a, tm, tmdO, grid, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "bwd_tc: head_dim %d", a.d.D);

@@ -26,10 +26,12 @@ TOL = {
 }
 
 
-def run_gpu(Q, K, V, dO, bm, scale, device="cuda", backward=True, two_pass=False):
+def run_gpu(Q, K, V, dO, bm, scale, device="cuda", backward=True, two_pass=False, api="per-call"):
     """Runs forward (+ backward) through the C ABI on `device`; returns CPU float64 numpy arrays.
 
-    ``two_pass`` runs the statistics-first forward (bsr_attn_fwd_two_pass)."""
+    ``api`` picks the entry points: "per-call" (bsr_attn_fwd / bsr_attn_bwd, which plan on every call) or
+    "plan" (bsr_attn_fwd_plan / bsr_attn_bwd_plan on a plan built first, the calls the benchmark times).
+    ``two_pass`` runs the statistics-first forward (bsr_attn_fwd_two_pass, per call)."""
     dev = torch.device(device)
     rp, ci = _bsr(bm)
     st = bsr.Structure(rp, ci, bm.shape[1], dev)
@@ -37,26 +39,46 @@ def run_gpu(Q, K, V, dO, bm, scale, device="cuda", backward=True, two_pass=False
     O = torch.empty_like(q)
     rm = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
     rd = torch.empty_like(rm)
-    bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, 128, scale, O, rm, rd, two_pass=two_pass)
+    plan = st.plan(q) if api == "plan" else None
+    if plan is not None:
+        bsr.bsr_attn_fwd_plan(plan, q, k, v, scale, O, rm, rd)
+    else:
+        bsr.bsr_attn_fwd(q, k, v, st.row_ptr, st.col_idx, st.n_brows, 128, scale, O, rm, rd, two_pass=two_pass)
     out = dict(O=O, row_max=rm, row_denom=rd)
     if backward:
         dQ, dK, dV = (torch.empty_like(q) for _ in range(3))
-        bsr.bsr_attn_bwd(q, k, v, O, do, rm, rd, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, scale,
-                         dQ, dK, dV)
+        if plan is not None:
+            bsr.bsr_attn_bwd_plan(plan, q, k, v, O, do, rm, rd, scale, dQ, dK, dV)
+        else:
+            bsr.bsr_attn_bwd(q, k, v, O, do, rm, rd, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, scale,
+                             dQ, dK, dV)
         out.update(dQ=dQ, dK=dK, dV=dV)
     bsr.bsr_attn_check()
-    return {n: t.double().cpu().numpy() for n, t in out.items()}
+    res = {n: t.double().cpu().numpy() for n, t in out.items()}
+    if plan is not None:
+        plan.close()
+    return res
 
 
-def kernels_run(Q, K, V, dO, bm, scale, device="cuda"):
+def kernels_run(Q, K, V, dO, bm, scale, device="cuda", api="per-call"):
     """Names of the library kernels one forward + backward launches (per-launch timing on)."""
     bsr.profile_collect()
     bsr.profile_enable(True)
     try:
-        run_gpu(Q, K, V, dO, bm, scale, device=device)
+        run_gpu(Q, K, V, dO, bm, scale, device=device, api=api)
     finally:
         bsr.profile_enable(False)
     return set(bsr.profile_collect())
+
+
+def expected_plan_kernels(dtype: str, D: int, empty_lines: bool = False) -> set:
+    """The kernels of a forward + backward on a plan: no planner; for 16-bit operands with head_dim 64 / 128
+    the dK/dV walk stores dS and the dQ walk sums dS K (dq_ds); the zero-lines pass where lines are empty."""
+    if dtype in ("bf16", "f16") and D <= 128:
+        k = {"fwd_tc", "delta", "dkdv_tc", "dq_ds"}
+    else:
+        k = {"fwd_wide", "delta", "dq_wide", "dv_wide", "dk_wide"} | ({"split3"} if dtype == "f32" else set())
+    return k | {"zero_lines"} if empty_lines else k
 
 
 def expected_kernels(dtype: str, D: int) -> set:

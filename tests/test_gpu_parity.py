@@ -1,10 +1,11 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU fp64 oracle.
 
-Every workload runs in full on the GPU, in the launch configuration the
-benchmark times.  The global-mask and head_dim-256 / 512 workloads are
-compared element by element on every (batch, head); the density sweep on four
-heads of sixteen, each recomputed whole by the oracle.  A separate test
-checks which kernels served each workload.
+Every workload runs in full on the GPU through both sets of entry points:
+on a plan (the launch configuration the benchmark times) and per call.  The
+global-mask and head_dim-256 / 512 workloads are compared element by element
+on every (batch, head); the density sweep on four heads of sixteen, each
+recomputed whole by the oracle.  Separate tests check which kernels served
+each workload.
 """
 
 import numpy as np
@@ -13,20 +14,24 @@ import torch
 
 from block_sparse_attention_bsr_gb300 import inputs
 
-from parity import compare, expected_kernels, kernels_run, oracle_heads, run_gpu
+from parity import compare, expected_kernels, expected_plan_kernels, kernels_run, oracle_heads, run_gpu
 
 pytestmark = pytest.mark.gpu
 
 
+def _both_apis(Q, K, V, dO, bm, scale, dtype, heads, what):
+    # the plan's entry points and the per-call ones against one oracle run
+    got = {api: run_gpu(Q, K, V, dO, bm, scale, api=api) for api in ("plan", "per-call")}
+    ref = oracle_heads(Q, K, V, dO, bm, scale, heads)
+    return {api: compare(g, ref, dtype, heads=heads, what=f"{what} ({api})") for api, g in got.items()}
+
+
 def _workload(name, heads=None, seed=0):
     wl = inputs.WORKLOADS[name]
-    bm = wl.block_mask()
     Q, K, V, dO = wl.inputs(seed=seed)
-    got = run_gpu(Q, K, V, dO, bm, wl.scale)
     if heads is None:
         heads = [(b, h) for b in range(wl.batch) for h in range(wl.heads)]
-    ref = oracle_heads(Q, K, V, dO, bm, wl.scale, heads)
-    return compare(got, ref, wl.dtype, heads=heads, what=name)
+    return _both_apis(Q, K, V, dO, wl.block_mask(), wl.scale, wl.dtype, heads, name)
 
 
 def test_tiny_fp32_all_heads():
@@ -40,13 +45,10 @@ def test_dilated_s2048_bf16_all_heads():
 def _workload_as(name, dtype, heads=None, seed=0):
     # a workload's mask and shape with operands drawn in another dtype
     wl = inputs.WORKLOADS[name]
-    bm = wl.block_mask()
     Q, K, V, dO = inputs.make_qkvdo(wl.batch, wl.heads, wl.seq, wl.head_dim, dtype, 1.0, seed)
-    got = run_gpu(Q, K, V, dO, bm, wl.scale)
     if heads is None:
         heads = [(b, h) for b in range(wl.batch) for h in range(wl.heads)]
-    ref = oracle_heads(Q, K, V, dO, bm, wl.scale, heads)
-    return compare(got, ref, dtype, heads=heads, what=f"{name} {dtype}")
+    return _both_apis(Q, K, V, dO, wl.block_mask(), wl.scale, dtype, heads, f"{name} {dtype}")
 
 
 def test_dilated_s2048_f16_all_heads():
@@ -77,8 +79,12 @@ def test_workload_runs_on_its_tensor_core_kernels(name):
     # the kernels each workload launches, by name: no other code path serves it
     wl = inputs.WORKLOADS[name]
     Q, K, V, dO = wl.inputs(seed=0)
-    got = kernels_run(Q, K, V, dO, wl.block_mask(), wl.scale)
+    bm = wl.block_mask()
+    got = kernels_run(Q, K, V, dO, bm, wl.scale)
     assert got == expected_kernels(wl.dtype, wl.head_dim), (name, sorted(got))
+    empty = bool((bm.sum(1) == 0).any() or (bm.sum(0) == 0).any())
+    got = kernels_run(Q, K, V, dO, bm, wl.scale, api="plan")
+    assert got == expected_plan_kernels(wl.dtype, wl.head_dim, empty), (name, "plan", sorted(got))
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
@@ -88,17 +94,23 @@ def test_every_dtype_and_head_dim_runs_on_tensor_core_kernels(dtype, D):
     Q, K, V, dO = inputs.make_qkvdo(1, 2, 3 * 128, D, dtype, 1.0, 1)
     got = kernels_run(Q, K, V, dO, bm, 1.0 / np.sqrt(D))
     assert got == expected_kernels(dtype, D), (dtype, D, sorted(got))
+    got = kernels_run(Q, K, V, dO, bm, 1.0 / np.sqrt(D), api="plan")
+    assert got == expected_plan_kernels(dtype, D), (dtype, D, "plan", sorted(got))
 
 
 # ------------------------------------------------------------ edge cases --
 
 def _edge(bm, dtype, D=64, B=1, H=2, std=1.0, seed=3):
+    # both sets of entry points against the oracle; returns the plan's results
     nb = bm.shape[0]
     Q, K, V, dO = inputs.make_qkvdo(B, H, nb * 128, D, dtype, std, seed)
     scale = 1.0 / np.sqrt(D)
-    got = run_gpu(Q, K, V, dO, bm, scale)
-    ref = oracle_heads(Q, K, V, dO, bm, scale, [(b, h) for b in range(B) for h in range(H)])
-    return got, compare(got, ref, dtype, heads=[(b, h) for b in range(B) for h in range(H)])
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    ref = oracle_heads(Q, K, V, dO, bm, scale, heads)
+    for api in ("per-call", "plan"):
+        got = run_gpu(Q, K, V, dO, bm, scale, api=api)
+        errs = compare(got, ref, dtype, heads=heads, what=api)
+    return got, errs
 
 
 DTYPES = ["f32", "bf16", "f16"]
@@ -131,13 +143,15 @@ def test_mostly_empty_lines(dtype, D):
     bm[0:2, 0:4] = True
     Q, K, V, dO = inputs.make_qkvdo(B, H, nb * 128, D, dtype, 1.0, 5)
     scale = 1.0 / np.sqrt(D)
-    got = run_gpu(Q, K, V, dO, bm, scale)
     heads = [(0, 0), (0, 5), (1, 2), (1, 7)]
-    compare(got, oracle_heads(Q, K, V, dO, bm, scale, heads), dtype, heads=heads, what="mostly empty")
-    rows, cols = slice(2 * 128, None), slice(4 * 128, None)
-    assert np.all(got["O"][:, :, rows] == 0) and np.all(got["dQ"][:, :, rows] == 0)
-    assert np.all(got["row_max"][:, :, rows] == -np.inf) and np.all(got["row_denom"][:, :, rows] == 0)
-    assert np.all(got["dK"][:, :, cols] == 0) and np.all(got["dV"][:, :, cols] == 0)
+    ref = oracle_heads(Q, K, V, dO, bm, scale, heads)
+    for api in ("per-call", "plan"):
+        got = run_gpu(Q, K, V, dO, bm, scale, api=api)
+        compare(got, ref, dtype, heads=heads, what=f"mostly empty ({api})")
+        rows, cols = slice(2 * 128, None), slice(4 * 128, None)
+        assert np.all(got["O"][:, :, rows] == 0) and np.all(got["dQ"][:, :, rows] == 0)
+        assert np.all(got["row_max"][:, :, rows] == -np.inf) and np.all(got["row_denom"][:, :, rows] == 0)
+        assert np.all(got["dK"][:, :, cols] == 0) and np.all(got["dV"][:, :, cols] == 0)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -494,9 +508,12 @@ def test_two_pass_forward_refuses_fp32():
 def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
     # Forward and backward on one plan, three times in a row (after each
     # launch the kernels put the plan's work-queue counter back to the grid
-    # size and its other counters back to 0), give the per-call entry points'
-    # results bit for bit; nb = 20 has block row 0 and column 0 long enough
-    # to be split into chunks.
+    # size and its other counters back to 0), give the same results every
+    # time, and the per-call entry points' results bit for bit -- except dQ
+    # of 16-bit operands with head_dim 64 / 128, which the plan sums from the
+    # dS tiles of the dK/dV walk (the per-call walk recomputes dS): that dQ
+    # is held to the oracle.  nb = 20 has block row 0 and column 0 long
+    # enough to be split into chunks.
     import block_sparse_attention_bsr_gb300 as bsr
 
     dev = torch.device("cuda")
@@ -504,10 +521,12 @@ def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
     Q, K, V, dO = inputs.make_qkvdo(1, H, nb * 128, D, dtype, 1.0, 17)
     scale = 1.0 / np.sqrt(D)
     ref = run_gpu(Q, K, V, dO, bm, scale)
+    ds_walk = dtype in ("bf16", "f16") and D <= 128
     rp, ci = inputs.bsr_from_block_mask(bm)
     st = bsr.Structure(rp, ci, nb, dev)
     q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
     plan = st.plan(q)
+    first = None
     for _ in range(3):
         O = torch.empty_like(q)
         rm = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
@@ -516,16 +535,28 @@ def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
         bsr.bsr_attn_fwd_plan(plan, q, k, v, scale, O, rm, rd)
         bsr.bsr_attn_bwd_plan(plan, q, k, v, O, do, rm, rd, scale, dQ, dK, dV)
         bsr.bsr_attn_check()
-        got = dict(O=O, row_max=rm, row_denom=rd, dQ=dQ, dK=dK, dV=dV)
+        got = {n: t.double().cpu().numpy() for n, t in dict(O=O, row_max=rm, row_denom=rd, dQ=dQ, dK=dK,
+                                                               dV=dV).items()}
         for name, t in got.items():
-            assert np.array_equal(t.double().cpu().numpy(), ref[name]), name
+            if not (ds_walk and name == "dQ"):
+                assert np.array_equal(t, ref[name]), name
+        if first is None:
+            first = got
+        for name, t in got.items():
+            assert np.array_equal(t, first[name]), ("repeat", name)
+    if ds_walk:
+        heads = [(0, h) for h in range(H)]
+        compare({"dQ": first["dQ"]}, {"dQ": oracle_heads(Q, K, V, dO, bm, scale, heads)["dQ"]}, dtype,
+                heads=heads, what="plan dQ")
 
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
 def test_plan_with_empty_lines(dtype, D):
     # A plan over a mask with empty block rows and columns: the planned calls
     # write the empty lines' outputs (they are not in the plan's work lists)
-    # into NaN-filled outputs and match the per-call entry points bit for bit.
+    # into NaN-filled outputs and match the per-call entry points bit for bit
+    # (dQ of 16-bit operands, summed from the stored dS tiles on a plan: the
+    # empty rows exactly, the rest against the oracle).
     import block_sparse_attention_bsr_gb300 as bsr
 
     dev = torch.device("cuda")
@@ -550,6 +581,14 @@ def test_plan_with_empty_lines(dtype, D):
         bsr.bsr_attn_check()
         got = dict(O=O, row_max=rm, row_denom=rd, dQ=dQ, dK=dK, dV=dV)
         for name, t in got.items():
+            if name == "dQ" and dtype != "f32":
+                g = t.double().cpu().numpy()
+                empty = np.repeat(bm.sum(1) == 0, 128)
+                assert np.all(g[:, :, empty] == 0), "dQ of empty block rows"
+                heads = [(0, h) for h in range(H)]
+                compare({"dQ": g}, {"dQ": oracle_heads(Q, K, V, dO, bm, scale, heads)["dQ"]}, dtype, heads=heads,
+                        what="plan dQ")
+                continue
             assert np.array_equal(t.double().cpu().numpy(), ref[name]), name
 
 
