@@ -178,7 +178,8 @@ __device__ __forceinline__ void tc_fence_after() {
 // -------------------------------------------------------- descriptors --
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), the fixed version field (1 at bit 46)
-// and the swizzle mode in bits 61..63 (2 = 128-byte swizzle).
+// and the swizzle mode in bits 61..63 (0 = none, 2 = 128-byte, 6 = 32-byte
+// swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t swizzle = 2) {
   uint64_t d = 0;
@@ -366,6 +367,13 @@ struct Half16<__half> {
   static constexpr uint32_t kFmt = 0;
   __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
 };
+
+// 256-bit global store (p 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, uint4 lo, uint4 hi) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(lo.x), "r"(lo.y), "r"(lo.z),
+               "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+               : "memory");
+}
 
 // Stores 16 words (32 16-bit values) at p (16-byte aligned): two 256-bit stores when
 // p is 32-byte aligned (each then fills whole 32-byte sectors), else four

@@ -881,12 +881,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->ds_ready);
           if (jb >= 0) {
             // the dS tile of (block row m, this column) for the dQ walk, in
-            // 16-byte groups of 8 queries: group c / 8 of key r at
-            // ((c / 8) * 128 + r) * 16 bytes, so the warp's 32 keys fill
-            // 512 contiguous bytes per store
-            uint4* dst = (uint4*)((T*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (128 * 128)) + hg * 8 * 128 + r;
+            // the layout dq_ds_kernel stages it in (see there): 32-byte
+            // units of 16 queries, unit c / 16 of key r at
+            // (c / 16) * 4096 + (r / 8) * 256 + (r % 8) * 32 bytes with its
+            // 16-byte halves swapped for r % 8 >= 4, so each store of the
+            // warp's 32 keys fills 1 KB of contiguous memory.
+            uint8_t* dst = (uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (128 * 128 * 2) + hg * 4 * 4096 +
+                           (r / 8) * 256 + (r % 8) * 32;
+            const bool swap = (r & 4) != 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j * 128] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            for (int u = 0; u < 4; ++u) {
+              const uint4 q0 = make_uint4(w[8 * u], w[8 * u + 1], w[8 * u + 2], w[8 * u + 3]);
+              const uint4 q1 = make_uint4(w[8 * u + 4], w[8 * u + 5], w[8 * u + 6], w[8 * u + 7]);
+              st_global_v8(dst + u * 4096, swap ? q1 : q0, swap ? q0 : q1);
+            }
           }
         }
         if (!ok) break;
@@ -945,12 +953,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // back per block, which HBM has room for beside the MMA-bound dK/dV walk.
 //
 // A dS tile (128 queries x 128 keys, 16-bit) sits in memory as the dK/dV
-// walk writes it: 16-byte groups of 8 consecutive queries, key-fastest
-// (group c / 8 of key r at ((c / 8) * 128 + r) * 16 bytes).  As the A
-// operand of dQ += dS K (M = queries, K = keys) that is the MN-major layout
-// without swizzle: 8 x 8 core matrices of 128 contiguous bytes, the next 8
-// keys 128 bytes on (leading byte offset) and the next 8 queries 2048 bytes
-// on (stride byte offset), so a plain bulk copy stages it for the MMA.
+// walk writes it: the MN-major operand layout with 32-byte swizzling, so a
+// plain bulk copy to a 1024-byte aligned stage is ready for the MMA as the
+// A operand of dQ += dS K (M = queries, K = keys).  Its atoms are 8 keys x
+// 16 queries (8 rows of 32 bytes, the 16-byte halves of rows 4..7 swapped);
+// the atoms of the next 8 keys follow at 256 bytes (stride byte offset) and
+// those of the next 16 queries at 4096 bytes (leading byte offset).
 //
 // Warp roles (320 threads): warp 0 the producer (the tile pair of each block
 // through a ring of stages), warp 1 TMEM owner and MMA issuer, warps 2..9
@@ -1089,11 +1097,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
           if (!(ok = warp_wait(&bars->full[st], (g / C::kStages) & 1, ab, a.status))) break;
           tc_fence_after();
           const uint32_t sds = base + st * C::kStageBytes;
-          const uint64_t dA = smem_desc(sds, 128, 2048, 0);  // dS: MN-major, no swizzle
+          const uint64_t dA = smem_desc(sds, 4096, 256, 6);  // dS: MN-major, 32-byte swizzle
           const SDesc dK(sds + C::kDsTile, 16384, 1024);     // K: MN-major, 128-byte swizzle
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: two core matrices of dS, 16 rows of K
-            mma_ss_by(leader, tmem + buf * D, dA + (uint64_t)(kk * 16), dK.at(kk * 2048), idDQ,
+          for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: two atom rows of dS (512 bytes), 16 rows of K
+            mma_ss_by(leader, tmem + buf * D, dA + (uint64_t)(kk * 32), dK.at(kk * 2048), idDQ,
                       (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit_by(leader, &bars->empty[st]);
         }

@@ -72,12 +72,13 @@ def kernels_run(Q, K, V, dO, bm, scale, device="cuda", api="per-call"):
 
 
 def expected_plan_kernels(dtype: str, D: int, empty_lines: bool = False) -> set:
-    """The kernels of a forward + backward on a plan: no planner; for 16-bit operands with head_dim 64 / 128
-    the dK/dV walk stores dS and the dQ walk sums dS K (dq_ds); the zero-lines pass where lines are empty."""
+    """The kernels of a plan's creation (the planner, once) and of a forward + backward on it: for 16-bit
+    operands with head_dim 64 / 128 the dK/dV walk stores dS and the dQ walk sums dS K (dq_ds); the zero-lines
+    pass where lines are empty."""
     if dtype in ("bf16", "f16") and D <= 128:
-        k = {"fwd_tc", "delta", "dkdv_tc", "dq_ds"}
+        k = {"plan", "fwd_tc", "delta", "dkdv_tc", "dq_ds"}
     else:
-        k = {"fwd_wide", "delta", "dq_wide", "dv_wide", "dk_wide"} | ({"split3"} if dtype == "f32" else set())
+        k = {"plan", "fwd_wide", "delta", "dq_wide", "dv_wide", "dk_wide"} | ({"split3"} if dtype == "f32" else set())
     return k | {"zero_lines"} if empty_lines else k
 
 
