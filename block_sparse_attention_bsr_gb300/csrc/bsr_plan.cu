@@ -13,7 +13,7 @@
 //   the forward's split-line partial tiles and the backward's
 //   the bf16 pieces of fp32 operands (wide kernels)
 //   delta and lse2 (one fp32 value each per query row)
-//   (bf16 / fp16, head_dim 64 / 128) the BSR position of each BSC entry
+//   (bf16 / fp16) the BSR position of each BSC entry
 // and, in a second cudaMalloc block for those operands, the dS tiles the
 // dK/dV walk stores for the dQ walk (batch * heads * nnzb tiles of 32 KB;
 // without that memory the plan's dQ walk recomputes the scores instead).
@@ -113,10 +113,10 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
     empty_rows += rp[i + 1] == rp[i] ? 1 : 0;
     empty_cols += cp[i + 1] == cp[i] ? 1 : 0;
   }
-  // 16-bit operands with head_dim 64 / 128: the dK/dV walk hands its dS
-  // tiles to the dQ walk, stored by BSR position; map each BSC entry to it
+  // 16-bit operands: the dK/dV (or dK) walk hands its dS tiles to the dQ
+  // walk, stored by BSR position; map each BSC entry to it
   std::vector<int32_t> bsr_of_bsc;
-  const bool want_ds = tc_bwd_supported(d) && nnzb > 0 &&
+  const bool want_ds = d.dtype != BSR_F32 && nnzb > 0 &&
                        (size_t)d.BH * (size_t)nnzb <= ((size_t)1 << 62) / (128 * 128 * 2);
   if (want_ds) {
     std::vector<int32_t> ci(nnzb), ri(nnzb);

@@ -373,5 +373,10 @@ int tc_grid(const Dims& d);
 // Bytes of one forward partial-result tile (split rows), head_dim 64 / 128.
 size_t fwd_part_bytes(int D);
 bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
+// The dQ walk over stored dS tiles (a.dS, a.nnzb) for 16-bit operands with
+// head_dim 256 / 512, on the wide kernels' block-row plan (a.row_plan,
+// plan_heads(d) heads, partial tiles at a.part_q), after the dK walk that
+// stored the tiles.
+bsr_status launch_dq_ds(const BwdArgs& a, cudaStream_t s);
 
 }  // namespace bsr

@@ -375,6 +375,24 @@ __device__ __forceinline__ void st_global_v8(void* p, uint4 lo, uint4 hi) {
                : "memory");
 }
 
+// Stores one key row's 64 16-bit values (w: 32 packed pairs, queries
+// [64 h, 64 h + 64) of key r) into a 128 x 128 tile laid out as the MN-major
+// MMA operand with 32-byte swizzling (M = queries, K = keys): 32-byte units
+// of 16 queries, unit c / 16 of key r at (c / 16) * 4096 + (r / 8) * 256 +
+// (r % 8) * 32 bytes from the (1024-byte aligned) tile, its 16-byte halves
+// swapped for r % 8 >= 4.  Four 256-bit stores; the 32 lanes of a warp (32
+// consecutive keys) fill 1 KB of contiguous memory with each.
+__device__ __forceinline__ void st_tile_sw32_row64(uint8_t* tile, int r, int h, const uint32_t (&w)[32]) {
+  uint8_t* dst = tile + h * 4 * 4096 + (r / 8) * 256 + (r % 8) * 32;
+  const bool swap = (r & 4) != 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint4 q0 = make_uint4(w[8 * u], w[8 * u + 1], w[8 * u + 2], w[8 * u + 3]);
+    const uint4 q1 = make_uint4(w[8 * u + 4], w[8 * u + 5], w[8 * u + 6], w[8 * u + 7]);
+    st_global_v8(dst + u * 4096, swap ? q1 : q0, swap ? q0 : q1);
+  }
+}
+
 // Stores 16 words (32 16-bit values) at p (16-byte aligned): two 256-bit stores when
 // p is 32-byte aligned (each then fills whole 32-byte sectors), else four
 // 128-bit stores.

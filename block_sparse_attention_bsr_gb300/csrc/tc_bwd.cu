@@ -879,23 +879,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->ds_ready);
-          if (jb >= 0) {
-            // the dS tile of (block row m, this column) for the dQ walk, in
-            // the layout dq_ds_kernel stages it in (see there): 32-byte
-            // units of 16 queries, unit c / 16 of key r at
-            // (c / 16) * 4096 + (r / 8) * 256 + (r % 8) * 32 bytes with its
-            // 16-byte halves swapped for r % 8 >= 4, so each store of the
-            // warp's 32 keys fills 1 KB of contiguous memory.
-            uint8_t* dst = (uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (128 * 128 * 2) + hg * 4 * 4096 +
-                           (r / 8) * 256 + (r % 8) * 32;
-            const bool swap = (r & 4) != 0;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint4 q0 = make_uint4(w[8 * u], w[8 * u + 1], w[8 * u + 2], w[8 * u + 3]);
-              const uint4 q1 = make_uint4(w[8 * u + 4], w[8 * u + 5], w[8 * u + 6], w[8 * u + 7]);
-              st_global_v8(dst + u * 4096, swap ? q1 : q0, swap ? q0 : q1);
-            }
-          }
+          if (jb >= 0)  // the dS tile of (block row m, this column), in the layout dq_ds_kernel stages
+            st_tile_sw32_row64((uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (128 * 128 * 2), r, hg, w);
         }
         if (!ok) break;
         if (cur.slot < 0) {
@@ -960,21 +945,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the atoms of the next 8 keys follow at 256 bytes (stride byte offset) and
 // those of the next 16 queries at 4096 bytes (leading byte offset).
 //
+// A work item covers W = min(D, 256) output columns: head_dim 512 runs as
+// two slices, planned as heads of their own (the wide kernels' plan, so a
+// split row's chunks merge per slice), each reading every dS tile of its row
+// once and the slice's columns of K.
+//
 // Warp roles (320 threads): warp 0 the producer (the tile pair of each block
 // through a ring of stages), warp 1 TMEM owner and MMA issuer, warps 2..9
-// the epilogue (thread (w, l) owns dQ row 32 (w % 4) + l and half of its
-// columns), which stores an item's dQ from one of two TMEM accumulators
-// while the MMAs of the next item fill the other.
+// the epilogue (thread (w, l) owns dQ row 32 (w % 4) + l and half of the
+// slice's columns), which stores an item's dQ from one of two TMEM
+// accumulators while the MMAs of the next item fill the other.
 template <int D>
 struct DsCfg {
-  static constexpr int kBoxes = D / 64;
-  static constexpr int kKTile = 128 * D * 2;
+  static constexpr int W = D < 256 ? D : 256;  // output columns per work item
+  static constexpr int NSL = D / W;
+  static constexpr int kBoxes = W / 64;
+  static constexpr int kKTile = 128 * W * 2;
   static constexpr int kDsTile = 128 * 128 * 2;
   static constexpr int kStageBytes = kDsTile + kKTile;  // a multiple of 1024 (the K boxes are swizzled)
-  static constexpr int kStages = D == 64 ? 4 : 3;
+  static constexpr int kStages = D == 64 ? 4 : (W == 256 ? 2 : 3);
   static constexpr int kBarOff = kStageBytes * kStages;
   static constexpr int kSmem = kBarOff + 512 + 1024;
-  static constexpr uint32_t kCols = D == 64 ? 128 : 256;  // two accumulators of D columns
+  static constexpr uint32_t kCols = 2 * W <= 128 ? 128 : (2 * W <= 256 ? 256 : 512);  // two accumulators of W columns
 };
 
 struct DsBars {
@@ -1003,10 +995,12 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
   static_assert(C::kSmem <= 232448, "shared memory over the per-CTA limit");
   static_assert(C::kStageBytes % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled boxes");
 
+  constexpr int W = C::W, NSL = C::NSL;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
-  const PlanLayout lay = plan_layout(a.row_plan, a.d.nb, (int)gridDim.x, a.d.BH);
-  if (warp == 0) plan_prefetch_l2(a.row_plan, plan_words(a.d.nb, (int)gridDim.x, a.d.BH));
+  const int BHp = a.d.BH * NSL;  // the planner's heads: one per (batch, head, slice)
+  const PlanLayout lay = plan_layout(a.row_plan, a.d.nb, (int)gridDim.x, BHp);
+  if (warp == 0) plan_prefetch_l2(a.row_plan, plan_words(a.d.nb, (int)gridDim.x, BHp));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -1034,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   griddep_wait();
-  const Walk walk = make_walk(lay, a.d.BH);
+  const Walk walk = make_walk(lay, BHp);
   const uint32_t tmem = bars->tmem_slot;
   volatile int* ab = &bars->abort_flag;
   RingSmem* ring = &bars->ring;
@@ -1049,8 +1043,9 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
         if (!(ok = ring_put(ring, t, lay.header + 1, walk.total, &k, ab, a.status)) || k < 0) break;
         Cursor cur;
         walk.decode(k, cur);
+        const int bh = cur.bh / NSL, sl = cur.bh % NSL;
         // the row's dS tiles are consecutive (BSR order)
-        const uint8_t* ds = (const uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + cur.first) * C::kDsTile;
+        const uint8_t* ds = (const uint8_t*)a.dS + ((size_t)bh * a.nnzb + cur.first) * C::kDsTile;
         for (int i = 0; i < cur.n; ++i, ++g) {
           int n = a.col_idx[cur.first + i];
           if (n < 0 || n >= a.d.nb) {
@@ -1065,7 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
           bulk_load(dst + C::kDsTile / 2, ds + (size_t)i * C::kDsTile + C::kDsTile / 2, C::kDsTile / 2,
                     &bars->full[st]);
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_2d(dst + C::kDsTile + b * 16384, &tmK, b * 64, cur.bh * S + n * 128, &bars->full[st]);
+            tma_load_2d(dst + C::kDsTile + b * 16384, &tmK, sl * W + b * 64, bh * S + n * 128, &bars->full[st]);
         }
       }
       // drain: every copy issued must land before the CTA exits
@@ -1075,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA --
     const uint32_t leader = elect_one();
-    const uint32_t idDQ = instr_desc(Half16<T>::kFmt, 1, 1, D, 128);
+    const uint32_t idDQ = instr_desc(Half16<T>::kFmt, 1, 1, W, 128);
     const uint32_t base = smem_u32(sm);
     int g = 0, q = 0;  // blocks, non-empty items
     bool ok = true;
@@ -1101,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
           const SDesc dK(sds + C::kDsTile, 16384, 1024);     // K: MN-major, 128-byte swizzle
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: two atom rows of dS (512 bytes), 16 rows of K
-            mma_ss_by(leader, tmem + buf * D, dA + (uint64_t)(kk * 32), dK.at(kk * 2048), idDQ,
+            mma_ss_by(leader, tmem + buf * W, dA + (uint64_t)(kk * 32), dK.at(kk * 2048), idDQ,
                       (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit_by(leader, &bars->empty[st]);
         }
@@ -1131,35 +1126,36 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
       if (!ok || k < 0) break;
       Cursor cur;
       walk.decode_warp(k, cur);
-      const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
-      T* dqrow = (T*)a.dQ + grow * D + hg * (D / 2);
+      const int bh = cur.bh / NSL, sl = cur.bh % NSL;
+      const size_t grow = (size_t)bh * S + (size_t)cur.line * 128 + r;
+      T* dqrow = (T*)a.dQ + grow * D + sl * W + hg * (W / 2);
       if (cur.n == 0) {
-        zero_cols<D / 2>(dqrow);
+        zero_cols<W / 2>(dqrow);
       } else {
         const int buf = q & 1;
         if (!(ok = warp_wait(&bars->acc_full[buf], (q >> 1) & 1, ab, a.status))) break;
         tc_fence_after();
-        const uint32_t acc = tmem + lane_base + buf * D + hg * (D / 2);
+        const uint32_t acc = tmem + lane_base + buf * W + hg * (W / 2);
         ++q;
         if (cur.slot < 0) {
-          store_acc_cols<D / 2>(acc, dqrow, a.d.scale, (size_t)D);
+          store_acc_cols<W / 2>(acc, dqrow, a.d.scale, (size_t)D);
           tc_fence_before();
           mbar_arrive(&bars->acc_empty[buf]);
         } else {
           // chunk of a split row: publish the fp32 partial, the last chunk merges
-          const size_t kTileF = (size_t)128 * D;
-          store_acc_part<D / 2>(acc, a.part_q + (size_t)(cur.slot * a.d.BH + cur.bh) * kTileF, hg * (D / 8), r);
+          const size_t kTileF = (size_t)128 * W;
+          store_acc_part<W / 2>(acc, a.part_q + (size_t)(cur.slot * BHp + cur.bh) * kTileF, hg * (W / 8), r);
           tc_fence_before();
           mbar_arrive(&bars->acc_empty[buf]);
           bool last = false;
-          if (!(ok = merge_arrive(lay, cur.slot, cur.bh, a.d.BH, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
+          if (!(ok = merge_arrive(lay, cur.slot, cur.bh, BHp, hg, r, &bars->merge_flag[hg], &bars->wg_sync[hg],
                                   sync_phase, ab, a.status, &last)))
             break;
           if (last) {
             const int sl = lay.slot_line[cur.slot];
             const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
-            merge_tiles<D / 2>(a.part_q + (size_t)(base * a.d.BH + cur.bh) * kTileF, (size_t)a.d.BH * kTileF, nc,
-                               hg * (D / 8), r, dqrow, a.d.scale);
+            merge_tiles<W / 2>(a.part_q + (size_t)(base * BHp + cur.bh) * kTileF, (size_t)BHp * kTileF, nc,
+                               hg * (W / 8), r, dqrow, a.d.scale);
           }
         }
       }
@@ -1175,36 +1171,44 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
   if (threadIdx.x == 0) plan_exit(lay);
 }
 
+// The dQ walk over the stored dS tiles, in `s` as a programmatic dependent
+// of the walk that stored them.
+template <typename T, int D>
+bsr_status launch_dq(const BwdArgs& a, const CUtensorMap& tmK, int grid, cudaStream_t s) {
+  auto dq = dq_ds_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, DsCfg<D>::kSmem);
+  if (e != cudaSuccess)
+    return fail(BSR_ERR_CUDA, "dq_ds: cudaFuncSetAttribute(%d): %s", DsCfg<D>::kSmem, cudaGetErrorString(e));
+  if (profiling_launches()) {
+    LaunchTimer timer("dq_ds", s);
+    dq<<<grid, kThreads, DsCfg<D>::kSmem, s>>>(tmK, a);
+    return check_launch("dq_ds launch");
+  }
+  e = launch_dependent(dq, dim3(grid), dim3(kThreads), DsCfg<D>::kSmem, s, tmK, a);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_ds launch: %s", cudaGetErrorString(e));
+  return check_launch("dq_ds launch");
+}
+
 // On a plan (a.dS set): the dK/dV walk, which stores the dS tiles, then the
 // dQ walk over them, both in `s` as programmatic dependents.
 template <typename T, int D>
 bsr_status launch_bwd_ds(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap& tmdO, int grid, cudaStream_t s) {
   auto dkdv = dkdv_tc_kernel<T, D>;
-  auto dq = dq_ds_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<D>::kSmem);
   if (e != cudaSuccess)
     return fail(BSR_ERR_CUDA, "dkdv_tc: cudaFuncSetAttribute(%d): %s", DkvCfg<D>::kSmem, cudaGetErrorString(e));
-  e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, DsCfg<D>::kSmem);
-  if (e != cudaSuccess)
-    return fail(BSR_ERR_CUDA, "dq_ds: cudaFuncSetAttribute(%d): %s", DsCfg<D>::kSmem, cudaGetErrorString(e));
   if (profiling_launches()) {
-    {
-      LaunchTimer timer("dkdv_tc", s);
-      dkdv<<<grid, kThreads, DkvCfg<D>::kSmem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
-      bsr_status st = check_launch("dkdv_tc launch");
-      if (st != BSR_OK) return st;
-    }
-    LaunchTimer timer("dq_ds", s);
-    dq<<<grid, kThreads, DsCfg<D>::kSmem, s>>>(tm.k, a);
-    return check_launch("dq_ds launch");
+    LaunchTimer timer("dkdv_tc", s);
+    dkdv<<<grid, kThreads, DkvCfg<D>::kSmem, s>>>(tm.q, tm.k, tm.v, tmdO, a);
+    bsr_status st = check_launch("dkdv_tc launch");
+    if (st != BSR_OK) return st;
+  } else {
+    e = launch_dependent(dkdv, dim3(grid), dim3(kThreads), DkvCfg<D>::kSmem, s, tm.q, tm.k, tm.v, tmdO, a);
+    if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dkdv_tc launch: %s", cudaGetErrorString(e));
+    bsr_status st = check_launch("dkdv_tc launch");
+    if (st != BSR_OK) return st;
   }
-  e = launch_dependent(dkdv, dim3(grid), dim3(kThreads), DkvCfg<D>::kSmem, s, tm.q, tm.k, tm.v, tmdO, a);
-  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dkdv_tc launch: %s", cudaGetErrorString(e));
-  bsr_status st = check_launch("dkdv_tc launch");
-  if (st != BSR_OK) return st;
-  e = launch_dependent(dq, dim3(grid), dim3(kThreads), DsCfg<D>::kSmem, s, tm.k, a);
-  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_ds launch: %s", cudaGetErrorString(e));
-  return check_launch("dq_ds launch");
+  return launch_dq<T, D>(a, tm.k, grid, s);
 }
 
 // dQ and dK / dV read the same inputs and write different outputs, so they
@@ -1252,6 +1256,22 @@ bsr_status launch_bwd(const BwdArgs& a, const TensorMaps& tm, const CUtensorMap&
 }
 
 }  // namespace
+
+bsr_status launch_dq_ds(const BwdArgs& a, cudaStream_t s) {
+  const int grid = tc_grid(a.d);
+  if (grid <= 0) return fail(BSR_ERR_CUDA, "dq_ds: cannot query the SM count");
+  if (!a.dS || (((uintptr_t)a.dS) & 15) || a.d.dtype == BSR_F32)
+    return fail(BSR_ERR_INVALID_ARG, "dq_ds: needs 16-byte aligned dS tiles of 16-bit operands");
+  CUtensorMap tmK;
+  bsr_status st = make_tensor_map(a.d, a.K, &tmK, "K");
+  if (st != BSR_OK) return st;
+  const bool h = a.d.dtype == BSR_F16;
+  switch (a.d.D) {
+    case 256: return h ? launch_dq<__half, 256>(a, tmK, grid, s) : launch_dq<__nv_bfloat16, 256>(a, tmK, grid, s);
+    case 512: return h ? launch_dq<__half, 512>(a, tmK, grid, s) : launch_dq<__nv_bfloat16, 512>(a, tmK, grid, s);
+    default: return fail(BSR_ERR_UNSUPPORTED, "dq_ds: head_dim %d", a.d.D);
+  }
+}
 
 bool tc_bwd_supported(const Dims& d) {
   return (d.dtype == BSR_BF16 || d.dtype == BSR_F16) && (d.D == 64 || d.D == 128);

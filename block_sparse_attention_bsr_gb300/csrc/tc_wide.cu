@@ -213,6 +213,11 @@ struct WideArgs {
   const float* delta;   // backward: per query row
   float* part;          // partial results of split lines (wide_part_floats per tile)
   int* status;
+  // DK with 16-bit operands on a plan: the dS tiles for the dQ walk over
+  // them (dq_ds_kernel, tc_bwd.cu), [BH][nnzb] tiles in BSR order (null: none)
+  void* dS;
+  const int32_t* bsr_of_bsc;
+  int nnzb;
 };
 
 struct WBars {
@@ -839,6 +844,16 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
         dl_r = a.delta[grow];
       }
       for (int i = 0; i < cur.n; ++i, ++g) {
+        int jb = -1;  // DK on a plan: the BSR position of the block, where its dS tile goes
+        if constexpr (MODE == kDk && NP == 1) {
+          if (a.dS && sl == 0) {
+            jb = a.bsr_of_bsc[cur.first + i];
+            if (jb < 0 || jb >= a.nnzb) {
+              atomicExch(a.status, kStatusDeviceCheck);
+              jb = -1;
+            }
+          }
+        }
         if (!(ok = warp_wait(&bars->x1_full, g & 1, ab, a.status))) break;
         if (C::kX2 && !(ok = warp_wait(&bars->x2_full, g & 1, ab, a.status))) break;
         if ((MODE == kDv || MODE == kDk) && !(ok = warp_wait(&bars->stat_full[g & 1], (g >> 1) & 1, ab, a.status)))
@@ -952,6 +967,14 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->z_full[g & 1]);
+        if constexpr (MODE == kDk && NP == 1) {
+          if (jb >= 0) {  // dS of (block row m, this column) for the dQ walk (first slice only)
+            uint32_t v[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = Half16<Op>::pack(z[2 * k], z[2 * k + 1]);
+            st_tile_sw32_row64((uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (128 * 128 * 2), r, hg, v);
+          }
+        }
       }
       if (!ok) break;
       // ------------------------------------------------------- epilogue --
@@ -1151,10 +1174,20 @@ bsr_status launch_bwd_wide(const BwdArgs& a, cudaStream_t s) {
   const size_t set = a.part_kv ? plan_tiles(a.d.nb, grid, plan_heads(a.d)) * (part_tile_bytes(a.d, false) / 4) : 0;
   const WideArgs q{a.d, a.col_idx, a.row_plan, a.dQ, nullptr, nullptr, a.lse2, a.delta, a.part_q, a.status};
   const WideArgs v{a.d, a.row_idx, a.col_plan, a.dV, nullptr, nullptr, a.lse2, a.delta, a.part_kv, a.status};
-  const WideArgs k{a.d, a.row_idx, a.col_plan2, a.dK, nullptr, nullptr, a.lse2, a.delta,
-                   a.part_kv ? a.part_kv + set : nullptr, a.status};
+  WideArgs k{a.d, a.row_idx, a.col_plan2, a.dK, nullptr, nullptr, a.lse2, a.delta,
+             a.part_kv ? a.part_kv + set : nullptr, a.status};
   // dQ, dV and dK read the same inputs and write different outputs; each is
-  // a persistent grid of its own work list
+  // a persistent grid of its own work list.  On a plan with 16-bit operands
+  // (a.dS) the dK walk stores its dS tiles and the dQ walk runs after it,
+  // summing dS K over them (dq_ds_kernel) instead of recomputing the scores.
+  if (a.dS && a.d.dtype != BSR_F32) {
+    k.dS = a.dS;
+    k.bsr_of_bsc = a.bsr_of_bsc;
+    k.nnzb = a.nnzb;
+    if ((st = dispatch_mode<kDv>(tm, v, grid, s, "dv_wide")) != BSR_OK) return st;
+    if ((st = dispatch_mode<kDk>(tm, k, grid, s, "dk_wide")) != BSR_OK) return st;
+    return launch_dq_ds(a, s);
+  }
   if ((st = dispatch_mode<kDq>(tm, q, grid, s, "dq_wide")) != BSR_OK) return st;
   if ((st = dispatch_mode<kDv>(tm, v, grid, s, "dv_wide")) != BSR_OK) return st;
   return dispatch_mode<kDk>(tm, k, grid, s, "dk_wide");
