@@ -54,18 +54,14 @@ def alg_flops(wl, nnzb, part="total"):
 # current sources still hash the same (otherwise the roofline's traffic is
 # null until the kernel is captured again).
 MEASURED_TRAFFIC = {
-    ("global_s8192", "dkdv_tc"): {"bytes": 206.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                  "sha256": "1227773f105e7cdb580449cf8ed477a3a5eabebe8f1f970e4a1133b78f593621"},
-    ("global_s8192", "dq_tc"): {"bytes": 176.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                "sha256": "1227773f105e7cdb580449cf8ed477a3a5eabebe8f1f970e4a1133b78f593621"},
-    ("global_s8192", "fwd_tc"): {"bytes": 134.1e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "454008d95f56c5d076ba97f9adb416c76aa7403a69379d7ec700507e6fa0dcf0"},
-    ("local_s8192_d256", "dq_wide"): {"bytes": 153.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "e08bc9dde37c17da6c7c35888f93e6b2df101e3d1c53299cfd63f5d5385224db"},
-    ("local_s8192_d512", "dq_wide"): {"bytes": 402.1e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "e08bc9dde37c17da6c7c35888f93e6b2df101e3d1c53299cfd63f5d5385224db"},
-    ("global_s8192_f32", "dk_wide"): {"bytes": 670.3e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "e08bc9dde37c17da6c7c35888f93e6b2df101e3d1c53299cfd63f5d5385224db"},
+    ("global_s8192", "dkdv_tc"): {"bytes": 433.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                  "sha256": "c4e8cb79e4c9dde6e2a681641e15bf9282ddf7236c4cc792dc4356747f9515be"},
+    ("global_s8192", "dq_ds"): {"bytes": 304.1e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                "sha256": "c4e8cb79e4c9dde6e2a681641e15bf9282ddf7236c4cc792dc4356747f9515be"},
+    ("local_s8192_d256", "dk_wide"): {"bytes": 251.7e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "dc14bf5b85f3d8d9a91ada639fd3e75cfe0b930f278a93551b6ca35d2aae93a9"},
+    ("local_s8192_d256", "dq_ds"): {"bytes": 165.1e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                    "sha256": "c4e8cb79e4c9dde6e2a681641e15bf9282ddf7236c4cc792dc4356747f9515be"},
 }
 
 

@@ -963,17 +963,23 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
             tc_fence_after();
           }
         }
-        store_z<Op, MODE, NP, C::kZP>(tmem + lb, hg, C::kZBufs == 2 ? (g & 1) : 0, z);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->z_full[g & 1]);
         if constexpr (MODE == kDk && NP == 1) {
-          if (jb >= 0) {  // dS of (block row m, this column) for the dQ walk (first slice only)
-            uint32_t v[32];
+          // dS^T as operand-type pairs: into TMEM for dK and, on a plan, into
+          // the dS tile of (block row m, this column) for the dQ walk (the
+          // first slice's walk only)
+          uint32_t v[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = Half16<Op>::pack(z[2 * k], z[2 * k + 1]);
-            st_tile_sw32_row64((uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (128 * 128 * 2), r, hg, v);
-          }
+          for (int k = 0; k < 32; ++k) v[k] = Half16<Op>::pack(z[2 * k], z[2 * k + 1]);
+          tmem_st32(tmem + lb + zcol<MODE, NP>(0, hg, 0), v);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->z_full[g & 1]);
+          if (jb >= 0) st_tile_sw32_row64((uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (128 * 128 * 2), r, hg, v);
+        } else {
+          store_z<Op, MODE, NP, C::kZP>(tmem + lb, hg, C::kZBufs == 2 ? (g & 1) : 0, z);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->z_full[g & 1]);
         }
       }
       if (!ok) break;
