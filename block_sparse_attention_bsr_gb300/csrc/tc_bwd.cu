@@ -1,37 +1,40 @@
 // Tensor-core backward pass for 16-bit operands (bf16 or fp16, fp32
-// accumulation; head_dim 64 / 128) on sm_103a.
+// accumulation; head_dim 64 / 128, and the dQ walk over stored dS tiles at
+// every head_dim) on sm_103a.
 //
-// Two kernels, each output tile with exactly one writer and no atomics
-// ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.5.1]):
+// Persistent kernels, each output tile with exactly one writer and no
+// atomics ("trnsparse 0.4.1 -> 0.6.0" diff, CHANGELOG [0.5.1]):
 //
-//  * dQ (row-first, mirrors the forward, _attn_bwd_dq_kernel): one CTA per
-//    block row m of one (batch, head).  For every stored block (m, n):
-//        S  = Q_m K_n^T,  dP = dO_m V_n^T                   (tcgen05, TMEM)
-//        P  = exp(scale S - row_max) / row_denom,  dS = P * (dP - D_m)
-//        dQ_m += dS K_n                                       (tcgen05, TMEM)
-//    and dQ_m * scale is stored at the end.
-//  * dK/dV (column-first over the BSC lists, _attn_bwd_dkdv_kernel): one CTA
-//    per block column n.  For every block row m that stores (m, n):
-//        S^T = K_n Q_m^T,  dP^T = V_n dO_m^T
-//        P^T, dS^T as above with the statistics of the 128 queries of m
-//        dV_n += P^T dO_m,   dK_n += dS^T Q_m
-//    and dK_n * scale, dV_n are stored at the end.
+//  * dK/dV (column-first over the BSC lists, _attn_bwd_dkdv_kernel): work
+//    items are block columns n of one (batch, head).  For every block row m
+//    that stores (m, n):
+//        S^T = K_n Q_m^T,  dP^T = V_n dO_m^T                 (tcgen05, TMEM)
+//        P^T = exp(scale S^T - row_max) / row_denom,  dS^T = P^T * (dP^T - D_m)
+//        dV_n += P^T dO_m,   dK_n += dS^T Q_m                  (tcgen05, TMEM)
+//    and dK_n * scale, dV_n are stored at the end.  On a plan it also stores
+//    each dS tile (bf16 / fp16) for the dQ walk below.
+//  * dQ over stored dS (row-first, on a plan): items are block rows m; for
+//    every stored block (m, n), dQ_m += dS_mn K_n, and dQ_m * scale is
+//    stored at the end (dq_ds_kernel).
+//  * dQ recomputing (row-first, mirrors the forward, _attn_bwd_dq_kernel; the
+//    per-call entry points): for every stored block (m, n)
+//        S  = Q_m K_n^T,  dP = dO_m V_n^T,  P and dS as above,  dQ_m += dS K_n.
 //
 // The statistics enter as one base-2 log-sum-exp per query,
 // lse2 = row_max log2(e) + log2(row_denom), so P = 2^(scale log2(e) S - lse2);
 // lse2 and the delta D_i = dO_i . O_i ("trnsparse 0.4.1 -> 0.6.0" diff,
 // CHANGELOG [0.5.0]) come from the delta kernel that runs first.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
-// issuer, warps 2..9 two elementwise warpgroups.  Thread (warp w, lane l)
-// owns TMEM lane 32 (w % 4) + l (a query row in dQ, a key row in dK/dV);
-// warpgroup g = (w - 2) / 4 handles columns [64 g, 64 g + 64) of the 128 x 128
-// score tiles and half of the output columns in the epilogue.  A warpgroup
-// copies its S / dP columns into registers at once and releases them, so the
-// MMA of the next block overlaps the elementwise work of this one.  dS (dQ
-// kernel) and P^T (dK/dV kernel) go back to TMEM as bf16 and feed the next
-// MMA as its A operand from TMEM; dS^T goes to shared memory.
-// All waits are bounded (see sm100.cuh).
+// Warp roles of the dK/dV and recomputing dQ kernels (320 threads): warp 0
+// TMA producer, warp 1 TMEM owner and MMA issuer, warps 2..9 two elementwise
+// warpgroups.  Thread (warp w, lane l) owns TMEM lane 32 (w % 4) + l (a query
+// row in dQ, a key row in dK/dV); warpgroup g = (w - 2) / 4 handles columns
+// [64 g, 64 g + 64) of the 128 x 128 score tiles and half of the output
+// columns in the epilogue.  A warpgroup copies its S / dP columns into
+// registers at once and releases them, so the MMA of the next block overlaps
+// the elementwise work of this one.  dS (dQ kernel), P^T and dS^T (dK/dV
+// kernel) go back to TMEM as 16-bit values and feed the next MMA as its A
+// operand from TMEM.  All waits are bounded (see sm100.cuh).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
