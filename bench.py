@@ -54,14 +54,20 @@ def alg_flops(wl, nnzb, part="total"):
 # current sources still hash the same (otherwise the roofline's traffic is
 # null until the kernel is captured again).
 MEASURED_TRAFFIC = {
-    ("global_s8192", "dkdv_tc"): {"bytes": 433.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                  "sha256": "c4e8cb79e4c9dde6e2a681641e15bf9282ddf7236c4cc792dc4356747f9515be"},
-    ("global_s8192", "dq_ds"): {"bytes": 304.1e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                "sha256": "c4e8cb79e4c9dde6e2a681641e15bf9282ddf7236c4cc792dc4356747f9515be"},
-    ("local_s8192_d256", "dk_wide"): {"bytes": 251.7e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+    ("global_s8192", "dkdv_tc"): {"bytes": 429.8e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                  "sha256": "de916ed94338ae996b25bee23a1300e9173fa08234f488fb820f782c211a715e"},
+    ("global_s8192", "dq_ds"): {"bytes": 300.7e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                "sha256": "de916ed94338ae996b25bee23a1300e9173fa08234f488fb820f782c211a715e"},
+    ("global_s8192", "fwd_tc"): {"bytes": 137.8e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+                                 "sha256": "6b348a4d57aa31d13d83b62106bb1fe180754b6caba85bc0d31858b530f06bca"},
+    ("local_s8192_d256", "fwd_wide"): {"bytes": 116.9e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                       "sha256": "dc14bf5b85f3d8d9a91ada639fd3e75cfe0b930f278a93551b6ca35d2aae93a9"},
+    ("local_s8192_d256", "dv_wide"): {"bytes": 112.5e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
                                       "sha256": "dc14bf5b85f3d8d9a91ada639fd3e75cfe0b930f278a93551b6ca35d2aae93a9"},
-    ("local_s8192_d256", "dq_ds"): {"bytes": 165.1e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                    "sha256": "c4e8cb79e4c9dde6e2a681641e15bf9282ddf7236c4cc792dc4356747f9515be"},
+    ("local_s8192_d256", "dk_wide"): {"bytes": 244.7e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+                                      "sha256": "dc14bf5b85f3d8d9a91ada639fd3e75cfe0b930f278a93551b6ca35d2aae93a9"},
+    ("local_s8192_d256", "dq_ds"): {"bytes": 163.1e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+                                    "sha256": "de916ed94338ae996b25bee23a1300e9173fa08234f488fb820f782c211a715e"},
 }
 
 
