@@ -13,10 +13,11 @@
 //   the forward's split-line partial tiles and the backward's
 //   the bf16 pieces of fp32 operands (wide kernels)
 //   delta and lse2 (one fp32 value each per query row)
-//   (bf16 / fp16) the BSR position of each BSC entry
-// and, in a second cudaMalloc block for those operands, the dS tiles the
-// dK/dV walk stores for the dQ walk (batch * heads * nnzb tiles of 32 KB;
-// without that memory the plan's dQ walk recomputes the scores instead).
+//   the BSR position of each BSC entry
+// and, in a second cudaMalloc block, the dS tiles the dK/dV (or dK) walk
+// stores for the dQ walk (batch * heads * nnzb tiles of 32 KB, 64 KB for
+// fp32 operands; without that memory the plan's dQ walk recomputes the
+// scores instead).
 // The kernels put the plans' work-queue counters back to the grid size and
 // their arrival counters back to 0 when they finish, so the lists are built
 // once, at creation.
@@ -113,11 +114,12 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
     empty_rows += rp[i + 1] == rp[i] ? 1 : 0;
     empty_cols += cp[i + 1] == cp[i] ? 1 : 0;
   }
-  // 16-bit operands: the dK/dV (or dK) walk hands its dS tiles to the dQ
-  // walk, stored by BSR position; map each BSC entry to it
+  // the dK/dV (or dK) walk hands its dS tiles to the dQ walk, stored by BSR
+  // position; map each BSC entry to it
   std::vector<int32_t> bsr_of_bsc;
-  const bool want_ds = d.dtype != BSR_F32 && nnzb > 0 &&
-                       (size_t)d.BH * (size_t)nnzb <= ((size_t)1 << 62) / (128 * 128 * 2);
+  // a block's dS: one 16-bit tile, or two bf16 piece tiles for fp32 operands
+  const size_t ds_tile_b = d.dtype == BSR_F32 ? 2 * 128 * 128 * 2 : 128 * 128 * 2;
+  const bool want_ds = nnzb > 0 && (size_t)d.BH * (size_t)nnzb <= ((size_t)1 << 62) / ds_tile_b;
   if (want_ds) {
     std::vector<int32_t> ci(nnzb), ri(nnzb);
     e = cudaMemcpyAsync(ci.data(), col_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToHost, s);
@@ -204,7 +206,7 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   p->dS = nullptr;
   if (want_ds) {
     void* ds = nullptr;
-    if (cudaMalloc(&ds, (size_t)d.BH * nnzb * (128 * 128 * 2)) == cudaSuccess) {
+    if (cudaMalloc(&ds, (size_t)d.BH * nnzb * ds_tile_b) == cudaSuccess) {
       p->dS = ds;
       p->bsr_of_bsc = (int32_t*)c;
     } else {

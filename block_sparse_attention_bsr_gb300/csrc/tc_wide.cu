@@ -845,7 +845,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
       }
       for (int i = 0; i < cur.n; ++i, ++g) {
         int jb = -1;  // DK on a plan: the BSR position of the block, where its dS tile goes
-        if constexpr (MODE == kDk && NP == 1) {
+        if constexpr (MODE == kDk) {
           if (a.dS && sl == 0) {
             jb = a.bsr_of_bsc[cur.first + i];
             if (jb < 0 || jb >= a.nnzb) {
@@ -980,6 +980,23 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->z_full[g & 1]);
+          if constexpr (MODE == kDk && NP == 3) {
+            if (jb >= 0) {
+              // fp32 on a plan: dS as two bf16 pieces s0 = bf16(dS), s1 =
+              // bf16(dS - s0) (2^-16 |dS|), one tile each, for dq_ds32_kernel
+              uint32_t v0[32], v1[32];
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const float a0 = __bfloat162float(__float2bfloat16_rn(z[2 * k]));
+                const float b0 = __bfloat162float(__float2bfloat16_rn(z[2 * k + 1]));
+                v0[k] = pack_bf16x2(a0, b0);
+                v1[k] = pack_bf16x2(z[2 * k] - a0, z[2 * k + 1] - b0);
+              }
+              uint8_t* tile = (uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (2 * 128 * 128 * 2);
+              st_tile_sw32_row64(tile, r, hg, v0);
+              st_tile_sw32_row64(tile + 128 * 128 * 2, r, hg, v1);
+            }
+          }
         }
       }
       if (!ok) break;
@@ -1029,6 +1046,264 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0) plan_exit(lay);
+}
+
+// ------------------------------------------------ fp32 dQ over stored dS ----
+// fp32 operands on a plan: the dK walk stores dS as two bf16 pieces (dS =
+// s0 + s1 to 2^-16 |dS|, one tile each in the layout of st_tile_sw32_row64,
+// 64 KB per block), and this walk sums dQ_m = scale sum_n dS_mn K_n with the
+// five piece products s_i k_j, i + j <= 2, over the three bf16 pieces k_j of
+// K (the products with i + j > 2, and s2, are below 2^-24 |dS K|), smallest
+// first, into one fp32 TMEM accumulator.  It replaces the recomputing dQ
+// mode (six piece products for each of S and dP and for the accumulate)
+// and runs on the same plan: items (block row, head, output slice of W =
+// min(D, 128) columns).  The block's two dS tiles (64 KB) come through a
+// ring of two stages, K's slice as 64-column chunks of three pieces (48 KB)
+// through another; MMAs of N = 64 per chunk.  Warp roles as dq_ds_kernel
+// (tc_bwd.cu): warp 0 producer, warp 1 MMA issuer, warps 2..9 the epilogue
+// with two TMEM accumulators.
+constexpr int kDs32Threads = 320;
+
+template <int D>
+struct Ds32Cfg {
+  static constexpr int W = D < 128 ? D : 128;
+  static constexpr int NSL = D / W;
+  static constexpr int KCH = W / 64;          // 64-column chunks of K per slice
+  static constexpr int kDsBytes = 2 * 32768;  // the two dS piece tiles of one block
+  static constexpr int kKBytes = 3 * 16384;   // the three K pieces of one chunk
+  static constexpr int kOffK = 2 * kDsBytes;
+  static constexpr int kOffBar = kOffK + 2 * kKBytes;
+  static constexpr int kSmem = kOffBar + 512;
+  static constexpr uint32_t kCols = 2 * W <= 128 ? 128 : 256;  // two accumulators of W columns
+};
+
+struct Ds32Bars {
+  uint64_t ds_full[2], ds_empty[2];
+  uint64_t k_full[2], k_empty[2];
+  uint64_t acc_full[2];   // the item's last MMA into accumulator b is done
+  uint64_t acc_empty[2];  // the epilogue has read accumulator b
+  uint64_t final_mma;
+  uint64_t wg_sync[2];
+  RingSmem work;
+  int merge_flag[2];
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+static_assert(sizeof(Ds32Bars) <= 512, "barrier block overflows its shared-memory slot");
+
+template <int D>
+__global__ void __launch_bounds__(kDs32Threads, 1) dq_ds32_kernel(const __grid_constant__ WideMaps tm, WideArgs a) {
+  // runs as a programmatic dependent of the dK walk that stored the tiles:
+  // the prologue touches only shared memory and TMEM
+  griddep_launch_dependents();
+  using C = Ds32Cfg<D>;
+  constexpr int W = C::W, NSL = C::NSL, KCH = C::KCH;
+  static_assert(C::kSmem <= 232448, "shared memory over the per-CTA limit");
+  extern __shared__ uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023) {  // the layout assumes a 1024-byte aligned base: refuse otherwise
+    griddep_wait();
+    if (threadIdx.x == 0) atomicExch(a.status, kStatusDeviceCheck);
+    return;
+  }
+  uint8_t* sm = smem_raw;
+  Ds32Bars* bars = (Ds32Bars*)(sm + C::kOffBar);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int S = a.d.S;
+  const int BHp = a.d.BH * NSL;
+  const PlanLayout lay = plan_layout(a.plan, a.d.nb, (int)gridDim.x, BHp);
+  if (warp == 0) plan_prefetch_l2(a.plan, plan_words(a.d.nb, (int)gridDim.x, BHp));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->ds_full[i], 1);
+      mbar_init(&bars->ds_empty[i], 1);
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->acc_full[i], 1);
+      mbar_init(&bars->acc_empty[i], kEw);
+      mbar_init(&bars->wg_sync[i], 128);
+    }
+    mbar_init(&bars->final_mma, 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bars->work.full[i], 1);
+      mbar_init(&bars->work.empty[i], 1 + kEw / 32);  // MMA warp + epilogue warps
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_slot, C::kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_wait();
+  const Walk walk = make_walk(lay, BHp);
+  auto decode = [&](int w, Cursor& c, int& slice) {
+    walk.decode(w, c);
+    slice = c.bh % NSL;
+    c.bh /= NSL;
+  };
+  const uint32_t tmem = bars->tmem_slot;
+  volatile int* ab = &bars->abort_flag;
+  RingSmem* ring = &bars->work;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ producer --
+      int g = 0, h = 0;  // blocks and K chunks whose copies were issued
+      bool ok = true;
+      for (int t = 0; ok; ++t) {
+        int w;
+        if (!(ok = ring_put(ring, t, lay.header + 1, walk.total, &w, ab, a.status)) || w < 0) break;
+        Cursor cur;
+        int slice;
+        decode(w, cur, slice);
+        // the row's dS tile pairs are consecutive (BSR order)
+        const uint8_t* ds = (const uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + cur.first) * C::kDsBytes;
+        for (int i = 0; i < cur.n && ok; ++i, ++g) {
+          int n = a.idx[cur.first + i];
+          if (n < 0 || n >= a.d.nb) {
+            atomicExch(a.status, kStatusDeviceCheck);
+            n = 0;
+          }
+          const int st = g & 1;
+          if (!(ok = mbar_wait(&bars->ds_empty[st], ((g >> 1) & 1) ^ 1, ab, a.status))) break;
+          mbar_arrive_expect_tx(&bars->ds_full[st], C::kDsBytes);
+          for (int q = 0; q < 4; ++q)
+            bulk_load(sm + st * C::kDsBytes + q * 16384, ds + (size_t)i * C::kDsBytes + q * 16384, 16384,
+                      &bars->ds_full[st]);
+          for (int c = 0; c < KCH; ++c, ++h) {
+            const int ks = h & 1;
+            if (!(ok = mbar_wait(&bars->k_empty[ks], ((h >> 1) & 1) ^ 1, ab, a.status))) break;
+            mbar_arrive_expect_tx(&bars->k_full[ks], C::kKBytes);
+            for (int p = 0; p < 3; ++p)
+              tma_load_2d(sm + C::kOffK + ks * C::kKBytes + p * 16384, &tm.m[kMapK][p], slice * W + c * 64,
+                          cur.bh * S + n * 128, &bars->k_full[ks]);
+          }
+        }
+      }
+      // drain: every copy issued must land before the CTA exits
+      for (int i = (g > 2 ? g - 2 : 0); i < g; ++i) drain_wait(&bars->ds_full[i & 1], (i >> 1) & 1);
+      for (int i = (h > 2 ? h - 2 : 0); i < h; ++i) drain_wait(&bars->k_full[i & 1], (i >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA --
+    const uint32_t leader = elect_one();
+    const uint32_t idK = instr_desc(1, 1, 1, 64, 128);  // bf16 pieces, A and B MN-major, N = 64
+    const uint32_t base = smem_u32(sm);
+    // the five piece products s_i k_j, smallest first
+    constexpr int kSi[5] = {1, 0, 1, 0, 0};
+    constexpr int kKj[5] = {1, 2, 0, 1, 0};
+    int g = 0, h = 0, q = 0;
+    bool ok = true;
+    for (int t = 0; ok; ++t) {
+      int w0 = -1;
+      bool good = true;
+      if (lane == 0) good = ring_get(ring, t, &w0, ab, a.status);
+      ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+      const int w = __shfl_sync(0xffffffffu, w0, 0);
+      if (!ok || w < 0) break;
+      Cursor cur;
+      int slice;
+      decode(w, cur, slice);
+      if (cur.n > 0) {
+        const int buf = q & 1;
+        if (!(ok = warp_wait(&bars->acc_empty[buf], ((q >> 1) & 1) ^ 1, ab, a.status))) break;
+        tc_fence_after();
+        for (int i = 0; i < cur.n && ok; ++i, ++g) {
+          const int st = g & 1;
+          if (!(ok = warp_wait(&bars->ds_full[st], (g >> 1) & 1, ab, a.status))) break;
+          tc_fence_after();
+          for (int c = 0; c < KCH; ++c, ++h) {
+            const int ks = h & 1;
+            if (!(ok = warp_wait(&bars->k_full[ks], (h >> 1) & 1, ab, a.status))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int pr = 0; pr < 5; ++pr) {
+              const uint64_t dA = smem_desc(base + st * C::kDsBytes + kSi[pr] * 32768, 4096, 256, 6);
+              const SDesc dK(base + C::kOffK + ks * C::kKBytes + kKj[pr] * 16384, 16384, 1024);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ss_by(leader, tmem + buf * W + c * 64, dA + (uint64_t)(kk * 32), dK.at(kk * 2048), idK,
+                          (i > 0 || pr > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit_by(leader, &bars->k_empty[ks]);
+          }
+          if (!ok) break;
+          mma_commit_by(leader, &bars->ds_empty[st]);
+        }
+        if (!ok) break;
+        mma_commit_by(leader, &bars->acc_full[buf]);
+        ++q;
+      }
+      __syncwarp();
+      if (lane == 0) ring_release(ring, t);
+    }
+    mma_commit_by(leader, &bars->final_mma);
+    if (leader) drain_wait(&bars->final_mma, 0);
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------- epilogue --
+    const int hg = (warp - 2) / 4;  // column half of the slice
+    const int wl = warp % 4;
+    const int r = wl * 32 + lane;
+    const uint32_t lb = (uint32_t)(wl * 32) << 16;
+    int q = 0, merge_phase = 0;
+    bool ok = true;
+    for (int t = 0; ok; ++t) {
+      int w = -1;
+      if (lane == 0) ok = ring_get(ring, t, &w, ab, a.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!ok || w < 0) break;
+      Cursor cur;
+      int slice;
+      decode(w, cur, slice);
+      const int bhp = cur.bh * NSL + slice;
+      const size_t grow = (size_t)cur.bh * S + (size_t)cur.line * 128 + r;
+      float* orow = (float*)a.out + grow * D + slice * W + hg * (W / 2);
+      if (cur.n == 0) {
+        zero_out<float, W / 2>(orow);
+      } else {
+        const int buf = q & 1;
+        if (!(ok = warp_wait(&bars->acc_full[buf], (q >> 1) & 1, ab, a.status))) break;
+        tc_fence_after();
+        const uint32_t tacc = tmem + lb + buf * W + hg * (W / 2);
+        ++q;
+        if (cur.slot < 0) {
+          store_out<W / 2, float>(tacc, orow, a.d.scale, (size_t)D);
+        } else if (!(ok = split_epilogue<float, kDq, W>(lay, a.part, cur.slot, bhp, BHp, hg, r, tacc, orow, a.d.scale,
+                                                        0.f, 0.f, 0.f, nullptr, nullptr, &bars->merge_flag[hg],
+                                                        &bars->wg_sync[hg], &merge_phase, ab, a.status))) {
+          break;
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->acc_empty[buf]);
+      }
+      __syncwarp();
+      if (lane == 0) ring_release(ring, t);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kCols);
+  if (threadIdx.x == 0) plan_exit(lay);
+}
+
+template <int D>
+bsr_status launch_ds32(const WideMaps& tm, const WideArgs& a, int grid, cudaStream_t s) {
+  using C = Ds32Cfg<D>;
+  auto kern = dq_ds32_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_ds: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
+  LaunchTimer timer("dq_ds", s);
+  e = launch_dependent(kern, dim3(grid), dim3(kDs32Threads), C::kSmem, s, tm, a);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_ds launch: %s", cudaGetErrorString(e));
+  return check_launch("dq_ds launch");
 }
 
 // fp32 -> three bf16 pieces, x = x0 + x1 + x2 (see the file comment), for
@@ -1186,13 +1461,23 @@ bsr_status launch_bwd_wide(const BwdArgs& a, cudaStream_t s) {
   // a persistent grid of its own work list.  On a plan with 16-bit operands
   // (a.dS) the dK walk stores its dS tiles and the dQ walk runs after it,
   // summing dS K over them (dq_ds_kernel) instead of recomputing the scores.
-  if (a.dS && a.d.dtype != BSR_F32) {
+  if (a.dS) {
     k.dS = a.dS;
     k.bsr_of_bsc = a.bsr_of_bsc;
     k.nnzb = a.nnzb;
     if ((st = dispatch_mode<kDv>(tm, v, grid, s, "dv_wide")) != BSR_OK) return st;
     if ((st = dispatch_mode<kDk>(tm, k, grid, s, "dk_wide")) != BSR_OK) return st;
-    return launch_dq_ds(a, s);
+    if (a.d.dtype != BSR_F32) return launch_dq_ds(a, s);
+    WideArgs q32 = q;  // fp32: the five-product walk over the two dS pieces, on the same plan
+    q32.dS = a.dS;
+    q32.nnzb = a.nnzb;
+    switch (a.d.D) {
+      case 64: return launch_ds32<64>(tm, q32, grid, s);
+      case 128: return launch_ds32<128>(tm, q32, grid, s);
+      case 256: return launch_ds32<256>(tm, q32, grid, s);
+      case 512: return launch_ds32<512>(tm, q32, grid, s);
+      default: return fail(BSR_ERR_UNSUPPORTED, "dq_ds: fp32 head_dim %d", a.d.D);
+    }
   }
   if ((st = dispatch_mode<kDq>(tm, q, grid, s, "dq_wide")) != BSR_OK) return st;
   if ((st = dispatch_mode<kDv>(tm, v, grid, s, "dv_wide")) != BSR_OK) return st;

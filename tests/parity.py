@@ -72,15 +72,15 @@ def kernels_run(Q, K, V, dO, bm, scale, device="cuda", api="per-call"):
 
 
 def expected_plan_kernels(dtype: str, D: int, empty_lines: bool = False) -> set:
-    """The kernels of a plan's creation (the planner, once) and of a forward + backward on it: for 16-bit
-    operands the dK/dV walk (head_dim 64 / 128) or the dK walk (256 / 512) stores dS and the dQ walk sums dS K
-    (dq_ds); fp32 recomputes in the wide dQ walk; the zero-lines pass where lines are empty."""
+    """The kernels of a plan's creation (the planner, once) and of a forward + backward on it: the dK/dV walk
+    (16-bit, head_dim 64 / 128) or the wide dK walk stores dS (fp32: as two bf16 pieces) and the dQ walk sums
+    dS K over the stored tiles (dq_ds); the zero-lines pass where lines are empty."""
     if dtype in ("bf16", "f16") and D <= 128:
         k = {"plan", "fwd_tc", "delta", "dkdv_tc", "dq_ds"}
     elif dtype in ("bf16", "f16"):
         k = {"plan", "fwd_wide", "delta", "dv_wide", "dk_wide", "dq_ds"}
     else:
-        k = {"plan", "split3", "fwd_wide", "delta", "dq_wide", "dv_wide", "dk_wide"}
+        k = {"plan", "split3", "fwd_wide", "delta", "dv_wide", "dk_wide", "dq_ds"}
     return k | {"zero_lines"} if empty_lines else k
 
 

@@ -509,10 +509,9 @@ def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
     # Forward and backward on one plan, three times in a row (after each
     # launch the kernels put the plan's work-queue counter back to the grid
     # size and its other counters back to 0), give the same results every
-    # time, and the per-call entry points' results bit for bit -- except dQ
-    # of 16-bit operands, which the plan sums from the dS tiles of the dK/dV
-    # (or dK) walk (the per-call walk recomputes dS): that dQ is held to the
-    # oracle.  nb = 20 has block row 0 and column 0 long
+    # time, and the per-call entry points' results bit for bit -- except dQ,
+    # which the plan sums from the dS tiles of the dK/dV (or dK) walk (the
+    # per-call walk recomputes dS): that dQ is held to the oracle.  nb = 20 has block row 0 and column 0 long
     # enough to be split into chunks.
     import block_sparse_attention_bsr_gb300 as bsr
 
@@ -521,7 +520,7 @@ def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
     Q, K, V, dO = inputs.make_qkvdo(1, H, nb * 128, D, dtype, 1.0, 17)
     scale = 1.0 / np.sqrt(D)
     ref = run_gpu(Q, K, V, dO, bm, scale)
-    ds_walk = dtype in ("bf16", "f16")
+    ds_walk = True
     rp, ci = inputs.bsr_from_block_mask(bm)
     st = bsr.Structure(rp, ci, nb, dev)
     q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
@@ -555,8 +554,8 @@ def test_plan_with_empty_lines(dtype, D):
     # A plan over a mask with empty block rows and columns: the planned calls
     # write the empty lines' outputs (they are not in the plan's work lists)
     # into NaN-filled outputs and match the per-call entry points bit for bit
-    # (dQ of 16-bit operands, summed from the stored dS tiles on a plan: the
-    # empty rows exactly, the rest against the oracle).
+    # (dQ, summed from the stored dS tiles on a plan: the empty rows exactly,
+    # the rest against the oracle).
     import block_sparse_attention_bsr_gb300 as bsr
 
     dev = torch.device("cuda")
@@ -581,7 +580,7 @@ def test_plan_with_empty_lines(dtype, D):
         bsr.bsr_attn_check()
         got = dict(O=O, row_max=rm, row_denom=rd, dQ=dQ, dK=dK, dV=dV)
         for name, t in got.items():
-            if name == "dQ" and dtype != "f32":
+            if name == "dQ":
                 g = t.double().cpu().numpy()
                 empty = np.repeat(bm.sum(1) == 0, 128)
                 assert np.all(g[:, :, empty] == 0), "dQ of empty block rows"
