@@ -233,13 +233,14 @@ bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor* K, const 
  *   device (it synchronises `stream`), allocates the plan's device memory
  *   with cudaMalloc on the current device and builds the lists on `stream`;
  *   use the plan on that stream (or synchronise first).  *out receives the
- *   handle (NULL on failure).  For bf16 / fp16 operands with head_dim 64 /
- *   128 the plan also holds a dS workspace of batch * heads * nnzb tiles of
- *   32 KiB (the dK/dV walk stores each dS tile there and the plan's dQ walk
- *   sums dS K over them instead of recomputing the scores); it reads col_idx
- *   and row_idx to the host to map every BSC entry to its BSR position, and
- *   if that workspace cannot be allocated the plan's dQ walk recomputes the
- *   scores instead (same results within the tolerances).  Errors:
+ *   handle (NULL on failure).  The plan also holds a dS workspace of
+ *   batch * heads * nnzb tiles of 32 KiB (64 KiB for fp32 operands: dS in
+ *   two bf16 pieces): the dK/dV (or dK) walk stores each dS tile there and
+ *   the plan's dQ walk sums dS K over them instead of recomputing the
+ *   scores.  It reads col_idx and row_idx to the host to map every BSC entry
+ *   to its BSR position, and if that workspace cannot be allocated the
+ *   plan's dQ walk recomputes the scores instead (same results within the
+ *   tolerances).  Errors:
  *   BSR_ERR_INVALID_ARG for null pointers, bad sizes, row_ptr / col_ptr whose
  *   last entries disagree, or a BSC entry that is not a stored block of the
  *   BSR lists; BSR_ERR_UNSUPPORTED for a head_dim / dtype outside the
