@@ -848,12 +848,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* lse = sStat + ss * 256 + hg * 64;
           const float* dl = lse + 128;
           const float2 sc = make_float2(sl2, sl2);
+          // (statistics four at a time: the ring's stage is 16-byte aligned)
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float2 l2 = *(const float2*)(lse + 2 * k);
-            const float2 x = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc, make_float2(-l2.x, -l2.y));
-            s[2 * k] = ex2(x.x);
-            s[2 * k + 1] = ex2(x.y);
+          for (int k = 0; k < 16; ++k) {
+            const float4 l4 = *(const float4*)(lse + 4 * k);
+            const float2 x = fma2(make_float2(s[4 * k], s[4 * k + 1]), sc, make_float2(-l4.x, -l4.y));
+            const float2 y = fma2(make_float2(s[4 * k + 2], s[4 * k + 3]), sc, make_float2(-l4.z, -l4.w));
+            s[4 * k] = ex2(x.x);
+            s[4 * k + 1] = ex2(x.y);
+            s[4 * k + 2] = ex2(y.x);
+            s[4 * k + 3] = ex2(y.y);
           }
           // P^T over this warpgroup's own S^T columns (already read above;
           // dV of the previous block finished before S^T of this one began)
@@ -865,12 +869,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           tmem_ld64(tmem + lane_base + kColDPT + hg * 64, dp);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float2 d2 = *(const float2*)(dl + 2 * k);
-            const float2 x = mul2(make_float2(s[2 * k], s[2 * k + 1]),
-                                  add2(make_float2(dp[2 * k], dp[2 * k + 1]), make_float2(-d2.x, -d2.y)));
-            dp[2 * k] = x.x;
-            dp[2 * k + 1] = x.y;
+          for (int k = 0; k < 16; ++k) {
+            const float4 d4 = *(const float4*)(dl + 4 * k);
+            const float2 x = mul2(make_float2(s[4 * k], s[4 * k + 1]),
+                                  add2(make_float2(dp[4 * k], dp[4 * k + 1]), make_float2(-d4.x, -d4.y)));
+            const float2 y = mul2(make_float2(s[4 * k + 2], s[4 * k + 3]),
+                                  add2(make_float2(dp[4 * k + 2], dp[4 * k + 3]), make_float2(-d4.z, -d4.w)));
+            dp[4 * k] = x.x;
+            dp[4 * k + 1] = x.y;
+            dp[4 * k + 2] = y.x;
+            dp[4 * k + 3] = y.y;
           }
           mbar_arrive(&bars->stat_empty[ss]);
           // dS^T over this warpgroup's own dP^T columns (read above; dK of

@@ -942,14 +942,33 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
               mbar_arrive(&bars->x2_free);
             }
           }
+          if constexpr (MODE == kDq) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            if constexpr (MODE == kDq) {
-              z[k] = ex2(fmaf(z[k], sl2, -lse_r)) * (dp[k] - dl_r);
-            } else if constexpr (MODE == kDv) {
-              z[k] = ex2(fmaf(z[k], sl2, -st[hg * 64 + k]));
-            } else {
-              z[k] = ex2(fmaf(z[k], sl2, -st[hg * 64 + k])) * (dp[k] - st[128 + hg * 64 + k]);
+            for (int k = 0; k < 64; ++k) z[k] = ex2(fmaf(z[k], sl2, -lse_r)) * (dp[k] - dl_r);
+          } else {
+            // the block's statistics four at a time (the auxiliary area is
+            // 1024-byte aligned)
+#pragma unroll
+            for (int k4 = 0; k4 < 16; ++k4) {
+              const float4 l4 = *(const float4*)(st + hg * 64 + 4 * k4);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              float dv[4] = {0.f, 0.f, 0.f, 0.f};
+              if constexpr (MODE == kDk) {
+                const float4 d4 = *(const float4*)(st + 128 + hg * 64 + 4 * k4);
+                dv[0] = d4.x;
+                dv[1] = d4.y;
+                dv[2] = d4.z;
+                dv[3] = d4.w;
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int k = 4 * k4 + j;
+                if constexpr (MODE == kDv) {
+                  z[k] = ex2(fmaf(z[k], sl2, -lv[j]));
+                } else {
+                  z[k] = ex2(fmaf(z[k], sl2, -lv[j])) * (dp[k] - dv[j]);
+                }
+              }
             }
           }
           if constexpr (MODE == kDv || MODE == kDk) mbar_arrive(&bars->stat_empty[g & 1]);
