@@ -54,20 +54,28 @@ def alg_flops(wl, nnzb, part="total"):
 # current sources still hash the same (otherwise the roofline's traffic is
 # null until the kernel is captured again).
 MEASURED_TRAFFIC = {
-    ("global_s8192", "dkdv_tc"): {"bytes": 429.8e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                  "sha256": "de916ed94338ae996b25bee23a1300e9173fa08234f488fb820f782c211a715e"},
-    ("global_s8192", "dq_ds"): {"bytes": 300.7e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                "sha256": "de916ed94338ae996b25bee23a1300e9173fa08234f488fb820f782c211a715e"},
-    ("global_s8192", "fwd_tc"): {"bytes": 137.8e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
-                                 "sha256": "6b348a4d57aa31d13d83b62106bb1fe180754b6caba85bc0d31858b530f06bca"},
-    ("local_s8192_d256", "fwd_wide"): {"bytes": 116.9e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                       "sha256": "dc14bf5b85f3d8d9a91ada639fd3e75cfe0b930f278a93551b6ca35d2aae93a9"},
-    ("local_s8192_d256", "dv_wide"): {"bytes": 112.5e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "dc14bf5b85f3d8d9a91ada639fd3e75cfe0b930f278a93551b6ca35d2aae93a9"},
-    ("local_s8192_d256", "dk_wide"): {"bytes": 244.7e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-                                      "sha256": "dc14bf5b85f3d8d9a91ada639fd3e75cfe0b930f278a93551b6ca35d2aae93a9"},
-    ("local_s8192_d256", "dq_ds"): {"bytes": 163.1e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-                                    "sha256": "de916ed94338ae996b25bee23a1300e9173fa08234f488fb820f782c211a715e"},
+    ("global_s8192", "fwd_tc"): {"bytes": 136.4e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "6b348a4d57aa31d13d83b62106bb1fe180754b6caba85bc0d31858b530f06bca"},
+    ("global_s8192", "dkdv_tc"): {"bytes": 429.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "85d10eba6362f4f32d8fcae9f8ea3ac83946dded19160dc2e0e6b5263573199b"},
+    ("global_s8192", "dq_ds"): {"bytes": 300.8e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "85d10eba6362f4f32d8fcae9f8ea3ac83946dded19160dc2e0e6b5263573199b"},
+    ("local_s8192_d256", "fwd_wide"): {"bytes": 118.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
+    ("local_s8192_d256", "dv_wide"): {"bytes": 115.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
+    ("local_s8192_d256", "dk_wide"): {"bytes": 249.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
+    ("local_s8192_d256", "dq_ds"): {"bytes": 162.8e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "85d10eba6362f4f32d8fcae9f8ea3ac83946dded19160dc2e0e6b5263573199b"},
+    ("global_s8192_f32", "fwd_wide"): {"bytes": 530.3e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
+    ("global_s8192_f32", "dv_wide"): {"bytes": 524.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
+    ("global_s8192_f32", "dk_wide"): {"bytes": 1186.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
+    ("global_s8192_f32", "dq_ds"): {"bytes": 695.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
 }
 
 

@@ -610,11 +610,10 @@ def test_plan_refuses_other_shapes():
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_plan_refuses_a_bsc_view_of_other_blocks(dtype):
-    # The plan maps every BSC entry to its BSR position (where the dK/dV walk
-    # stores that block's dS tile for the dQ walk); a row_idx naming a block
-    # that the BSR lists do not store is refused at creation, on the host,
-    # before any kernel reads the map (16-bit operands).  fp32 plans keep no
-    # dS tiles, build no map and accept the arrays as given.
+    # The plan maps every BSC entry to its BSR position (where the dK/dV or
+    # dK walk stores that block's dS tile for the dQ walk); a row_idx naming
+    # a block that the BSR lists do not store is refused at creation, on the
+    # host, before any kernel reads the map.
     import block_sparse_attention_bsr_gb300 as bsr
 
     dev = torch.device("cuda")
@@ -624,9 +623,6 @@ def test_plan_refuses_a_bsc_view_of_other_blocks(dtype):
     ri = st.host["row_idx"].copy()
     ri[0] = 5  # column 0 holds rows 0 and 1; block (5, 0) is not stored
     st.dev["row_idx"] = torch.from_numpy(ri).to(dev)
-    if dtype == torch.float32:
-        bsr.Plan(st, 1, 1, 64, dtype).close()
-        return
     with pytest.raises(bsr.BsrError) as e:
         bsr.Plan(st, 1, 1, 64, dtype)
     assert e.value.status == 1 and "BSC entry 0" in str(e.value)
