@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import weakref
 
 import numpy as np
 
@@ -221,6 +222,18 @@ def bsr_attn_bwd_noalloc(Q, K, V, O, dO, row_max, row_denom, row_ptr, col_idx, c
                                     _stream(stream, Q)))
 
 
+# Live plans by handle (weak: a plan lives as long as its owner holds it);
+# the planned custom ops carry only the handle.
+_PLANS = weakref.WeakValueDictionary()
+
+
+def _plan_of(handle: int) -> "Plan":
+    p = _PLANS.get(int(handle))
+    if p is None:
+        raise ValueError(f"no live plan with handle {handle:#x}")
+    return p
+
+
 class Plan:
     """A reusable plan (bsr_plan_create): the work lists and scratch of one block mask for operands of
     shape [batch, heads, n_brows * 128, head_dim] and one dtype.  Freed with bsr_plan_destroy when
@@ -242,6 +255,7 @@ class Plan:
                                    int(batch), int(heads), int(head_dim), codes[dtype], s, ctypes.byref(h)))
         self.handle = h.value
         self.key = (int(batch), int(heads), int(head_dim), dtype)
+        _PLANS[self.handle] = self
 
     def work_list(self, which: int = 0, stream=None):
         """One of the plan's work lists (bsr_plan_work_list): an int32 array [items, 4] of
@@ -261,6 +275,8 @@ class Plan:
 
     def close(self) -> None:
         if getattr(self, "handle", None):
+            if _PLANS.get(self.handle) is self:
+                del _PLANS[self.handle]
             load_library().bsr_plan_destroy(self.handle)
             self.handle = None
 
@@ -449,6 +465,52 @@ def register_ops():
         return dQ, dK, dV, None, None, None, None, None
 
     _fwd.register_autograd(_backward, setup_context=_setup_context)
+
+    # The same pair on a reusable plan (bsr_attn_fwd_plan / bsr_attn_bwd_plan),
+    # the plan passed as its handle: block_sparse_attention runs these with the
+    # plan its Structure keeps for the operands' shape.  The autograd context
+    # holds the plan itself, so it outlives the forward until the backward ran.
+    @torch.library.custom_op("bsr::bsr_attn_planned", mutates_args=(),
+                             schema="(Tensor Q, Tensor K, Tensor V, int plan, float scale) -> (Tensor, Tensor, Tensor)")
+    def _pfwd(Q, K, V, plan, scale):
+        O = torch.empty_like(Q)
+        rm = torch.empty(Q.shape[:3], device=Q.device, dtype=torch.float32)
+        rd = torch.empty_like(rm)
+        bsr_attn_fwd_plan(_plan_of(plan), Q, K, V, scale, O, rm, rd)
+        return O, rm, rd
+
+    @_pfwd.register_fake
+    def _pfwd_fake(Q, K, V, plan, scale):
+        rm = Q.new_empty(Q.shape[:3], dtype=torch.float32)
+        return torch.empty_like(Q), rm, torch.empty_like(rm)
+
+    @torch.library.custom_op("bsr::bsr_attn_planned_bwd", mutates_args=(),
+                             schema="(Tensor Q, Tensor K, Tensor V, Tensor O, Tensor dO, Tensor row_max, "
+                                    "Tensor row_denom, int plan, float scale) -> (Tensor, Tensor, Tensor)")
+    def _pbwd(Q, K, V, O, dO, row_max, row_denom, plan, scale):
+        dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
+        bsr_attn_bwd_plan(_plan_of(plan), Q, K, V, O, dO.contiguous(), row_max, row_denom, scale, dQ, dK, dV)
+        return dQ, dK, dV
+
+    @_pbwd.register_fake
+    def _pbwd_fake(Q, K, V, O, dO, row_max, row_denom, plan, scale):
+        return torch.empty_like(Q), torch.empty_like(Q), torch.empty_like(Q)
+
+    def _psetup_context(ctx, inputs, output):
+        Q, K, V, plan, scale = inputs
+        O, rm, rd = output
+        ctx.save_for_backward(Q, K, V, O, rm, rd)
+        ctx.plan = plan
+        ctx.plan_obj = _PLANS.get(plan)
+        ctx.scale = scale
+        ctx.mark_non_differentiable(rm, rd)
+
+    def _pbackward(ctx, dO, _drm, _drd):
+        Q, K, V, O, rm, rd = ctx.saved_tensors
+        dQ, dK, dV = torch.ops.bsr.bsr_attn_planned_bwd(Q, K, V, O, dO.contiguous(), rm, rd, ctx.plan, ctx.scale)
+        return dQ, dK, dV, None, None
+
+    _pfwd.register_autograd(_pbackward, setup_context=_psetup_context)
     _OPS = torch.ops.bsr
     return _OPS
 
@@ -459,14 +521,26 @@ def block_sparse_attention(Q, K, V, structure: "Structure", scale=None, return_s
     Q, K, V: contiguous CUDA tensors [batch, heads, seq, head_dim] (bf16, fp16 or
     fp32, 16-byte aligned); `structure`: a Structure of the block mask on the same
     device; scale defaults to 1 / sqrt(head_dim).  Runs the custom op
-    torch.ops.bsr.bsr_attn (bsr_attn_fwd on the current stream) with its
-    registered backward torch.ops.bsr.bsr_attn_bwd (bsr_attn_bwd).  With
+    torch.ops.bsr.bsr_attn_planned (bsr_attn_fwd_plan on the current stream, on
+    the plan the structure keeps for Q's shape and dtype, built on first use)
+    with its registered backward torch.ops.bsr.bsr_attn_planned_bwd
+    (bsr_attn_bwd_plan).  While torch.compile traces it, it runs the per-call
+    pair torch.ops.bsr.bsr_attn / bsr_attn_bwd instead (building a plan is a
+    host-side library call the tracer cannot take into a graph).  With
     return_stats the fp32 row_max / row_denom statistics come back as well
     (they carry no gradient).
     """
+    import torch
+
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if not getattr(t, "is_cuda", False):
+            raise ValueError(f"{name} must be a CUDA tensor")
     if scale is None:
         scale = 1.0 / float(Q.shape[-1]) ** 0.5
     ops = register_ops()
-    O, rm, rd = ops.bsr_attn(Q, K, V, structure.row_ptr, structure.col_idx, structure.col_ptr, structure.row_idx,
-                             float(scale))
+    if torch.compiler.is_compiling():
+        O, rm, rd = ops.bsr_attn(Q, K, V, structure.row_ptr, structure.col_idx, structure.col_ptr,
+                                 structure.row_idx, float(scale))
+    else:
+        O, rm, rd = ops.bsr_attn_planned(Q, K, V, structure.plan(Q).handle, float(scale))
     return (O, rm, rd) if return_stats else O

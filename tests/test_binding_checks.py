@@ -64,3 +64,12 @@ def test_custom_op_pair_is_registered_with_fake_implementations():
         assert rm.shape == (2, 3, 256) and rm.dtype == torch.float32 and rd.shape == rm.shape
         dq, dk, dv = ops.bsr_attn_bwd(q, q, q, O, O, rm, rd, i, i, i, i, 0.125)
         assert dq.shape == dk.shape == dv.shape == q.shape and dq.dtype == q.dtype
+    # the planned pair (a plan handle instead of the structure tensors)
+    assert "int plan" in str(ops.bsr_attn_planned.default._schema)
+    assert "int plan" in str(ops.bsr_attn_planned_bwd.default._schema)
+    with FakeTensorMode():
+        q = torch.empty(2, 3, 256, 64, dtype=torch.float16)
+        O, rm, rd = ops.bsr_attn_planned(q, q, q, 12345, 0.125)
+        assert O.shape == q.shape and O.dtype == q.dtype and rm.shape == (2, 3, 256) and rd.dtype == torch.float32
+        dq, dk, dv = ops.bsr_attn_planned_bwd(q, q, q, O, O, rm, rd, 12345, 0.125)
+        assert dq.shape == dk.shape == dv.shape == q.shape and dv.dtype == q.dtype

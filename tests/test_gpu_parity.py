@@ -389,13 +389,13 @@ def test_misaligned_output_is_rejected():
     assert e.value.status == 1 and "aligned" in str(e.value)
 
 
-def _wrapper_inputs(dtype="bf16", D=128):
+def _wrapper_inputs(dtype="bf16", D=128, api="plan"):
     import block_sparse_attention_bsr_gb300 as bsr
 
     dev = torch.device("cuda")
     bm = inputs.block_mask("local", 8, radius=2)
     Q, K, V, dO = inputs.make_qkvdo(1, 2, 8 * 128, D, dtype, 1.0, 21)
-    direct = run_gpu(Q, K, V, dO, bm, 1.0 / np.sqrt(D))
+    direct = run_gpu(Q, K, V, dO, bm, 1.0 / np.sqrt(D), api=api)
     rp, ci = inputs.bsr_from_block_mask(bm)
     st = bsr.Structure(rp, ci, bm.shape[1], dev)
     return Q, K, V, dO, st, direct, dev
@@ -403,8 +403,10 @@ def _wrapper_inputs(dtype="bf16", D=128):
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64), ("bf16", 256)])
 def test_autograd_wrapper_matches_direct_calls(dtype, D):
-    # block_sparse_attention (the custom-op pair with its registered
-    # autograd formula) gives the direct calls' outputs and gradients bit for bit.
+    # block_sparse_attention (the planned custom-op pair with its registered
+    # autograd formula, on the structure's plan) gives the plan entry points'
+    # outputs and gradients bit for bit; the per-call pair torch.ops.bsr.
+    # bsr_attn / bsr_attn_bwd gives the per-call entry points' bit for bit.
     import block_sparse_attention_bsr_gb300 as bsr
 
     Q, K, V, dO, st, direct, dev = _wrapper_inputs(dtype, D)
@@ -415,15 +417,24 @@ def test_autograd_wrapper_matches_direct_calls(dtype, D):
     for name, t in got.items():
         assert np.array_equal(t.double().cpu().numpy(), direct[name]), name
 
+    direct = run_gpu(Q, K, V, dO, inputs.block_mask("local", 8, radius=2), 1.0 / np.sqrt(D), api="per-call")
+    ops = bsr.register_ops()
+    q, k, v = (t.to(dev).requires_grad_() for t in (Q, K, V))
+    O, rm, rd = ops.bsr_attn(q, k, v, st.row_ptr, st.col_idx, st.col_ptr, st.row_idx, 1.0 / float(np.sqrt(D)))
+    O.backward(dO.to(dev))
+    got = dict(O=O.detach(), row_max=rm, row_denom=rd, dQ=q.grad, dK=k.grad, dV=v.grad)
+    for name, t in got.items():
+        assert np.array_equal(t.double().cpu().numpy(), direct[name]), ("per-call ops", name)
+
 
 def test_custom_op_pair_under_torch_compile_fullgraph():
-    # torch.compile traces torch.ops.bsr.bsr_attn and its registered backward
-    # as single ops (fullgraph: no graph break); the compiled forward and
-    # backward (aot_eager backend: no generated kernels) match the direct
-    # calls bit for bit.
+    # torch.compile traces block_sparse_attention as torch.ops.bsr.bsr_attn
+    # and its registered backward, single ops (fullgraph: no graph break);
+    # the compiled forward and backward (aot_eager backend: no generated
+    # kernels) match the per-call entry points bit for bit.
     import block_sparse_attention_bsr_gb300 as bsr
 
-    Q, K, V, dO, st, direct, dev = _wrapper_inputs()
+    Q, K, V, dO, st, direct, dev = _wrapper_inputs(api="per-call")
 
     def f(q, k, v):
         return bsr.block_sparse_attention(q, k, v, st, return_stats=True)
