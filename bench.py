@@ -39,7 +39,7 @@ METRIC = "fwd+bwd ms & TFLOP/s over stored blocks at seq 8192; % of GB300 bf16 T
 # call it recomputes S and dP as well (dq_tc); the wide kernels recompute the scores once per output slice
 # of W columns (W = 256 for 16-bit operands, 128 for fp32) and run fp32 as six
 # bf16 piece products, all counted here as the bf16 MMAs they issue.
-FLOP_PER_BLOCK = {"fwd_tc": 4, "fwd2p_stats": 2, "fwd2p_out": 4, "dq_tc": 6, "dq_ds": 2, "dkdv_tc": 8}
+FLOP_PER_BLOCK = {"fwd_tc": 4, "fwd2p_stats": 2, "fwd2p_out": 4, "dq_tc": 6, "dq_ds": 2, "dv_ps": 2, "dkdv_tc": 8}
 WIDE_SCORE_MMAS = {"fwd_wide": 1, "dq_wide": 2, "dv_wide": 1, "dk_wide": 2}  # score contractions per slice
 
 
@@ -116,7 +116,7 @@ def kernel_bytes(name, wl, nnzb):
     """Algorithmic DRAM bytes of one launch of a streaming kernel, else None: the dQ walk over stored dS
     tiles (dq_ds) reads every dS tile once (128 x 128 16-bit values per stored block and head), each head's
     K once and writes dQ once."""
-    if name == "dq_ds":
+    if name in ("dq_ds", "dv_ps"):  # dV over stored P^T tiles: the same stream
         e = 2
         return wl.batch * wl.heads * (nnzb * BLOCK * BLOCK * e + 2 * wl.seq * wl.head_dim * e)
     return None

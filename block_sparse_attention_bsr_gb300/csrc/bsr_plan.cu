@@ -42,6 +42,7 @@ struct bsr_plan_s {
   void* pieces;
   int32_t* bsr_of_bsc;  // null unless dS is set
   void* dS;             // own cudaMalloc block, or null
+  void* dP;             // in the dS block (16-bit operands, head_dim 256 / 512), or null
 };
 
 namespace bsr {
@@ -120,6 +121,9 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   // a block's dS: one 16-bit tile, or two bf16 piece tiles for fp32 operands
   const size_t ds_tile_b = d.dtype == BSR_F32 ? 2 * 128 * 128 * 2 : 128 * 128 * 2;
   const bool want_ds = nnzb > 0 && (size_t)d.BH * (size_t)nnzb <= ((size_t)1 << 62) / ds_tile_b;
+  // 16-bit operands at head_dim 256 / 512: the dK walk also stores P^T for
+  // a streaming dV walk (the head_dim-64 / 128 dK/dV walk computes dV itself)
+  const bool want_dp = want_ds && !tc_bwd_supported(d) && d.dtype != BSR_F32;
   if (want_ds) {
     std::vector<int32_t> ci(nnzb), ri(nnzb);
     e = cudaMemcpyAsync(ci.data(), col_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToHost, s);
@@ -204,10 +208,13 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   c += piece_b;
   p->bsr_of_bsc = nullptr;
   p->dS = nullptr;
+  p->dP = nullptr;
   if (want_ds) {
     void* ds = nullptr;
-    if (cudaMalloc(&ds, (size_t)d.BH * nnzb * ds_tile_b) == cudaSuccess) {
+    const size_t ds_b = (size_t)d.BH * nnzb * ds_tile_b;
+    if (cudaMalloc(&ds, want_dp ? 2 * ds_b : ds_b) == cudaSuccess) {
       p->dS = ds;
+      p->dP = want_dp ? (void*)((char*)ds + ds_b) : nullptr;
       p->bsr_of_bsc = (int32_t*)c;
     } else {
       cudaGetLastError();  // out of memory: the dQ walk recomputes the scores
@@ -299,6 +306,7 @@ extern "C" bsr_status bsr_attn_bwd_plan(const bsr_plan* plan, const bsr_tensor* 
   a.part_kv = plan->part_kv;
   a.pieces = plan->pieces;
   a.dS = plan->dS;
+  a.dP = plan->dP;
   a.bsr_of_bsc = plan->bsr_of_bsc;
   a.nnzb = plan->nnzb;
   return run_bwd(a, (cudaStream_t)stream, true, true, plan->empty_rows + plan->empty_cols > 0);

@@ -71,6 +71,10 @@ struct BwdArgs {
   void* dS;
   const int32_t* bsr_of_bsc;  // [nnzb] BSR position of each BSC entry (with dS)
   int nnzb;                   // stored blocks (with dS)
+  // head_dim 256 / 512, 16-bit, on a plan: the wide dK walk also stores each
+  // P^T tile ([BH][nnzb] in BSC order) and the dV walk streams them
+  // (launch_dv_ps) instead of recomputing the scores; null: it recomputes.
+  void* dP;
   int* status;
 };
 
@@ -378,5 +382,9 @@ bsr_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
 // plan_heads(d) heads, partial tiles at a.part_q), after the dK walk that
 // stored the tiles.
 bsr_status launch_dq_ds(const BwdArgs& a, cudaStream_t s);
+// dV_n = sum_m P^T_nm dO_m over stored P^T tiles (a.dP) for 16-bit operands
+// with head_dim 256 / 512, on the wide kernels' dV plan (a.col_plan, partial
+// tiles at a.part_kv), after the dK walk that stored the tiles.
+bsr_status launch_dv_ps(const BwdArgs& a, cudaStream_t s);
 
 }  // namespace bsr

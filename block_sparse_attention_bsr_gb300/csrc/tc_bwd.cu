@@ -994,7 +994,13 @@ struct DsBars {
 };
 static_assert(sizeof(DsBars) <= 512, "barrier block overflows its shared-memory slot");
 
-template <typename T, int D>
+// kDV: the same streaming walk for dV at head_dim 256 / 512 on a plan: the
+// wide dK walk also stores each P^T tile (keys x queries, in BSC order, the
+// same byte layout: read here as the K-major A operand with 32-byte
+// swizzling, M = keys: 8 keys x 16 queries per atom, the next 8 keys 256
+// bytes on, the next 16 queries 4096 bytes on), and dV_n = sum_m P^T_nm dO_m
+// walks the block columns (the dV plan, dO as the B operand, no scale).
+template <typename T, int D, bool kDV>
 __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constant__ CUtensorMap tmK, BwdArgs a) {
   // runs as a programmatic dependent of the dK/dV walk: the prologue below
   // touches only shared memory and TMEM; global memory waits for that grid
@@ -1010,8 +1016,14 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = a.d.S;
   const int BHp = a.d.BH * NSL;  // the planner's heads: one per (batch, head, slice)
-  const PlanLayout lay = plan_layout(a.row_plan, a.d.nb, (int)gridDim.x, BHp);
-  if (warp == 0) plan_prefetch_l2(a.row_plan, plan_words(a.d.nb, (int)gridDim.x, BHp));
+  int32_t* const plan = kDV ? a.col_plan : a.row_plan;
+  const int32_t* const idx = kDV ? a.row_idx : a.col_idx;
+  const uint8_t* const tiles = (const uint8_t*)(kDV ? a.dP : a.dS);
+  T* const out = (T*)(kDV ? a.dV : a.dQ);
+  float* const part = kDV ? a.part_kv : a.part_q;
+  const float mul = kDV ? 1.f : a.d.scale;
+  const PlanLayout lay = plan_layout(plan, a.d.nb, (int)gridDim.x, BHp);
+  if (warp == 0) plan_prefetch_l2(plan, plan_words(a.d.nb, (int)gridDim.x, BHp));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -1055,10 +1067,10 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
         Cursor cur;
         walk.decode(k, cur);
         const int bh = cur.bh / NSL, sl = cur.bh % NSL;
-        // the row's dS tiles are consecutive (BSR order)
-        const uint8_t* ds = (const uint8_t*)a.dS + ((size_t)bh * a.nnzb + cur.first) * C::kDsTile;
+        // the line's tiles are consecutive (dS: BSR order; P^T: BSC order)
+        const uint8_t* ds = tiles + ((size_t)bh * a.nnzb + cur.first) * C::kDsTile;
         for (int i = 0; i < cur.n; ++i, ++g) {
-          int n = a.col_idx[cur.first + i];
+          int n = idx[cur.first + i];
           if (n < 0 || n >= a.d.nb) {
             atomicExch(a.status, kStatusDeviceCheck);
             n = 0;
@@ -1081,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA --
     const uint32_t leader = elect_one();
-    const uint32_t idDQ = instr_desc(Half16<T>::kFmt, 1, 1, W, 128);
+    const uint32_t idDQ = instr_desc(Half16<T>::kFmt, kDV ? 0 : 1, 1, W, 128);
     const uint32_t base = smem_u32(sm);
     int g = 0, q = 0;  // blocks, non-empty items
     bool ok = true;
@@ -1103,11 +1115,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
           if (!(ok = warp_wait(&bars->full[st], (g / C::kStages) & 1, ab, a.status))) break;
           tc_fence_after();
           const uint32_t sds = base + st * C::kStageBytes;
-          const uint64_t dA = smem_desc(sds, 4096, 256, 6);  // dS: MN-major, 32-byte swizzle
-          const SDesc dK(sds + C::kDsTile, 16384, 1024);     // K: MN-major, 128-byte swizzle
+          // dS: MN-major with 32-byte swizzle; P^T (kDV): K-major with 32-byte
+          // swizzle (one atom per MMA's 16 queries: the leading offset is unused)
+          const uint64_t dA = kDV ? smem_desc(sds, 16, 256, 6) : smem_desc(sds, 4096, 256, 6);
+          const SDesc dK(sds + C::kDsTile, 16384, 1024);  // K / dO: MN-major, 128-byte swizzle
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: two atom rows of dS (512 bytes), 16 rows of K
-            mma_ss_by(leader, tmem + buf * W, dA + (uint64_t)(kk * 32), dK.at(kk * 2048), idDQ,
+          for (int kk = 0; kk < 8; ++kk)  // 16 keys (queries for kDV) per MMA: 16 rows of K (dO)
+            mma_ss_by(leader, tmem + buf * W, dA + (uint64_t)(kk * (kDV ? 256 : 32)), dK.at(kk * 2048), idDQ,
                       (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit_by(leader, &bars->empty[st]);
         }
@@ -1139,7 +1153,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
       walk.decode_warp(k, cur);
       const int bh = cur.bh / NSL, sl = cur.bh % NSL;
       const size_t grow = (size_t)bh * S + (size_t)cur.line * 128 + r;
-      T* dqrow = (T*)a.dQ + grow * D + sl * W + hg * (W / 2);
+      T* dqrow = out + grow * D + sl * W + hg * (W / 2);
       if (cur.n == 0) {
         zero_cols<W / 2>(dqrow);
       } else {
@@ -1149,13 +1163,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
         const uint32_t acc = tmem + lane_base + buf * W + hg * (W / 2);
         ++q;
         if (cur.slot < 0) {
-          store_acc_cols<W / 2>(acc, dqrow, a.d.scale, (size_t)D);
+          store_acc_cols<W / 2>(acc, dqrow, mul, (size_t)D);
           tc_fence_before();
           mbar_arrive(&bars->acc_empty[buf]);
         } else {
           // chunk of a split row: publish the fp32 partial, the last chunk merges
           const size_t kTileF = (size_t)128 * W;
-          store_acc_part<W / 2>(acc, a.part_q + (size_t)(cur.slot * BHp + cur.bh) * kTileF, hg * (W / 8), r);
+          store_acc_part<W / 2>(acc, part + (size_t)(cur.slot * BHp + cur.bh) * kTileF, hg * (W / 8), r);
           tc_fence_before();
           mbar_arrive(&bars->acc_empty[buf]);
           bool last = false;
@@ -1165,8 +1179,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
           if (last) {
             const int sl = lay.slot_line[cur.slot];
             const int base = lay.line_base[sl], nc = lay.line_chunks[sl];
-            merge_tiles<W / 2>(a.part_q + (size_t)(base * BHp + cur.bh) * kTileF, (size_t)BHp * kTileF, nc,
-                               hg * (W / 8), r, dqrow, a.d.scale);
+            merge_tiles<W / 2>(part + (size_t)(base * BHp + cur.bh) * kTileF, (size_t)BHp * kTileF, nc,
+                               hg * (W / 8), r, dqrow, mul);
           }
         }
       }
@@ -1184,20 +1198,21 @@ __global__ void __launch_bounds__(kThreads, 1) dq_ds_kernel(const __grid_constan
 
 // The dQ walk over the stored dS tiles, in `s` as a programmatic dependent
 // of the walk that stored them.
-template <typename T, int D>
-bsr_status launch_dq(const BwdArgs& a, const CUtensorMap& tmK, int grid, cudaStream_t s) {
-  auto dq = dq_ds_kernel<T, D>;
+template <typename T, int D, bool kDV = false>
+bsr_status launch_dq(const BwdArgs& a, const CUtensorMap& tmB, int grid, cudaStream_t s) {
+  auto dq = dq_ds_kernel<T, D, kDV>;
+  const char* name = kDV ? "dv_ps" : "dq_ds";
   cudaError_t e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, DsCfg<D>::kSmem);
   if (e != cudaSuccess)
-    return fail(BSR_ERR_CUDA, "dq_ds: cudaFuncSetAttribute(%d): %s", DsCfg<D>::kSmem, cudaGetErrorString(e));
+    return fail(BSR_ERR_CUDA, "%s: cudaFuncSetAttribute(%d): %s", name, DsCfg<D>::kSmem, cudaGetErrorString(e));
   if (profiling_launches()) {
-    LaunchTimer timer("dq_ds", s);
-    dq<<<grid, kThreads, DsCfg<D>::kSmem, s>>>(tmK, a);
-    return check_launch("dq_ds launch");
+    LaunchTimer timer(name, s);
+    dq<<<grid, kThreads, DsCfg<D>::kSmem, s>>>(tmB, a);
+    return check_launch(name);
   }
-  e = launch_dependent(dq, dim3(grid), dim3(kThreads), DsCfg<D>::kSmem, s, tmK, a);
-  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_ds launch: %s", cudaGetErrorString(e));
-  return check_launch("dq_ds launch");
+  e = launch_dependent(dq, dim3(grid), dim3(kThreads), DsCfg<D>::kSmem, s, tmB, a);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "%s launch: %s", name, cudaGetErrorString(e));
+  return check_launch(name);
 }
 
 // On a plan (a.dS set): the dK/dV walk, which stores the dS tiles, then the
@@ -1281,6 +1296,24 @@ bsr_status launch_dq_ds(const BwdArgs& a, cudaStream_t s) {
     case 256: return h ? launch_dq<__half, 256>(a, tmK, grid, s) : launch_dq<__nv_bfloat16, 256>(a, tmK, grid, s);
     case 512: return h ? launch_dq<__half, 512>(a, tmK, grid, s) : launch_dq<__nv_bfloat16, 512>(a, tmK, grid, s);
     default: return fail(BSR_ERR_UNSUPPORTED, "dq_ds: head_dim %d", a.d.D);
+  }
+}
+
+bsr_status launch_dv_ps(const BwdArgs& a, cudaStream_t s) {
+  const int grid = tc_grid(a.d);
+  if (grid <= 0) return fail(BSR_ERR_CUDA, "dv_ps: cannot query the SM count");
+  if (!a.dP || (((uintptr_t)a.dP) & 15) || a.d.dtype == BSR_F32)
+    return fail(BSR_ERR_INVALID_ARG, "dv_ps: needs 16-byte aligned P^T tiles of 16-bit operands");
+  CUtensorMap tmdO;
+  bsr_status st = make_tensor_map(a.d, a.dO, &tmdO, "dO");
+  if (st != BSR_OK) return st;
+  const bool h = a.d.dtype == BSR_F16;
+  switch (a.d.D) {
+    case 256:
+      return h ? launch_dq<__half, 256, true>(a, tmdO, grid, s) : launch_dq<__nv_bfloat16, 256, true>(a, tmdO, grid, s);
+    case 512:
+      return h ? launch_dq<__half, 512, true>(a, tmdO, grid, s) : launch_dq<__nv_bfloat16, 512, true>(a, tmdO, grid, s);
+    default: return fail(BSR_ERR_UNSUPPORTED, "dv_ps: head_dim %d", a.d.D);
   }
 }
 

@@ -218,6 +218,9 @@ struct WideArgs {
   void* dS;
   const int32_t* bsr_of_bsc;
   int nnzb;
+  // DK with 16-bit operands on a plan: the P^T tiles for the dV walk over
+  // them (dq_ds_kernel with kDV), [BH][nnzb] tiles in BSC order (null: none)
+  void* dP;
 };
 
 struct WBars {
@@ -946,28 +949,37 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
 #pragma unroll
             for (int k = 0; k < 64; ++k) z[k] = ex2(fmaf(z[k], sl2, -lse_r)) * (dp[k] - dl_r);
           } else {
-            // the block's statistics four at a time (the auxiliary area is
-            // 1024-byte aligned)
+            // P^T from the block's statistics, four at a time (the auxiliary
+            // area is 1024-byte aligned)
 #pragma unroll
             for (int k4 = 0; k4 < 16; ++k4) {
               const float4 l4 = *(const float4*)(st + hg * 64 + 4 * k4);
               const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-              float dv[4] = {0.f, 0.f, 0.f, 0.f};
-              if constexpr (MODE == kDk) {
-                const float4 d4 = *(const float4*)(st + 128 + hg * 64 + 4 * k4);
-                dv[0] = d4.x;
-                dv[1] = d4.y;
-                dv[2] = d4.z;
-                dv[3] = d4.w;
-              }
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int k = 4 * k4 + j;
-                if constexpr (MODE == kDv) {
-                  z[k] = ex2(fmaf(z[k], sl2, -lv[j]));
-                } else {
-                  z[k] = ex2(fmaf(z[k], sl2, -lv[j])) * (dp[k] - dv[j]);
+              for (int j = 0; j < 4; ++j) z[4 * k4 + j] = ex2(fmaf(z[4 * k4 + j], sl2, -lv[j]));
+            }
+            if constexpr (MODE == kDk) {
+              if constexpr (NP == 1) {
+                if (a.dP && sl == 0) {
+                  // P^T of the block, by BSC position, for the dV walk over it
+                  const int pp = cur.first + i;
+                  if (pp < a.nnzb) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = Half16<Op>::pack(z[2 * k], z[2 * k + 1]);
+                    st_tile_sw32_row64((uint8_t*)a.dP + ((size_t)cur.bh * a.nnzb + pp) * (128 * 128 * 2), r, hg, v);
+                  } else {
+                    atomicExch(a.status, kStatusDeviceCheck);
+                  }
                 }
+              }
+              // dS^T = P^T (dP^T - D)
+#pragma unroll
+              for (int k4 = 0; k4 < 16; ++k4) {
+                const float4 d4 = *(const float4*)(st + 128 + hg * 64 + 4 * k4);
+                const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) z[4 * k4 + j] *= dp[4 * k4 + j] - dv[j];
               }
             }
           }
@@ -1484,6 +1496,13 @@ bsr_status launch_bwd_wide(const BwdArgs& a, cudaStream_t s) {
     k.dS = a.dS;
     k.bsr_of_bsc = a.bsr_of_bsc;
     k.nnzb = a.nnzb;
+    if (a.dP && a.d.dtype != BSR_F32) {
+      // 16-bit: the dK walk also stores P^T; dQ and dV then stream dS and P^T
+      k.dP = a.dP;
+      if ((st = dispatch_mode<kDk>(tm, k, grid, s, "dk_wide")) != BSR_OK) return st;
+      if ((st = launch_dq_ds(a, s)) != BSR_OK) return st;
+      return launch_dv_ps(a, s);
+    }
     if ((st = dispatch_mode<kDv>(tm, v, grid, s, "dv_wide")) != BSR_OK) return st;
     if ((st = dispatch_mode<kDk>(tm, k, grid, s, "dk_wide")) != BSR_OK) return st;
     if (a.d.dtype != BSR_F32) return launch_dq_ds(a, s);
