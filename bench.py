@@ -95,7 +95,7 @@ def measured_traffic(workload, kernel):
 
 def kernel_flops(name, wl, nnzb):
     per_head = BLOCK * BLOCK * wl.head_dim * nnzb * wl.batch * wl.heads
-    if name == "dq_ds" and wl.dtype == "f32":  # five bf16 piece products per product
+    if name in ("dq_ds", "dv_ps") and wl.dtype == "f32":  # five bf16 piece products per product
         return 10 * per_head
     for key, mult in FLOP_PER_BLOCK.items():
         if name.startswith(key):

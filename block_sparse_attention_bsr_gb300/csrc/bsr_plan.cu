@@ -42,7 +42,7 @@ struct bsr_plan_s {
   void* pieces;
   int32_t* bsr_of_bsc;  // null unless dS is set
   void* dS;             // own cudaMalloc block, or null
-  void* dP;             // in the dS block (16-bit operands, head_dim 256 / 512), or null
+  void* dP;             // in the dS block (the wide kernels' operands), or null
 };
 
 namespace bsr {
@@ -121,9 +121,10 @@ extern "C" bsr_status bsr_plan_create(const int32_t* row_ptr, const int32_t* col
   // a block's dS: one 16-bit tile, or two bf16 piece tiles for fp32 operands
   const size_t ds_tile_b = d.dtype == BSR_F32 ? 2 * 128 * 128 * 2 : 128 * 128 * 2;
   const bool want_ds = nnzb > 0 && (size_t)d.BH * (size_t)nnzb <= ((size_t)1 << 62) / ds_tile_b;
-  // 16-bit operands at head_dim 256 / 512: the dK walk also stores P^T for
-  // a streaming dV walk (the head_dim-64 / 128 dK/dV walk computes dV itself)
-  const bool want_dp = want_ds && !tc_bwd_supported(d) && d.dtype != BSR_F32;
+  // the wide kernels (16-bit at head_dim 256 / 512, fp32): the dK walk also
+  // stores P^T for a streaming dV walk (the head_dim-64 / 128 dK/dV walk
+  // computes dV itself)
+  const bool want_dp = want_ds && !tc_bwd_supported(d);
   if (want_ds) {
     std::vector<int32_t> ci(nnzb), ri(nnzb);
     e = cudaMemcpyAsync(ci.data(), col_idx, sizeof(int32_t) * nnzb, cudaMemcpyDeviceToHost, s);

@@ -959,18 +959,31 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
               for (int j = 0; j < 4; ++j) z[4 * k4 + j] = ex2(fmaf(z[4 * k4 + j], sl2, -lv[j]));
             }
             if constexpr (MODE == kDk) {
-              if constexpr (NP == 1) {
-                if (a.dP && sl == 0) {
-                  // P^T of the block, by BSC position, for the dV walk over it
-                  const int pp = cur.first + i;
-                  if (pp < a.nnzb) {
+              if (a.dP && sl == 0) {
+                // P^T of the block, by BSC position, for the dV walk over it
+                // (fp32: two bf16 pieces, one tile each)
+                const int pp = cur.first + i;
+                if (pp < a.nnzb) {
+                  if constexpr (NP == 1) {
                     uint32_t v[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = Half16<Op>::pack(z[2 * k], z[2 * k + 1]);
                     st_tile_sw32_row64((uint8_t*)a.dP + ((size_t)cur.bh * a.nnzb + pp) * (128 * 128 * 2), r, hg, v);
                   } else {
-                    atomicExch(a.status, kStatusDeviceCheck);
+                    uint32_t v0[32], v1[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                      const float a0 = __bfloat162float(__float2bfloat16_rn(z[2 * k]));
+                      const float b0 = __bfloat162float(__float2bfloat16_rn(z[2 * k + 1]));
+                      v0[k] = pack_bf16x2(a0, b0);
+                      v1[k] = pack_bf16x2(z[2 * k] - a0, z[2 * k + 1] - b0);
+                    }
+                    uint8_t* tile = (uint8_t*)a.dP + ((size_t)cur.bh * a.nnzb + pp) * (2 * 128 * 128 * 2);
+                    st_tile_sw32_row64(tile, r, hg, v0);
+                    st_tile_sw32_row64(tile + 128 * 128 * 2, r, hg, v1);
                   }
+                } else {
+                  atomicExch(a.status, kStatusDeviceCheck);
                 }
               }
               // dS^T = P^T (dP^T - D)
@@ -1122,7 +1135,10 @@ struct Ds32Bars {
 };
 static_assert(sizeof(Ds32Bars) <= 512, "barrier block overflows its shared-memory slot");
 
-template <int D>
+// kDV: dV_n = sum_m P^T_nm dO_m the same way over the two bf16 pieces of
+// P^T the dK walk stored (BSC order; read as the K-major A operand with
+// 32-byte swizzling, M = keys) and dO's three pieces, on the dV plan.
+template <int D, bool kDV>
 __global__ void __launch_bounds__(kDs32Threads, 1) dq_ds32_kernel(const __grid_constant__ WideMaps tm, WideArgs a) {
   // runs as a programmatic dependent of the dK walk that stored the tiles:
   // the prologue touches only shared memory and TMEM
@@ -1191,8 +1207,8 @@ __global__ void __launch_bounds__(kDs32Threads, 1) dq_ds32_kernel(const __grid_c
         Cursor cur;
         int slice;
         decode(w, cur, slice);
-        // the row's dS tile pairs are consecutive (BSR order)
-        const uint8_t* ds = (const uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + cur.first) * C::kDsBytes;
+        // the line's tile pairs are consecutive (dS: BSR order; P^T: BSC order)
+        const uint8_t* ds = (const uint8_t*)(kDV ? a.dP : a.dS) + ((size_t)cur.bh * a.nnzb + cur.first) * C::kDsBytes;
         for (int i = 0; i < cur.n && ok; ++i, ++g) {
           int n = a.idx[cur.first + i];
           if (n < 0 || n >= a.d.nb) {
@@ -1210,7 +1226,7 @@ __global__ void __launch_bounds__(kDs32Threads, 1) dq_ds32_kernel(const __grid_c
             if (!(ok = mbar_wait(&bars->k_empty[ks], ((h >> 1) & 1) ^ 1, ab, a.status))) break;
             mbar_arrive_expect_tx(&bars->k_full[ks], C::kKBytes);
             for (int p = 0; p < 3; ++p)
-              tma_load_2d(sm + C::kOffK + ks * C::kKBytes + p * 16384, &tm.m[kMapK][p], slice * W + c * 64,
+              tma_load_2d(sm + C::kOffK + ks * C::kKBytes + p * 16384, &tm.m[kDV ? kMapdO : kMapK][p], slice * W + c * 64,
                           cur.bh * S + n * 128, &bars->k_full[ks]);
           }
         }
@@ -1222,7 +1238,7 @@ __global__ void __launch_bounds__(kDs32Threads, 1) dq_ds32_kernel(const __grid_c
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA --
     const uint32_t leader = elect_one();
-    const uint32_t idK = instr_desc(1, 1, 1, 64, 128);  // bf16 pieces, A and B MN-major, N = 64
+    const uint32_t idK = instr_desc(1, kDV ? 0 : 1, 1, 64, 128);  // bf16 pieces; A MN-major (dS) or K-major (P^T), N = 64
     const uint32_t base = smem_u32(sm);
     // the five piece products s_i k_j, smallest first
     constexpr int kSi[5] = {1, 0, 1, 0, 0};
@@ -1253,11 +1269,12 @@ __global__ void __launch_bounds__(kDs32Threads, 1) dq_ds32_kernel(const __grid_c
             tc_fence_after();
 #pragma unroll
             for (int pr = 0; pr < 5; ++pr) {
-              const uint64_t dA = smem_desc(base + st * C::kDsBytes + kSi[pr] * 32768, 4096, 256, 6);
+              const uint64_t dA = kDV ? smem_desc(base + st * C::kDsBytes + kSi[pr] * 32768, 16, 256, 6)
+                                      : smem_desc(base + st * C::kDsBytes + kSi[pr] * 32768, 4096, 256, 6);
               const SDesc dK(base + C::kOffK + ks * C::kKBytes + kKj[pr] * 16384, 16384, 1024);
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_ss_by(leader, tmem + buf * W + c * 64, dA + (uint64_t)(kk * 32), dK.at(kk * 2048), idK,
+                mma_ss_by(leader, tmem + buf * W + c * 64, dA + (uint64_t)(kk * (kDV ? 256 : 32)), dK.at(kk * 2048), idK,
                           (i > 0 || pr > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit_by(leader, &bars->k_empty[ks]);
@@ -1303,9 +1320,10 @@ __global__ void __launch_bounds__(kDs32Threads, 1) dq_ds32_kernel(const __grid_c
         tc_fence_after();
         const uint32_t tacc = tmem + lb + buf * W + hg * (W / 2);
         ++q;
+        const float mul = kDV ? 1.f : a.d.scale;
         if (cur.slot < 0) {
-          store_out<W / 2, float>(tacc, orow, a.d.scale, (size_t)D);
-        } else if (!(ok = split_epilogue<float, kDq, W>(lay, a.part, cur.slot, bhp, BHp, hg, r, tacc, orow, a.d.scale,
+          store_out<W / 2, float>(tacc, orow, mul, (size_t)D);
+        } else if (!(ok = split_epilogue<float, kDq, W>(lay, a.part, cur.slot, bhp, BHp, hg, r, tacc, orow, mul,
                                                         0.f, 0.f, 0.f, nullptr, nullptr, &bars->merge_flag[hg],
                                                         &bars->wg_sync[hg], &merge_phase, ab, a.status))) {
           break;
@@ -1325,16 +1343,26 @@ __global__ void __launch_bounds__(kDs32Threads, 1) dq_ds32_kernel(const __grid_c
   if (threadIdx.x == 0) plan_exit(lay);
 }
 
-template <int D>
+template <int D, bool kDV = false>
 bsr_status launch_ds32(const WideMaps& tm, const WideArgs& a, int grid, cudaStream_t s) {
   using C = Ds32Cfg<D>;
-  auto kern = dq_ds32_kernel<D>;
+  auto kern = dq_ds32_kernel<D, kDV>;
+  const char* name = kDV ? "dv_ps" : "dq_ds";
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_ds: cudaFuncSetAttribute(%d): %s", C::kSmem, cudaGetErrorString(e));
-  LaunchTimer timer("dq_ds", s);
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "%s: cudaFuncSetAttribute(%d): %s", name, C::kSmem, cudaGetErrorString(e));
+  LaunchTimer timer(name, s);
   e = launch_dependent(kern, dim3(grid), dim3(kDs32Threads), C::kSmem, s, tm, a);
-  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "dq_ds launch: %s", cudaGetErrorString(e));
-  return check_launch("dq_ds launch");
+  if (e != cudaSuccess) return fail(BSR_ERR_CUDA, "%s launch: %s", name, cudaGetErrorString(e));
+  return check_launch(name);
+}
+
+// fp32 on a plan: dQ over the stored dS pieces, then (with a.dP) dV over the
+// stored P^T pieces.
+template <int D>
+bsr_status launch_ds32_walks(const WideMaps& tm, const WideArgs& q, const WideArgs& v, int grid, cudaStream_t s) {
+  bsr_status st = launch_ds32<D>(tm, q, grid, s);
+  if (st != BSR_OK || !v.dP) return st;
+  return launch_ds32<D, true>(tm, v, grid, s);
 }
 
 // fp32 -> three bf16 pieces, x = x0 + x1 + x2 (see the file comment), for
@@ -1503,17 +1531,24 @@ bsr_status launch_bwd_wide(const BwdArgs& a, cudaStream_t s) {
       if ((st = launch_dq_ds(a, s)) != BSR_OK) return st;
       return launch_dv_ps(a, s);
     }
-    if ((st = dispatch_mode<kDv>(tm, v, grid, s, "dv_wide")) != BSR_OK) return st;
+    if (a.d.dtype != BSR_F32 || !a.dP) {
+      if ((st = dispatch_mode<kDv>(tm, v, grid, s, "dv_wide")) != BSR_OK) return st;
+    } else {
+      k.dP = a.dP;  // fp32: the dK walk also stores P^T (two pieces) for the dV walk below
+    }
     if ((st = dispatch_mode<kDk>(tm, k, grid, s, "dk_wide")) != BSR_OK) return st;
     if (a.d.dtype != BSR_F32) return launch_dq_ds(a, s);
-    WideArgs q32 = q;  // fp32: the five-product walk over the two dS pieces, on the same plan
+    WideArgs q32 = q;  // fp32: the five-product walks over the stored pieces, on the same plans
     q32.dS = a.dS;
     q32.nnzb = a.nnzb;
+    WideArgs v32 = v;
+    v32.dP = a.dP;
+    v32.nnzb = a.nnzb;
     switch (a.d.D) {
-      case 64: return launch_ds32<64>(tm, q32, grid, s);
-      case 128: return launch_ds32<128>(tm, q32, grid, s);
-      case 256: return launch_ds32<256>(tm, q32, grid, s);
-      case 512: return launch_ds32<512>(tm, q32, grid, s);
+      case 64: return launch_ds32_walks<64>(tm, q32, v32, grid, s);
+      case 128: return launch_ds32_walks<128>(tm, q32, v32, grid, s);
+      case 256: return launch_ds32_walks<256>(tm, q32, v32, grid, s);
+      case 512: return launch_ds32_walks<512>(tm, q32, v32, grid, s);
       default: return fail(BSR_ERR_UNSUPPORTED, "dq_ds: fp32 head_dim %d", a.d.D);
     }
   }

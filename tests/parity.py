@@ -74,14 +74,14 @@ def kernels_run(Q, K, V, dO, bm, scale, device="cuda", api="per-call"):
 def expected_plan_kernels(dtype: str, D: int, empty_lines: bool = False) -> set:
     """The kernels of a plan's creation (the planner, once) and of a forward + backward on it: the dK/dV walk
     (16-bit, head_dim 64 / 128) or the wide dK walk stores dS (fp32: as two bf16 pieces) and the dQ walk sums
-    dS K over the stored tiles (dq_ds); at head_dim 256 / 512 with 16-bit operands the dK walk also stores P^T
-    and dV sums P^T dO over it (dv_ps); the zero-lines pass where lines are empty."""
+    dS K over the stored tiles (dq_ds); in the wide kernels (head_dim 256 / 512, fp32) the dK walk also stores
+    P^T and dV sums P^T dO over it (dv_ps); the zero-lines pass where lines are empty."""
     if dtype in ("bf16", "f16") and D <= 128:
         k = {"plan", "fwd_tc", "delta", "dkdv_tc", "dq_ds"}
     elif dtype in ("bf16", "f16"):  # the dK walk also stores P^T; dV streams it (dv_ps)
         k = {"plan", "fwd_wide", "delta", "dk_wide", "dq_ds", "dv_ps"}
-    else:
-        k = {"plan", "split3", "fwd_wide", "delta", "dv_wide", "dk_wide", "dq_ds"}
+    else:  # fp32: dS and P^T as two bf16 pieces each
+        k = {"plan", "split3", "fwd_wide", "delta", "dk_wide", "dq_ds", "dv_ps"}
     return k | {"zero_lines"} if empty_lines else k
 
 

@@ -522,7 +522,9 @@ def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
     # size and its other counters back to 0), give the same results every
     # time, and the per-call entry points' results bit for bit -- except dQ,
     # which the plan sums from the dS tiles of the dK/dV (or dK) walk (the
-    # per-call walk recomputes dS): that dQ is held to the oracle.  nb = 20 has block row 0 and column 0 long
+    # per-call walk recomputes dS), and the wide kernels' dV, summed from the
+    # P^T tiles of the dK walk (for fp32 with the piece products in another
+    # order): those are held to the oracle.  nb = 20 has block row 0 and column 0 long
     # enough to be split into chunks.
     import block_sparse_attention_bsr_gb300 as bsr
 
@@ -531,7 +533,7 @@ def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
     Q, K, V, dO = inputs.make_qkvdo(1, H, nb * 128, D, dtype, 1.0, 17)
     scale = 1.0 / np.sqrt(D)
     ref = run_gpu(Q, K, V, dO, bm, scale)
-    ds_walk = True
+    streamed = {"dQ"} | ({"dV"} if dtype == "f32" or D > 128 else set())
     rp, ci = inputs.bsr_from_block_mask(bm)
     st = bsr.Structure(rp, ci, nb, dev)
     q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
@@ -548,16 +550,16 @@ def test_plan_calls_match_unplanned_calls_repeatedly(dtype, D, nb, H):
         got = {n: t.double().cpu().numpy() for n, t in dict(O=O, row_max=rm, row_denom=rd, dQ=dQ, dK=dK,
                                                                dV=dV).items()}
         for name, t in got.items():
-            if not (ds_walk and name == "dQ"):
+            if name not in streamed:
                 assert np.array_equal(t, ref[name]), name
         if first is None:
             first = got
         for name, t in got.items():
             assert np.array_equal(t, first[name]), ("repeat", name)
-    if ds_walk:
-        heads = [(0, h) for h in range(H)]
-        compare({"dQ": first["dQ"]}, {"dQ": oracle_heads(Q, K, V, dO, bm, scale, heads)["dQ"]}, dtype,
-                heads=heads, what="plan dQ")
+    heads = [(0, h) for h in range(H)]
+    ref_o = oracle_heads(Q, K, V, dO, bm, scale, heads)
+    compare({n: first[n] for n in streamed}, {n: ref_o[n] for n in streamed}, dtype, heads=heads,
+            what="plan, streamed walks")
 
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
@@ -591,13 +593,13 @@ def test_plan_with_empty_lines(dtype, D):
         bsr.bsr_attn_check()
         got = dict(O=O, row_max=rm, row_denom=rd, dQ=dQ, dK=dK, dV=dV)
         for name, t in got.items():
-            if name == "dQ":
+            if name == "dQ" or (name == "dV" and dtype == "f32"):
                 g = t.double().cpu().numpy()
-                empty = np.repeat(bm.sum(1) == 0, 128)
-                assert np.all(g[:, :, empty] == 0), "dQ of empty block rows"
+                empty = np.repeat((bm.sum(1) if name == "dQ" else bm.sum(0)) == 0, 128)
+                assert np.all(g[:, :, empty] == 0), f"{name} of empty lines"
                 heads = [(0, h) for h in range(H)]
-                compare({"dQ": g}, {"dQ": oracle_heads(Q, K, V, dO, bm, scale, heads)["dQ"]}, dtype, heads=heads,
-                        what="plan dQ")
+                compare({name: g}, {name: oracle_heads(Q, K, V, dO, bm, scale, heads)[name]}, dtype, heads=heads,
+                        what=f"plan {name}")
                 continue
             assert np.array_equal(t.double().cpu().numpy(), ref[name]), name
 
