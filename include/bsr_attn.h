@@ -237,7 +237,7 @@ bsr_status bsr_attn_bwd_noalloc(const bsr_tensor* Q, const bsr_tensor* K, const 
  *   batch * heads * nnzb tiles of 32 KiB (64 KiB for fp32 operands: dS in
  *   two bf16 pieces): the dK/dV (or dK) walk stores each dS tile there and
  *   the plan's dQ walk sums dS K over them instead of recomputing the
- *   scores (bf16 / fp16 at head_dim 256 / 512: as many P^T tiles again,
+ *   scores (head_dim 256 / 512 and fp32 operands: as many P^T tiles again,
  *   which the dV walk sums P^T dO over).  It reads col_idx and row_idx to the host to map every BSC entry
  *   to its BSR position, and if that workspace cannot be allocated the
  *   plan's dQ walk recomputes the scores instead (same results within the
