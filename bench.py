@@ -56,26 +56,26 @@ def alg_flops(wl, nnzb, part="total"):
 MEASURED_TRAFFIC = {
     ("global_s8192", "fwd_tc"): {"bytes": 136.4e6, "sources": ("tc_fwd2.cu", "sm100.cuh", "sched.cuh"),
         "sha256": "6b348a4d57aa31d13d83b62106bb1fe180754b6caba85bc0d31858b530f06bca"},
-    ("global_s8192", "dkdv_tc"): {"bytes": 429.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "85d10eba6362f4f32d8fcae9f8ea3ac83946dded19160dc2e0e6b5263573199b"},
-    ("global_s8192", "dq_ds"): {"bytes": 300.8e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "85d10eba6362f4f32d8fcae9f8ea3ac83946dded19160dc2e0e6b5263573199b"},
-    ("local_s8192_d256", "fwd_wide"): {"bytes": 118.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
-    ("local_s8192_d256", "dv_wide"): {"bytes": 115.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
-    ("local_s8192_d256", "dk_wide"): {"bytes": 249.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
-    ("local_s8192_d256", "dq_ds"): {"bytes": 162.8e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "85d10eba6362f4f32d8fcae9f8ea3ac83946dded19160dc2e0e6b5263573199b"},
-    ("global_s8192_f32", "fwd_wide"): {"bytes": 530.3e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
-    ("global_s8192_f32", "dv_wide"): {"bytes": 524.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
-    ("global_s8192_f32", "dk_wide"): {"bytes": 1186.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
-    ("global_s8192_f32", "dq_ds"): {"bytes": 695.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
-        "sha256": "15cdcbbbea8b4270eaa725762d41275b787f027b9f06c2b1051dc840736c4726"},
+    ("global_s8192", "dkdv_tc"): {"bytes": 429.5e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "f6edce16f7f0891c387bf9277bb89b8a8a71a150b47ac2839e4e0fecc62a5d89"},
+    ("global_s8192", "dq_ds"): {"bytes": 300.3e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "f6edce16f7f0891c387bf9277bb89b8a8a71a150b47ac2839e4e0fecc62a5d89"},
+    ("local_s8192_d256", "fwd_wide"): {"bytes": 114.6e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "5fa2010596880ff8b1fab5eb3282367a0570e2874181c90e6333c03d1c77a5aa"},
+    ("local_s8192_d256", "dk_wide"): {"bytes": 364.4e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "5fa2010596880ff8b1fab5eb3282367a0570e2874181c90e6333c03d1c77a5aa"},
+    ("local_s8192_d256", "dq_ds"): {"bytes": 162.1e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "f6edce16f7f0891c387bf9277bb89b8a8a71a150b47ac2839e4e0fecc62a5d89"},
+    ("local_s8192_d256", "dv_ps"): {"bytes": 161.6e6, "sources": ("tc_bwd.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "f6edce16f7f0891c387bf9277bb89b8a8a71a150b47ac2839e4e0fecc62a5d89"},
+    ("global_s8192_f32", "fwd_wide"): {"bytes": 526.3e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "5fa2010596880ff8b1fab5eb3282367a0570e2874181c90e6333c03d1c77a5aa"},
+    ("global_s8192_f32", "dk_wide"): {"bytes": 1872.4e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "5fa2010596880ff8b1fab5eb3282367a0570e2874181c90e6333c03d1c77a5aa"},
+    ("global_s8192_f32", "dq_ds"): {"bytes": 696.2e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "5fa2010596880ff8b1fab5eb3282367a0570e2874181c90e6333c03d1c77a5aa"},
+    ("global_s8192_f32", "dv_ps"): {"bytes": 696.8e6, "sources": ("tc_wide.cu", "sm100.cuh", "sched.cuh"),
+        "sha256": "5fa2010596880ff8b1fab5eb3282367a0570e2874181c90e6333c03d1c77a5aa"},
 }
 
 

@@ -259,6 +259,23 @@ __device__ __forceinline__ void split3(float x, float& x0, float& x1, float& x2)
   x2 = r - x1;
 }
 
+// Stores 64 fp32 values of key row r as two bf16 piece tiles, x = x0 + x1
+// (x0 = bf16(x), x1 = bf16(x - x0)), at tile and tile + 32 KB (the layout of
+// st_tile_sw32_row64), one piece at a time (32 packed words live, not 64).
+__device__ __forceinline__ void st_tile_pieces2(uint8_t* tile, int r, int h, const float (&x)[64]) {
+  uint32_t v[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) v[k] = pack_bf16x2(x[2 * k], x[2 * k + 1]);
+  st_tile_sw32_row64(tile, r, h, v);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const float a0 = __bfloat162float(__float2bfloat16_rn(x[2 * k]));
+    const float b0 = __bfloat162float(__float2bfloat16_rn(x[2 * k + 1]));
+    v[k] = pack_bf16x2(x[2 * k] - a0, x[2 * k + 1] - b0);
+  }
+  st_tile_sw32_row64(tile + 128 * 128 * 2, r, h, v);
+}
+
 // Writes this warpgroup's 64 values of Z (one per key, fp32) into TMEM as
 // ZP pieces of the operand type (pairs of keys per column).
 template <typename Op, int MODE, int NP, int ZP>
@@ -970,17 +987,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
                     for (int k = 0; k < 32; ++k) v[k] = Half16<Op>::pack(z[2 * k], z[2 * k + 1]);
                     st_tile_sw32_row64((uint8_t*)a.dP + ((size_t)cur.bh * a.nnzb + pp) * (128 * 128 * 2), r, hg, v);
                   } else {
-                    uint32_t v0[32], v1[32];
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                      const float a0 = __bfloat162float(__float2bfloat16_rn(z[2 * k]));
-                      const float b0 = __bfloat162float(__float2bfloat16_rn(z[2 * k + 1]));
-                      v0[k] = pack_bf16x2(a0, b0);
-                      v1[k] = pack_bf16x2(z[2 * k] - a0, z[2 * k + 1] - b0);
-                    }
-                    uint8_t* tile = (uint8_t*)a.dP + ((size_t)cur.bh * a.nnzb + pp) * (2 * 128 * 128 * 2);
-                    st_tile_sw32_row64(tile, r, hg, v0);
-                    st_tile_sw32_row64(tile + 128 * 128 * 2, r, hg, v1);
+                    st_tile_pieces2((uint8_t*)a.dP + ((size_t)cur.bh * a.nnzb + pp) * (2 * 128 * 128 * 2), r, hg, z);
                   }
                 } else {
                   atomicExch(a.status, kStatusDeviceCheck);
@@ -1025,21 +1032,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
           tc_fence_before();
           mbar_arrive(&bars->z_full[g & 1]);
           if constexpr (MODE == kDk && NP == 3) {
-            if (jb >= 0) {
-              // fp32 on a plan: dS as two bf16 pieces s0 = bf16(dS), s1 =
-              // bf16(dS - s0) (2^-16 |dS|), one tile each, for dq_ds32_kernel
-              uint32_t v0[32], v1[32];
-#pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                const float a0 = __bfloat162float(__float2bfloat16_rn(z[2 * k]));
-                const float b0 = __bfloat162float(__float2bfloat16_rn(z[2 * k + 1]));
-                v0[k] = pack_bf16x2(a0, b0);
-                v1[k] = pack_bf16x2(z[2 * k] - a0, z[2 * k + 1] - b0);
-              }
-              uint8_t* tile = (uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (2 * 128 * 128 * 2);
-              st_tile_sw32_row64(tile, r, hg, v0);
-              st_tile_sw32_row64(tile + 128 * 128 * 2, r, hg, v1);
-            }
+            if (jb >= 0)  // fp32 on a plan: dS as two bf16 pieces (2^-16 |dS|) for dq_ds32_kernel
+              st_tile_pieces2((uint8_t*)a.dS + ((size_t)cur.bh * a.nnzb + jb) * (2 * 128 * 128 * 2), r, hg, z);
           }
         }
       }
